@@ -1,0 +1,426 @@
+/*
+ * bsg_oracle.c -- the CPU oracle for the block-scaled int8 GEMM.
+ *
+ * TEST INFRASTRUCTURE.  This file is the plain, slow, obviously correct
+ * statement of what the GPU path must compute.  Only the test suite, the
+ * smoke check and the benchmark's CPU-baseline leg may load it.  It shares
+ * no code, header, table or constant generator with the CUDA library, and
+ * it never calls into it.
+ *
+ * Source of every rule (cited per function below):
+ *   [V]  "Verification -- why you can trust the numbers" (DaisyChain-Train,
+ *        web/docs/VERIFICATION.md), section "The verified INT8 units",
+ *        steps 1-3; section "Layer 3: the kernel probe"; section
+ *        "Layer 5: properties and mutation scores"; section
+ *        "Hardware ground truth (RDNA2 ISA audit)".
+ *
+ * Build: plain C99, `-O2 -ffp-contract=off -fno-fast-math` (every float
+ * statement below is one IEEE-754 round-to-nearest-even operation; no
+ * multiply-add contraction, no flush to zero).  OpenMP, when present, only
+ * splits the integer contraction over output rows: integer sums are exact,
+ * so the split cannot change a result.
+ *
+ * Readings taken where the page is silent (each is listed with its reason in
+ * the design notes):
+ *   R1  the 1e-8 floor is applied to the f64 quotient, before rounding to f32;
+ *   R2  inv = f32(1 / f64(scale_f32)) -- the reciprocal of the stored scale,
+ *       formed in f64 on the host side of the page's design;
+ *   R3  the quantize arithmetic is f32 with two roundings: RN(RN(x*inv)+0.5),
+ *       then floor; ties therefore go up (x*inv = -2.5 gives -2);
+ *   R4  epi(s,a,b) multiplies by the row scale a first, then the column
+ *       scale b, exactly as written;
+ *   R5  the fused ReLU returns +0 for every value that is not > 0 (so -0 and
+ *       NaN become +0: the output is never negative at the bit level);
+ *   R6  probe inputs: SplitMix64 outputs (Steele, Lea, Flood, "Fast
+ *       splittable pseudorandom number generators", OOPSLA 2014), A first
+ *       then B, each mapped exactly to a float in [-1, 1);
+ *   R7  the probe hash is a 4-ary SHA-256 (FIPS 180-4) tree over 256-byte
+ *       leaves of C's little-endian bytes, row-major, rows packed.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_OK 0
+#define ORC_ERR_ARG 1
+#define ORC_ERR_RANGE 2     /* a quantized value or an accumulator left its range */
+#define ORC_ERR_NONFINITE 5 /* an input row or column held Inf or NaN */
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------------ */
+/* [V] "The verified INT8 units", step 1: scale = max(|row|)/127, floored at */
+/* 1e-8.  The scale is derived in f64 (the page: scales come from JS f64,    */
+/* which is exactly rounded) and stored as f32.  Readings R1, R2.            */
+/* ------------------------------------------------------------------------ */
+static int absmax_strided(const float *x, int64_t n, int64_t stride, float *m_out) {
+    float m = 0.0f;
+    int finite = 1;
+    for (int64_t k = 0; k < n; ++k) {
+        float v = x[k * stride];
+        if (!isfinite(v)) finite = 0;
+        float a = fabsf(v); /* |-0| = +0 */
+        if (a > m) m = a;
+    }
+    *m_out = m;
+    return finite;
+}
+
+void orc_scale_from_max(float m, float *scale, float *inv) {
+    double s = (double)m / 127.0; /* one IEEE f64 division, RN */
+    if (s < 1e-8) s = 1e-8;       /* R1: floor on the f64 value */
+    float sf = (float)s;          /* RN to binary32 */
+    *scale = sf;
+    *inv = (float)(1.0 / (double)sf); /* R2 */
+}
+
+/* [V] "Hardware ground truth": the quantize computes floor(x*inv + 0.5);    */
+/* reading R3 fixes two roundings (no fused multiply-add).                   */
+int orc_quantize_value(float x, float inv) {
+    float t = x * inv;   /* RN */
+    float u = t + 0.5f;  /* RN */
+    float f = floorf(u);
+    if (!(f >= -128.0f && f <= 128.0f)) return 1000; /* non-finite input only */
+    return (int)f;
+}
+
+/* Quantize `count` vectors of length n.  Vector v starts at x + v*vstride  */
+/* and steps by estride; its int8 values go to q + v*qv + k*qe.             */
+static int quantize_vectors(const float *x, int64_t count, int64_t n, int64_t vstride,
+                            int64_t estride, int8_t *q, int64_t qv, int64_t qe,
+                            float *scale, float *inv) {
+    int status = ORC_OK;
+    for (int64_t v = 0; v < count; ++v) {
+        const float *xv = x + v * vstride;
+        float m, s, iv;
+        if (!absmax_strided(xv, n, estride, &m)) status = ORC_ERR_NONFINITE;
+        orc_scale_from_max(m, &s, &iv);
+        scale[v] = s;
+        if (inv) inv[v] = iv;
+        for (int64_t k = 0; k < n; ++k) {
+            int qq = orc_quantize_value(xv[k * estride], iv);
+            if (qq < -127 || qq > 127) {
+                /* only reachable with non-finite input */
+                if (status == ORC_OK) status = ORC_ERR_RANGE;
+                qq = qq < -127 ? -127 : 127;
+            }
+            q[v * qv + k * qe] = (int8_t)qq;
+        }
+    }
+    return status;
+}
+
+/* Rows of A (M x K, row stride lda) -> Q (M x K, row stride ldq), one scale */
+/* per row.                                                                 */
+int orc_quantize_rows(const float *A, int64_t M, int64_t K, int64_t lda, int8_t *Q,
+                      int64_t ldq, float *scale, float *inv) {
+    if (M < 0 || K < 1 || lda < K || ldq < K) return ORC_ERR_ARG;
+    return quantize_vectors(A, M, K, lda, 1, Q, ldq, 1, scale, inv);
+}
+
+/* Columns of B (K x N, row stride ldb) -> Q (K x N, row stride ldq), one    */
+/* scale per column j, reduced over k.                                      */
+int orc_quantize_cols(const float *B, int64_t K, int64_t N, int64_t ldb, int8_t *Q,
+                      int64_t ldq, float *scale, float *inv) {
+    if (N < 0 || K < 1 || ldb < N || ldq < N) return ORC_ERR_ARG;
+    return quantize_vectors(B, N, K, 1, ldb, Q, 1, ldq, scale, inv);
+}
+
+/* ------------------------------------------------------------------------ */
+/* [V] "The verified INT8 units", step 2: exact int8 products accumulated in */
+/* int32 (exact; no overflow).  The sum is formed in int64 and checked to    */
+/* fit int32, so an overflow is reported instead of wrapped.                */
+/* S[i][j] = sum_k Aq[i][k] * Bq[k][j];  Aq M x K, Bq K x N, S M x N.        */
+/* ------------------------------------------------------------------------ */
+int orc_gemm_s32(const int8_t *Aq, const int8_t *Bq, int64_t M, int64_t N, int64_t K,
+                 int32_t *S) {
+    if (M < 0 || N < 0 || K < 1) return ORC_ERR_ARG;
+    int status = ORC_OK;
+#pragma omp parallel
+    {
+        int64_t *acc = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
+        int local = ORC_OK;
+#pragma omp for schedule(static)
+        for (int64_t i = 0; i < M; ++i) {
+            for (int64_t j = 0; j < N; ++j) acc[j] = 0;
+            for (int64_t k = 0; k < K; ++k) {
+                int64_t a = Aq[i * K + k];
+                const int8_t *brow = Bq + k * N;
+                for (int64_t j = 0; j < N; ++j) acc[j] += a * (int64_t)brow[j];
+            }
+            for (int64_t j = 0; j < N; ++j) {
+                if (acc[j] > INT32_MAX || acc[j] < INT32_MIN) local = ORC_ERR_RANGE;
+                S[i * N + j] = (int32_t)acc[j];
+            }
+        }
+        free(acc);
+        if (local != ORC_OK) {
+#pragma omp critical
+            status = local;
+        }
+    }
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [V] "The verified INT8 units", step 3: epi(s,a,b) = f32(f32(f32(s)*a)*b), */
+/* rounded after the int->float conversion and after each multiply.  The     */
+/* fused ReLU is [V] "Layer 5": its output is never negative (reading R5).   */
+/* ------------------------------------------------------------------------ */
+float orc_epi(int32_t s, float a, float b) {
+    float f = (float)s; /* RN from int32 */
+    float t = f * a;    /* RN */
+    float c = t * b;    /* RN */
+    return c;
+}
+
+float orc_relu(float c) { return (c > 0.0f) ? c : 0.0f; }
+
+int orc_epilogue(const int32_t *S, const float *sa, const float *sb, int64_t M, int64_t N,
+                 int relu, float *C) {
+    if (M < 0 || N < 0) return ORC_ERR_ARG;
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            float c = orc_epi(S[i * N + j], sa[i], sb[j]);
+            C[i * N + j] = relu ? orc_relu(c) : c;
+        }
+    return ORC_OK;
+}
+
+/* The whole unit: C = epi(Aq.Bq, sa, sb) with A quantized per row and B per */
+/* column.  A is M x K, B is K x N, C is M x N, all row-major and packed.    */
+/* If S is not NULL the int32 accumulators are returned too.                 */
+int orc_bsgemm_i8(const float *A, const float *B, int64_t M, int64_t N, int64_t K, int relu,
+                  float *C, int32_t *S_out, float *sa_out, float *sb_out) {
+    if (M < 0 || N < 0 || K < 1) return ORC_ERR_ARG;
+    int8_t *Aq = (int8_t *)malloc((size_t)(M * K > 0 ? M * K : 1));
+    int8_t *Bq = (int8_t *)malloc((size_t)(K * N > 0 ? K * N : 1));
+    float *sa = (float *)malloc(sizeof(float) * (size_t)(M > 0 ? M : 1));
+    float *sb = (float *)malloc(sizeof(float) * (size_t)(N > 0 ? N : 1));
+    int32_t *S = S_out ? S_out : (int32_t *)malloc(sizeof(int32_t) * (size_t)(M * N > 0 ? M * N : 1));
+    int st = ORC_OK, r;
+    r = orc_quantize_rows(A, M, K, K, Aq, K, sa, NULL);
+    if (r != ORC_OK) st = r;
+    r = orc_quantize_cols(B, K, N, N, Bq, N, sb, NULL);
+    if (r != ORC_OK && st == ORC_OK) st = r;
+    r = orc_gemm_s32(Aq, Bq, M, N, K, S);
+    if (r != ORC_OK && st == ORC_OK) st = r;
+    orc_epilogue(S, sa, sb, M, N, relu, C);
+    if (sa_out) memcpy(sa_out, sa, sizeof(float) * (size_t)M);
+    if (sb_out) memcpy(sb_out, sb, sizeof(float) * (size_t)N);
+    if (!S_out) free(S);
+    free(Aq); free(Bq); free(sa); free(sb);
+    return st;
+}
+
+/* Selected cells of the same product, one by one: for each p, C[rows[p]][cols[p]].
+ * Only the rows and columns asked for are quantized, so this works at sizes
+ * where the full product is too slow on a CPU.  S_out may be NULL.          */
+int orc_bsgemm_cells(const float *A, const float *B, int64_t M, int64_t N, int64_t K, int relu,
+                     const int64_t *rows, const int64_t *cols, int64_t n, float *out,
+                     int32_t *S_out) {
+    if (M < 0 || N < 0 || K < 1 || n < 0) return ORC_ERR_ARG;
+    int8_t *qa = (int8_t *)malloc((size_t)K);
+    int8_t *qb = (int8_t *)malloc((size_t)K);
+    int st = ORC_OK;
+    for (int64_t p = 0; p < n; ++p) {
+        int64_t i = rows[p], j = cols[p];
+        if (i < 0 || i >= M || j < 0 || j >= N) { st = ORC_ERR_ARG; break; }
+        float sa, sb, ia, ib;
+        int r1 = quantize_vectors(A + i * K, 1, K, K, 1, qa, K, 1, &sa, &ia);
+        int r2 = quantize_vectors(B + j, 1, K, 1, N, qb, K, 1, &sb, &ib);
+        if (r1 != ORC_OK && st == ORC_OK) st = r1;
+        if (r2 != ORC_OK && st == ORC_OK) st = r2;
+        int64_t acc = 0;
+        for (int64_t k = 0; k < K; ++k) acc += (int64_t)qa[k] * (int64_t)qb[k];
+        if ((acc > INT32_MAX || acc < INT32_MIN) && st == ORC_OK) st = ORC_ERR_RANGE;
+        float c = orc_epi((int32_t)acc, sa, sb);
+        out[p] = relu ? orc_relu(c) : c;
+        if (S_out) S_out[p] = (int32_t)acc;
+    }
+    free(qa); free(qb);
+    return st;
+}
+
+/* ------------------------------------------------------------------------ */
+/* SHA-256, written from FIPS 180-4 sections 4.1.2, 4.2.2, 5.1.1, 5.3.3 and */
+/* 6.2.2.  Used by the probe hash ([V] "Layer 3: the kernel probe").         */
+/* ------------------------------------------------------------------------ */
+static const uint32_t SHA_K[64] = {
+    0x428a2f98u, 0x71374491u, 0xb5c0fbcfu, 0xe9b5dba5u, 0x3956c25bu, 0x59f111f1u, 0x923f82a4u,
+    0xab1c5ed5u, 0xd807aa98u, 0x12835b01u, 0x243185beu, 0x550c7dc3u, 0x72be5d74u, 0x80deb1feu,
+    0x9bdc06a7u, 0xc19bf174u, 0xe49b69c1u, 0xefbe4786u, 0x0fc19dc6u, 0x240ca1ccu, 0x2de92c6fu,
+    0x4a7484aau, 0x5cb0a9dcu, 0x76f988dau, 0x983e5152u, 0xa831c66du, 0xb00327c8u, 0xbf597fc7u,
+    0xc6e00bf3u, 0xd5a79147u, 0x06ca6351u, 0x14292967u, 0x27b70a85u, 0x2e1b2138u, 0x4d2c6dfcu,
+    0x53380d13u, 0x650a7354u, 0x766a0abbu, 0x81c2c92eu, 0x92722c85u, 0xa2bfe8a1u, 0xa81a664bu,
+    0xc24b8b70u, 0xc76c51a3u, 0xd192e819u, 0xd6990624u, 0xf40e3585u, 0x106aa070u, 0x19a4c116u,
+    0x1e376c08u, 0x2748774cu, 0x34b0bcb5u, 0x391c0cb3u, 0x4ed8aa4au, 0x5b9cca4fu, 0x682e6ff3u,
+    0x748f82eeu, 0x78a5636fu, 0x84c87814u, 0x8cc70208u, 0x90befffau, 0xa4506cebu, 0xbef9a3f7u,
+    0xc67178f2u};
+
+static uint32_t rotr32(uint32_t x, int n) { return (x >> n) | (x << (32 - n)); }
+
+static void sha256_block(uint32_t H[8], const uint8_t blk[64]) {
+    uint32_t W[64];
+    for (int t = 0; t < 16; ++t)
+        W[t] = ((uint32_t)blk[4 * t] << 24) | ((uint32_t)blk[4 * t + 1] << 16) |
+               ((uint32_t)blk[4 * t + 2] << 8) | (uint32_t)blk[4 * t + 3];
+    for (int t = 16; t < 64; ++t) {
+        uint32_t s0 = rotr32(W[t - 15], 7) ^ rotr32(W[t - 15], 18) ^ (W[t - 15] >> 3);
+        uint32_t s1 = rotr32(W[t - 2], 17) ^ rotr32(W[t - 2], 19) ^ (W[t - 2] >> 10);
+        W[t] = W[t - 16] + s0 + W[t - 7] + s1;
+    }
+    uint32_t a = H[0], b = H[1], c = H[2], d = H[3], e = H[4], f = H[5], g = H[6], h = H[7];
+    for (int t = 0; t < 64; ++t) {
+        uint32_t S1 = rotr32(e, 6) ^ rotr32(e, 11) ^ rotr32(e, 25);
+        uint32_t ch = (e & f) ^ (~e & g);
+        uint32_t T1 = h + S1 + ch + SHA_K[t] + W[t];
+        uint32_t S0 = rotr32(a, 2) ^ rotr32(a, 13) ^ rotr32(a, 22);
+        uint32_t maj = (a & b) ^ (a & c) ^ (b & c);
+        uint32_t T2 = S0 + maj;
+        h = g; g = f; f = e; e = d + T1; d = c; c = b; b = a; a = T1 + T2;
+    }
+    H[0] += a; H[1] += b; H[2] += c; H[3] += d;
+    H[4] += e; H[5] += f; H[6] += g; H[7] += h;
+}
+
+/* SHA-256 of (prefix byte, if prefix >= 0) followed by msg[0..len). */
+static void sha256_prefixed(int prefix, const uint8_t *msg, size_t len, uint8_t out[32]) {
+    uint32_t H[8] = {0x6a09e667u, 0xbb67ae85u, 0x3c6ef372u, 0xa54ff53au,
+                     0x510e527fu, 0x9b05688cu, 0x1f83d9abu, 0x5be0cd19u};
+    size_t total = len + (prefix >= 0 ? 1 : 0);
+    uint8_t blk[64];
+    size_t fill = 0;
+    if (prefix >= 0) blk[fill++] = (uint8_t)prefix;
+    for (size_t p = 0; p < len; ++p) {
+        blk[fill++] = msg[p];
+        if (fill == 64) { sha256_block(H, blk); fill = 0; }
+    }
+    /* padding: a 1 bit, zeros, then the 64-bit big-endian bit length */
+    blk[fill++] = 0x80;
+    if (fill > 56) {
+        while (fill < 64) blk[fill++] = 0;
+        sha256_block(H, blk);
+        fill = 0;
+    }
+    while (fill < 56) blk[fill++] = 0;
+    uint64_t bits = (uint64_t)total * 8u;
+    for (int i = 7; i >= 0; --i) blk[fill++] = (uint8_t)(bits >> (8 * i));
+    sha256_block(H, blk);
+    for (int i = 0; i < 8; ++i) {
+        out[4 * i] = (uint8_t)(H[i] >> 24);
+        out[4 * i + 1] = (uint8_t)(H[i] >> 16);
+        out[4 * i + 2] = (uint8_t)(H[i] >> 8);
+        out[4 * i + 3] = (uint8_t)H[i];
+    }
+}
+
+void orc_sha256(const uint8_t *msg, size_t len, uint8_t out[32]) {
+    sha256_prefixed(-1, msg, len, out);
+}
+
+/* Reading R7, the tree hash of a byte string D:                             */
+/*   level 0: D cut into 256-byte leaves (the last may be shorter; an empty */
+/*            D is one empty leaf); digest = SHA-256(0x00 || leaf);          */
+/*   level l+1: level l's digests taken four at a time in order (the last   */
+/*            group may hold 1-3); digest = SHA-256(0x01 || d1 || ... );     */
+/*   the hash is the single digest of the first level that has one.         */
+#define ORC_LEAF_BYTES 256
+#define ORC_FANIN 4
+void orc_tree_hash(const uint8_t *data, size_t len, uint8_t out[32]) {
+    size_t nleaf = len == 0 ? 1 : (len + ORC_LEAF_BYTES - 1) / ORC_LEAF_BYTES;
+    uint8_t *cur = (uint8_t *)malloc(32 * nleaf);
+    for (size_t l = 0; l < nleaf; ++l) {
+        size_t off = l * ORC_LEAF_BYTES;
+        size_t n = len - off < ORC_LEAF_BYTES ? len - off : ORC_LEAF_BYTES;
+        if (len == 0) n = 0;
+        sha256_prefixed(0x00, data + off, n, cur + 32 * l);
+    }
+    size_t count = nleaf;
+    while (count > 1) {
+        size_t next = (count + ORC_FANIN - 1) / ORC_FANIN;
+        uint8_t *nxt = (uint8_t *)malloc(32 * next);
+        for (size_t g = 0; g < next; ++g) {
+            size_t first = g * ORC_FANIN;
+            size_t m = count - first < ORC_FANIN ? count - first : ORC_FANIN;
+            sha256_prefixed(0x01, cur + 32 * first, 32 * m, nxt + 32 * g);
+        }
+        free(cur);
+        cur = nxt;
+        count = next;
+    }
+    memcpy(out, cur, 32);
+    free(cur);
+}
+
+/* Hash of an M x N f32 matrix with row stride ldc: its rows' little-endian */
+/* bytes, packed row after row.                                             */
+int orc_hash_f32(const float *C, int64_t M, int64_t N, int64_t ldc, uint8_t out[32]) {
+    if (M < 0 || N < 0 || ldc < N) return ORC_ERR_ARG;
+    size_t len = (size_t)(M * N) * 4u;
+    uint8_t *bytes = (uint8_t *)malloc(len > 0 ? len : 1);
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            uint32_t u;
+            memcpy(&u, &C[i * ldc + j], 4);
+            uint8_t *p = bytes + 4 * (size_t)(i * N + j);
+            p[0] = (uint8_t)u; p[1] = (uint8_t)(u >> 8);
+            p[2] = (uint8_t)(u >> 16); p[3] = (uint8_t)(u >> 24);
+        }
+    orc_tree_hash(bytes, len, out);
+    free(bytes);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Reading R6: the probe's inputs.  SplitMix64 from its published definition:*/
+/* the state advances by the odd constant 0x9e3779b97f4a7c15 and each output */
+/* is the state passed through the mixing function below.  The i-th output  */
+/* (i = 0, 1, ...) of the generator seeded with `seed` is                    */
+/* mix(seed + (i+1)*0x9e3779b97f4a7c15 mod 2^64).                            */
+/* ------------------------------------------------------------------------ */
+uint64_t orc_splitmix64(uint64_t seed, uint64_t i) {
+    uint64_t z = seed + (i + 1u) * 0x9e3779b97f4a7c15ull;
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+    return z ^ (z >> 31);
+}
+
+/* The top 24 bits of an output, as an integer in [-2^23, 2^23), times 2^-23: */
+/* a float in [-1, 1) that is exact in binary32.                             */
+float orc_probe_value(uint64_t z) {
+    int32_t v = (int32_t)(z >> 40) - (1 << 23);
+    return (float)v * (1.0f / 8388608.0f);
+}
+
+/* A (M x K) takes outputs 0 .. M*K-1 in row-major order, B (K x N) the next */
+/* K*N outputs.                                                             */
+void orc_probe_inputs(uint64_t seed, int64_t M, int64_t N, int64_t K, float *A, float *B) {
+    for (int64_t e = 0; e < M * K; ++e) A[e] = orc_probe_value(orc_splitmix64(seed, (uint64_t)e));
+    for (int64_t e = 0; e < K * N; ++e)
+        B[e] = orc_probe_value(orc_splitmix64(seed, (uint64_t)(M * K + e)));
+}
+
+/* [V] "Layer 3": the same seeded int8 GEMM (no ReLU), hashed.             */
+int orc_probe_hash(uint64_t seed, int64_t M, int64_t N, int64_t K, uint8_t out[32]) {
+    if (M < 1 || N < 1 || K < 1) return ORC_ERR_ARG;
+    float *A = (float *)malloc(sizeof(float) * (size_t)(M * K));
+    float *B = (float *)malloc(sizeof(float) * (size_t)(K * N));
+    float *C = (float *)malloc(sizeof(float) * (size_t)(M * N));
+    orc_probe_inputs(seed, M, N, K, A, B);
+    int st = orc_bsgemm_i8(A, B, M, N, K, 0, C, NULL, NULL, NULL);
+    orc_hash_f32(C, M, N, N, out);
+    free(A); free(B); free(C);
+    return st;
+}
