@@ -1,0 +1,443 @@
+"""Benchmark of the bit-exact block-scaled int8 GEMM on GB300.
+
+One step = one pass of the whole hot path over one batch: the three
+GPT-2-small linears at M = 8192 tokens -- QKV (K 768 -> N 2304), fc
+(768 -> 3072, fused ReLU), proj (3072 -> 768) -- each a full bsgemm_i8
+(per-row quantize of A, per-column quantize of B, exact int8 contraction on
+the tensor cores, f32 epilogue), plus the step's probe hash (the seeded
+1024^3 GEMM hashed to 32 bytes).  Throughput counts 2*M*N*K operations per
+GEMM.  Inputs are synthetic (seeded, GPT-2-small-shaped), resident in HBM
+before the timed region; L2 is flushed between timed steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  `--impl reference` times the CPU oracle on a bounded
+sample of the same workload on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "bit-exact block-scaled int8 GEMM TOPS and % of GB300 dense INT8 peak"
+WORKLOAD = "gpt2_small_linears_M8192_qkv_fc_proj+probe1024"
+PROBE = (1024, 1024, 1024)
+PROBE_SEED = 0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def step_ops():
+    from verifiable_quantize_rows_gb300 import inputs
+    ops = sum(2 * M * N * K for _, M, N, K, _, _ in inputs.GPT2_LINEARS)
+    return ops + 2 * PROBE[0] * PROBE[1] * PROBE[2]
+
+
+def config_dict(n_gpus):
+    from verifiable_quantize_rows_gb300 import inputs
+    return {
+        "workload": WORKLOAD,
+        "gemms": [{"name": n, "M": M, "N": N, "K": K, "relu": r}
+                  for n, M, N, K, r, _ in inputs.GPT2_LINEARS]
+                 + [{"name": "probe", "M": PROBE[0], "N": PROBE[1], "K": PROBE[2], "relu": False}],
+        "inputs": "activations N(0,1) with 0.1% x20 outliers, weights N(0,0.02), seeded",
+        "l2": "flushed between timed steps (256 MiB write); inputs resident in HBM",
+        "parallelism": f"replicas x{n_gpus} (weak: each GPU runs the full step)",
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# -------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_selector(local_rank):
+    """nvidia-smi -i argument for this process's GPU (its UUID when known)."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(local_rank).uuid)
+        if u:
+            return u if u.startswith("GPU-") else f"GPU-{u}"
+    except Exception:
+        pass
+    return str(local_rank)
+
+
+# -------------------------------------------------------------- GPU arm
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import verifiable_quantize_rows_gb300 as bsg
+    from verifiable_quantize_rows_gb300 import build as bsg_build
+    from verifiable_quantize_rows_gb300 import inputs
+
+    if not os.path.exists(bsg.LIB_PATH):
+        bsg_build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    lib = bsg.load()
+
+    # resident inputs and outputs
+    lin = []
+    for name, M, N, K, relu, seed in inputs.GPT2_LINEARS:
+        A, B, _ = inputs.gpt2_linear_inputs(name)
+        ws = bsg.Workspace(dev)
+        ws.get(lib.bsgemm_i8_workspace_size(M, N, K))
+        lin.append(dict(name=name, M=M, N=N, K=K, relu=relu, A=A.to(dev), B=B.to(dev),
+                        C=torch.empty(M, N, device=dev), ws=ws, Ah=A.pin_memory(),
+                        Bh=B.pin_memory(), Ch=torch.empty(M, N, pin_memory=True)))
+    pws = bsg.Workspace(dev)
+    pws.get(lib.bsg_probe_workspace_size(*PROBE))
+    probe_out = torch.empty(32, dtype=torch.uint8, device=dev)
+    dstatus = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    host_ws = bsg.Workspace(dev)
+    host_ws.get(max(lib.bsgemm_i8_host_workspace_size(L["M"], L["N"], L["K"]) for L in lin))
+
+    def step(ev=None):
+        """One step; ev: list of (start, end) event pairs to fill per stage."""
+        k = 0
+        for L in lin:
+            if ev is not None:
+                ev[k][0].record(stream)
+            bsg.bsgemm_i8_quantize(L["A"], L["B"], L["ws"], dstatus=dstatus)
+            if ev is not None:
+                ev[k][1].record(stream)
+                ev[k + 1][0].record(stream)
+            bsg.bsgemm_i8_contract(L["M"], L["N"], L["K"], L["C"], L["ws"], relu=L["relu"],
+                                   dstatus=dstatus)
+            if ev is not None:
+                ev[k + 1][1].record(stream)
+            k += 2
+        if ev is not None:
+            ev[k][0].record(stream)
+        bsg.probe_hash_async(PROBE_SEED, *PROBE, out=probe_out, dstatus=dstatus, workspace=pws)
+        if ev is not None:
+            ev[k][1].record(stream)
+
+    n_stage = 2 * len(lin) + 1
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: device-resident inputs
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(n_stage)] for _ in range(args.steps)]
+    clocks = ClockSampler(gpu_selector(local_rank))
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = bsg.launch_count()
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()                      # L2 flush, outside the event pairs
+        step(evs[s])
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - wall0
+    launches = bsg.launch_count() - launches0
+    clk = clocks.stop()
+
+    stage_ms = [[a.elapsed_time(b) for a, b in ev] for ev in evs]
+    step_ms = [sum(x) for x in stage_ms]
+    ms_per_step = statistics.mean(step_ms)
+    # ---- end-to-end through the host-buffer entry point (copies inside)
+    def e2e_step():
+        for L in lin:
+            bsg.bsgemm_i8_host(L["Ah"], L["Bh"], relu=L["relu"], out=L["Ch"], workspace=host_ws)
+        probe_out.zero_()
+        h = bsg.probe_hash(PROBE_SEED, *PROBE, workspace=pws)
+        return h
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e2e_times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        e2e_step()                         # synchronizes: C and the hash are on the host
+        e2e_times.append(time.perf_counter() - t)
+    barrier()
+    e2e_ms = statistics.mean(e2e_times) * 1e3
+
+    # ---- max over ranks
+    t_local = torch.tensor([ms_per_step, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
+    ms_max, e2e_max = float(t_local[0]), float(t_local[1])
+
+    # ---- probe agreement across replicas (the pages' cross-device check)
+    probe_hex = bytes(probe_out.cpu().tolist()).hex()
+    golden = None
+    gpath = os.path.join(ROOT, "tests", "golden", "probe_hash.txt")
+    if os.path.exists(gpath):
+        for line in open(gpath):
+            p = line.split()
+            if len(p) == 5 and p[:4] == [str(PROBE_SEED), *map(str, PROBE)]:
+                golden = p[4]
+    replicas_agree = True
+    if world > 1:
+        mine = torch.tensor(list(probe_out.cpu().tolist()), dtype=torch.int32, device=dev)
+        allh = [torch.empty_like(mine) for _ in range(world)]
+        dist.all_gather(allh, mine)
+        replicas_agree = all(torch.equal(allh[0], h) for h in allh)
+    torch.cuda.synchronize()
+    dstat = int(dstatus.item())
+
+    if rank != 0:
+        return None
+
+    ops = step_ops()
+    peaks, peak_kind = load_peaks()
+    # dominant kernel: the tensor-core contraction (one launch per linear)
+    gemm_ms = [statistics.mean(sm[2 * i + 1] for sm in stage_ms) for i in range(len(lin))]
+    quant_ms = [statistics.mean(sm[2 * i] for sm in stage_ms) for i in range(len(lin))]
+    probe_ms = statistics.mean(sm[-1] for sm in stage_ms)
+    gemm_ops = [2 * L["M"] * L["N"] * L["K"] for L in lin]
+    achieved = sum(gemm_ops) / (sum(gemm_ms) * 1e-3) / 1e12      # TFLOP/s (f16 pipe)
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    quant_bytes = [4 * (L["M"] * L["K"] + L["K"] * L["N"]) + 2 * (L["M"] * L["K"] + L["K"] * L["N"])
+                   for L in lin]
+    quant_gbs = sum(quant_bytes) / (sum(quant_ms) * 1e-3) / 1e9
+    value = ops * world / (ms_max * 1e-3) / 1e12
+    h2d = sum(4 * (L["M"] * L["K"] + L["K"] * L["N"]) for L in lin)
+    d2h = sum(4 * L["M"] * L["N"] for L in lin) + 32
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8",
+        "data": "synthetic",
+        "config": config_dict(world),
+        "roofline": {
+            "bound": "tensor",
+            "kernel": "gemm_tc_kernel (tcgen05 kind::f16, exact int8 contraction + epilogue)",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "peak_source": f"{peak_kind} bf16 burst (f16 dense rate = bf16 nominal)",
+            "traffic": None,
+            "per_gemm_ms": {L["name"]: round(g, 4) for L, g in zip(lin, gemm_ms)},
+        },
+        "quantize": {
+            "bound": "hbm",
+            "achieved_gbs": round(quant_gbs, 1),
+            "peak_gbs": float(peaks.get("hbm_gbs", 6800.0)),
+            "frac": round(quant_gbs / float(peaks.get("hbm_gbs", 6800.0)), 4),
+            "bytes": "4 B read + 2 B f16 operand write per element of A and B",
+            "per_gemm_ms": {L["name"]: round(q, 4) for L, q in zip(lin, quant_ms)},
+        },
+        "probe_ms": round(probe_ms, 4),
+        "int8_peak_note": ("sm_103a has no int8 tensor-core MMA (ptxas rejects tcgen05 "
+                           "kind::i8); the exact contraction runs on the f16 pipe, so the "
+                           "roofline peak is the measured 16-bit dense rate"),
+        "e2e": {"value": round(ops * world / (e2e_max * 1e-3) / 1e12, 3), "unit": "TOPS",
+                "ms_per_step": round(e2e_max, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "api": "bsgemm_i8_host (pinned host A, B in; C out) + bsg_probe_hash"},
+        "clocks": clk,
+        "gpu_launches": launches,
+        "wall_s_timed": round(wall, 4),
+        "probe_hash": probe_hex,
+        "probe_hash_matches_golden": (golden == probe_hex) if golden else None,
+        "replicas_agree": replicas_agree,
+        "device_status": dstat,
+    }
+    return line
+
+
+# -------------------------------------------------------------- CPU oracle
+def oracle_sample_step(orc, rows):
+    """The oracle on the step's workload with each linear cut to `rows`
+    rows of A (the probe at full size); returns (ops, seconds)."""
+    from verifiable_quantize_rows_gb300 import inputs
+    ops = 0
+    t = 0.0
+    for name, M, N, K, relu, seed in inputs.GPT2_LINEARS:
+        A, B, _ = inputs.gpt2_linear_inputs(name)
+        a = A[:rows].numpy()
+        b = B.numpy()
+        t0 = time.perf_counter()
+        orc.bsgemm_i8(a, b, relu)
+        t += time.perf_counter() - t0
+        ops += 2 * a.shape[0] * N * K
+    t0 = time.perf_counter()
+    orc.probe_hash(PROBE_SEED, *PROBE)
+    t += time.perf_counter() - t0
+    ops += 2 * PROBE[0] * PROBE[1] * PROBE[2]
+    return ops, t
+
+
+def cpu_baseline(budget_s=12.0):
+    import oracle
+    orc = oracle.load()
+    ops, t = oracle_sample_step(orc, 256)
+    rows = int(min(8192, max(256, 256 * budget_s / max(t, 1e-3))))
+    rows = max(256, (rows // 256) * 256)
+    ops, t = oracle_sample_step(orc, rows)
+    return {"value": round(ops / t / 1e12, 6), "unit": "TOPS", "cores": orc.num_threads(),
+            "kind": "oracle",
+            "sample": f"each GPT-2 linear on its first {rows} of 8192 rows (full N, K) plus the "
+                      f"full 1024^3 probe; {ops / 1e9:.1f} G ops in {t:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    orc = oracle.load()
+    _, t = oracle_sample_step(orc, 256)
+    total_budget = 150.0
+    per_step = max(1.0, min(10.0, total_budget / max(1, args.steps + args.warmup)))
+    rows = int(min(8192, max(256, 256 * per_step / max(t, 1e-3))))
+    rows = max(256, (rows // 256) * 256)
+    for _ in range(args.warmup):
+        oracle_sample_step(orc, rows)
+    times, ops = [], 0
+    for _ in range(args.steps):
+        ops, t = oracle_sample_step(orc, rows)
+        times.append(t)
+    ms = statistics.mean(times) * 1e3
+    value = ops / (ms * 1e-3) / 1e12
+    sample = (f"each GPT-2 linear on its first {rows} of 8192 rows (full N, K) plus the full "
+              f"1024^3 probe, {ops / 1e9:.1f} G ops per step")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TOPS",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic", "config": config_dict(world),
+        "cpu_baseline": {"value": round(value, 6), "unit": "TOPS", "cores": orc.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = env_int("WORLD_SIZE", 1)
+    rank = env_int("RANK", 0)
+    local_rank = env_int("LOCAL_RANK", 0)
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_gpu(args, rank, world, local_rank)
+    if line is not None:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+/*
+ * bsgemm.h -- C ABI of the bit-exact block-scaled int8 GEMM for GB300.
+ *
+ * The operation ("Verification -- why you can trust the numbers",
+ * DaisyChain-Train web/docs/VERIFICATION.md, section "The verified INT8
+ * units", steps 1-3):
+ *
+ *   1. A (M x K) is quantized per row and B (K x N) per column:
+ *        m      = max |x| over the row (column)
+ *        scale  = f32( max( f64(m) / 127, 1e-8 ) )      -- an IEEE f64 divide
+ *        inv    = f32( 1 / f64(scale) )                 -- an IEEE f64 divide
+ *        q      = floor( RN32( RN32(x * inv) + 0.5 ) )  -- int8 in [-127, 127]
+ *   2. S = Aq . Bq, exact int32 accumulation;
+ *   3. C = f32( f32( f32(S) * sa[i] ) * sb[j] ), each step rounded to
+ *      nearest-even binary32; with relu != 0, C = (C > 0) ? C : +0.
+ *
+ * and the kernel probe (same page, section "Layer 3: the kernel probe"): a
+ * seeded GEMM whose output bytes are hashed to 32 bytes.
+ *
+ * Readings of points the page leaves open (the floor is applied to the f64
+ * quotient; inv is the reciprocal of the stored f32 scale; the quantize uses
+ * two f32 roundings; ReLU maps -0 and NaN to +0; the probe's inputs come
+ * from SplitMix64 and its hash is a 4-ary SHA-256 tree over 256-byte leaves)
+ * are stated per entry point below.
+ *
+ * Conventions for every entry point:
+ *   - Matrices are row-major float32 / int8 / int32 with a leading dimension
+ *     in elements.  Unless an argument says "host", every pointer is a
+ *     DEVICE pointer owned by the caller; the library keeps no pointer after
+ *     it returns and frees nothing.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream) unless stated otherwise.
+ *   - Argument errors are returned synchronously before anything is
+ *     launched.  A failed launch returns BSG_ERR_CUDA.
+ *   - Data-dependent conditions are OR-ed into `*dstatus` (a device int32,
+ *     may be NULL) as BSG_DSTATUS_* bits; read it after the stream
+ *     synchronizes.  With a non-finite input the outputs are unspecified.
+ *   - Every wait inside a kernel is bounded; on expiry the kernel sets
+ *     BSG_DSTATUS_TIMEOUT, drains its own copies, frees its tensor memory and
+ *     returns.  Nothing traps or aborts.
+ *   - K <= BSG_MAX_K (133144): above it 127*127*K can leave int32.
+ */
+#ifndef BSGEMM_H
+#define BSGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BSG_OK = 0,
+    BSG_ERR_ARG = 1,         /* a size, pointer, leading dimension or flag is invalid */
+    BSG_ERR_K_TOO_LARGE = 2, /* K > BSG_MAX_K */
+    BSG_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned (256 B) or too small */
+    BSG_ERR_CUDA = 4,        /* a CUDA call or launch failed */
+    BSG_ERR_NONFINITE = 5,   /* only as a host-side summary; see BSG_DSTATUS_NONFINITE */
+    BSG_ERR_TIMEOUT = 6,     /* only as a host-side summary; see BSG_DSTATUS_TIMEOUT */
+    BSG_ERR_UNSUPPORTED = 7  /* the current device is not sm_103 */
+} bsg_status;
+
+#define BSG_MAX_K 133144
+#define BSG_DSTATUS_NONFINITE 0x1 /* an input row or column held Inf or NaN */
+#define BSG_DSTATUS_TIMEOUT 0x2   /* a bounded wait inside a kernel expired */
+
+/* Human-readable name of a status code (static storage). */
+const char *bsg_status_str(bsg_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int bsg_version(void);
+
+/* ---- step 1: quantize ---------------------------------------------------- */
+
+/* Rows of X (rows x cols, leading dimension ldx >= cols) to int8.
+ * Q: rows x cols int8 with leading dimension ldq >= cols.
+ * scale, inv: `rows` floats each (inv may be NULL).
+ * Page: "The verified INT8 units", step 1; "Hardware ground truth" for the
+ * floor(x*inv + 0.5) rule.  rows, cols >= 1. */
+bsg_status bsg_quantize_rows(const float *X, int64_t rows, int64_t cols, int64_t ldx, int8_t *Q,
+                             int64_t ldq, float *scale, float *inv, int32_t *dstatus,
+                             void *stream);
+
+/* Columns of X (rows x cols, leading dimension ldx >= cols) to int8: one
+ * scale per column j, reduced over the rows.  Q has X's layout: rows x cols
+ * int8 with leading dimension ldq >= cols.  scale, inv: `cols` floats (inv
+ * may be NULL).  `workspace` must hold bsg_quantize_cols_workspace_size()
+ * bytes (256-byte aligned).  Same passage as bsg_quantize_rows. */
+size_t bsg_quantize_cols_workspace_size(int64_t rows, int64_t cols);
+bsg_status bsg_quantize_cols(const float *X, int64_t rows, int64_t cols, int64_t ldx, int8_t *Q,
+                             int64_t ldq, float *scale, float *inv, void *workspace,
+                             size_t ws_bytes, int32_t *dstatus, void *stream);
+
+/* ---- step 2: the exact integer contraction -------------------------------- */
+
+/* S = Aq . Bq exactly, int32.  Aq: M x K int8 (lda >= K); Bq: K x N int8
+ * (ldb >= N); S: M x N int32 (lds >= N).  Runs the same tensor-core kernel
+ * as bsgemm_i8 with its int32 result stored instead of the epilogue.
+ * Page: "The verified INT8 units", step 2. */
+size_t bsg_gemm_s32_workspace_size(int64_t M, int64_t N, int64_t K);
+bsg_status bsg_gemm_s32(const int8_t *Aq, int64_t lda, const int8_t *Bq, int64_t ldb, int64_t M,
+                        int64_t N, int64_t K, int32_t *S, int64_t lds, void *workspace,
+                        size_t ws_bytes, int32_t *dstatus, void *stream);
+
+/* ---- step 3: the epilogue --------------------------------------------------- */
+
+/* C[i][j] = epi(S[i][j], sa[i], sb[j]) (then ReLU if relu != 0), for any
+ * int32 S and any float scales (subnormals and signed zeros are kept; a NaN
+ * result's payload is unspecified).  S: M x N int32 (lds >= N); C: M x N
+ * float (ldc >= N).  Page: "The verified INT8 units", step 3, and "Layer 5"
+ * for the ReLU. */
+bsg_status bsg_epilogue(const int32_t *S, int64_t lds, const float *sa, const float *sb,
+                        int64_t M, int64_t N, int relu, float *C, int64_t ldc, void *stream);
+
+/* ---- the whole unit ------------------------------------------------------------ */
+
+/* C = epi(q(A) . q(B)) with A (M x K) quantized per row and B (K x N) per
+ * column; all operands packed row-major.  `workspace`: at least
+ * bsgemm_i8_workspace_size(M, N, K) bytes, 256-byte aligned, device memory;
+ * its contents on return are unspecified.  Steps 1-3 of "The verified INT8
+ * units". */
+size_t bsgemm_i8_workspace_size(int64_t M, int64_t N, int64_t K);
+bsg_status bsgemm_i8(const float *A, const float *B, int64_t M, int64_t N, int64_t K, int relu,
+                     float *C, void *workspace, size_t ws_bytes, int32_t *dstatus,
+                     void *stream);
+
+/* The general form: op(A) = A (M x K, lda >= K) or, with transA, the
+ * transpose of a stored K x M matrix (lda >= M); op(B) = B (K x N, ldb >= N)
+ * or, with transB, the transpose of a stored N x K matrix (ldb >= K).  op(A)
+ * is quantized per row and op(B) per column, as if the transposes were
+ * materialised (transposing floats is exact).  C: M x N, ldc >= N.  Same
+ * workspace size as bsgemm_i8. */
+bsg_status bsgemm_i8_ex(const float *A, int64_t lda, int transA, const float *B, int64_t ldb,
+                        int transB, int64_t M, int64_t N, int64_t K, int relu, float *C,
+                        int64_t ldc, void *workspace, size_t ws_bytes, int32_t *dstatus,
+                        void *stream);
+
+/* The unit in two stages over one workspace (bsgemm_i8 is the pair):
+ * bsgemm_i8_quantize runs step 1 -- op(A) per row and op(B) per column into
+ * the workspace's f16 operands and scales (arguments as bsgemm_i8_ex) -- and
+ * bsgemm_i8_contract runs steps 2-3 from that workspace into C (M x N,
+ * ldc >= N).  Both on `stream`; the workspace must not be reused in between. */
+bsg_status bsgemm_i8_quantize(const float *A, int64_t lda, int transA, const float *B,
+                              int64_t ldb, int transB, int64_t M, int64_t N, int64_t K,
+                              void *workspace, size_t ws_bytes, int32_t *dstatus, void *stream);
+bsg_status bsgemm_i8_contract(int64_t M, int64_t N, int64_t K, int relu, float *C, int64_t ldc,
+                              void *workspace, size_t ws_bytes, int32_t *dstatus, void *stream);
+
+/* Number of kernels this library has launched in this process (host-side
+ * counter; every launch of every entry point counts). */
+uint64_t bsg_launch_count(void);
+
+/* bsgemm_i8 on HOST buffers (packed row-major; pinned memory gives
+ * asynchronous copies): copies A and B to the device, runs the unit, copies
+ * C back, and synchronizes `stream` before returning.  `workspace`: device
+ * memory of at least bsgemm_i8_host_workspace_size(M, N, K) bytes.
+ * *dstatus_host (may be NULL) receives the device status bits. */
+size_t bsgemm_i8_host_workspace_size(int64_t M, int64_t N, int64_t K);
+bsg_status bsgemm_i8_host(const float *A_host, const float *B_host, int64_t M, int64_t N,
+                          int64_t K, int relu, float *C_host, void *workspace, size_t ws_bytes,
+                          int32_t *dstatus_host, void *stream);
+
+/* ---- the probe --------------------------------------------------------------------- */
+
+/* 32-byte hash of an M x N float matrix (leading dimension ldc >= N): the
+ * matrix's little-endian bytes, row after row with no padding, cut into
+ * 256-byte leaves (the last may be shorter); leaf digest SHA-256(0x00 ||
+ * leaf); then, level by level, digests taken four at a time in order (the
+ * last group may be shorter) give SHA-256(0x01 || d1 || ...) until one
+ * digest remains.  SHA-256 is FIPS 180-4.  out32: 32 bytes of DEVICE memory.
+ * `workspace`: bsg_hash_f32_workspace_size(M, N) bytes.  Page: "Layer 3: the
+ * kernel probe" (the page names no hash function; this tree is our reading). */
+size_t bsg_hash_f32_workspace_size(int64_t M, int64_t N);
+bsg_status bsg_hash_f32(const float *C, int64_t M, int64_t N, int64_t ldc, uint8_t *out32,
+                        void *workspace, size_t ws_bytes, void *stream);
+
+/* The probe: A (M x K) and B (K x N) filled from SplitMix64 (Steele, Lea,
+ * Flood 2014) seeded with `seed` -- A takes outputs 0 .. M*K-1 row-major, B
+ * the next K*N -- each output z mapped exactly to ((z >> 40) - 2^23) * 2^-23
+ * in [-1, 1); then bsgemm_i8 without ReLU; then bsg_hash_f32 of C.
+ * out32: 32 bytes of DEVICE memory (asynchronous).  `workspace`:
+ * bsg_probe_workspace_size(M, N, K) bytes.  Page: "Layer 3: the kernel
+ * probe". */
+size_t bsg_probe_workspace_size(int64_t M, int64_t N, int64_t K);
+bsg_status bsg_probe_hash_async(uint64_t seed, int64_t M, int64_t N, int64_t K, uint8_t *out32,
+                                void *workspace, size_t ws_bytes, int32_t *dstatus,
+                                void *stream);
+
+/* As bsg_probe_hash_async, but out32_host is HOST memory and the call
+ * synchronizes `stream` before returning.  Returns BSG_ERR_TIMEOUT or
+ * BSG_ERR_NONFINITE if the device status says so. */
+bsg_status bsg_probe_hash(uint64_t seed, int64_t M, int64_t N, int64_t K, uint8_t *out32_host,
+                          void *workspace, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BSGEMM_H */

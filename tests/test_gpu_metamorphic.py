@@ -1,0 +1,121 @@
+"""Layer-5 properties on the GPU path, through the C ABI.
+
+"Verification -- why you can trust the numbers", section "Layer 5":
+relations (row permutation permutes outputs; a zero row yields zeros;
+batches decompose; single-cell sensitivity) and two absolutes (fused ReLU
+never negative; at unit scales the output is the exact integer dot
+product).  These hold at any size, so they also cover shapes too large for a
+full oracle comparison.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import assert_bits_equal, dev, host, u32
+from verifiable_quantize_rows_gb300 import inputs
+import verifiable_quantize_rows_gb300 as bsg
+
+pytestmark = pytest.mark.gpu
+
+
+def run(A, B, relu=False):
+    return host(bsg.bsgemm_i8(dev(A), dev(B), relu=relu))
+
+
+@pytest.fixture(scope="module")
+def case():
+    A = inputs.gpt2_activations(1024, 768, 21).numpy()
+    B = inputs.gpt2_weights(768, 640, 21).numpy()
+    return A, B, run(A, B)
+
+
+def test_row_and_column_permutation(case):
+    A, B, C = case
+    rng = np.random.default_rng(0)
+    pr, pc = rng.permutation(A.shape[0]), rng.permutation(B.shape[1])
+    assert_bits_equal(run(A[pr], B[:, pc]), C[pr][:, pc], "permuted")
+
+
+def test_zero_rows_and_columns(case):
+    A, B, _ = case
+    A2, B2 = A.copy(), B.copy()
+    A2[[3, 500, 1023]] = 0.0
+    A2[7] = -0.0
+    B2[:, [0, 255, 639]] = 0.0
+    for relu in (False, True):
+        C = run(A2, B2, relu)
+        for r in (3, 500, 1023, 7):
+            assert not u32(C[r]).any()
+        for c in (0, 255, 639):
+            assert not u32(C[:, c]).any()
+
+
+def test_batches_decompose(case):
+    A, B, C = case
+    parts = [run(A[a:b], B) for a, b in ((0, 1), (1, 129), (129, 700), (700, 1024))]
+    assert_bits_equal(np.concatenate(parts), C, "row batches")
+    cparts = [run(A, B[:, a:b]) for a, b in ((0, 256), (256, 257), (257, 640))]
+    assert_bits_equal(np.concatenate(cparts, axis=1), C, "column batches")
+
+
+def test_single_cell_sensitivity(case):
+    A, B, C = case
+    A2 = A.copy()
+    A2[300, 10] += 2.5
+    d = u32(run(A2, B)) != u32(C)
+    assert d[300].any() and not np.delete(d, 300, axis=0).any()
+    B2 = B.copy()
+    B2[100, 77] -= 0.5
+    d = u32(run(A, B2)) != u32(C)
+    assert d[:, 77].any() and not np.delete(d, 77, axis=1).any()
+
+
+def test_relu_never_negative():
+    A = inputs.adversarial(700, 900, 31).numpy()
+    B = inputs.adversarial(500, 900, 32, along_rows=False).numpy()
+    C = run(A, B, relu=True)
+    assert not (u32(C) >> 31).any()
+    C0 = run(A, B, relu=False)
+    assert (C0 < 0).any()
+
+
+@pytest.mark.parametrize("K", [700, 1024, 3000])
+def test_unit_scales_exact_integer_dot(K):
+    rng = np.random.default_rng(K)
+    M, N = 300, 260
+    A = rng.integers(-127, 128, (M, K)).astype(np.float32)
+    B = rng.integers(-127, 128, (K, N)).astype(np.float32)
+    A[:, 0] = 127
+    B[0, :] = -127
+    exact = A.astype(np.int64) @ B.astype(np.int64)
+    C = run(A, B)
+    # exact while |dot| < 2^24; beyond, f32(S) is the correctly rounded dot
+    np.testing.assert_array_equal(C, exact.astype(np.float32))
+    S = host(bsg.gemm_s32(dev(A.astype(np.int8)), dev(B.astype(np.int8))))
+    np.testing.assert_array_equal(S.astype(np.int64), exact)
+
+
+def test_probe_hash_is_deterministic_and_seeded():
+    h0 = bsg.probe_hash(0)
+    assert bsg.probe_hash(0) == h0
+    assert bsg.probe_hash(1) != h0
+
+
+def test_probe_hash_golden():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "probe_hash.txt")
+    for line in open(path):
+        if line.strip() and not line.startswith("#"):
+            seed, M, N, K, h = line.split()
+            assert bsg.probe_hash(int(seed), int(M), int(N), int(K)).hex() == h, line
+
+
+def test_host_buffer_entry_point(orc):
+    A = inputs.gpt2_activations(512, 768, 41).numpy()
+    B = inputs.gpt2_weights(768, 300, 41).numpy()
+    Ah = torch.from_numpy(A).pin_memory()
+    Bh = torch.from_numpy(B).pin_memory()
+    C, st = bsg.bsgemm_i8_host(Ah, Bh, relu=True)
+    assert st == 0
+    Co, _ = orc.bsgemm_i8(A, B, True)
+    assert_bits_equal(C.numpy(), Co, "host entry point")

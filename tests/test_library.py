@@ -1,0 +1,72 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every function
+include/bsgemm.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+
+import pytest
+
+import verifiable_quantize_rows_gb300 as bsg
+from verifiable_quantize_rows_gb300 import build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return bsg.load()
+
+
+def test_header_declares_the_boundary():
+    names = bsg.exported_symbols()
+    for required in ("bsg_quantize_rows", "bsg_quantize_cols", "bsg_gemm_s32", "bsg_epilogue",
+                     "bsgemm_i8", "bsgemm_i8_ex", "bsgemm_i8_host", "bsg_hash_f32",
+                     "bsg_probe_hash", "bsg_probe_hash_async", "bsg_status_str"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in bsg.exported_symbols() if not hasattr(lib, n)]
+    assert not missing
+
+
+def test_status_strings_and_version(lib):
+    assert lib.bsg_version() >= 100
+    for code in range(8):
+        assert lib.bsg_status_str(code).startswith(b"BSG_")
+
+
+def test_workspace_sizes(lib):
+    for M, N, K in ((1, 1, 1), (8192, 2304, 768), (4097, 12289, 8191)):
+        ws = lib.bsgemm_i8_workspace_size(M, N, K)
+        ldk = (K + 63) // 64 * 64
+        assert ws >= 2 * ldk * (M + N) + 4 * (M + N)
+        assert lib.bsgemm_i8_host_workspace_size(M, N, K) > ws
+        assert lib.bsg_probe_workspace_size(M, N, K) > ws
+    assert lib.bsgemm_i8_workspace_size(0, 5, 5) == 0
+
+
+def test_argument_errors_without_gpu(lib):
+    vp = ctypes.c_void_p
+    dummy = vp(256)
+    # null pointers, bad sizes, K over the limit, too-small workspace
+    assert lib.bsgemm_i8(None, dummy, 4, 4, 4, 0, dummy, dummy, 1 << 20, None, None) == 1
+    assert lib.bsgemm_i8(dummy, dummy, 0, 4, 4, 0, dummy, dummy, 1 << 20, None, None) == 1
+    assert lib.bsgemm_i8(dummy, dummy, 4, 4, bsg.MAX_K + 1, 0, dummy, dummy, 1 << 30, None,
+                         None) == 2
+    assert lib.bsgemm_i8(dummy, dummy, 4, 4, 4, 0, dummy, dummy, 16, None, None) == 3
+    assert lib.bsgemm_i8(dummy, dummy, 4, 4, 4, 0, dummy, vp(257), 1 << 20, None, None) == 3
+    assert lib.bsgemm_i8_ex(dummy, 3, 0, dummy, 4, 0, 4, 4, 4, 0, dummy, 4, dummy, 1 << 20,
+                            None, None) == 1   # lda < K
+    assert lib.bsgemm_i8_ex(dummy, 4, 2, dummy, 4, 0, 4, 4, 4, 0, dummy, 4, dummy, 1 << 20,
+                            None, None) == 1   # transA not 0/1
+    assert lib.bsg_quantize_rows(dummy, 4, 8, 7, dummy, 8, dummy, None, None, None) == 1
+    assert lib.bsg_quantize_cols(dummy, 4, 8, 8, dummy, 8, dummy, None, None, 0, None, None) == 3
+    assert lib.bsg_epilogue(dummy, 3, dummy, dummy, 4, 4, 0, dummy, 4, None) == 1
+    assert lib.bsg_gemm_s32(dummy, 4, dummy, 4, 4, 4, 4, dummy, 3, dummy, 1 << 20, None,
+                            None) == 1
+    assert lib.bsg_hash_f32(dummy, 2, 2, 2, None, dummy, 1 << 20, None) == 1
+    assert lib.bsg_probe_hash(0, 4, 4, 4, None, dummy, 1 << 20, None) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        bsg.load(str(tmp_path / "missing.so"))

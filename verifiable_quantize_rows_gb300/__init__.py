@@ -1,1 +1,353 @@
-"""Bit-exact block-scaled int8 GEMM for GB300 (sm_103a)."""
+"""Bit-exact block-scaled int8 GEMM for GB300 (sm_103a).
+
+A thin Python binding over the C ABI declared in ``include/bsgemm.h``
+(library ``_build/libbsgemm.so``).  Every step of the computation runs in the
+library's CUDA kernels; this module only checks and marshals arguments, and
+uses PyTorch for device memory and streams.  There is no CPU fallback: if the
+library is missing or the device is not sm_103, calls raise.
+
+Functions take contiguous row-major CUDA tensors and run on the current
+PyTorch stream (or the ``stream`` given).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+__all__ = ["BsgError", "load", "exported_symbols", "quantize_rows", "quantize_cols",
+           "gemm_s32", "epilogue", "bsgemm_i8", "bsgemm_i8_ex", "bsgemm_i8_host",
+           "bsgemm_i8_quantize", "bsgemm_i8_contract", "launch_count", "hash_f32", "probe_hash", "probe_hash_async", "workspace_size", "Workspace",
+           "DSTATUS_NONFINITE", "DSTATUS_TIMEOUT", "MAX_K"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libbsgemm.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "bsgemm.h")
+
+MAX_K = 133144
+DSTATUS_NONFINITE = 0x1
+DSTATUS_TIMEOUT = 0x2
+
+STATUS = {0: "BSG_OK", 1: "BSG_ERR_ARG", 2: "BSG_ERR_K_TOO_LARGE", 3: "BSG_ERR_WORKSPACE",
+          4: "BSG_ERR_CUDA", 5: "BSG_ERR_NONFINITE", 6: "BSG_ERR_TIMEOUT",
+          7: "BSG_ERR_UNSUPPORTED"}
+
+
+class BsgError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+_i64, _vp, _sz, _i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+
+
+def _declare(lib):
+    sigs = {
+        "bsg_status_str": ([_i32], ctypes.c_char_p),
+        "bsg_version": ([], _i32),
+        "bsg_quantize_rows": ([_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp], _i32),
+        "bsg_quantize_cols_workspace_size": ([_i64, _i64], _sz),
+        "bsg_quantize_cols": ([_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _sz, _vp, _vp],
+                              _i32),
+        "bsg_gemm_s32_workspace_size": ([_i64, _i64, _i64], _sz),
+        "bsg_gemm_s32": ([_vp, _i64, _vp, _i64, _i64, _i64, _i64, _vp, _i64, _vp, _sz, _vp, _vp],
+                         _i32),
+        "bsg_epilogue": ([_vp, _i64, _vp, _vp, _i64, _i64, _i32, _vp, _i64, _vp], _i32),
+        "bsgemm_i8_workspace_size": ([_i64, _i64, _i64], _sz),
+        "bsgemm_i8": ([_vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _sz, _vp, _vp], _i32),
+        "bsgemm_i8_ex": ([_vp, _i64, _i32, _vp, _i64, _i32, _i64, _i64, _i64, _i32, _vp, _i64,
+                          _vp, _sz, _vp, _vp], _i32),
+        "bsgemm_i8_quantize": ([_vp, _i64, _i32, _vp, _i64, _i32, _i64, _i64, _i64, _vp, _sz, _vp,
+                                _vp], _i32),
+        "bsgemm_i8_contract": ([_i64, _i64, _i64, _i32, _vp, _i64, _vp, _sz, _vp, _vp], _i32),
+        "bsg_launch_count": ([], ctypes.c_uint64),
+        "bsgemm_i8_host_workspace_size": ([_i64, _i64, _i64], _sz),
+        "bsgemm_i8_host": ([_vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _sz, _vp, _vp], _i32),
+        "bsg_hash_f32_workspace_size": ([_i64, _i64], _sz),
+        "bsg_hash_f32": ([_vp, _i64, _i64, _i64, _vp, _vp, _sz, _vp], _i32),
+        "bsg_probe_workspace_size": ([_i64, _i64, _i64], _sz),
+        "bsg_probe_hash_async": ([ctypes.c_uint64, _i64, _i64, _i64, _vp, _vp, _sz, _vp, _vp],
+                                 _i32),
+        "bsg_probe_hash": ([ctypes.c_uint64, _i64, _i64, _i64, _vp, _vp, _sz, _vp], _i32),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+def load(path: str | None = None):
+    """Load the CUDA library.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None or path is not None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(
+                    f"CUDA library not built: {p} is missing "
+                    "(run `python -m verifiable_quantize_rows_gb300.build`)")
+            lib = _declare(ctypes.CDLL(p))
+            if path is not None:
+                return lib
+            _lib = lib
+        return _lib
+
+
+def exported_symbols() -> list[str]:
+    """Function names declared in include/bsgemm.h."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b((?:bsg|bsgemm)_\w+)\s*\(", text)))
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise BsgError(code, where)
+
+
+# ---------------------------------------------------------------------------
+# torch-side helpers (memory and streams only)
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _need(t, dtype, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor of dtype {dtype}")
+    if t.dim() != 2 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D tensor")
+
+
+class Workspace:
+    """A growable device byte buffer (256-byte aligned, from PyTorch)."""
+
+    def __init__(self, device=None):
+        self.device = device
+        self.buf = None
+
+    def get(self, nbytes: int):
+        torch = _torch()
+        nbytes = max(int(nbytes), 256)
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, device=self.device or "cuda")
+        return self.buf
+
+    def ptr_size(self, nbytes: int):
+        b = self.get(nbytes)
+        return ctypes.c_void_p(b.data_ptr()), b.numel()
+
+
+_default_ws: dict = {}
+
+
+def _ws(workspace, nbytes):
+    torch = _torch()
+    if workspace is None:
+        dev = torch.cuda.current_device()
+        workspace = _default_ws.setdefault(dev, Workspace(torch.device("cuda", dev)))
+    return workspace.ptr_size(nbytes)
+
+
+def workspace_size(M: int, N: int, K: int) -> int:
+    return int(load().bsgemm_i8_workspace_size(M, N, K))
+
+
+# ---------------------------------------------------------------------------
+def quantize_rows(X, stream=None, dstatus=None):
+    """Per-row int8 quantization: (Q int8, scale f32, inv f32)."""
+    torch = _torch()
+    _need(X, torch.float32, "X")
+    R, C = X.shape
+    Q = torch.empty((R, C), dtype=torch.int8, device=X.device)
+    sc = torch.empty(R, dtype=torch.float32, device=X.device)
+    iv = torch.empty(R, dtype=torch.float32, device=X.device)
+    _check(load().bsg_quantize_rows(_ptr(X), R, C, C, _ptr(Q), C, _ptr(sc), _ptr(iv),
+                                    _ptr(dstatus), _stream_ptr(stream)), "bsg_quantize_rows")
+    return Q, sc, iv
+
+
+def quantize_cols(X, stream=None, dstatus=None, workspace=None):
+    """Per-column int8 quantization (Q keeps X's layout): (Q, scale, inv)."""
+    torch = _torch()
+    _need(X, torch.float32, "X")
+    R, C = X.shape
+    lib = load()
+    Q = torch.empty((R, C), dtype=torch.int8, device=X.device)
+    sc = torch.empty(C, dtype=torch.float32, device=X.device)
+    iv = torch.empty(C, dtype=torch.float32, device=X.device)
+    wp, wn = _ws(workspace, lib.bsg_quantize_cols_workspace_size(R, C))
+    _check(lib.bsg_quantize_cols(_ptr(X), R, C, C, _ptr(Q), C, _ptr(sc), _ptr(iv), wp, wn,
+                                 _ptr(dstatus), _stream_ptr(stream)), "bsg_quantize_cols")
+    return Q, sc, iv
+
+
+def gemm_s32(Aq, Bq, stream=None, dstatus=None, workspace=None):
+    """Exact int32 S = Aq . Bq on the tensor cores."""
+    torch = _torch()
+    _need(Aq, torch.int8, "Aq")
+    _need(Bq, torch.int8, "Bq")
+    M, K = Aq.shape
+    K2, N = Bq.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    lib = load()
+    S = torch.empty((M, N), dtype=torch.int32, device=Aq.device)
+    wp, wn = _ws(workspace, lib.bsg_gemm_s32_workspace_size(M, N, K))
+    _check(lib.bsg_gemm_s32(_ptr(Aq), K, _ptr(Bq), N, M, N, K, _ptr(S), N, wp, wn,
+                            _ptr(dstatus), _stream_ptr(stream)), "bsg_gemm_s32")
+    return S
+
+
+def epilogue(S, sa, sb, relu: bool = False, stream=None):
+    """C = epi(S, sa, sb) (+ReLU) for arbitrary int32 S and float scales."""
+    torch = _torch()
+    _need(S, torch.int32, "S")
+    M, N = S.shape
+    if sa.numel() != M or sb.numel() != N:
+        raise ValueError("scale lengths do not match S")
+    C = torch.empty((M, N), dtype=torch.float32, device=S.device)
+    _check(load().bsg_epilogue(_ptr(S), N, _ptr(sa.contiguous()), _ptr(sb.contiguous()), M, N,
+                               int(bool(relu)), _ptr(C), N, _stream_ptr(stream)), "bsg_epilogue")
+    return C
+
+
+def bsgemm_i8(A, B, relu: bool = False, out=None, stream=None, dstatus=None, workspace=None):
+    """C = epi(q_rows(A) . q_cols(B)) (+ReLU), bit-exact."""
+    torch = _torch()
+    _need(A, torch.float32, "A")
+    _need(B, torch.float32, "B")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    lib = load()
+    C = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=A.device)
+    wp, wn = _ws(workspace, lib.bsgemm_i8_workspace_size(M, N, K))
+    _check(lib.bsgemm_i8(_ptr(A), _ptr(B), M, N, K, int(bool(relu)), _ptr(C), wp, wn,
+                         _ptr(dstatus), _stream_ptr(stream)), "bsgemm_i8")
+    return C
+
+
+def bsgemm_i8_ex(A, B, transA: bool = False, transB: bool = False, relu: bool = False,
+                 out=None, stream=None, dstatus=None, workspace=None):
+    """C = epi(q_rows(op(A)) . q_cols(op(B))) with op = transpose when asked."""
+    torch = _torch()
+    _need(A, torch.float32, "A")
+    _need(B, torch.float32, "B")
+    M, K = (A.shape[1], A.shape[0]) if transA else A.shape
+    K2, N = (B.shape[1], B.shape[0]) if transB else B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    lib = load()
+    C = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=A.device)
+    wp, wn = _ws(workspace, lib.bsgemm_i8_workspace_size(M, N, K))
+    _check(lib.bsgemm_i8_ex(_ptr(A), A.shape[1], int(bool(transA)), _ptr(B), B.shape[1],
+                            int(bool(transB)), M, N, K, int(bool(relu)), _ptr(C), N, wp, wn,
+                            _ptr(dstatus), _stream_ptr(stream)), "bsgemm_i8_ex")
+    return C
+
+
+def launch_count() -> int:
+    """Kernels the library has launched in this process."""
+    return int(load().bsg_launch_count())
+
+
+def bsgemm_i8_quantize(A, B, workspace, transA: bool = False, transB: bool = False,
+                       stream=None, dstatus=None):
+    """Step 1 into `workspace` (a Workspace); returns (M, N, K)."""
+    torch = _torch()
+    _need(A, torch.float32, "A")
+    _need(B, torch.float32, "B")
+    M, K = (A.shape[1], A.shape[0]) if transA else A.shape
+    K2, N = (B.shape[1], B.shape[0]) if transB else B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    lib = load()
+    wp, wn = workspace.ptr_size(lib.bsgemm_i8_workspace_size(M, N, K))
+    _check(lib.bsgemm_i8_quantize(_ptr(A), A.shape[1], int(bool(transA)), _ptr(B), B.shape[1],
+                                  int(bool(transB)), M, N, K, wp, wn, _ptr(dstatus),
+                                  _stream_ptr(stream)), "bsgemm_i8_quantize")
+    return M, N, K
+
+
+def bsgemm_i8_contract(M, N, K, C, workspace, relu: bool = False, stream=None, dstatus=None):
+    """Steps 2-3 from `workspace` into the M x N float32 tensor C."""
+    lib = load()
+    wp, wn = workspace.ptr_size(lib.bsgemm_i8_workspace_size(M, N, K))
+    _check(lib.bsgemm_i8_contract(M, N, K, int(bool(relu)), _ptr(C), C.shape[1], wp, wn,
+                                  _ptr(dstatus), _stream_ptr(stream)), "bsgemm_i8_contract")
+    return C
+
+
+def bsgemm_i8_host(A, B, relu: bool = False, out=None, stream=None, workspace=None):
+    """The unit on HOST float32 tensors (pinned for asynchronous copies);
+    returns (C on the host, device status bits).  Synchronizes the stream."""
+    torch = _torch()
+    for name, t in (("A", A), ("B", B)):
+        if t.dtype != torch.float32 or t.is_cuda or t.dim() != 2 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous 2-D float32 host tensor")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    lib = load()
+    C = out if out is not None else torch.empty((M, N), dtype=torch.float32, pin_memory=True)
+    wp, wn = _ws(workspace, lib.bsgemm_i8_host_workspace_size(M, N, K))
+    st = ctypes.c_int32(0)
+    _check(lib.bsgemm_i8_host(_ptr(A), _ptr(B), M, N, K, int(bool(relu)), _ptr(C), wp, wn,
+                              ctypes.byref(st), _stream_ptr(stream)), "bsgemm_i8_host")
+    return C, st.value
+
+
+def hash_f32(C, stream=None, workspace=None) -> bytes:
+    """32-byte tree hash of a float32 matrix's bytes (synchronizes)."""
+    torch = _torch()
+    _need(C, torch.float32, "C")
+    M, N = C.shape
+    lib = load()
+    out = torch.empty(32, dtype=torch.uint8, device=C.device)
+    wp, wn = _ws(workspace, lib.bsg_hash_f32_workspace_size(M, N))
+    _check(lib.bsg_hash_f32(_ptr(C), M, N, N, _ptr(out), wp, wn, _stream_ptr(stream)),
+           "bsg_hash_f32")
+    return bytes(out.cpu().tolist())
+
+
+def probe_hash_async(seed: int, M: int = 1024, N: int = 1024, K: int = 1024, out=None,
+                     stream=None, dstatus=None, workspace=None):
+    """The probe hash into a 32-byte device tensor (asynchronous)."""
+    torch = _torch()
+    lib = load()
+    out = out if out is not None else torch.empty(32, dtype=torch.uint8, device="cuda")
+    wp, wn = _ws(workspace, lib.bsg_probe_workspace_size(M, N, K))
+    _check(lib.bsg_probe_hash_async(ctypes.c_uint64(seed), M, N, K, _ptr(out), wp, wn,
+                                    _ptr(dstatus), _stream_ptr(stream)), "bsg_probe_hash_async")
+    return out
+
+
+def probe_hash(seed: int, M: int = 1024, N: int = 1024, K: int = 1024, stream=None,
+               workspace=None) -> bytes:
+    """The probe hash as 32 host bytes (synchronizes)."""
+    lib = load()
+    buf = (ctypes.c_uint8 * 32)()
+    wp, wn = _ws(workspace, lib.bsg_probe_workspace_size(M, N, K))
+    _check(lib.bsg_probe_hash(ctypes.c_uint64(seed), M, N, K, buf, wp, wn, _stream_ptr(stream)),
+           "bsg_probe_hash")
+    return bytes(buf)

@@ -1,0 +1,76 @@
+// bsg_internal.h -- launchers shared by the library's translation units.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace bsg {
+
+// Output encodings of the quantize kernels.
+enum QuantOut : int {
+    kOutInt8 = 0,        // int8, same layout as the input
+    kOutHalfKMajor = 1,  // f16-encoded int8 in the GEMM's K-major operand layout
+};
+
+// GEMM tile: 128 x 256 output per CTA, K in blocks of 64.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+// fp32 accumulation of int8 x int8 products stays exact while every partial
+// sum stays below 2^24: 1024 * 127 * 127 = 16,516,096 < 16,777,216.
+constexpr int kChunkK = 1024;
+
+inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// Padded row length (elements) of the f16 operand arrays: a whole number of
+// K-blocks, so the quantize kernels can write full 64-wide blocks.
+inline int64_t operand_ld(int64_t K) { return round_up(K, kBK); }
+
+// Column absmax is reduced in `nsplit` slices of rows.
+int colmax_nsplit(int64_t rows);
+size_t colmax_partial_bytes(int64_t rows, int64_t cols);
+
+int device_sm_count();
+
+// Host-side count of kernel launches made by this library.
+void count_launches(int n);
+
+cudaError_t launch_quantize_rows(const float *X, int64_t rows, int64_t cols, int64_t ldx,
+                                 int out_kind, void *Q, int64_t ldq, float *scale, float *inv,
+                                 int32_t *dstatus, cudaStream_t st);
+
+// Columns: a partial-max pass over row slices, then a quantize pass.
+// kOutInt8 keeps X's layout (Q is rows x cols); kOutHalfKMajor writes the
+// transpose (Q is cols x ldq, each row a column of X).
+cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int64_t ldx,
+                                 int out_kind, void *Q, int64_t ldq, float *scale, float *inv,
+                                 uint32_t *partial, int32_t *dstatus, cudaStream_t st);
+
+// int8 -> f16 operand conversions for the integer-only entry point.
+cudaError_t launch_i8_rows_to_half(const int8_t *Q, int64_t rows, int64_t cols, int64_t ldq,
+                                   __half *out, int64_t ldo, cudaStream_t st);
+cudaError_t launch_i8_cols_to_half(const int8_t *Q, int64_t rows, int64_t cols, int64_t ldq,
+                                   __half *out, int64_t ldo, cudaStream_t st);
+
+// The tensor-core GEMM.  Aop: M x ldk f16, Bop: N x ldk f16 (both K-major,
+// ldk = operand_ld(K)).  mode 0: C = epi(S, sa, sb) (+ReLU) as float;
+// mode 1: S stored as int32.  sa / sb must hold round_up(M, kBM) /
+// round_up(N, kBN) floats (mode 0).
+cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int64_t N,
+                           int64_t K, const float *sa, const float *sb, int relu, int mode,
+                           void *out, int64_t ldo, int32_t *dstatus, cudaStream_t st);
+
+cudaError_t launch_epilogue(const int32_t *S, int64_t lds, const float *sa, const float *sb,
+                            int64_t M, int64_t N, int relu, float *C, int64_t ldc,
+                            cudaStream_t st);
+
+cudaError_t launch_probe_fill(uint64_t seed, int64_t M, int64_t N, int64_t K, float *A,
+                              float *B, cudaStream_t st);
+
+size_t hash_workspace_bytes(int64_t M, int64_t N);
+cudaError_t launch_hash_f32(const float *C, int64_t M, int64_t N, int64_t ldc, uint8_t *out32,
+                            void *ws, cudaStream_t st);
+
+}  // namespace bsg

@@ -1,0 +1,417 @@
+// bsgemm_api.cu -- the C ABI: argument checks, workspace layout, launches.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "bsg_internal.h"
+#include "bsgemm.h"
+
+namespace bsg {
+
+static std::atomic<unsigned long long> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+int device_sm_count() {
+    static int count[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (count[dev] == 0) {
+        int c = 0;
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0)
+            c = 148;
+        count[dev] = c;
+    }
+    return count[dev];
+}
+
+namespace {
+
+// The kernels are built for sm_103a only.
+bsg_status check_device() {
+    static int ok[64] = {0};  // 0 unknown, 1 yes, 2 no
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BSG_ERR_CUDA;
+    if (ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return BSG_ERR_CUDA;
+        ok[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    }
+    return ok[dev] == 1 ? BSG_OK : BSG_ERR_UNSUPPORTED;
+}
+
+bsg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA; }
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace of the whole unit:
+//   Aop  f16 [M][ldk]        (ldk = K rounded up to 64)
+//   Bop  f16 [N][ldk]
+//   sa   f32 [round_up(M, 128)]
+//   sb   f32 [round_up(N, 256)]
+//   partial column maxima (uint32) for the column quantize
+struct UnitLayout {
+    size_t aop, bop, sa, sb, part, total;
+};
+
+UnitLayout unit_layout(int64_t M, int64_t N, int64_t K, int transA, int transB) {
+    UnitLayout L;
+    const int64_t ldk = operand_ld(K);
+    size_t off = 0;
+    L.aop = off;
+    off = align256(off + (size_t)M * ldk * 2);
+    L.bop = off;
+    off = align256(off + (size_t)N * ldk * 2);
+    L.sa = off;
+    off = align256(off + (size_t)round_up(M, kBM) * 4);
+    L.sb = off;
+    off = align256(off + (size_t)round_up(N, kBN) * 4);
+    L.part = off;
+    size_t part = 0;
+    if (transA) part = colmax_partial_bytes(K, M);
+    if (!transB) part = part > colmax_partial_bytes(K, N) ? part : colmax_partial_bytes(K, N);
+    off = align256(off + part);
+    L.total = off;
+    return L;
+}
+
+bool ws_ok(const void *ws, size_t have, size_t need) {
+    return ws != nullptr && (reinterpret_cast<uintptr_t>(ws) % 256) == 0 && have >= need;
+}
+
+bool dims_ok(int64_t M, int64_t N, int64_t K) {
+    return M >= 1 && N >= 1 && K >= 1 && M <= INT32_MAX && N <= INT32_MAX;
+}
+
+template <typename T>
+T *at(void *ws, size_t off) {
+    return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off);
+}
+
+bsg_status check_unit_args(const float *A, int64_t lda, int transA, const float *B, int64_t ldb,
+                           int transB, int64_t M, int64_t N, int64_t K) {
+    if (!A || !B) return BSG_ERR_ARG;
+    if (!dims_ok(M, N, K)) return BSG_ERR_ARG;
+    if (K > BSG_MAX_K) return BSG_ERR_K_TOO_LARGE;
+    if (transA ? lda < M : lda < K) return BSG_ERR_ARG;
+    if (transB ? ldb < K : ldb < N) return BSG_ERR_ARG;
+    return BSG_OK;
+}
+
+// Step 1 into the workspace: op(A) per row, op(B) per column, as f16
+// K-major operands plus scales.
+bsg_status unit_quantize(const float *A, int64_t lda, int transA, const float *B, int64_t ldb,
+                         int transB, int64_t M, int64_t N, int64_t K, void *ws, size_t ws_bytes,
+                         int32_t *dstatus, cudaStream_t st) {
+    bsg_status s = check_unit_args(A, lda, transA, B, ldb, transB, M, N, K);
+    if (s != BSG_OK) return s;
+    const UnitLayout L = unit_layout(M, N, K, transA, transB);
+    if (!ws_ok(ws, ws_bytes, L.total)) return BSG_ERR_WORKSPACE;
+    s = check_device();
+    if (s != BSG_OK) return s;
+    const int64_t ldk = operand_ld(K);
+    __half *aop = at<__half>(ws, L.aop);
+    __half *bop = at<__half>(ws, L.bop);
+    float *sa = at<float>(ws, L.sa);
+    float *sb = at<float>(ws, L.sb);
+    uint32_t *part = at<uint32_t>(ws, L.part);
+    cudaError_t e;
+    // op(A) per row: a row quantize of A, or a column quantize of the stored K x M.
+    if (!transA)
+        e = launch_quantize_rows(A, M, K, lda, kOutHalfKMajor, aop, ldk, sa, nullptr, dstatus, st);
+    else
+        e = launch_quantize_cols(A, K, M, lda, kOutHalfKMajor, aop, ldk, sa, nullptr, part,
+                                 dstatus, st);
+    if (e != cudaSuccess) return BSG_ERR_CUDA;
+    // op(B) per column: a column quantize of B, or a row quantize of the stored N x K.
+    if (!transB)
+        e = launch_quantize_cols(B, K, N, ldb, kOutHalfKMajor, bop, ldk, sb, nullptr, part,
+                                 dstatus, st);
+    else
+        e = launch_quantize_rows(B, N, K, ldb, kOutHalfKMajor, bop, ldk, sb, nullptr, dstatus, st);
+    return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
+}
+
+// Steps 2-3 from the workspace: the tensor-core contraction with the fused
+// epilogue.
+bsg_status unit_contract(int64_t M, int64_t N, int64_t K, int relu, float *C, int64_t ldc,
+                         void *ws, size_t ws_bytes, int32_t *dstatus, cudaStream_t st) {
+    if (!C || !dims_ok(M, N, K) || ldc < N) return BSG_ERR_ARG;
+    if (K > BSG_MAX_K) return BSG_ERR_K_TOO_LARGE;
+    const UnitLayout L = unit_layout(M, N, K, 0, 0);
+    if (!ws_ok(ws, ws_bytes, L.part)) return BSG_ERR_WORKSPACE;
+    bsg_status s = check_device();
+    if (s != BSG_OK) return s;
+    return from_cuda(launch_gemm_tc(at<__half>(ws, L.aop), at<__half>(ws, L.bop), M, N, K,
+                                    at<float>(ws, L.sa), at<float>(ws, L.sb), relu, 0, C, ldc,
+                                    dstatus, st));
+}
+
+bsg_status unit(const float *A, int64_t lda, int transA, const float *B, int64_t ldb,
+                int transB, int64_t M, int64_t N, int64_t K, int relu, float *C, int64_t ldc,
+                void *ws, size_t ws_bytes, int32_t *dstatus, cudaStream_t st) {
+    if (!C || ldc < N) return BSG_ERR_ARG;
+    bsg_status s = unit_quantize(A, lda, transA, B, ldb, transB, M, N, K, ws, ws_bytes, dstatus, st);
+    if (s != BSG_OK) return s;
+    return unit_contract(M, N, K, relu, C, ldc, ws, ws_bytes, dstatus, st);
+}
+
+}  // namespace
+}  // namespace bsg
+
+using namespace bsg;
+
+extern "C" {
+
+const char *bsg_status_str(bsg_status s) {
+    switch (s) {
+        case BSG_OK: return "BSG_OK";
+        case BSG_ERR_ARG: return "BSG_ERR_ARG: invalid argument";
+        case BSG_ERR_K_TOO_LARGE: return "BSG_ERR_K_TOO_LARGE: K > 133144 can overflow int32";
+        case BSG_ERR_WORKSPACE: return "BSG_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case BSG_ERR_CUDA: return "BSG_ERR_CUDA: a CUDA call failed";
+        case BSG_ERR_NONFINITE: return "BSG_ERR_NONFINITE: non-finite input";
+        case BSG_ERR_TIMEOUT: return "BSG_ERR_TIMEOUT: a bounded device wait expired";
+        case BSG_ERR_UNSUPPORTED: return "BSG_ERR_UNSUPPORTED: device is not sm_103";
+    }
+    return "unknown bsg_status";
+}
+
+int bsg_version(void) { return 100; }
+
+bsg_status bsg_quantize_rows(const float *X, int64_t rows, int64_t cols, int64_t ldx, int8_t *Q,
+                             int64_t ldq, float *scale, float *inv, int32_t *dstatus,
+                             void *stream) {
+    if (!X || !Q || !scale || rows < 1 || cols < 1 || ldx < cols || ldq < cols) return BSG_ERR_ARG;
+    bsg_status s = check_device();
+    if (s != BSG_OK) return s;
+    return from_cuda(launch_quantize_rows(X, rows, cols, ldx, kOutInt8, Q, ldq, scale, inv,
+                                          dstatus, static_cast<cudaStream_t>(stream)));
+}
+
+size_t bsg_quantize_cols_workspace_size(int64_t rows, int64_t cols) {
+    if (rows < 1 || cols < 1) return 0;
+    return align256(colmax_partial_bytes(rows, cols));
+}
+
+bsg_status bsg_quantize_cols(const float *X, int64_t rows, int64_t cols, int64_t ldx, int8_t *Q,
+                             int64_t ldq, float *scale, float *inv, void *workspace,
+                             size_t ws_bytes, int32_t *dstatus, void *stream) {
+    if (!X || !Q || !scale || rows < 1 || cols < 1 || ldx < cols || ldq < cols) return BSG_ERR_ARG;
+    if (!ws_ok(workspace, ws_bytes, bsg_quantize_cols_workspace_size(rows, cols)))
+        return BSG_ERR_WORKSPACE;
+    bsg_status s = check_device();
+    if (s != BSG_OK) return s;
+    return from_cuda(launch_quantize_cols(X, rows, cols, ldx, kOutInt8, Q, ldq, scale, inv,
+                                          static_cast<uint32_t *>(workspace), dstatus,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+size_t bsg_gemm_s32_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (!dims_ok(M, N, K)) return 0;
+    const int64_t ldk = operand_ld(K);
+    return align256((size_t)M * ldk * 2) + align256((size_t)N * ldk * 2);
+}
+
+bsg_status bsg_gemm_s32(const int8_t *Aq, int64_t lda, const int8_t *Bq, int64_t ldb, int64_t M,
+                        int64_t N, int64_t K, int32_t *S, int64_t lds, void *workspace,
+                        size_t ws_bytes, int32_t *dstatus, void *stream) {
+    if (!Aq || !Bq || !S || !dims_ok(M, N, K) || lda < K || ldb < N || lds < N) return BSG_ERR_ARG;
+    if (K > BSG_MAX_K) return BSG_ERR_K_TOO_LARGE;
+    if (!ws_ok(workspace, ws_bytes, bsg_gemm_s32_workspace_size(M, N, K))) return BSG_ERR_WORKSPACE;
+    bsg_status s = check_device();
+    if (s != BSG_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t ldk = operand_ld(K);
+    __half *aop = static_cast<__half *>(workspace);
+    __half *bop = at<__half>(workspace, align256((size_t)M * ldk * 2));
+    if (launch_i8_rows_to_half(Aq, M, K, lda, aop, ldk, st) != cudaSuccess) return BSG_ERR_CUDA;
+    if (launch_i8_cols_to_half(Bq, K, N, ldb, bop, ldk, st) != cudaSuccess) return BSG_ERR_CUDA;
+    return from_cuda(launch_gemm_tc(aop, bop, M, N, K, nullptr, nullptr, 0, 1, S, lds, dstatus, st));
+}
+
+bsg_status bsg_epilogue(const int32_t *S, int64_t lds, const float *sa, const float *sb,
+                        int64_t M, int64_t N, int relu, float *C, int64_t ldc, void *stream) {
+    if (!S || !sa || !sb || !C || M < 1 || N < 1 || lds < N || ldc < N) return BSG_ERR_ARG;
+    bsg_status s = check_device();
+    if (s != BSG_OK) return s;
+    return from_cuda(
+        launch_epilogue(S, lds, sa, sb, M, N, relu, C, ldc, static_cast<cudaStream_t>(stream)));
+}
+
+size_t bsgemm_i8_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (!dims_ok(M, N, K)) return 0;
+    // large enough for every transpose combination
+    const size_t a = unit_layout(M, N, K, 0, 0).total;
+    const size_t b = unit_layout(M, N, K, 1, 0).total;
+    return a > b ? a : b;
+}
+
+bsg_status bsgemm_i8(const float *A, const float *B, int64_t M, int64_t N, int64_t K, int relu,
+                     float *C, void *workspace, size_t ws_bytes, int32_t *dstatus,
+                     void *stream) {
+    return unit(A, K, 0, B, N, 0, M, N, K, relu, C, N, workspace, ws_bytes, dstatus,
+                static_cast<cudaStream_t>(stream));
+}
+
+bsg_status bsgemm_i8_ex(const float *A, int64_t lda, int transA, const float *B, int64_t ldb,
+                        int transB, int64_t M, int64_t N, int64_t K, int relu, float *C,
+                        int64_t ldc, void *workspace, size_t ws_bytes, int32_t *dstatus,
+                        void *stream) {
+    if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return BSG_ERR_ARG;
+    return unit(A, lda, transA, B, ldb, transB, M, N, K, relu, C, ldc, workspace, ws_bytes,
+                dstatus, static_cast<cudaStream_t>(stream));
+}
+
+bsg_status bsgemm_i8_quantize(const float *A, int64_t lda, int transA, const float *B,
+                              int64_t ldb, int transB, int64_t M, int64_t N, int64_t K,
+                              void *workspace, size_t ws_bytes, int32_t *dstatus, void *stream) {
+    if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return BSG_ERR_ARG;
+    return unit_quantize(A, lda, transA, B, ldb, transB, M, N, K, workspace, ws_bytes, dstatus,
+                         static_cast<cudaStream_t>(stream));
+}
+
+bsg_status bsgemm_i8_contract(int64_t M, int64_t N, int64_t K, int relu, float *C, int64_t ldc,
+                              void *workspace, size_t ws_bytes, int32_t *dstatus, void *stream) {
+    return unit_contract(M, N, K, relu, C, ldc, workspace, ws_bytes, dstatus,
+                         static_cast<cudaStream_t>(stream));
+}
+
+uint64_t bsg_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+// Host-buffer form: device copies of A, B, C and a status word sit in front
+// of the unit's own workspace.
+static size_t host_prefix(int64_t M, int64_t N, int64_t K) {
+    return align256((size_t)M * K * 4) + align256((size_t)K * N * 4) +
+           align256((size_t)M * N * 4) + 256;
+}
+
+size_t bsgemm_i8_host_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (!dims_ok(M, N, K)) return 0;
+    return host_prefix(M, N, K) + bsgemm_i8_workspace_size(M, N, K);
+}
+
+bsg_status bsgemm_i8_host(const float *A_host, const float *B_host, int64_t M, int64_t N,
+                          int64_t K, int relu, float *C_host, void *workspace, size_t ws_bytes,
+                          int32_t *dstatus_host, void *stream) {
+    if (!A_host || !B_host || !C_host || !dims_ok(M, N, K)) return BSG_ERR_ARG;
+    if (K > BSG_MAX_K) return BSG_ERR_K_TOO_LARGE;
+    if (!ws_ok(workspace, ws_bytes, bsgemm_i8_host_workspace_size(M, N, K)))
+        return BSG_ERR_WORKSPACE;
+    bsg_status s = check_device();
+    if (s != BSG_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    size_t off = 0;
+    float *dA = at<float>(workspace, off);
+    off += align256((size_t)M * K * 4);
+    float *dB = at<float>(workspace, off);
+    off += align256((size_t)K * N * 4);
+    float *dC = at<float>(workspace, off);
+    off += align256((size_t)M * N * 4);
+    int32_t *dstat = at<int32_t>(workspace, off);
+    off += 256;
+    void *uws = at<void>(workspace, off);
+    if (cudaMemsetAsync(dstat, 0, sizeof(int32_t), st) != cudaSuccess) return BSG_ERR_CUDA;
+    if (cudaMemcpyAsync(dA, A_host, (size_t)M * K * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(dB, B_host, (size_t)K * N * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    s = unit(dA, K, 0, dB, N, 0, M, N, K, relu, dC, N, uws, ws_bytes - off, dstat, st);
+    if (s != BSG_OK) return s;
+    int32_t hstat = 0;
+    if (cudaMemcpyAsync(C_host, dC, (size_t)M * N * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyAsync(&hstat, dstat, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return BSG_ERR_CUDA;
+    if (dstatus_host) *dstatus_host = hstat;
+    return BSG_OK;
+}
+
+size_t bsg_hash_f32_workspace_size(int64_t M, int64_t N) {
+    if (M < 0 || N < 0) return 0;
+    return hash_workspace_bytes(M, N);
+}
+
+bsg_status bsg_hash_f32(const float *C, int64_t M, int64_t N, int64_t ldc, uint8_t *out32,
+                        void *workspace, size_t ws_bytes, void *stream) {
+    if (!out32 || M < 0 || N < 0 || ldc < N || (M * N > 0 && !C)) return BSG_ERR_ARG;
+    if (!ws_ok(workspace, ws_bytes, bsg_hash_f32_workspace_size(M, N))) return BSG_ERR_WORKSPACE;
+    bsg_status s = check_device();
+    if (s != BSG_OK) return s;
+    return from_cuda(launch_hash_f32(C, M, N, ldc, out32, workspace,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+// Probe workspace: A (M x K), B (K x N), C (M x N) floats, the unit's
+// workspace, the hash workspace, and a status word.
+static size_t probe_parts(int64_t M, int64_t N, int64_t K, size_t *offs) {
+    size_t off = 0;
+    offs[0] = off;  // A
+    off += align256((size_t)M * K * 4);
+    offs[1] = off;  // B
+    off += align256((size_t)K * N * 4);
+    offs[2] = off;  // C
+    off += align256((size_t)M * N * 4);
+    offs[3] = off;  // unit workspace
+    off += align256(bsgemm_i8_workspace_size(M, N, K));
+    offs[4] = off;  // hash workspace
+    off += align256(hash_workspace_bytes(M, N));
+    offs[5] = off;  // status word + device digest
+    off += 256;
+    return off;
+}
+
+size_t bsg_probe_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (!dims_ok(M, N, K)) return 0;
+    size_t offs[6];
+    return probe_parts(M, N, K, offs);
+}
+
+bsg_status bsg_probe_hash_async(uint64_t seed, int64_t M, int64_t N, int64_t K, uint8_t *out32,
+                                void *workspace, size_t ws_bytes, int32_t *dstatus,
+                                void *stream) {
+    if (!out32 || !dims_ok(M, N, K)) return BSG_ERR_ARG;
+    if (K > BSG_MAX_K) return BSG_ERR_K_TOO_LARGE;
+    size_t offs[6];
+    const size_t need = probe_parts(M, N, K, offs);
+    if (!ws_ok(workspace, ws_bytes, need)) return BSG_ERR_WORKSPACE;
+    bsg_status s = check_device();
+    if (s != BSG_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float *A = at<float>(workspace, offs[0]);
+    float *B = at<float>(workspace, offs[1]);
+    float *C = at<float>(workspace, offs[2]);
+    if (launch_probe_fill(seed, M, N, K, A, B, st) != cudaSuccess) return BSG_ERR_CUDA;
+    s = unit(A, K, 0, B, N, 0, M, N, K, 0, C, N, at<void>(workspace, offs[3]),
+             offs[4] - offs[3], dstatus, st);
+    if (s != BSG_OK) return s;
+    return from_cuda(launch_hash_f32(C, M, N, N, out32, at<void>(workspace, offs[4]), st));
+}
+
+bsg_status bsg_probe_hash(uint64_t seed, int64_t M, int64_t N, int64_t K, uint8_t *out32_host,
+                          void *workspace, size_t ws_bytes, void *stream) {
+    if (!out32_host || !dims_ok(M, N, K)) return BSG_ERR_ARG;
+    size_t offs[6];
+    const size_t need = probe_parts(M, N, K, offs);
+    if (!ws_ok(workspace, ws_bytes, need)) return BSG_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t *dstat = at<int32_t>(workspace, offs[5]);
+    uint8_t *ddig = at<uint8_t>(workspace, offs[5] + 64);
+    if (cudaMemsetAsync(dstat, 0, sizeof(int32_t), st) != cudaSuccess) return BSG_ERR_CUDA;
+    bsg_status s = bsg_probe_hash_async(seed, M, N, K, ddig, workspace, ws_bytes, dstat, stream);
+    if (s != BSG_OK) return s;
+    int32_t hstat = 0;
+    if (cudaMemcpyAsync(out32_host, ddig, 32, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyAsync(&hstat, dstat, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return BSG_ERR_CUDA;
+    if (hstat & BSG_DSTATUS_TIMEOUT) return BSG_ERR_TIMEOUT;
+    if (hstat & BSG_DSTATUS_NONFINITE) return BSG_ERR_NONFINITE;
+    return BSG_OK;
+}
+
+}  // extern "C"
