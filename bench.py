@@ -86,7 +86,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -166,66 +166,106 @@ def run_gpu(args, rank, world, local_rank):
     host_ws = bsg.Workspace(dev)
     host_ws.get(max(lib.bsgemm_i8_host_workspace_size(L["M"], L["N"], L["K"]) for L in lin))
 
-    def step(ev=None):
-        """One step; ev: list of (start, end) event pairs to fill per stage."""
-        k = 0
-        for L in lin:
-            if ev is not None:
-                ev[k][0].record(stream)
-            bsg.bsgemm_i8_quantize(L["A"], L["B"], L["ws"], dstatus=dstatus)
-            if ev is not None:
-                ev[k][1].record(stream)
-                ev[k + 1][0].record(stream)
-            bsg.bsgemm_i8_contract(L["M"], L["N"], L["K"], L["C"], L["ws"], relu=L["relu"],
-                                   dstatus=dstatus)
-            if ev is not None:
-                ev[k + 1][1].record(stream)
-            k += 2
-        if ev is not None:
-            ev[k][0].record(stream)
-        bsg.probe_hash_async(PROBE_SEED, *PROBE, out=probe_out, dstatus=dstatus, workspace=pws)
-        if ev is not None:
-            ev[k][1].record(stream)
+    side = torch.cuda.Stream(device=dev)
 
-    n_stage = 2 * len(lin) + 1
+    def stage_quantize(L):
+        bsg.bsgemm_i8_quantize(L["A"], L["B"], L["ws"], dstatus=dstatus)
+
+    def stage_contract(L):
+        bsg.bsgemm_i8_contract(L["M"], L["N"], L["K"], L["C"], L["ws"], relu=L["relu"],
+                               dstatus=dstatus)
+
+    def stage_probe():
+        bsg.probe_hash_async(PROBE_SEED, *PROBE, out=probe_out, dstatus=dstatus, workspace=pws)
+
+    def step_body():
+        """One step on the current stream; the probe runs on a side stream
+        forked from it and joined at the end, so it overlaps the linears."""
+        cur = torch.cuda.current_stream()
+        if args.probe_overlap:
+            side.wait_stream(cur)
+            with torch.cuda.stream(side):
+                stage_probe()
+        for L in lin:
+            stage_quantize(L)
+            stage_contract(L)
+        if args.probe_overlap:
+            cur.wait_stream(side)
+        else:
+            stage_probe()
+
+    stages = []
+    for L in lin:
+        stages.append(("quantize_" + L["name"], (lambda L=L: stage_quantize(L))))
+        stages.append(("gemm_" + L["name"], (lambda L=L: stage_contract(L))))
+    stages.append(("probe", stage_probe))
 
     def barrier():
         if world > 1:
             dist.barrier()
 
+    # warm up eagerly (first calls set kernel attributes), then capture graphs
     for _ in range(args.warmup):
-        step()
+        step_body()
+    torch.cuda.synchronize()
+    capture = torch.cuda.Stream(device=dev)
+    n0 = bsg.launch_count()
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=capture):
+        step_body()
+    launches_step = bsg.launch_count() - n0
+    g_stages = []
+    launches_stages = 0
+    for name, fn in stages:
+        g = torch.cuda.CUDAGraph()
+        n0 = bsg.launch_count()
+        with torch.cuda.graph(g, stream=capture):
+            fn()
+        launches_stages += bsg.launch_count() - n0
+        g_stages.append((name, g))
+    for _ in range(args.warmup):
+        g_step.replay()
+        for _, g in g_stages:
+            g.replay()
     torch.cuda.synchronize()
 
-    # ---- timed region: device-resident inputs
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(n_stage)] for _ in range(args.steps)]
+    # ---- timed region: device-resident inputs, L2 flushed between steps
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(g_stages) + 1)]
+           for _ in range(args.steps)]
     clocks = ClockSampler(gpu_selector(local_rank))
     clocks.start()
     time.sleep(0.3)
-    launches0 = bsg.launch_count()
     barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for s in range(args.steps):
-        flush.zero_()                      # L2 flush, outside the event pairs
-        step(evs[s])
+        flush.zero_()                      # L2 flush, outside the timed pair
+        ev_step[s][0].record(stream)
+        g_step.replay()
+        ev_step[s][1].record(stream)
+    for s in range(args.steps):
+        flush.zero_()
+        evs[s][0].record(stream)
+        for k, (_, g) in enumerate(g_stages):
+            g.replay()
+            evs[s][k + 1].record(stream)
     torch.cuda.synchronize()
     barrier()
     wall = time.perf_counter() - wall0
-    launches = bsg.launch_count() - launches0
+    launches = (launches_step + launches_stages) * args.steps
     clk = clocks.stop()
 
-    stage_ms = [[a.elapsed_time(b) for a, b in ev] for ev in evs]
-    step_ms = [sum(x) for x in stage_ms]
-    ms_per_step = statistics.mean(step_ms)
+    step_ms_list = [a.elapsed_time(b) for a, b in ev_step]
+    stage_ms = [[ev[k].elapsed_time(ev[k + 1]) for k in range(len(g_stages))] for ev in evs]
+    ms_per_step = statistics.mean(step_ms_list)
+    probe_hex = bytes(probe_out.cpu().tolist()).hex()
     # ---- end-to-end through the host-buffer entry point (copies inside)
     def e2e_step():
         for L in lin:
             bsg.bsgemm_i8_host(L["Ah"], L["Bh"], relu=L["relu"], out=L["Ch"], workspace=host_ws)
-        probe_out.zero_()
-        h = bsg.probe_hash(PROBE_SEED, *PROBE, workspace=pws)
-        return h
+        return bsg.probe_hash(PROBE_SEED, *PROBE, workspace=pws)
 
     for _ in range(max(1, args.warmup // 2)):
         e2e_step()
@@ -248,7 +288,6 @@ def run_gpu(args, rank, world, local_rank):
     ms_max, e2e_max = float(t_local[0]), float(t_local[1])
 
     # ---- probe agreement across replicas (the pages' cross-device check)
-    probe_hex = bytes(probe_out.cpu().tolist()).hex()
     golden = None
     gpath = os.path.join(ROOT, "tests", "golden", "probe_hash.txt")
     if os.path.exists(gpath):
@@ -270,7 +309,8 @@ def run_gpu(args, rank, world, local_rank):
 
     ops = step_ops()
     peaks, peak_kind = load_peaks()
-    # dominant kernel: the tensor-core contraction (one launch per linear)
+    # dominant kernel: the tensor-core contraction (one launch per linear),
+    # timed per stage graph in the second half of the timed region
     gemm_ms = [statistics.mean(sm[2 * i + 1] for sm in stage_ms) for i in range(len(lin))]
     quant_ms = [statistics.mean(sm[2 * i] for sm in stage_ms) for i in range(len(lin))]
     probe_ms = statistics.mean(sm[-1] for sm in stage_ms)
@@ -327,6 +367,11 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clk,
         "gpu_launches": launches,
         "wall_s_timed": round(wall, 4),
+        "timing": ("value/ms_per_step: the whole step replayed as one CUDA graph, CUDA events "
+                   "around each replay; roofline/quantize/probe: the same stages replayed as "
+                   "separate graphs with events between them, in the same timed region"),
+        "probe_overlap": bool(args.probe_overlap),
+        "stage_sum_ms": round(statistics.mean(sum(x) for x in stage_ms), 4),
         "probe_hash": probe_hex,
         "probe_hash_matches_golden": (golden == probe_hex) if golden else None,
         "replicas_agree": replicas_agree,
@@ -405,10 +450,12 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--probe-overlap", type=int, default=1,
+                    help="1: the probe runs on a side stream alongside the linears")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

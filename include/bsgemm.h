@@ -20,7 +20,7 @@
  * Readings of points the page leaves open (the floor is applied to the f64
  * quotient; inv is the reciprocal of the stored f32 scale; the quantize uses
  * two f32 roundings; ReLU maps -0 and NaN to +0; the probe's inputs come
- * from SplitMix64 and its hash is a 4-ary SHA-256 tree over 256-byte leaves)
+ * from SplitMix64 and its hash is a BLAKE2s tree over 256-byte leaves)
  * are stated per entry point below.
  *
  * Conventions for every entry point:
@@ -147,6 +147,24 @@ bsg_status bsgemm_i8_quantize(const float *A, int64_t lda, int transA, const flo
 bsg_status bsgemm_i8_contract(int64_t M, int64_t N, int64_t K, int relu, float *C, int64_t ldc,
                               void *workspace, size_t ws_bytes, int32_t *dstatus, void *stream);
 
+/* Self-test of the scale derivation on the current device.  The kernels
+ * derive scale and inv with IEEE f32 divides, which equal the f64 definition
+ * for every input (the double rounding can never meet an f32 midpoint);
+ * this call checks that claim for every absmax bit pattern in
+ * [first_bits, last_bits] against the device's own f64 divide and stores
+ * the number of mismatches in *mismatches_host.  Synchronous (default
+ * stream); allocates 8 bytes of device memory.  In the spirit of the init
+ * gates of "Layer 1: exact init gates". */
+bsg_status bsg_selftest_scales(uint32_t first_bits, uint32_t last_bits,
+                               uint64_t *mismatches_host);
+
+/* The output tile width (64, 128 or 256 columns; tiles are 128 rows) the
+ * GEMM kernel uses for an M x N problem on `sms` SMs: the width with the
+ * fewest idle SMs in the last wave, weighted by the narrower tiles' lower
+ * MMA efficiency.  Host-only; -1 on bad arguments.  No counterpart in the
+ * pages: it documents this library's schedule. */
+int bsg_gemm_tile_width(int64_t M, int64_t N, int sms);
+
 /* Number of kernels this library has launched in this process (host-side
  * counter; every launch of every entry point counts). */
 uint64_t bsg_launch_count(void);
@@ -164,13 +182,16 @@ bsg_status bsgemm_i8_host(const float *A_host, const float *B_host, int64_t M, i
 /* ---- the probe --------------------------------------------------------------------- */
 
 /* 32-byte hash of an M x N float matrix (leading dimension ldc >= N): the
- * matrix's little-endian bytes, row after row with no padding, cut into
- * 256-byte leaves (the last may be shorter); leaf digest SHA-256(0x00 ||
- * leaf); then, level by level, digests taken four at a time in order (the
- * last group may be shorter) give SHA-256(0x01 || d1 || ...) until one
- * digest remains.  SHA-256 is FIPS 180-4.  out32: 32 bytes of DEVICE memory.
- * `workspace`: bsg_hash_f32_workspace_size(M, N) bytes.  Page: "Layer 3: the
- * kernel probe" (the page names no hash function; this tree is our reading). */
+ * matrix's little-endian bytes, row after row with no padding, hashed as a
+ * BLAKE2s-256 tree (RFC 7693; BLAKE2 tree mode with fanout 4, unlimited
+ * depth, leaf length 256, inner length 32): leaf i (256 bytes, the last may
+ * be shorter) at node offset i, depth 0; then, level by level, groups of
+ * four digests concatenated and hashed at node offset = group index, node
+ * depth = level; the last node of each level carries the last-node flag;
+ * the hash is the single digest of the first level that has one.
+ * out32: 32 bytes of DEVICE memory.  `workspace`: bsg_hash_f32_workspace_size
+ * (M, N) bytes.  Page: "Layer 3: the kernel probe" (the page names no hash
+ * function; this tree is our reading). */
 size_t bsg_hash_f32_workspace_size(int64_t M, int64_t N);
 bsg_status bsg_hash_f32(const float *C, int64_t M, int64_t N, int64_t ldc, uint8_t *out32,
                         void *workspace, size_t ws_bytes, void *stream);

@@ -17,7 +17,8 @@ than itself) live in ``tests/``.  Parity status per function:
 * integer contraction: pinned by big-integer brute force and the unit-scale
   absolute.
 * epilogue and ReLU: pinned by the exact-rational referee.
-* SHA-256 / tree hash: pinned by FIPS 180-4 vectors and Python's hashlib.
+* BLAKE2s / tree hash: pinned by the RFC 7693 test vector and Python's
+  hashlib.blake2s (which implements the tree parameters).
 * SplitMix64 probe inputs: pinned by the generator's published outputs.
 * probe hash as a whole: "parity unpinned" against the pages' system (the
   pages give neither the probe's inputs nor its hash function).
@@ -79,6 +80,7 @@ def _declare(lib):
     lib.orc_num_threads.restype = ctypes.c_int
     lib.orc_scale_from_max.argtypes = [ctypes.c_float, ctypes.POINTER(ctypes.c_float),
                                        ctypes.POINTER(ctypes.c_float)]
+    lib.orc_scales_from_max.argtypes = [_F32P, _i64, _F32P, _F32P]
     lib.orc_quantize_value.argtypes = [ctypes.c_float, ctypes.c_float]
     lib.orc_quantize_value.restype = ctypes.c_int
     lib.orc_quantize_rows.argtypes = [_F32P, _i64, _i64, _i64, _I8P, _i64, _F32P, _F32P]
@@ -93,7 +95,9 @@ def _declare(lib):
                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     lib.orc_bsgemm_cells.argtypes = [_F32P, _F32P, _i64, _i64, _i64, ctypes.c_int, _I64P,
                                      _I64P, _i64, _F32P, ctypes.c_void_p]
-    lib.orc_sha256.argtypes = [ctypes.c_char_p, ctypes.c_size_t, _U8P]
+    lib.orc_blake2s.argtypes = [ctypes.c_char_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_int, _U8P]
     lib.orc_tree_hash.argtypes = [ctypes.c_char_p, ctypes.c_size_t, _U8P]
     lib.orc_hash_f32.argtypes = [_F32P, _i64, _i64, _i64, _U8P]
     lib.orc_splitmix64.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
@@ -140,6 +144,13 @@ class Oracle:
         s, i = ctypes.c_float(), ctypes.c_float()
         self.lib.orc_scale_from_max(ctypes.c_float(m), ctypes.byref(s), ctypes.byref(i))
         return s.value, i.value
+
+    def scales_from_max(self, m):
+        m = _c(m, np.float32).reshape(-1)
+        sc = np.zeros(max(len(m), 1), np.float32)
+        iv = np.zeros(max(len(m), 1), np.float32)
+        self.lib.orc_scales_from_max(m if len(m) else np.zeros(1, np.float32), len(m), sc, iv)
+        return sc[:len(m)], iv[:len(m)]
 
     def quantize_value(self, x: float, inv: float) -> int:
         return int(self.lib.orc_quantize_value(ctypes.c_float(x), ctypes.c_float(inv)))
@@ -212,9 +223,11 @@ class Oracle:
         return out[:len(rows)], S[:len(rows)], st
 
     # -- the probe ---------------------------------------------------------
-    def sha256(self, data: bytes) -> bytes:
+    def blake2s(self, data: bytes, fanout=1, depth=1, leaf_size=0, node_offset=0,
+                node_depth=0, inner_size=0, last_node=False) -> bytes:
         out = np.zeros(32, np.uint8)
-        self.lib.orc_sha256(data, len(data), out)
+        self.lib.orc_blake2s(data, len(data), fanout, depth, leaf_size, node_offset, node_depth,
+                             inner_size, int(bool(last_node)), out)
         return out.tobytes()
 
     def tree_hash(self, data: bytes) -> bytes:

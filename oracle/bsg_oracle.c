@@ -34,8 +34,9 @@
  *   R6  probe inputs: SplitMix64 outputs (Steele, Lea, Flood, "Fast
  *       splittable pseudorandom number generators", OOPSLA 2014), A first
  *       then B, each mapped exactly to a float in [-1, 1);
- *   R7  the probe hash is a 4-ary SHA-256 (FIPS 180-4) tree over 256-byte
- *       leaves of C's little-endian bytes, row-major, rows packed.
+ *   R7  the probe hash is a BLAKE2s-256 (RFC 7693) tree in the BLAKE2 tree
+ *       mode -- fanout 4, leaves of 256 bytes of C's little-endian bytes,
+ *       row-major, rows packed.
  */
 #include <math.h>
 #include <stddef.h>
@@ -83,6 +84,11 @@ void orc_scale_from_max(float m, float *scale, float *inv) {
     float sf = (float)s;          /* RN to binary32 */
     *scale = sf;
     *inv = (float)(1.0 / (double)sf); /* R2 */
+}
+
+/* orc_scale_from_max over an array (for exhaustive checks). */
+void orc_scales_from_max(const float *m, int64_t n, float *scale, float *inv) {
+    for (int64_t i = 0; i < n; ++i) orc_scale_from_max(m[i], &scale[i], &inv[i]);
 }
 
 /* [V] "Hardware ground truth": the quantize computes floor(x*inv + 0.5);    */
@@ -254,90 +260,120 @@ int orc_bsgemm_cells(const float *A, const float *B, int64_t M, int64_t N, int64
 }
 
 /* ------------------------------------------------------------------------ */
-/* SHA-256, written from FIPS 180-4 sections 4.1.2, 4.2.2, 5.1.1, 5.3.3 and */
-/* 6.2.2.  Used by the probe hash ([V] "Layer 3: the kernel probe").         */
+/* BLAKE2s-256, written from RFC 7693 (sections 2.1-2.7, 3.1-3.3) with the   */
+/* tree parameters of the BLAKE2 specification (parameter block: digest     */
+/* length, key length, fanout, depth, leaf length, node offset, node depth, */
+/* inner length; "last node" finalization flag).  Used by the probe hash     */
+/* ([V] "Layer 3: the kernel probe").                                        */
 /* ------------------------------------------------------------------------ */
-static const uint32_t SHA_K[64] = {
-    0x428a2f98u, 0x71374491u, 0xb5c0fbcfu, 0xe9b5dba5u, 0x3956c25bu, 0x59f111f1u, 0x923f82a4u,
-    0xab1c5ed5u, 0xd807aa98u, 0x12835b01u, 0x243185beu, 0x550c7dc3u, 0x72be5d74u, 0x80deb1feu,
-    0x9bdc06a7u, 0xc19bf174u, 0xe49b69c1u, 0xefbe4786u, 0x0fc19dc6u, 0x240ca1ccu, 0x2de92c6fu,
-    0x4a7484aau, 0x5cb0a9dcu, 0x76f988dau, 0x983e5152u, 0xa831c66du, 0xb00327c8u, 0xbf597fc7u,
-    0xc6e00bf3u, 0xd5a79147u, 0x06ca6351u, 0x14292967u, 0x27b70a85u, 0x2e1b2138u, 0x4d2c6dfcu,
-    0x53380d13u, 0x650a7354u, 0x766a0abbu, 0x81c2c92eu, 0x92722c85u, 0xa2bfe8a1u, 0xa81a664bu,
-    0xc24b8b70u, 0xc76c51a3u, 0xd192e819u, 0xd6990624u, 0xf40e3585u, 0x106aa070u, 0x19a4c116u,
-    0x1e376c08u, 0x2748774cu, 0x34b0bcb5u, 0x391c0cb3u, 0x4ed8aa4au, 0x5b9cca4fu, 0x682e6ff3u,
-    0x748f82eeu, 0x78a5636fu, 0x84c87814u, 0x8cc70208u, 0x90befffau, 0xa4506cebu, 0xbef9a3f7u,
-    0xc67178f2u};
+static const uint32_t B2S_IV[8] = {0x6A09E667u, 0xBB67AE85u, 0x3C6EF372u, 0xA54FF53Au,
+                                   0x510E527Fu, 0x9B05688Cu, 0x1F83D9ABu, 0x5BE0CD19u};
+
+static const uint8_t B2S_SIGMA[10][16] = {
+    {0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15},
+    {14, 10, 4, 8, 9, 15, 13, 6, 1, 12, 0, 2, 11, 7, 5, 3},
+    {11, 8, 12, 0, 5, 2, 15, 13, 10, 14, 3, 6, 7, 1, 9, 4},
+    {7, 9, 3, 1, 13, 12, 11, 14, 2, 6, 5, 10, 4, 0, 15, 8},
+    {9, 0, 5, 7, 2, 4, 10, 15, 14, 1, 11, 12, 6, 8, 3, 13},
+    {2, 12, 6, 10, 0, 11, 8, 3, 4, 13, 7, 5, 15, 14, 1, 9},
+    {12, 5, 1, 15, 14, 13, 4, 10, 0, 7, 6, 3, 9, 2, 8, 11},
+    {13, 11, 7, 14, 12, 1, 3, 9, 5, 0, 15, 4, 8, 6, 2, 10},
+    {6, 15, 14, 9, 11, 3, 0, 8, 12, 2, 13, 7, 1, 4, 10, 5},
+    {10, 2, 8, 4, 7, 6, 1, 5, 15, 11, 9, 14, 3, 12, 13, 0}};
 
 static uint32_t rotr32(uint32_t x, int n) { return (x >> n) | (x << (32 - n)); }
 
-static void sha256_block(uint32_t H[8], const uint8_t blk[64]) {
-    uint32_t W[64];
-    for (int t = 0; t < 16; ++t)
-        W[t] = ((uint32_t)blk[4 * t] << 24) | ((uint32_t)blk[4 * t + 1] << 16) |
-               ((uint32_t)blk[4 * t + 2] << 8) | (uint32_t)blk[4 * t + 3];
-    for (int t = 16; t < 64; ++t) {
-        uint32_t s0 = rotr32(W[t - 15], 7) ^ rotr32(W[t - 15], 18) ^ (W[t - 15] >> 3);
-        uint32_t s1 = rotr32(W[t - 2], 17) ^ rotr32(W[t - 2], 19) ^ (W[t - 2] >> 10);
-        W[t] = W[t - 16] + s0 + W[t - 7] + s1;
-    }
-    uint32_t a = H[0], b = H[1], c = H[2], d = H[3], e = H[4], f = H[5], g = H[6], h = H[7];
-    for (int t = 0; t < 64; ++t) {
-        uint32_t S1 = rotr32(e, 6) ^ rotr32(e, 11) ^ rotr32(e, 25);
-        uint32_t ch = (e & f) ^ (~e & g);
-        uint32_t T1 = h + S1 + ch + SHA_K[t] + W[t];
-        uint32_t S0 = rotr32(a, 2) ^ rotr32(a, 13) ^ rotr32(a, 22);
-        uint32_t maj = (a & b) ^ (a & c) ^ (b & c);
-        uint32_t T2 = S0 + maj;
-        h = g; g = f; f = e; e = d + T1; d = c; c = b; b = a; a = T1 + T2;
-    }
-    H[0] += a; H[1] += b; H[2] += c; H[3] += d;
-    H[4] += e; H[5] += f; H[6] += g; H[7] += h;
+static uint32_t load_le32(const uint8_t *p) {
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
 }
 
-/* SHA-256 of (prefix byte, if prefix >= 0) followed by msg[0..len). */
-static void sha256_prefixed(int prefix, const uint8_t *msg, size_t len, uint8_t out[32]) {
-    uint32_t H[8] = {0x6a09e667u, 0xbb67ae85u, 0x3c6ef372u, 0xa54ff53au,
-                     0x510e527fu, 0x9b05688cu, 0x1f83d9abu, 0x5be0cd19u};
-    size_t total = len + (prefix >= 0 ? 1 : 0);
-    uint8_t blk[64];
-    size_t fill = 0;
-    if (prefix >= 0) blk[fill++] = (uint8_t)prefix;
-    for (size_t p = 0; p < len; ++p) {
-        blk[fill++] = msg[p];
-        if (fill == 64) { sha256_block(H, blk); fill = 0; }
-    }
-    /* padding: a 1 bit, zeros, then the 64-bit big-endian bit length */
-    blk[fill++] = 0x80;
-    if (fill > 56) {
-        while (fill < 64) blk[fill++] = 0;
-        sha256_block(H, blk);
-        fill = 0;
-    }
-    while (fill < 56) blk[fill++] = 0;
-    uint64_t bits = (uint64_t)total * 8u;
-    for (int i = 7; i >= 0; --i) blk[fill++] = (uint8_t)(bits >> (8 * i));
-    sha256_block(H, blk);
+/* The mixing function G of RFC 7693 section 3.1 (rotations 16, 12, 8, 7). */
+static void b2s_g(uint32_t v[16], int a, int b, int c, int d, uint32_t x, uint32_t y) {
+    v[a] = v[a] + v[b] + x;
+    v[d] = rotr32(v[d] ^ v[a], 16);
+    v[c] = v[c] + v[d];
+    v[b] = rotr32(v[b] ^ v[c], 12);
+    v[a] = v[a] + v[b] + y;
+    v[d] = rotr32(v[d] ^ v[a], 8);
+    v[c] = v[c] + v[d];
+    v[b] = rotr32(v[b] ^ v[c], 7);
+}
+
+/* The compression function F (RFC 7693 section 3.2); t = bytes so far, f0 /
+ * f1 the last-block and last-node flags. */
+static void b2s_compress(uint32_t h[8], const uint8_t block[64], uint64_t t, int last_block,
+                         int last_node) {
+    uint32_t m[16], v[16];
+    for (int i = 0; i < 16; ++i) m[i] = load_le32(block + 4 * i);
     for (int i = 0; i < 8; ++i) {
-        out[4 * i] = (uint8_t)(H[i] >> 24);
-        out[4 * i + 1] = (uint8_t)(H[i] >> 16);
-        out[4 * i + 2] = (uint8_t)(H[i] >> 8);
-        out[4 * i + 3] = (uint8_t)H[i];
+        v[i] = h[i];
+        v[i + 8] = B2S_IV[i];
+    }
+    v[12] ^= (uint32_t)t;
+    v[13] ^= (uint32_t)(t >> 32);
+    if (last_block) v[14] = ~v[14];
+    if (last_block && last_node) v[15] = ~v[15];
+    for (int r = 0; r < 10; ++r) {
+        const uint8_t *s = B2S_SIGMA[r];
+        b2s_g(v, 0, 4, 8, 12, m[s[0]], m[s[1]]);
+        b2s_g(v, 1, 5, 9, 13, m[s[2]], m[s[3]]);
+        b2s_g(v, 2, 6, 10, 14, m[s[4]], m[s[5]]);
+        b2s_g(v, 3, 7, 11, 15, m[s[6]], m[s[7]]);
+        b2s_g(v, 0, 5, 10, 15, m[s[8]], m[s[9]]);
+        b2s_g(v, 1, 6, 11, 12, m[s[10]], m[s[11]]);
+        b2s_g(v, 2, 7, 8, 13, m[s[12]], m[s[13]]);
+        b2s_g(v, 3, 4, 9, 14, m[s[14]], m[s[15]]);
+    }
+    for (int i = 0; i < 8; ++i) h[i] ^= v[i] ^ v[i + 8];
+}
+
+/* BLAKE2s-256 with the given tree parameters (no key, no salt, no
+ * personalization).  Sequential hashing is fanout 1, depth 1, the rest 0. */
+void orc_blake2s(const uint8_t *msg, size_t len, int fanout, int depth, uint32_t leaf_length,
+                 uint64_t node_offset, int node_depth, int inner_length, int last_node,
+                 uint8_t out[32]) {
+    uint32_t h[8];
+    for (int i = 0; i < 8; ++i) h[i] = B2S_IV[i];
+    /* parameter block words 0-3 */
+    h[0] ^= 32u | (0u << 8) | ((uint32_t)fanout << 16) | ((uint32_t)depth << 24);
+    h[1] ^= leaf_length;
+    h[2] ^= (uint32_t)node_offset;
+    h[3] ^= (uint32_t)((node_offset >> 32) & 0xFFFFu) | ((uint32_t)node_depth << 16) |
+            ((uint32_t)inner_length << 24);
+    uint8_t block[64];
+    size_t done = 0;
+    if (len == 0) {
+        memset(block, 0, 64);
+        b2s_compress(h, block, 0, 1, last_node);
+    }
+    while (done < len) {
+        size_t n = len - done < 64 ? len - done : 64;
+        memset(block, 0, 64);
+        memcpy(block, msg + done, n);
+        done += n;
+        b2s_compress(h, block, (uint64_t)done, done == len, last_node);
+    }
+    for (int i = 0; i < 8; ++i) {
+        out[4 * i] = (uint8_t)h[i];
+        out[4 * i + 1] = (uint8_t)(h[i] >> 8);
+        out[4 * i + 2] = (uint8_t)(h[i] >> 16);
+        out[4 * i + 3] = (uint8_t)(h[i] >> 24);
     }
 }
 
-void orc_sha256(const uint8_t *msg, size_t len, uint8_t out[32]) {
-    sha256_prefixed(-1, msg, len, out);
-}
-
-/* Reading R7, the tree hash of a byte string D:                             */
+/* Reading R7, the tree hash of a byte string D, in BLAKE2s tree mode with  */
+/* fanout 4, unlimited depth (255), leaf length 256, inner length 32:        */
 /*   level 0: D cut into 256-byte leaves (the last may be shorter; an empty */
-/*            D is one empty leaf); digest = SHA-256(0x00 || leaf);          */
+/*            D is one empty leaf); leaf i is hashed with node offset i,     */
+/*            node depth 0;                                                  */
 /*   level l+1: level l's digests taken four at a time in order (the last   */
-/*            group may hold 1-3); digest = SHA-256(0x01 || d1 || ... );     */
-/*   the hash is the single digest of the first level that has one.         */
+/*            group may hold 1-3), concatenated and hashed with node offset  */
+/*            = group index, node depth l+1;                                 */
+/*   the last node of every level carries the last-node flag; the hash is   */
+/*   the single digest of the first level that has one.                     */
 #define ORC_LEAF_BYTES 256
 #define ORC_FANIN 4
+#define ORC_DEPTH 255
 void orc_tree_hash(const uint8_t *data, size_t len, uint8_t out[32]) {
     size_t nleaf = len == 0 ? 1 : (len + ORC_LEAF_BYTES - 1) / ORC_LEAF_BYTES;
     uint8_t *cur = (uint8_t *)malloc(32 * nleaf);
@@ -345,16 +381,20 @@ void orc_tree_hash(const uint8_t *data, size_t len, uint8_t out[32]) {
         size_t off = l * ORC_LEAF_BYTES;
         size_t n = len - off < ORC_LEAF_BYTES ? len - off : ORC_LEAF_BYTES;
         if (len == 0) n = 0;
-        sha256_prefixed(0x00, data + off, n, cur + 32 * l);
+        orc_blake2s(data + off, n, ORC_FANIN, ORC_DEPTH, ORC_LEAF_BYTES, (uint64_t)l, 0, 32,
+                    l == nleaf - 1, cur + 32 * l);
     }
     size_t count = nleaf;
+    int depth = 0;
     while (count > 1) {
         size_t next = (count + ORC_FANIN - 1) / ORC_FANIN;
         uint8_t *nxt = (uint8_t *)malloc(32 * next);
+        ++depth;
         for (size_t g = 0; g < next; ++g) {
             size_t first = g * ORC_FANIN;
             size_t m = count - first < ORC_FANIN ? count - first : ORC_FANIN;
-            sha256_prefixed(0x01, cur + 32 * first, 32 * m, nxt + 32 * g);
+            orc_blake2s(cur + 32 * first, 32 * m, ORC_FANIN, ORC_DEPTH, ORC_LEAF_BYTES,
+                        (uint64_t)g, depth, 32, g == next - 1, nxt + 32 * g);
         }
         free(cur);
         cur = nxt;

@@ -224,3 +224,28 @@ def test_ragged_sampled_and_adversarial(orc):
     assert_bits_equal(C[rows, cols], out, "ragged cells")
     o, _, _ = orc.bsgemm_cells(A, B, np.full(N, M - 1), np.arange(N))
     assert_bits_equal(C[M - 1], o, "ragged last row")
+
+
+@pytest.mark.parametrize("shape", [(384, 512, 6400), (8192, 768, 3072), (1024, 1024, 1024),
+                                   (1280, 2560, 1100), (640, 300, 4097), (150 * 128, 256, 768)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_split_tiles_exact_and_deterministic(orc, shape):
+    """Shapes whose tiles are split along K across CTAs (and across exact
+    chunks): the int32 sums combined from several CTAs equal the oracle's,
+    and two runs give the same bits."""
+    M, N, K = shape
+    rng = np.random.default_rng(M + N + K)
+    Aq = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    Bq = rng.integers(-127, 128, (K, N)).astype(np.int8)
+    Aq[0] = 127
+    Bq[:, 0] = 127
+    S1 = host(bsg.gemm_s32(dev(Aq), dev(Bq)))
+    S2 = host(bsg.gemm_s32(dev(Aq), dev(Bq)))
+    np.testing.assert_array_equal(S1, S2)
+    if M * N * K <= 4_000_000_000:
+        So, st = orc.gemm_s32(Aq, Bq)
+        assert_bits_equal(S1, So, f"S {shape}")
+    else:
+        rows, cols = sample_cells(M, N, 2000, 3)
+        exact = np.einsum("ik,ki->i", Aq[rows].astype(np.int64), Bq[:, cols].astype(np.int64))
+        np.testing.assert_array_equal(S1[rows, cols].astype(np.int64), exact)

@@ -27,7 +27,8 @@ def _matrix(kind, rows, cols, seed):
 
 
 SHAPES = [(1, 1), (3, 5), (17, 13), (64, 768), (129, 1000), (300, 1024), (37, 1025),
-          (8, 3072), (5, 5003), (1000, 33)]
+          (8, 3072), (5, 5003), (1000, 33), (9, 16384), (2, 20000), (8200, 40), (16, 252),
+          (2048, 96)]
 
 
 @pytest.mark.parametrize("kind", ["normal", "gpt2", "adversarial", "uniform"])
@@ -128,3 +129,9 @@ def test_hash_strided_rows(orc):
     assert rc == 0
     torch.cuda.synchronize()
     assert bytes(out.cpu().tolist()) == orc.hash_f32(view.cpu().numpy())
+
+
+def test_scale_derivation_selftest_exhaustive():
+    """The device's f32 scale derivation equals its own f64 definition for
+    every finite non-negative absmax bit pattern."""
+    assert bsg.selftest_scales(0, 0x7F7FFFFF) == 0

@@ -1,11 +1,12 @@
-"""Pins of the oracle's probe pieces: SHA-256, the tree hash, SplitMix64.
+"""Pins of the oracle's probe pieces: BLAKE2s, the tree hash, SplitMix64.
 
 The probe is "Verification -- why you can trust the numbers", section
 "Layer 3: the kernel probe": every device hashes the same seeded int8 GEMM
 through its live kernel.  The page names neither the generator nor the hash;
-the oracle's readings R6 (SplitMix64 inputs) and R7 (a 4-ary SHA-256 tree over
-256-byte leaves) are pinned here to their own published definitions: FIPS
-180-4 digests, Python's hashlib, and SplitMix64's published outputs.
+the oracle's readings R6 (SplitMix64 inputs) and R7 (a BLAKE2s tree, fanout
+4, 256-byte leaves) are pinned here to their own published definitions: the
+RFC 7693 test vector, Python's hashlib.blake2s (sequential and with the tree
+parameters), and SplitMix64's published outputs.
 """
 import hashlib
 import os
@@ -25,26 +26,40 @@ def read_golden(name):
     return rows
 
 
-def test_sha256_fips_vectors(orc):
-    for msg, digest in read_golden("sha256_fips180.txt"):
-        m = b"" if msg == "EMPTY" else msg.encode()
-        assert orc.sha256(m).hex() == digest
+def test_blake2s_rfc7693_vector(orc):
+    for msg, digest in read_golden("blake2s_rfc7693.txt"):
+        assert orc.blake2s(msg.encode()).hex() == digest
 
 
-def test_sha256_all_lengths_vs_hashlib(orc):
+def test_blake2s_all_lengths_vs_hashlib(orc):
     rng = np.random.default_rng(0)
     data = rng.integers(0, 256, 5000, dtype=np.uint8).tobytes()
     for n in list(range(0, 300)) + [447, 448, 511, 512, 1000, 4096, 5000]:
-        assert orc.sha256(data[:n]) == hashlib.sha256(data[:n]).digest(), n
+        assert orc.blake2s(data[:n]) == hashlib.blake2s(data[:n]).digest(), n
+
+
+def test_blake2s_tree_parameters_vs_hashlib(orc):
+    rng = np.random.default_rng(1)
+    data = rng.integers(0, 256, 400, dtype=np.uint8).tobytes()
+    for n in (0, 1, 32, 64, 96, 128, 256, 300):
+        for off, dep, last in ((0, 0, False), (5, 0, True), (2**40 + 3, 3, False), (7, 9, True)):
+            want = hashlib.blake2s(data[:n], fanout=4, depth=255, leaf_size=256, node_offset=off,
+                                   node_depth=dep, inner_size=32, last_node=last).digest()
+            assert orc.blake2s(data[:n], 4, 255, 256, off, dep, 32, last) == want
 
 
 def tree_hash_py(data: bytes) -> bytes:
-    """The tree of reading R7, restated with hashlib's SHA-256."""
+    """The tree of reading R7, restated with hashlib.blake2s."""
+    def node(msg, offset, depth, last):
+        return hashlib.blake2s(msg, fanout=4, depth=255, leaf_size=256, node_offset=offset,
+                               node_depth=depth, inner_size=32, last_node=last).digest()
     leaves = [data[i:i + 256] for i in range(0, len(data), 256)] or [b""]
-    level = [hashlib.sha256(b"\x00" + leaf).digest() for leaf in leaves]
+    level = [node(x, i, 0, i == len(leaves) - 1) for i, x in enumerate(leaves)]
+    depth = 0
     while len(level) > 1:
-        level = [hashlib.sha256(b"\x01" + b"".join(level[i:i + 4])).digest()
-                 for i in range(0, len(level), 4)]
+        depth += 1
+        groups = [b"".join(level[i:i + 4]) for i in range(0, len(level), 4)]
+        level = [node(g, j, depth, j == len(groups) - 1) for j, g in enumerate(groups)]
     return level[0]
 
 

@@ -55,10 +55,11 @@ MUTANTS = {
                            "float c = orc_epi(S[i * N + j], sa[j % (M ? M : 1)], sb[i % (N ? N : 1)]);")],
     "relu_keeps_negative_zero": [("return (c > 0.0f) ? c : 0.0f;", "return (c >= 0.0f) ? c : 0.0f;")],
     "relu_dropped": [("C[i * N + j] = relu ? orc_relu(c) : c;", "C[i * N + j] = c;")],
-    "sha256_rotation": [("rotr32(e, 6) ^ rotr32(e, 11) ^ rotr32(e, 25)",
-                         "rotr32(e, 6) ^ rotr32(e, 11) ^ rotr32(e, 24)")],
-    "hash_leaf_prefix_missing": [("sha256_prefixed(0x00, data + off, n, cur + 32 * l);",
-                                  "sha256_prefixed(-1, data + off, n, cur + 32 * l);")],
+    "blake2s_rotation": [("    v[b] = rotr32(v[b] ^ v[c], 7);", "    v[b] = rotr32(v[b] ^ v[c], 8);")],
+    "hash_last_node_flag_missing": [("                    l == nleaf - 1, cur + 32 * l);",
+                                     "                    0, cur + 32 * l);")],
+    "hash_node_depth_not_counted": [("                        (uint64_t)g, depth, 32, g == next - 1, nxt + 32 * g);",
+                                     "                        (uint64_t)g, 1, 32, g == next - 1, nxt + 32 * g);")],
     "hash_fanin_2": [("#define ORC_FANIN 4", "#define ORC_FANIN 2")],
     "hash_leaf_128": [("#define ORC_LEAF_BYTES 256", "#define ORC_LEAF_BYTES 128")],
     "hash_column_major": [("uint8_t *p = bytes + 4 * (size_t)(i * N + j);",
@@ -76,12 +77,8 @@ def _u32(a):
 
 
 def _tree_py(data: bytes) -> bytes:
-    leaves = [data[i:i + 256] for i in range(0, len(data), 256)] or [b""]
-    level = [hashlib.sha256(b"\x00" + x).digest() for x in leaves]
-    while len(level) > 1:
-        level = [hashlib.sha256(b"\x01" + b"".join(level[i:i + 4])).digest()
-                 for i in range(0, len(level), 4)]
-    return level[0]
+    from test_hash import tree_hash_py
+    return tree_hash_py(data)
 
 
 def _splitmix_py(seed, i):
@@ -165,10 +162,10 @@ def pin_zero_row(o):
 
 
 def pin_hash(o):
-    for line in open(os.path.join(os.path.dirname(__file__), "golden", "sha256_fips180.txt")):
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "blake2s_rfc7693.txt")):
         if line.strip() and not line.startswith("#"):
             msg, dig = line.split()
-            assert o.sha256(b"" if msg == "EMPTY" else msg.encode()).hex() == dig
+            assert o.blake2s(msg.encode()).hex() == dig
     data = np.random.default_rng(1).integers(0, 256, 70_000, dtype=np.uint8).tobytes()
     assert o.tree_hash(data) == _tree_py(data)
     Cm = np.random.default_rng(2).standard_normal((7, 5)).astype(np.float32)

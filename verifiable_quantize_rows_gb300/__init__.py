@@ -18,7 +18,7 @@ import threading
 
 __all__ = ["BsgError", "load", "exported_symbols", "quantize_rows", "quantize_cols",
            "gemm_s32", "epilogue", "bsgemm_i8", "bsgemm_i8_ex", "bsgemm_i8_host",
-           "bsgemm_i8_quantize", "bsgemm_i8_contract", "launch_count", "hash_f32", "probe_hash", "probe_hash_async", "workspace_size", "Workspace",
+           "bsgemm_i8_quantize", "bsgemm_i8_contract", "launch_count", "selftest_scales", "gemm_tile_width", "hash_f32", "probe_hash", "probe_hash_async", "workspace_size", "Workspace",
            "DSTATUS_NONFINITE", "DSTATUS_TIMEOUT", "MAX_K"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -66,6 +66,8 @@ def _declare(lib):
                                 _vp], _i32),
         "bsgemm_i8_contract": ([_i64, _i64, _i64, _i32, _vp, _i64, _vp, _sz, _vp, _vp], _i32),
         "bsg_launch_count": ([], ctypes.c_uint64),
+        "bsg_gemm_tile_width": ([_i64, _i64, _i32], _i32),
+        "bsg_selftest_scales": ([ctypes.c_uint32, ctypes.c_uint32, _vp], _i32),
         "bsgemm_i8_host_workspace_size": ([_i64, _i64, _i64], _sz),
         "bsgemm_i8_host": ([_vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _sz, _vp, _vp], _i32),
         "bsg_hash_f32_workspace_size": ([_i64, _i64], _sz),
@@ -263,6 +265,20 @@ def bsgemm_i8_ex(A, B, transA: bool = False, transB: bool = False, relu: bool = 
                             int(bool(transB)), M, N, K, int(bool(relu)), _ptr(C), N, wp, wn,
                             _ptr(dstatus), _stream_ptr(stream)), "bsgemm_i8_ex")
     return C
+
+
+def selftest_scales(first_bits: int = 0, last_bits: int = 0x7F7FFFFF) -> int:
+    """Mismatches between the device's f32 scale derivation and its f64
+    definition over absmax bit patterns [first_bits, last_bits]."""
+    n = ctypes.c_uint64(0)
+    _check(load().bsg_selftest_scales(first_bits, last_bits, ctypes.byref(n)),
+           "bsg_selftest_scales")
+    return int(n.value)
+
+
+def gemm_tile_width(M: int, N: int, sms: int) -> int:
+    """Output tile width the GEMM kernel picks for an M x N problem."""
+    return int(load().bsg_gemm_tile_width(M, N, sms))
 
 
 def launch_count() -> int:

@@ -14,7 +14,8 @@ enum QuantOut : int {
     kOutHalfKMajor = 1,  // f16-encoded int8 in the GEMM's K-major operand layout
 };
 
-// GEMM tile: 128 x 256 output per CTA, K in blocks of 64.
+// GEMM tile: 128 x (64, 128 or 256) output per CTA, K in blocks of 64.
+// kBN is the widest tile; per-column arrays are padded to it.
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
@@ -29,7 +30,7 @@ inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 inline int64_t operand_ld(int64_t K) { return round_up(K, kBK); }
 
 // Column absmax is reduced in `nsplit` slices of rows.
-int colmax_nsplit(int64_t rows);
+int colmax_nsplit(int64_t rows, int64_t cols);
 size_t colmax_partial_bytes(int64_t rows, int64_t cols);
 
 int device_sm_count();
@@ -48,6 +49,10 @@ cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int
                                  int out_kind, void *Q, int64_t ldq, float *scale, float *inv,
                                  uint32_t *partial, int32_t *dstatus, cudaStream_t st);
 
+// Device check of the scale derivation over absmax bit patterns [first, last].
+cudaError_t launch_selftest_scales(uint32_t first, uint32_t last, unsigned long long *bad,
+                                   cudaStream_t st);
+
 // int8 -> f16 operand conversions for the integer-only entry point.
 cudaError_t launch_i8_rows_to_half(const int8_t *Q, int64_t rows, int64_t cols, int64_t ldq,
                                    __half *out, int64_t ldo, cudaStream_t st);
@@ -58,6 +63,8 @@ cudaError_t launch_i8_cols_to_half(const int8_t *Q, int64_t rows, int64_t cols, 
 // ldk = operand_ld(K)).  mode 0: C = epi(S, sa, sb) (+ReLU) as float;
 // mode 1: S stored as int32.  sa / sb must hold round_up(M, kBM) /
 // round_up(N, kBN) floats (mode 0).
+// The tile width (64, 128 or 256) the GEMM uses for an M x N problem.
+int gemm_tile_width(int64_t M, int64_t N, int sms);
 cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int64_t N,
                            int64_t K, const float *sa, const float *sb, int relu, int mode,
                            void *out, int64_t ldo, int32_t *dstatus, cudaStream_t st);

@@ -232,7 +232,8 @@ bsg_status bsg_gemm_s32(const int8_t *Aq, int64_t lda, const int8_t *Bq, int64_t
     __half *bop = at<__half>(workspace, align256((size_t)M * ldk * 2));
     if (launch_i8_rows_to_half(Aq, M, K, lda, aop, ldk, st) != cudaSuccess) return BSG_ERR_CUDA;
     if (launch_i8_cols_to_half(Bq, K, N, ldb, bop, ldk, st) != cudaSuccess) return BSG_ERR_CUDA;
-    return from_cuda(launch_gemm_tc(aop, bop, M, N, K, nullptr, nullptr, 0, 1, S, lds, dstatus, st));
+    return from_cuda(
+        launch_gemm_tc(aop, bop, M, N, K, nullptr, nullptr, 0, 1, S, lds, dstatus, st));
 }
 
 bsg_status bsg_epilogue(const int32_t *S, int64_t lds, const float *sa, const float *sb,
@@ -280,6 +281,28 @@ bsg_status bsgemm_i8_contract(int64_t M, int64_t N, int64_t K, int relu, float *
                               void *workspace, size_t ws_bytes, int32_t *dstatus, void *stream) {
     return unit_contract(M, N, K, relu, C, ldc, workspace, ws_bytes, dstatus,
                          static_cast<cudaStream_t>(stream));
+}
+
+bsg_status bsg_selftest_scales(uint32_t first_bits, uint32_t last_bits,
+                               uint64_t *mismatches_host) {
+    if (!mismatches_host || first_bits > last_bits) return BSG_ERR_ARG;
+    bsg_status s = check_device();
+    if (s != BSG_OK) return s;
+    unsigned long long *d = nullptr;
+    if (cudaMalloc(&d, sizeof(*d)) != cudaSuccess) return BSG_ERR_CUDA;
+    unsigned long long h = 0;
+    cudaError_t e = cudaMemset(d, 0, sizeof(*d));
+    if (e == cudaSuccess) e = launch_selftest_scales(first_bits, last_bits, d, 0);
+    if (e == cudaSuccess) e = cudaMemcpy(&h, d, sizeof(h), cudaMemcpyDeviceToHost);
+    cudaFree(d);
+    if (e != cudaSuccess) return BSG_ERR_CUDA;
+    *mismatches_host = h;
+    return BSG_OK;
+}
+
+int bsg_gemm_tile_width(int64_t M, int64_t N, int sms) {
+    if (M < 1 || N < 1 || sms < 1) return -1;
+    return gemm_tile_width(M, N, sms);
 }
 
 uint64_t bsg_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

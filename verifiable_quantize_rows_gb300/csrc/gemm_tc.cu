@@ -17,17 +17,22 @@
 // into chunks of 1024; each chunk's fp32 tile is converted to int32 and the
 // chunks are summed in int32, which is exact.
 //
-// Structure (one CTA per SM, persistent over 128 x 256 output tiles):
+// Tiles are 128 x BN with BN in {64, 128, 256}, chosen per problem so that
+// the last wave of tiles leaves few SMs idle; one CTA per SM walks its tiles
+// round-robin (persistent).
+//
+// Roles (one CTA per SM):
 //   warp 0      TMA producer: A and B k-blocks (64 wide, 128-byte swizzle)
-//               into a 4-stage shared-memory ring;
+//               into a shared-memory ring (4 stages at BN 256, 6 below);
 //   warp 1      MMA issuer (one thread): 4 x tcgen05.mma (K = 16) per
 //               k-block into a tensor-memory accumulator, double-buffered
-//               (2 x 256 columns) so the epilogue of one chunk or tile
+//               (2 x BN columns) so the epilogue of one chunk or tile
 //               overlaps the next one's MMAs;
-//   warp 2      allocates / frees the 512 tensor-memory columns;
-//   warps 4-11  epilogue: tcgen05.ld, int32 chunk sums, f32 epilogue,
-//               ReLU, staging in shared memory and TMA stores (or plain
-//               stores where C's rows are not 16-byte aligned).
+//   warp 2      allocates / frees the tensor-memory columns;
+//   warps 4-11  epilogue: tcgen05.ld of each chunk into int32 registers
+//               (the tensor memory is released at once), then the f32
+//               epilogue, ReLU, staging in shared memory and TMA stores (or
+//               plain stores where C's rows are not 16-byte aligned).
 // Every mbarrier wait is bounded; on expiry the CTA records
 // BSG_DSTATUS_TIMEOUT, drains its copies and MMAs, frees tensor memory and
 // returns.
@@ -35,6 +40,7 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 #include <stdint.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -44,50 +50,54 @@
 namespace bsg {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kChunkBlocks = kChunkK / kBK;  // 16 k-blocks per exact chunk
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 128 + kEpiWarps * 32;
-constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KiB
-constexpr uint32_t kBBytes = kBN * kBK * 2;  // 32 KiB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kABytes = kBM * kBK * 2;     // 16 KiB
 constexpr uint32_t kEpiBufBytes = 32 * 32 * 4;  // one 32 x 32 fp32 box per epilogue warp
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = kBN;  // one accumulator buffer
+constexpr int kGroupM = 16;                     // tile raster: 16 m-tiles per group
 
-constexpr uint32_t kOffEpi = kStages * kStageBytes;
-constexpr uint32_t kOffBar = kOffEpi + kEpiWarps * kEpiBufBytes;
-// barriers: full[kStages], empty[kStages], tfull[2], tempty[2], drain
-constexpr uint32_t kNumBars = 2 * kStages + 5;
-constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
-constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
-constexpr uint32_t kSmemUsed = kOffAbort + 4;
-constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
-
-constexpr uint32_t kIdesc = idesc_f16_f32(kBM, kBN);
-constexpr int kGroupM = 16;  // tile raster: 16 m-tiles per group
+// Compile-time layout of one tile width.
+template <int BN>
+struct Cfg {
+    static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
+    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr uint32_t kBBytes = BN * kBK * 2;
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kAccCols = BN;  // one accumulator buffer
+    static constexpr uint32_t kTmemCols = 2 * BN;
+    static constexpr int kWarpCols = BN / 2;  // columns per epilogue warp
+    static constexpr int kPieces = kWarpCols / 32;
+    static constexpr uint32_t kOffEpi = kStages * kStageBytes;
+    static constexpr uint32_t kOffBar = kOffEpi + kEpiWarps * kEpiBufBytes;
+    // barriers: full[kStages], empty[kStages], tfull[2], tempty[2], drain
+    static constexpr uint32_t kNumBars = 2 * kStages + 5;
+    static constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
+    static constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
+    static constexpr uint32_t kSmemBytes = kOffAbort + 4 + 1024;  // + 1024-byte alignment slack
+    static constexpr uint32_t kIdesc = idesc_f16_f32(kBM, BN);
+};
 
 struct Params {
     int M, N, K;
-    int num_kb;        // k-blocks
-    int num_chunks;    // exact chunks per tile
+    int num_kb;        // k-blocks per tile
     int num_m, num_n;  // tiles
     int num_tiles;
     const float *sa;
     const float *sb;
     void *out;
     int64_t ldo;
-    int mode;           // 0: f32 epilogue, 1: int32 accumulators
+    int mode;       // 0: f32 epilogue, 1: int32 accumulators
     int relu;
-    int tma_store;      // 1: C/S rows are 16-byte aligned; store through tmap_c
+    int tma_store;  // 1: C/S rows are 16-byte aligned; store through tmap_c
     int32_t *dstatus;
 };
 
-__device__ __forceinline__ void tile_coords(const Params &p, int t, int &mb, int &nb) {
+__host__ __device__ __forceinline__ void tile_coords(const Params &p, int t, int &mb, int &nb) {
     const int per_group = kGroupM * p.num_n;
     const int g = t / per_group;
     const int first_m = g * kGroupM;
-    const int gm = min(kGroupM, p.num_m - first_m);
+    const int gm = (p.num_m - first_m) < kGroupM ? (p.num_m - first_m) : kGroupM;
     const int r = t - g * per_group;
     mb = first_m + r % gm;
     nb = r / gm;
@@ -139,28 +149,31 @@ __device__ __forceinline__ void emit_box(const Params &p, const CUtensorMap *tma
     }
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c, const Params p) {
+    using K = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
 
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + K::kOffBar);
     uint64_t *full = bars;
-    uint64_t *empty = bars + kStages;
-    uint64_t *tfull = bars + 2 * kStages;
-    uint64_t *tempty = bars + 2 * kStages + 2;
-    uint64_t *drain = bars + 2 * kStages + 4;
-    uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + kOffTmemPtr);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
+    uint64_t *empty = bars + K::kStages;
+    uint64_t *tfull = bars + 2 * K::kStages;
+    uint64_t *tempty = bars + 2 * K::kStages + 2;
+    uint64_t *drain = bars + 2 * K::kStages + 4;
+    uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + K::kOffTmemPtr);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K::kOffAbort);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int num_chunks = (p.num_kb + kChunkBlocks - 1) / kChunkBlocks;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < K::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -174,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_async_shared();
     }
     if (warp == 2) {
-        tmem_alloc(tmem_ptr, kTmemCols);
+        tmem_alloc(tmem_ptr, K::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -189,9 +202,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tmap_b);
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t issued_parity[kStages];
-            bool issued[kStages];
-            for (int s = 0; s < kStages; ++s) issued[s] = false, issued_parity[s] = 0;
+            uint32_t issued_parity[K::kStages];
+            bool issued[K::kStages];
+            for (int s = 0; s < K::kStages; ++s) issued[s] = false, issued_parity[s] = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
                 int mb, nb;
@@ -202,21 +215,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    uint8_t *sa_tile = smem + stage * kStageBytes;
+                    uint8_t *sa_tile = smem + stage * K::kStageBytes;
                     uint8_t *sb_tile = sa_tile + kABytes;
-                    mbar_arrive_expect_tx(&full[stage], kStageBytes);
+                    mbar_arrive_expect_tx(&full[stage], K::kStageBytes);
                     tma_load_2d(&tmap_a, &full[stage], sa_tile, kb * kBK, mb * kBM);
-                    tma_load_2d(&tmap_b, &full[stage], sb_tile, kb * kBK, nb * kBN);
+                    tma_load_2d(&tmap_b, &full[stage], sb_tile, kb * kBK, nb * BN);
                     issued[stage] = true;
                     issued_parity[stage] = phase;
-                    if (++stage == kStages) stage = 0, phase ^= 1;
+                    if (++stage == K::kStages) stage = 0, phase ^= 1;
                 }
             }
             // Never leave with a copy still landing in shared memory.
-            for (int s = 0; s < kStages; ++s)
+            for (int s = 0; s < K::kStages; ++s)
                 if (issued[s] && !mbar_wait(&full[s], issued_parity[s], abort_flag)) {
-                    // the copy is still pending after the limit: wait for it
-                    // without the abort shortcut, once more bounded
                     const long long t0 = clock64();
                     while (!mbar_try_wait(&full[s], issued_parity[s]) &&
                            clock64() - t0 < kWaitLimitCycles) {
@@ -232,7 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             bool any_mma = false;
             for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-                for (int c = 0; ok && c < p.num_chunks; ++c) {
+                for (int c = 0; ok && c < num_chunks; ++c) {
+                    const int kb0 = c * kChunkBlocks;
+                    const int kb1 = min(p.num_kb, kb0 + kChunkBlocks);
                     const uint32_t b = acc_iter & 1;
                     const uint32_t acc_phase = (acc_iter >> 1) & 1;
                     if (!mbar_wait(&tempty[b], acc_phase ^ 1, abort_flag)) {
@@ -241,9 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + b * kAccCols;
-                    const int kb0 = c * kChunkBlocks;
-                    const int kb1 = min(p.num_kb, kb0 + kChunkBlocks);
+                    const uint32_t d_tmem = tmem_base + b * K::kAccCols;
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(&full[stage], phase, abort_flag)) {
                             record_abort(abort_flag, p.dstatus);
@@ -251,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
+                        const uint32_t a_addr = smem_u32(smem + stage * K::kStageBytes);
                         const uint32_t b_addr = a_addr + kABytes;
                         const uint64_t adesc = sdesc_k128(a_addr);
                         const uint64_t bdesc = sdesc_k128(b_addr);
@@ -259,11 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int k = 0; k < kBK / 16; ++k) {
                             // advance 16 f16 = 32 bytes along K inside the swizzle atom
                             mma_f16_ss(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k),
-                                       kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                                       K::kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
                         }
                         any_mma = true;
                         mma_commit(&empty[stage]);
-                        if (++stage == kStages) stage = 0, phase ^= 1;
+                        if (++stage == K::kStages) stage = 0, phase ^= 1;
                     }
                     if (!ok) break;
                     mma_commit(&tfull[b]);
@@ -280,21 +291,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 4) {
         // ------------------------------------------------ epilogue
-        const int q = warp & 3;              // tensor-memory lane quadrant
-        const int h = (warp - 4) >> 2;       // column half of the tile
-        const int ew = warp - 4;             // epilogue warp index
-        uint8_t *box = smem + kOffEpi + ew * kEpiBufBytes;
+        const int q = warp & 3;         // tensor-memory lane quadrant
+        const int h = (warp - 4) >> 2;  // column half of the tile
+        const int ew = warp - 4;        // epilogue warp index
+        uint8_t *box = smem + K::kOffEpi + ew * kEpiBufBytes;
         bool box_busy = false;
         uint32_t acc_iter = 0;
         bool ok = true;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-            int mb, nb;
-            tile_coords(p, t, mb, nb);
-            const int row0 = mb * kBM + q * 32;
-            const int colh = nb * kBN + h * 128;
-            const float a = p.mode == 0 ? __ldg(p.sa + row0 + lane) : 0.0f;
-            if (p.num_chunks == 1) {
+            // ---- drain every chunk into int32 sums
+            uint32_t acc[K::kWarpCols];  // int32 bit patterns
+            for (int c = 0; c < num_chunks; ++c) {
                 const uint32_t b = acc_iter & 1;
                 const uint32_t acc_phase = (acc_iter >> 1) & 1;
                 // warp-uniform: every lane must agree before the .sync.aligned loads
@@ -304,90 +312,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t tbase = tmem_base + b * kAccCols + h * 128 + lane_addr;
-#pragma unroll 1
-                for (int piece = 0; piece < 4; ++piece) {
-                    uint32_t r0[16], r1[16];
-                    tmem_ld16(tbase + piece * 32, r0);
-                    tmem_ld16(tbase + piece * 32 + 16, r1);
+                const uint32_t tbase = tmem_base + b * K::kAccCols + h * K::kWarpCols + lane_addr;
+                if (c == 0) {
+#pragma unroll
+                    for (int piece = 0; piece < K::kWarpCols / 16; ++piece)
+                        tmem_ld16(tbase + piece * 16,
+                                  *reinterpret_cast<uint32_t(*)[16]>(&acc[piece * 16]));
                     tmem_ld_wait();
-                    uint32_t v[32];
-                    const int col0 = colh + piece * 32;
-                    if (p.mode == 0) {
-                        const float4 *sbv = reinterpret_cast<const float4 *>(p.sb + col0);
 #pragma unroll
-                        for (int j4 = 0; j4 < 8; ++j4) {
-                            const float4 bb = __ldg(sbv + j4);
-                            const float bj[4] = {bb.x, bb.y, bb.z, bb.w};
+                    for (int j = 0; j < K::kWarpCols; ++j)
+                        acc[j] = (uint32_t)__float2int_rn(__uint_as_float(acc[j]));
+                } else {
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const int j = 4 * j4 + u;
-                                const uint32_t acc = j < 16 ? r0[j] : r1[j - 16];
-                                const int32_t s = __float2int_rn(__uint_as_float(acc));
-                                v[j] = __float_as_uint(epi_value(s, a, bj[u], p.relu));
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            v[j] = (uint32_t)__float2int_rn(
-                                __uint_as_float(j < 16 ? r0[j] : r1[j - 16]));
-                    }
-                    emit_box(p, &tmap_c, box, v, row0, col0, lane, box_busy);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[b]);
-                ++acc_iter;
-            } else {
-                int32_t sum[128];
-#pragma unroll
-                for (int j = 0; j < 128; ++j) sum[j] = 0;
-                for (int c = 0; c < p.num_chunks; ++c) {
-                    const uint32_t b = acc_iter & 1;
-                    const uint32_t acc_phase = (acc_iter >> 1) & 1;
-                    if (!__all_sync(0xffffffffu, mbar_wait(&tfull[b], acc_phase, abort_flag))) {
-                        if (lane == 0) record_abort(abort_flag, p.dstatus);
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t tbase = tmem_base + b * kAccCols + h * 128 + lane_addr;
-#pragma unroll
-                    for (int piece = 0; piece < 8; ++piece) {
+                    for (int piece = 0; piece < K::kWarpCols / 16; ++piece) {
                         uint32_t r[16];
                         tmem_ld16(tbase + piece * 16, r);
                         tmem_ld_wait();
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            sum[piece * 16 + j] += __float2int_rn(__uint_as_float(r[j]));
+                            acc[piece * 16 + j] = (uint32_t)((int32_t)acc[piece * 16 + j] +
+                                                             __float2int_rn(__uint_as_float(r[j])));
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[b]);
-                    ++acc_iter;
                 }
-                if (!ok) break;
+                // the accumulator buffer is free again
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[b]);
+                ++acc_iter;
+            }
+            if (!ok) break;
+
+            // ---- final epilogue of the tile from the int32 sums
+            int mb, nb;
+            tile_coords(p, t, mb, nb);
+            const int row0 = mb * kBM + q * 32;
+            const int colh = nb * BN + h * K::kWarpCols;
+            const float a = p.mode == 0 ? __ldg(p.sa + row0 + lane) : 0.0f;
 #pragma unroll
-                for (int piece = 0; piece < 4; ++piece) {
-                    uint32_t v[32];
-                    const int col0 = colh + piece * 32;
-                    if (p.mode == 0) {
-                        const float4 *sbv = reinterpret_cast<const float4 *>(p.sb + col0);
+            for (int piece = 0; piece < K::kPieces; ++piece) {
+                uint32_t(&v)[32] = *reinterpret_cast<uint32_t(*)[32]>(&acc[piece * 32]);
+                const int col0 = colh + piece * 32;
+                if (p.mode == 0) {
+                    // in place: the int32 sums become the output bits
+                    const float4 *sbv = reinterpret_cast<const float4 *>(p.sb + col0);
 #pragma unroll
-                        for (int j4 = 0; j4 < 8; ++j4) {
-                            const float4 bb = __ldg(sbv + j4);
-                            v[4 * j4 + 0] = __float_as_uint(epi_value(sum[piece * 32 + 4 * j4 + 0], a, bb.x, p.relu));
-                            v[4 * j4 + 1] = __float_as_uint(epi_value(sum[piece * 32 + 4 * j4 + 1], a, bb.y, p.relu));
-                            v[4 * j4 + 2] = __float_as_uint(epi_value(sum[piece * 32 + 4 * j4 + 2], a, bb.z, p.relu));
-                            v[4 * j4 + 3] = __float_as_uint(epi_value(sum[piece * 32 + 4 * j4 + 3], a, bb.w, p.relu));
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = (uint32_t)sum[piece * 32 + j];
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 bb = __ldg(sbv + j4);
+                        v[4 * j4 + 0] = __float_as_uint(epi_value((int32_t)v[4 * j4 + 0], a, bb.x, p.relu));
+                        v[4 * j4 + 1] = __float_as_uint(epi_value((int32_t)v[4 * j4 + 1], a, bb.y, p.relu));
+                        v[4 * j4 + 2] = __float_as_uint(epi_value((int32_t)v[4 * j4 + 2], a, bb.z, p.relu));
+                        v[4 * j4 + 3] = __float_as_uint(epi_value((int32_t)v[4 * j4 + 3], a, bb.w, p.relu));
                     }
-                    emit_box(p, &tmap_c, box, v, row0, col0, lane, box_busy);
                 }
+                emit_box(p, &tmap_c, box, v, row0, col0, lane, box_busy);
             }
         }
         if (p.tma_store && lane == 0) bulk_wait0();
@@ -398,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 2) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc(tmem_base, K::kTmemCols);
     }
 }
 
@@ -432,25 +409,63 @@ bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, size_t esz, const void
     return r == CUDA_SUCCESS;
 }
 
+template <int BN>
+cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tc, const __half *Bop,
+                      int64_t N, int64_t K, const Params &p0, cudaStream_t st) {
+    using C = Cfg<BN>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    CUtensorMap tb;
+    if (!make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, Bop, (uint64_t)K, (uint64_t)N,
+                      (uint64_t)operand_ld(K), kBK, BN))
+        return cudaErrorInvalidValue;
+    Params p = p0;
+    p.num_n = (int)((N + BN - 1) / BN);
+    p.num_tiles = p.num_m * p.num_n;
+    const int sms = device_sm_count();
+    const int grid = p.num_tiles < sms ? p.num_tiles : sms;
+    gemm_tc_kernel<BN><<<grid, kThreads, C::kSmemBytes, st>>>(ta, tb, tc, p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+// Tile width for an M x N problem on `sms` SMs: the one with the least
+// estimated time, rounds of tiles times the cost of one tile.  A tile of
+// width BN costs BN/256 of a 256-wide one, times a penalty for the narrower
+// MMAs (which read more shared memory per multiply-add) and for the fixed
+// per-tile epilogue work.
+int gemm_tile_width(int64_t M, int64_t N, int sms) {
+    const int widths[3] = {256, 128, 64};
+    const double penalty[3] = {1.0, 1.37, 2.64};  // measured: 8192^3 at each width
+    const int64_t num_m = (M + kBM - 1) / kBM;
+    int best = 256;
+    double best_cost = 1e300;
+    for (int i = 0; i < 3; ++i) {
+        const int64_t tiles = num_m * ((N + widths[i] - 1) / widths[i]);
+        const int64_t rounds = (tiles + sms - 1) / sms;
+        const double cost = (double)rounds * widths[i] / 256.0 * penalty[i];
+        if (cost < best_cost * 0.999) {
+            best_cost = cost;
+            best = widths[i];
+        }
+    }
+    return best;
+}
 
 cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int64_t N,
                            int64_t K, const float *sa, const float *sb, int relu, int mode,
                            void *out, int64_t ldo, int32_t *dstatus, cudaStream_t st) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    const int64_t ldk = operand_ld(K);
-    CUtensorMap ta, tb, tc;
+    CUtensorMap ta, tc;
     if (!make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, Aop, (uint64_t)K, (uint64_t)M,
-                      (uint64_t)ldk, kBK, kBM) ||
-        !make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, Bop, (uint64_t)K, (uint64_t)N,
-                      (uint64_t)ldk, kBK, kBN))
+                      (uint64_t)operand_ld(K), kBK, kBM))
         return cudaErrorInvalidValue;
     const bool aligned = ((ldo * 4) % 16 == 0) && (reinterpret_cast<uintptr_t>(out) % 16 == 0);
     int tma_store = 0;
@@ -464,14 +479,12 @@ cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int6
                         : 0;
     }
     Params p;
+    memset(&p, 0, sizeof(p));
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
     p.num_kb = (int)((K + kBK - 1) / kBK);
-    p.num_chunks = (p.num_kb + kChunkBlocks - 1) / kChunkBlocks;
     p.num_m = (int)((M + kBM - 1) / kBM);
-    p.num_n = (int)((N + kBN - 1) / kBN);
-    p.num_tiles = p.num_m * p.num_n;
     p.sa = sa;
     p.sb = sb;
     p.out = out;
@@ -480,10 +493,11 @@ cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int6
     p.relu = relu;
     p.tma_store = tma_store;
     p.dstatus = dstatus;
-    const int grid = (int)std::min<int64_t>(p.num_tiles, device_sm_count());
-    gemm_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(ta, tb, tc, p);
-    count_launches(1);
-    return cudaGetLastError();
+    switch (gemm_tile_width(M, N, device_sm_count())) {
+        case 64: return launch_bn<64>(ta, tc, Bop, N, K, p, st);
+        case 128: return launch_bn<128>(ta, tc, Bop, N, K, p, st);
+        default: return launch_bn<256>(ta, tc, Bop, N, K, p, st);
+    }
 }
 
 }  // namespace bsg

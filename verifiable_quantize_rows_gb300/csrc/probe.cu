@@ -8,11 +8,13 @@
 //     generator seeded with s is mix(s + (i+1) * 0x9e3779b97f4a7c15), and an
 //     output z becomes the float ((z >> 40) - 2^23) * 2^-23, exact, in
 //     [-1, 1); A takes outputs 0 .. M*K-1, B the next K*N;
-//   * a 4-ary SHA-256 tree (FIPS 180-4) over C's little-endian bytes, rows
-//     packed: leaves of 256 bytes hashed as SHA-256(0x00 || leaf), then
-//     groups of four digests hashed as SHA-256(0x01 || d1 || ...), level by
-//     level, until one digest is left.  The tree lets every leaf hash in
-//     parallel; the serial depth is 5 + 3 * levels compressions.
+//   * a BLAKE2s-256 tree (RFC 7693, BLAKE2 tree mode: fanout 4, unlimited
+//     depth, 256-byte leaves, inner length 32) over C's little-endian bytes,
+//     rows packed: leaf i hashed with node offset i at depth 0; groups of
+//     four digests hashed level by level (node offset = group index, node
+//     depth = level); the last node of each level flagged; the hash is the
+//     single node of the first level that has one.  Every leaf hashes in
+//     parallel; the serial depth is 4 + 2 * levels compressions.
 #include <stdint.h>
 
 #include "bsg_internal.h"
@@ -46,94 +48,121 @@ __global__ void probe_fill_kernel(uint64_t seed, int64_t nA, int64_t nB, float *
     }
 }
 
-// ---------------------------------------------------------------- SHA-256
-// Round constants: FIPS 180-4 section 4.2.2 (first 32 bits of the
-// fractional parts of the cube roots of the first 64 primes).
-__constant__ uint32_t kRound[64] = {
-    0x428a2f98, 0x71374491, 0xb5c0fbcf, 0xe9b5dba5, 0x3956c25b, 0x59f111f1, 0x923f82a4,
-    0xab1c5ed5, 0xd807aa98, 0x12835b01, 0x243185be, 0x550c7dc3, 0x72be5d74, 0x80deb1fe,
-    0x9bdc06a7, 0xc19bf174, 0xe49b69c1, 0xefbe4786, 0x0fc19dc6, 0x240ca1cc, 0x2de92c6f,
-    0x4a7484aa, 0x5cb0a9dc, 0x76f988da, 0x983e5152, 0xa831c66d, 0xb00327c8, 0xbf597fc7,
-    0xc6e00bf3, 0xd5a79147, 0x06ca6351, 0x14292967, 0x27b70a85, 0x2e1b2138, 0x4d2c6dfc,
-    0x53380d13, 0x650a7354, 0x766a0abb, 0x81c2c92e, 0x92722c85, 0xa2bfe8a1, 0xa81a664b,
-    0xc24b8b70, 0xc76c51a3, 0xd192e819, 0xd6990624, 0xf40e3585, 0x106aa070, 0x19a4c116,
-    0x1e376c08, 0x2748774c, 0x34b0bcb5, 0x391c0cb3, 0x4ed8aa4a, 0x5b9cca4f, 0x682e6ff3,
-    0x748f82ee, 0x78a5636f, 0x84c87814, 0x8cc70208, 0x90befffa, 0xa4506ceb, 0xbef9a3f7,
-    0xc67178f2};
+// ---------------------------------------------------------------- BLAKE2s
+// BLAKE2s-256 (RFC 7693) in the BLAKE2 tree mode.  Messages here are always
+// a whole number of 32-bit little-endian words: a leaf is C's float bits, an
+// inner node its children's digests.
+constexpr uint32_t kFanout = 4;
+constexpr uint32_t kTreeDepth = 255;  // unlimited
+constexpr uint32_t kLeafBytes = 256;
+
+__device__ __forceinline__ uint32_t b2s_iv(int i) {
+    constexpr uint32_t iv[8] = {0x6A09E667u, 0xBB67AE85u, 0x3C6EF372u, 0xA54FF53Au,
+                                0x510E527Fu, 0x9B05688Cu, 0x1F83D9ABu, 0x5BE0CD19u};
+    return iv[i];
+}
 
 __device__ __forceinline__ uint32_t ror(uint32_t x, int n) { return __funnelshift_r(x, x, n); }
 
-// One compression of a 16-word big-endian block into state h (FIPS 180-4
-// section 6.2.2), message schedule kept as a rolling 16-word window.
-__device__ __forceinline__ void compress(uint32_t (&h)[8], uint32_t (&w)[16]) {
-    uint32_t a = h[0], b = h[1], c = h[2], d = h[3], e = h[4], f = h[5], g = h[6], hh = h[7];
+#define B2S_G(a, b, c, d, x, y)          \
+    do {                                 \
+        v[a] = v[a] + v[b] + (x);        \
+        v[d] = ror(v[d] ^ v[a], 16);     \
+        v[c] = v[c] + v[d];              \
+        v[b] = ror(v[b] ^ v[c], 12);     \
+        v[a] = v[a] + v[b] + (y);        \
+        v[d] = ror(v[d] ^ v[a], 8);      \
+        v[c] = v[c] + v[d];              \
+        v[b] = ror(v[b] ^ v[c], 7);      \
+    } while (0)
+
+// The compression function F (RFC 7693 section 3.2): t is the byte count so
+// far, last_block / last_node the finalization flags.
+__device__ __forceinline__ void b2s_compress(uint32_t (&h)[8], const uint32_t (&m)[16], uint32_t t,
+                                             bool last_block, bool last_node) {
+    constexpr uint8_t S[10][16] = {
+        {0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15},
+        {14, 10, 4, 8, 9, 15, 13, 6, 1, 12, 0, 2, 11, 7, 5, 3},
+        {11, 8, 12, 0, 5, 2, 15, 13, 10, 14, 3, 6, 7, 1, 9, 4},
+        {7, 9, 3, 1, 13, 12, 11, 14, 2, 6, 5, 10, 4, 0, 15, 8},
+        {9, 0, 5, 7, 2, 4, 10, 15, 14, 1, 11, 12, 6, 8, 3, 13},
+        {2, 12, 6, 10, 0, 11, 8, 3, 4, 13, 7, 5, 15, 14, 1, 9},
+        {12, 5, 1, 15, 14, 13, 4, 10, 0, 7, 6, 3, 9, 2, 8, 11},
+        {13, 11, 7, 14, 12, 1, 3, 9, 5, 0, 15, 4, 8, 6, 2, 10},
+        {6, 15, 14, 9, 11, 3, 0, 8, 12, 2, 13, 7, 1, 4, 10, 5},
+        {10, 2, 8, 4, 7, 6, 1, 5, 15, 11, 9, 14, 3, 12, 13, 0}};
+    uint32_t v[16];
 #pragma unroll
-    for (int t = 0; t < 64; ++t) {
-        uint32_t wt;
-        if (t < 16) {
-            wt = w[t];
-        } else {
-            const uint32_t w15 = w[(t - 15) & 15], w2 = w[(t - 2) & 15];
-            const uint32_t s0 = ror(w15, 7) ^ ror(w15, 18) ^ (w15 >> 3);
-            const uint32_t s1 = ror(w2, 17) ^ ror(w2, 19) ^ (w2 >> 10);
-            wt = w[t & 15] + s0 + w[(t - 7) & 15] + s1;
-            w[t & 15] = wt;
-        }
-        const uint32_t S1 = ror(e, 6) ^ ror(e, 11) ^ ror(e, 25);
-        const uint32_t ch = (e & f) ^ (~e & g);
-        const uint32_t t1 = hh + S1 + ch + kRound[t] + wt;
-        const uint32_t S0 = ror(a, 2) ^ ror(a, 13) ^ ror(a, 22);
-        const uint32_t mj = (a & b) ^ (a & c) ^ (b & c);
-        const uint32_t t2 = S0 + mj;
-        hh = g;
-        g = f;
-        f = e;
-        e = d + t1;
-        d = c;
-        c = b;
-        b = a;
-        a = t1 + t2;
+    for (int i = 0; i < 8; ++i) {
+        v[i] = h[i];
+        v[i + 8] = b2s_iv(i);
     }
-    h[0] += a; h[1] += b; h[2] += c; h[3] += d;
-    h[4] += e; h[5] += f; h[6] += g; h[7] += hh;
+    v[12] ^= t;  // messages here stay far below 2^32 bytes
+    if (last_block) v[14] = ~v[14];
+    if (last_block && last_node) v[15] = ~v[15];
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        B2S_G(0, 4, 8, 12, m[S[r][0]], m[S[r][1]]);
+        B2S_G(1, 5, 9, 13, m[S[r][2]], m[S[r][3]]);
+        B2S_G(2, 6, 10, 14, m[S[r][4]], m[S[r][5]]);
+        B2S_G(3, 7, 11, 15, m[S[r][6]], m[S[r][7]]);
+        B2S_G(0, 5, 10, 15, m[S[r][8]], m[S[r][9]]);
+        B2S_G(1, 6, 11, 12, m[S[r][10]], m[S[r][11]]);
+        B2S_G(2, 7, 8, 13, m[S[r][12]], m[S[r][13]]);
+        B2S_G(3, 4, 9, 14, m[S[r][14]], m[S[r][15]]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] ^= v[i] ^ v[i + 8];
 }
 
-// SHA-256 of the byte string  prefix || D_0 || ... || D_{W-1}  where each
-// D_i is a big-endian 32-bit word supplied by `word(i)`.  Words of the
-// padded message are the stream shifted by the one prefix byte.
+// Initial state of a tree node: the IV xor the parameter block (digest 32,
+// no key, fanout 4, unlimited depth, leaf 256 bytes, inner length 32).
+__device__ __forceinline__ void b2s_node_init(uint32_t (&h)[8], uint64_t node_offset,
+                                              uint32_t node_depth) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = b2s_iv(i);
+    h[0] ^= 32u | (kFanout << 16) | (kTreeDepth << 24);
+    h[1] ^= kLeafBytes;
+    h[2] ^= (uint32_t)node_offset;
+    h[3] ^= (uint32_t)((node_offset >> 32) & 0xFFFFu) | (node_depth << 16) | (32u << 24);
+}
+
+// Hash of W little-endian words supplied by word(i) as one tree node.
 template <typename WordFn>
-__device__ void sha256_prefixed(uint32_t prefix, int W, WordFn word, uint32_t (&h)[8]) {
-    h[0] = 0x6a09e667; h[1] = 0xbb67ae85; h[2] = 0x3c6ef372; h[3] = 0xa54ff53a;
-    h[4] = 0x510e527f; h[5] = 0x9b05688c; h[6] = 0x1f83d9ab; h[7] = 0x5be0cd19;
-    const uint32_t nbytes = 1u + 4u * (uint32_t)W;
-    const int nblocks = (int)((nbytes + 9u + 63u) / 64u);
-    uint32_t prev = prefix;  // D_{-1}
+__device__ void b2s_node(int W, WordFn word, uint64_t node_offset, uint32_t node_depth,
+                         bool last_node, uint32_t (&h)[8]) {
+    b2s_node_init(h, node_offset, node_depth);
+    const int nblocks = W == 0 ? 1 : (W + 15) / 16;
     for (int blk = 0; blk < nblocks; ++blk) {
         uint32_t m[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const int wi = blk * 16 + j;
-            uint32_t v;
-            if (wi < W) {
-                const uint32_t cur = word(wi);
-                v = (prev << 24) | (cur >> 8);
-                prev = cur;
-            } else if (wi == W) {
-                v = (prev << 24) | 0x00800000u;
-            } else {
-                v = 0u;
-            }
-            m[j] = v;
+            m[j] = wi < W ? word(wi) : 0u;
         }
-        if (blk == nblocks - 1) m[15] = nbytes * 8u;  // bit length < 2^32
-        compress(h, m);
+        const int words_done = min(W, (blk + 1) * 16);
+        b2s_compress(h, m, 4u * (uint32_t)words_done, blk == nblocks - 1, last_node);
     }
 }
 
-constexpr int kHashThreads = 256;   // inputs per block = 4^4
-constexpr int kLeafFloats = 64;     // 256-byte leaves
+// A full 64-word leaf from registers (the common case): 4 blocks.
+__device__ __forceinline__ void b2s_leaf64(const uint32_t (&w)[64], uint64_t node_offset,
+                                           bool last_node, uint32_t (&h)[8]) {
+    b2s_node_init(h, node_offset, 0);
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+        uint32_t m[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) m[j] = w[blk * 16 + j];
+        b2s_compress(h, m, 64u * (blk + 1), blk == 3, last_node);
+    }
+}
 
-__device__ __forceinline__ uint32_t bswap32(uint32_t u) { return __byte_perm(u, 0, 0x0123); }
+// Leaves are hashed 64 to a block (3 tree levels inside the block) so that
+// every SM takes part; higher levels 256 to a block (4 levels).
+constexpr int kLeafThreads = 64;
+constexpr int kNodeThreads = 256;
+constexpr int kLeafFloats = 64;  // 256-byte leaves
 
 struct LeafWords {
     const float *C;
@@ -143,7 +172,7 @@ struct LeafWords {
     __device__ uint32_t operator()(int i) const {
         const int64_t e = first + i;
         const float *p = packed ? C + e : C + (e / N) * ldc + (e % N);
-        return bswap32(__float_as_uint(__ldg(p)));
+        return __float_as_uint(__ldg(p));
     }
 };
 
@@ -152,16 +181,19 @@ struct SmemWords {
     __device__ uint32_t operator()(int i) const { return base[i]; }
 };
 
-// LEAF: this block's level-0 inputs are leaves of C; otherwise they are
-// digests in `in`.  The block reduces its 256 inputs through up to 4 levels
-// (stopping once the whole tree has one node) and writes its last node.
-template <bool LEAF>
-__global__ void __launch_bounds__(kHashThreads)
+// LEAF: this block's level-0 inputs are leaves of C; otherwise they are the
+// digests in `in` at tree depth `depth0`.  The block reduces its THREADS
+// inputs through up to LEVELS levels (stopping once the whole tree has one
+// node) and writes its last node.
+template <bool LEAF, int THREADS, int LEVELS>
+__global__ void __launch_bounds__(THREADS)
     hash_level_kernel(const float *__restrict__ C, int64_t M, int64_t N, int64_t ldc,
-                      const uint32_t *__restrict__ in, int64_t count, uint32_t *__restrict__ out) {
-    __shared__ uint32_t dig[2][kHashThreads][8];
+                      const uint32_t *__restrict__ in, int64_t count, uint32_t depth0,
+                      uint32_t *__restrict__ out) {
+    static_assert((1 << (2 * LEVELS)) == THREADS, "THREADS must be 4^LEVELS");
+    __shared__ uint32_t dig[2][THREADS][8];
     const int t = threadIdx.x;
-    const int64_t base = (int64_t)blockIdx.x * kHashThreads;
+    const int64_t base = (int64_t)blockIdx.x * THREADS;
     const int64_t idx = base + t;
     uint32_t h[8];
     if (idx < count) {
@@ -169,9 +201,27 @@ __global__ void __launch_bounds__(kHashThreads)
             const int64_t nfloat = M * N;
             const int64_t first = idx * kLeafFloats;
             const int64_t left = nfloat - first;
-            const int W = (int)(left < kLeafFloats ? (left > 0 ? left : 0) : kLeafFloats);
-            LeafWords lw{C, first, N, ldc, ldc == N};
-            sha256_prefixed(0x00u, W, lw, h);
+            const bool last = idx == count - 1;
+            if (left >= kLeafFloats && ldc == N) {
+                uint32_t w[64];
+                const uint4 *src = reinterpret_cast<const uint4 *>(C + first);
+                const bool vec = (reinterpret_cast<uintptr_t>(C + first) & 15) == 0;
+                if (vec) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const uint4 u = __ldg(src + j);
+                        w[4 * j] = u.x; w[4 * j + 1] = u.y; w[4 * j + 2] = u.z; w[4 * j + 3] = u.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) w[j] = __float_as_uint(__ldg(C + first + j));
+                }
+                b2s_leaf64(w, (uint64_t)idx, last, h);
+            } else {
+                const int W = (int)(left < kLeafFloats ? (left > 0 ? left : 0) : kLeafFloats);
+                LeafWords lw{C, first, N, ldc, ldc == N};
+                b2s_node(W, lw, (uint64_t)idx, 0u, last, h);
+            }
         } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) h[j] = in[idx * 8 + j];
@@ -182,19 +232,21 @@ __global__ void __launch_bounds__(kHashThreads)
     __syncthreads();
     int64_t n = count;       // nodes at the current level, whole tree
     int64_t lbase = base;    // index of this block's first node at this level
+    uint32_t depth = depth0;
     int cur = 0;
-    int64_t width = kHashThreads;
-    for (int level = 0; level < 4 && n > 1; ++level) {
+    int64_t width = THREADS;
+    for (int level = 0; level < LEVELS && n > 1; ++level) {
         const int64_t nn = (n + 3) / 4;
         const int64_t nbase = lbase / 4;
         width /= 4;
+        ++depth;
         if (t < width) {
             const int64_t node = nbase + t;
             if (node < nn) {
                 const int64_t first = node * 4;
                 const int g = (int)(n - first < 4 ? n - first : 4);
                 SmemWords sw{&dig[cur][first - lbase][0]};
-                sha256_prefixed(0x01u, 8 * g, sw, h);
+                b2s_node(8 * g, sw, (uint64_t)node, depth, node == nn - 1, h);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) dig[cur ^ 1][t][j] = h[j];
             }
@@ -208,15 +260,12 @@ __global__ void __launch_bounds__(kHashThreads)
     if (t < 8 && lbase < n) out[lbase * 8 + t] = dig[cur][0][t];
 }
 
+// The digest's bytes are its state words, little-endian.
 __global__ void digest_to_bytes_kernel(const uint32_t *__restrict__ d, uint8_t *__restrict__ out) {
     const int t = threadIdx.x;
-    if (t < 32) out[t] = (uint8_t)(d[t >> 2] >> (24 - 8 * (t & 3)));
+    if (t < 32) out[t] = (uint8_t)(d[t >> 2] >> (8 * (t & 3)));
 }
 
-int64_t levels_after(int64_t n) {
-    for (int l = 0; l < 4 && n > 1; ++l) n = (n + 3) / 4;
-    return n;
-}
 
 }  // namespace
 
@@ -236,27 +285,29 @@ static int64_t num_leaves(int64_t M, int64_t N) {
 }
 
 size_t hash_workspace_bytes(int64_t M, int64_t N) {
-    const int64_t n1 = (num_leaves(M, N) + kHashThreads - 1) / kHashThreads;
+    const int64_t n1 = (num_leaves(M, N) + kLeafThreads - 1) / kLeafThreads;
     return (size_t)round_up(2 * n1 * 32 + 64, 256);
 }
 
 cudaError_t launch_hash_f32(const float *C, int64_t M, int64_t N, int64_t ldc, uint8_t *out32,
                             void *ws, cudaStream_t st) {
     int64_t count = num_leaves(M, N);
-    const int64_t n1cap = (count + kHashThreads - 1) / kHashThreads;
+    const int64_t n1cap = (count + kLeafThreads - 1) / kLeafThreads;
     uint32_t *bufs[2] = {static_cast<uint32_t *>(ws), static_cast<uint32_t *>(ws) + n1cap * 8};
     int which = 0;
     int nlaunch = 2;  // leaves + digest bytes
-    int64_t blocks = (count + kHashThreads - 1) / kHashThreads;
-    hash_level_kernel<true><<<(int)blocks, kHashThreads, 0, st>>>(C, M, N, ldc, nullptr, count,
-                                                                   bufs[which]);
-    count = levels_after(count);
+    int64_t blocks = (count + kLeafThreads - 1) / kLeafThreads;
+    hash_level_kernel<true, kLeafThreads, 3><<<(int)blocks, kLeafThreads, 0, st>>>(
+        C, M, N, ldc, nullptr, count, 0u, bufs[which]);
+    // tree depth reached inside the leaf blocks
+    uint32_t depth = 0;
+    for (int l = 0; l < 3 && count > 1; ++l) count = (count + 3) / 4, ++depth;
     while (count > 1) {
-        blocks = (count + kHashThreads - 1) / kHashThreads;
-        hash_level_kernel<false><<<(int)blocks, kHashThreads, 0, st>>>(
-            nullptr, 0, 0, 0, bufs[which], count, bufs[which ^ 1]);
+        blocks = (count + kNodeThreads - 1) / kNodeThreads;
+        hash_level_kernel<false, kNodeThreads, 4><<<(int)blocks, kNodeThreads, 0, st>>>(
+            nullptr, 0, 0, 0, bufs[which], count, depth, bufs[which ^ 1]);
         which ^= 1;
-        count = levels_after(count);
+        for (int l = 0; l < 4 && count > 1; ++l) count = (count + 3) / 4, ++depth;
         ++nlaunch;
     }
     digest_to_bytes_kernel<<<1, 32, 0, st>>>(bufs[which], out32);

@@ -13,10 +13,14 @@
 // patterns (non-negative floats order like their bits; Inf/NaN show up as
 // >= 0x7f800000).  Columns take a partial-max pass over row slices and a
 // quantize pass over 64 x 64 tiles that also transposes for the GEMM.
+#include <cooperative_groups.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "bsg_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace bsg {
 namespace {
@@ -26,9 +30,33 @@ constexpr int kRowWarps = 8;  // rows per 256-thread block
 constexpr int kRowRegVec = 8; // float4 per lane kept in registers: rows up to 1024
 
 // Scale and reciprocal of one row or column from its absmax bit pattern.
+//
+// The definition is f64: scale = RN32(max(RN64(m / 127), RN64(1e-8))) and
+// inv = RN32(RN64(1 / scale)).  GB300's FP64 pipe is far too slow for a
+// divide per row, and two IEEE f32 divides give the same bits:
+//   * RN32(RN64(x)) differs from RN32(x) only if RN64(x) lands exactly on a
+//     midpoint of the f32 grid.  For x = m/127 with m = M 2^E (M a 24-bit
+//     integer) x is either exact (127 | M) or at least 1/(127 2^u) from any
+//     25-bit dyadic p/2^u -- a relative gap near 2^-32, far wider than the
+//     2^-53 an f64 rounding can close.  For y = 1/scale with scale = S 2^F,
+//     |1/S - k 2^-48| >= 1/(S 2^48): a relative gap >= 2^-48, again wider
+//     than 2^-53 (y is exact when S is a power of two).  So the f64 step is
+//     invisible and each value is one correctly rounded f32 divide.
+//   * The floor: max commutes with the monotone RN32, and f64(1e-8) sits
+//     0.07 ulp from its f32 rounding, so max(RN32(m/127), f32(f64(1e-8)))
+//     equals the f64 definition, ties at the boundary included.
+// The derivation is checked exhaustively against the f64 definition by
+// bsg_selftest_scales and against the CPU oracle by the tests.
+constexpr uint32_t kScaleFloorBits = 0x322bcc77u;  // RN32(RN64(1e-8))
+
 __device__ __forceinline__ void scale_from_max(uint32_t mbits, float &scale, float &inv) {
-    const double m = static_cast<double>(__uint_as_float(mbits));
-    double s = __ddiv_rn(m, 127.0);
+    scale = fmaxf(__fdiv_rn(__uint_as_float(mbits), 127.0f), __uint_as_float(kScaleFloorBits));
+    inv = __fdiv_rn(1.0f, scale);
+}
+
+// The f64 definition itself, for the self-test only.
+__device__ __forceinline__ void scale_from_max_f64(uint32_t mbits, float &scale, float &inv) {
+    double s = __ddiv_rn(static_cast<double>(__uint_as_float(mbits)), 127.0);
     if (s < 1e-8) s = 1e-8;
     scale = __double2float_rn(s);
     inv = __double2float_rn(__ddiv_rn(1.0, static_cast<double>(scale)));
@@ -138,54 +166,105 @@ __global__ void __launch_bounds__(kRowWarps * 32)
     }
 }
 
-// Partial column max over a slice of rows: block = 64 columns x 4 row lanes.
+// Column quantize, pass 1: partial |x| maxima of 128-column groups over
+// slices of rows.  Block = 32 column lanes (VW columns each) x 8 row lanes;
+// each thread keeps 4 row loads in flight.
+constexpr int kColLanes = 32;
+constexpr int kColRows = 8;
+
+template <int VW>
 __global__ void __launch_bounds__(256)
     colmax_partial_kernel(const float *__restrict__ X, int64_t rows, int64_t cols, int64_t ldx,
                           int64_t rows_per_split, uint32_t *__restrict__ partial) {
-    __shared__ uint32_t red[4][64];
-    const int cc = threadIdx.x & 63;
-    const int rg = threadIdx.x >> 6;
-    const int64_t col = (int64_t)blockIdx.x * 64 + cc;
+    __shared__ uint32_t red[kColRows][kColLanes * VW];
+    const int cl = threadIdx.x % kColLanes;
+    const int rg = threadIdx.x / kColLanes;
+    const int64_t col = (int64_t)blockIdx.x * (kColLanes * VW) + cl * VW;
     const int64_t r0 = (int64_t)blockIdx.y * rows_per_split;
     const int64_t r1 = min(rows, r0 + rows_per_split);
-    uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
+    uint32_t m[VW];
+#pragma unroll
+    for (int v = 0; v < VW; ++v) m[v] = 0;
     if (col < cols) {
         int64_t r = r0 + rg;
-        for (; r + 12 < r1; r += 16) {
-            m0 = max(m0, absbits(__ldg(X + r * ldx + col)));
-            m1 = max(m1, absbits(__ldg(X + (r + 4) * ldx + col)));
-            m2 = max(m2, absbits(__ldg(X + (r + 8) * ldx + col)));
-            m3 = max(m3, absbits(__ldg(X + (r + 12) * ldx + col)));
+        if (VW == 4) {
+            for (; r + 3 * kColRows < r1; r += 4 * kColRows) {
+                float4 t[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    t[u] = __ldg(reinterpret_cast<const float4 *>(X + (r + u * kColRows) * ldx + col));
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    m[0] = max(m[0], absbits(t[u].x));
+                    m[VW > 1 ? 1 : 0] = max(m[VW > 1 ? 1 : 0], absbits(t[u].y));
+                    m[VW > 2 ? 2 : 0] = max(m[VW > 2 ? 2 : 0], absbits(t[u].z));
+                    m[VW > 3 ? 3 : 0] = max(m[VW > 3 ? 3 : 0], absbits(t[u].w));
+                }
+            }
+            for (; r < r1; r += kColRows) {
+                const float4 t = __ldg(reinterpret_cast<const float4 *>(X + r * ldx + col));
+                m[0] = max(m[0], absbits(t.x));
+                m[VW > 1 ? 1 : 0] = max(m[VW > 1 ? 1 : 0], absbits(t.y));
+                m[VW > 2 ? 2 : 0] = max(m[VW > 2 ? 2 : 0], absbits(t.z));
+                m[VW > 3 ? 3 : 0] = max(m[VW > 3 ? 3 : 0], absbits(t.w));
+            }
+        } else {
+            for (; r + 3 * kColRows < r1; r += 4 * kColRows) {
+                float t[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) t[u] = __ldg(X + (r + u * kColRows) * ldx + col);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) m[0] = max(m[0], absbits(t[u]));
+            }
+            for (; r < r1; r += kColRows) m[0] = max(m[0], absbits(__ldg(X + r * ldx + col)));
         }
-        for (; r < r1; r += 4) m0 = max(m0, absbits(__ldg(X + r * ldx + col)));
     }
-    red[rg][cc] = max(max(m0, m1), max(m2, m3));
+#pragma unroll
+    for (int v = 0; v < VW; ++v) red[rg][cl * VW + v] = m[v];
     __syncthreads();
-    if (rg == 0 && col < cols)
-        partial[(int64_t)blockIdx.y * cols + col] =
-            max(max(red[0][cc], red[1][cc]), max(red[2][cc], red[3][cc]));
+    for (int c = threadIdx.x; c < kColLanes * VW; c += blockDim.x) {
+        const int64_t gc = (int64_t)blockIdx.x * (kColLanes * VW) + c;
+        if (gc < cols) {
+            uint32_t mm = red[0][c];
+#pragma unroll
+            for (int g = 1; g < kColRows; ++g) mm = max(mm, red[g][c]);
+            partial[(int64_t)blockIdx.y * cols + gc] = mm;
+        }
+    }
 }
 
-// Quantize a 64 x 64 tile of X with per-column scales (from the partial
-// maxima).  kOutInt8 writes Q in X's layout; kOutHalfKMajor writes the
-// transposed tile, Q[col][row], as f16.
-template <int OUT>
+// Column quantize, pass 2: a 64-row x (32 * VW)-column tile with per-column
+// scales from the partial maxima (at most kMaxSplit of them).  kOutInt8
+// writes Q in X's layout; kOutHalfKMajor writes the transposed tile,
+// Q[col][row], as f16 rows of 64 halves.
+constexpr int kMaxSplit = 32;
+
+template <int OUT, int VW>
 __global__ void __launch_bounds__(256)
     quantize_cols_kernel(const float *__restrict__ X, int64_t rows, int64_t cols, int64_t ldx,
                          const uint32_t *__restrict__ partial, int nsplit, void *__restrict__ Q,
                          int64_t ldq, float *__restrict__ scale, float *__restrict__ inv,
                          int32_t *__restrict__ dstatus) {
-    __shared__ float s_inv[64];
-    __shared__ __align__(16) __half tile[64][64 + 8];
+    constexpr int TC = kColLanes * VW;  // tile columns
+    __shared__ float s_inv[TC];
+    __shared__ __align__(16) __half tile[OUT == kOutHalfKMajor ? TC : 1][64 + 8];
     const int t = threadIdx.x;
-    const int64_t c0 = (int64_t)blockIdx.x * 64;
+    const int64_t c0 = (int64_t)blockIdx.x * TC;
     const int64_t r0 = (int64_t)blockIdx.y * 64;
-    if (t < 64) {
-        const int64_t col = c0 + t;
+    for (int c = t; c < TC; c += blockDim.x) {
+        const int64_t col = c0 + c;
         float iv = 0.f;
         if (col < cols) {
-            uint32_t m = 0;
-            for (int s = 0; s < nsplit; ++s) m = max(m, partial[(int64_t)s * cols + col]);
+            uint32_t mm[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mm[u] = 0;
+            for (int s = 0; s < nsplit; s += 8) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (s + u < nsplit) mm[u] = max(mm[u], partial[(int64_t)(s + u) * cols + col]);
+            }
+            uint32_t m = max(max(max(mm[0], mm[1]), max(mm[2], mm[3])),
+                             max(max(mm[4], mm[5]), max(mm[6], mm[7])));
             float sc;
             scale_from_max(m, sc, iv);
             if (blockIdx.y == 0) {
@@ -194,39 +273,223 @@ __global__ void __launch_bounds__(256)
                 if (m >= kNonfiniteBits && dstatus) atomicOr(dstatus, 1);
             }
         }
-        s_inv[t] = iv;
+        s_inv[c] = iv;
     }
     __syncthreads();
-    const int cc = t & 63;
-    const int rg = t >> 6;
-    const int64_t col = c0 + cc;
-    const float iv = s_inv[cc];
-#pragma unroll 4
-    for (int i = 0; i < 16; ++i) {
-        const int rr = rg + 4 * i;
-        const int64_t row = r0 + rr;
+    const int cl = t % kColLanes;
+    const int rg = t / kColLanes;
+    const int64_t col = c0 + cl * VW;
+    float ivv[VW];
+#pragma unroll
+    for (int v = 0; v < VW; ++v) ivv[v] = s_inv[cl * VW + v];
+    float x[8][VW];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t row = r0 + rg + kColRows * i;
         const bool ok = row < rows && col < cols;
-        const float q = ok ? quant(__ldg(X + row * ldx + col), iv) : 0.0f;
-        if (OUT == kOutInt8) {
-            if (ok) static_cast<int8_t *>(Q)[row * ldq + col] = (int8_t)(int)q;
+        if (VW == 4) {
+            float4 v4 = ok ? __ldg(reinterpret_cast<const float4 *>(X + row * ldx + col))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            x[i][0] = v4.x;
+            x[i][VW > 1 ? 1 : 0] = v4.y;
+            x[i][VW > 2 ? 2 : 0] = v4.z;
+            x[i][VW > 3 ? 3 : 0] = v4.w;
         } else {
-            tile[cc][rr] = __float2half_rn(q);
+            x[i][0] = ok ? __ldg(X + row * ldx + col) : 0.f;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int rr = rg + kColRows * i;
+        const int64_t row = r0 + rr;
+        if (OUT == kOutInt8) {
+            if (row < rows && col < cols) {
+                if (VW == 4) {
+                    const char4 q = make_char4((signed char)(int)quant(x[i][0], ivv[0]),
+                                               (signed char)(int)quant(x[i][VW > 1 ? 1 : 0], ivv[VW > 1 ? 1 : 0]),
+                                               (signed char)(int)quant(x[i][VW > 2 ? 2 : 0], ivv[VW > 2 ? 2 : 0]),
+                                               (signed char)(int)quant(x[i][VW > 3 ? 3 : 0], ivv[VW > 3 ? 3 : 0]));
+                    *reinterpret_cast<char4 *>(static_cast<int8_t *>(Q) + row * ldq + col) = q;
+                } else {
+                    static_cast<int8_t *>(Q)[row * ldq + col] = (int8_t)(int)quant(x[i][0], ivv[0]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int v = 0; v < VW; ++v) tile[cl * VW + v][rr] = __float2half_rn(quant(x[i][v], ivv[v]));
         }
     }
     if (OUT == kOutHalfKMajor) {
         __syncthreads();
-        // 64 output rows (columns of X) x 64 halves (128 bytes) each.
-        const int j = t >> 2;      // output row within the tile
-        const int part = t & 3;    // 16 halves each
-        const int64_t orow = c0 + j;
-        if (orow < cols) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(&tile[j][part * 16]);
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(Q) + orow * ldq + r0 +
-                                                   part * 16);
-            dst[0] = src[0];
-            dst[1] = src[1];
+        // TC output rows (columns of X) of 64 halves (128 bytes): 8 threads per row.
+        for (int idx = t; idx < TC * 8; idx += blockDim.x) {
+            const int j = idx >> 3;
+            const int part = idx & 7;
+            const int64_t orow = c0 + j;
+            if (orow < cols) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(&tile[j][part * 8]);
+                *reinterpret_cast<uint4 *>(static_cast<__half *>(Q) + orow * ldq + r0 + part * 8) = v;
+            }
         }
     }
+}
+
+// Rows, single pass: WPR warps share a row and each lane keeps RV float4 of
+// it in registers (rows up to 128 * RV * WPR elements), so the row is read
+// once, reduced (shuffles, then shared memory across the row's warps) and
+// quantized from registers.  8 warps per block: 8 / WPR rows per block.
+template <int OUT, int WPR, int RV>
+__global__ void __launch_bounds__(256)
+    quantize_rows_wide_kernel(const float *__restrict__ X, int64_t rows, int64_t cols,
+                              int64_t ldx, void *__restrict__ Q, int64_t ldq,
+                              float *__restrict__ scale, float *__restrict__ inv,
+                              int32_t *__restrict__ dstatus) {
+    constexpr int RPB = 8 / WPR;
+    __shared__ uint32_t red[8];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rloc = warp / WPR;
+    const int wr = warp % WPR;
+    const int64_t r = (int64_t)blockIdx.x * RPB + rloc;
+    const bool live = r < rows;
+    const int64_t c4n = cols / 4;
+    const float4 *xr = reinterpret_cast<const float4 *>(X + (live ? r : 0) * ldx);
+    float4 v[RV];
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < RV; ++i) {
+        const int64_t c4 = lane + 32 * (i + RV * wr);
+        if (live && c4 < c4n) {
+            v[i] = __ldcs(xr + c4);
+            m = max(m, max(max(absbits(v[i].x), absbits(v[i].y)), max(absbits(v[i].z), absbits(v[i].w))));
+        } else {
+            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    m = __reduce_max_sync(0xffffffffu, m);
+    if (WPR > 1) {
+        if (lane == 0) red[warp] = m;
+        __syncthreads();
+        m = 0;
+#pragma unroll
+        for (int w = 0; w < WPR; ++w) m = max(m, red[rloc * WPR + w]);
+    }
+    float sc, iv;
+    scale_from_max(m, sc, iv);
+    if (!live) return;
+    if (wr == 0 && lane == 0) {
+        scale[r] = sc;
+        if (inv) inv[r] = iv;
+        if (m >= kNonfiniteBits && dstatus) atomicOr(dstatus, 1);
+    }
+#pragma unroll
+    for (int i = 0; i < RV; ++i) {
+        const int64_t c4 = lane + 32 * (i + RV * wr);
+        if (c4 < c4n)
+            store4<OUT>(Q, r * ldq + 4 * c4, quant(v[i].x, iv), quant(v[i].y, iv), quant(v[i].z, iv),
+                        quant(v[i].w, iv));
+    }
+}
+
+// Columns, single pass: a cluster of CS CTAs shares a strip of 32 columns;
+// CTA `rank` stages rows [rank * R, rank * R + R) of the strip in shared
+// memory (one HBM read), the CTAs exchange their partial |x| maxima through
+// distributed shared memory, and each quantizes its rows from shared memory.
+// kOutHalfKMajor writes the transposed strip (Q[col][row], f16) through a
+// shared-memory transpose; kOutInt8 writes Q in X's layout.
+constexpr int kStripCols = 32;
+
+template <int OUT>
+__global__ void __launch_bounds__(256)
+    quantize_cols_cluster_kernel(const float *__restrict__ X, int64_t rows, int64_t cols,
+                                 int64_t ldx, int R, int vec, void *__restrict__ Q, int64_t ldq,
+                                 float *__restrict__ scale, float *__restrict__ inv,
+                                 int32_t *__restrict__ dstatus) {
+    extern __shared__ __align__(16) uint8_t dsm[];
+    float *xs = reinterpret_cast<float *>(dsm);                           // [R][32]
+    __half *ts = reinterpret_cast<__half *>(dsm + (size_t)R * kStripCols * 4);  // [32][R + 2]
+    const int tstride = R + 2;
+    __shared__ uint32_t red[8][kStripCols];
+    __shared__ uint32_t part[kStripCols];
+    __shared__ float s_inv[kStripCols];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int cs = (int)cluster.num_blocks();
+    const int t = threadIdx.x;
+    const int64_t c0 = (int64_t)blockIdx.x * kStripCols;
+    const int64_t r0 = (int64_t)rank * R;
+    const int64_t left = rows - r0;
+    const int nr = left <= 0 ? 0 : (left < R ? (int)left : R);
+
+    // stage the block: 8 chunks of 16 bytes per row
+    for (int q = t; q < nr * 8; q += blockDim.x) {
+        const int row = q >> 3, c4 = q & 7;
+        const int64_t col = c0 + 4 * c4;
+        float *dst = xs + row * kStripCols + 4 * c4;
+        const float *src = X + (r0 + row) * ldx + col;
+        if (vec && col + 3 < cols) {
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                             static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                         "l"(src)
+                         : "memory");
+        } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) dst[u] = (col + u < cols) ? __ldg(src + u) : 0.0f;
+        }
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+
+    // partial column max over this CTA's rows
+    const int c = t & 31, g = t >> 5;
+    uint32_t m = 0;
+    for (int row = g; row < nr; row += 8) m = max(m, absbits(xs[row * kStripCols + c]));
+    red[g][c] = m;
+    __syncthreads();
+    if (t < kStripCols) {
+        uint32_t mm = red[0][t];
+#pragma unroll
+        for (int gg = 1; gg < 8; ++gg) mm = max(mm, red[gg][t]);
+        part[t] = mm;
+    }
+    cluster.sync();  // every CTA's partial maxima are visible cluster-wide
+    if (t < kStripCols) {
+        uint32_t mm = 0;
+        for (int rk = 0; rk < cs; ++rk) mm = max(mm, *cluster.map_shared_rank(&part[t], rk));
+        float sc, iv;
+        scale_from_max(mm, sc, iv);
+        s_inv[t] = iv;
+        if (rank == 0 && c0 + t < cols) {
+            scale[c0 + t] = sc;
+            if (inv) inv[c0 + t] = iv;
+            if (mm >= kNonfiniteBits && dstatus) atomicOr(dstatus, 1);
+        }
+    }
+    __syncthreads();
+    const float iv = s_inv[c];
+    if (OUT == kOutInt8) {
+        if (c0 + c < cols)
+            for (int row = g; row < nr; row += 8)
+                static_cast<int8_t *>(Q)[(r0 + row) * ldq + c0 + c] =
+                    (int8_t)(int)quant(xs[row * kStripCols + c], iv);
+    } else {
+        for (int row = g; row < nr; row += 8)
+            ts[c * tstride + row] = __float2half_rn(quant(xs[row * kStripCols + c], iv));
+        __syncthreads();
+        // 32 output rows (columns of X), nr halves each, from row r0: one
+        // warp per output row at a time, 4-byte pairs, coalesced.
+        const int w = t >> 5, lane = t & 31;
+        const int pairs = nr >> 1;
+        for (int n = w; n < kStripCols; n += 8) {
+            if (c0 + n >= cols) continue;
+            __half *dst = static_cast<__half *>(Q) + (c0 + n) * ldq + r0;
+            const __half *src = ts + n * tstride;
+            for (int k2 = lane; k2 < pairs; k2 += 32)
+                reinterpret_cast<uint32_t *>(dst)[k2] = reinterpret_cast<const uint32_t *>(src)[k2];
+            if ((nr & 1) && lane == 0) dst[nr - 1] = src[nr - 1];
+        }
+    }
+    cluster.sync();  // no CTA leaves while another may still read its maxima
 }
 
 __global__ void i8_rows_to_half_kernel(const int8_t *__restrict__ Q, int64_t rows, int64_t cols,
@@ -260,15 +523,46 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Compare the f32 derivation with the f64 definition for every absmax bit
+// pattern in [first, last]; count the mismatches.
+__global__ void selftest_scales_kernel(uint32_t first, uint32_t last,
+                                       unsigned long long *__restrict__ bad) {
+    unsigned long long local = 0;
+    const uint64_t n = (uint64_t)last - first + 1;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (uint64_t)gridDim.x * blockDim.x) {
+        const uint32_t m = first + (uint32_t)i;
+        float s1, i1, s2, i2;
+        scale_from_max(m, s1, i1);
+        scale_from_max_f64(m, s2, i2);
+        if (__float_as_uint(s1) != __float_as_uint(s2) || __float_as_uint(i1) != __float_as_uint(i2))
+            ++local;
+    }
+    if (local) atomicAdd(bad, local);
+}
+
 }  // namespace
 
-int colmax_nsplit(int64_t rows) {
-    const int64_t s = (rows + 127) / 128;
-    return (int)(s < 1 ? 1 : (s > 256 ? 256 : s));
+cudaError_t launch_selftest_scales(uint32_t first, uint32_t last, unsigned long long *bad,
+                                   cudaStream_t st) {
+    selftest_scales_kernel<<<device_sm_count() * 8, 256, 0, st>>>(first, last, bad);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// Row slices of the column absmax: enough blocks to fill the GPU, at most
+// kMaxSplit (the quantize pass reads them all), at least 8 rows each.
+int colmax_nsplit(int64_t rows, int64_t cols) {
+    const int64_t groups = (cols + 127) / 128;
+    int64_t s = (1216 + groups - 1) / groups;
+    const int64_t cap_rows = (rows + 7) / 8;
+    if (s > cap_rows) s = cap_rows;
+    if (s > kMaxSplit) s = kMaxSplit;
+    return (int)(s < 1 ? 1 : s);
 }
 
 size_t colmax_partial_bytes(int64_t rows, int64_t cols) {
-    return (size_t)colmax_nsplit(rows) * (size_t)cols * sizeof(uint32_t);
+    return (size_t)colmax_nsplit(rows, cols) * (size_t)cols * sizeof(uint32_t);
 }
 
 static int grid_for(int64_t work, int per_block) {
@@ -277,23 +571,73 @@ static int grid_for(int64_t work, int per_block) {
     return (int)(b < 1 ? 1 : (b > cap ? cap : b));
 }
 
+template <int OUT, int WPR, int RV>
+static void launch_rows_wide(const float *X, int64_t rows, int64_t cols, int64_t ldx, void *Q,
+                             int64_t ldq, float *scale, float *inv, int32_t *dstatus,
+                             cudaStream_t st) {
+    constexpr int RPB = 8 / WPR;
+    const int64_t blocks = (rows + RPB - 1) / RPB;
+    quantize_rows_wide_kernel<OUT, WPR, RV><<<(unsigned)blocks, 256, 0, st>>>(
+        X, rows, cols, ldx, Q, ldq, scale, inv, dstatus);
+}
+
+// Smallest single-pass layout (warps per row, float4 per lane) that holds a
+// row of `cols` elements; -1 when the row is too long.
+static int row_layout(int64_t cols) {
+    static const int cap[9] = {256, 512, 768, 1024, 2048, 3072, 4096, 8192, 16384};
+    for (int i = 0; i < 9; ++i)
+        if (cols <= cap[i]) return i;
+    return -1;
+}
+
+template <int OUT>
+static bool dispatch_rows_wide(int layout, const float *X, int64_t rows, int64_t cols,
+                               int64_t ldx, void *Q, int64_t ldq, float *scale, float *inv,
+                               int32_t *dstatus, cudaStream_t st) {
+    switch (layout) {
+        case 0: launch_rows_wide<OUT, 1, 2>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
+        case 1: launch_rows_wide<OUT, 1, 4>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
+        case 2: launch_rows_wide<OUT, 1, 6>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
+        case 3: launch_rows_wide<OUT, 1, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
+        case 4: launch_rows_wide<OUT, 2, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
+        case 5: launch_rows_wide<OUT, 4, 6>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
+        case 6: launch_rows_wide<OUT, 4, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
+        case 7: launch_rows_wide<OUT, 8, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
+        case 8: launch_rows_wide<OUT, 8, 16>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
+    }
+    return false;
+}
+
 cudaError_t launch_quantize_rows(const float *X, int64_t rows, int64_t cols, int64_t ldx,
                                  int out_kind, void *Q, int64_t ldq, float *scale, float *inv,
                                  int32_t *dstatus, cudaStream_t st) {
-    const int grid = grid_for(rows, kRowWarps);
     const size_t qalign = out_kind == kOutInt8 ? 4 : 8;
     const size_t qesz = out_kind == kOutInt8 ? 1 : 2;
-    const bool vec = (ldx % 4 == 0) && (reinterpret_cast<uintptr_t>(X) % 16 == 0) &&
-                     ((ldq * qesz) % qalign == 0) && (reinterpret_cast<uintptr_t>(Q) % qalign == 0);
+    const bool vec = (cols % 4 == 0) && (ldx % 4 == 0) &&
+                     (reinterpret_cast<uintptr_t>(X) % 16 == 0) && ((ldq * qesz) % qalign == 0) &&
+                     (reinterpret_cast<uintptr_t>(Q) % qalign == 0);
+    const int layout = vec ? row_layout(cols) : -1;
+    if (layout >= 0) {
+        if (out_kind == kOutInt8)
+            dispatch_rows_wide<kOutInt8>(layout, X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st);
+        else
+            dispatch_rows_wide<kOutHalfKMajor>(layout, X, rows, cols, ldx, Q, ldq, scale, inv, dstatus,
+                                              st);
+        count_launches(1);
+        return cudaGetLastError();
+    }
+    const int grid = grid_for(rows, kRowWarps);
+    const bool vec2 = (ldx % 4 == 0) && (reinterpret_cast<uintptr_t>(X) % 16 == 0) &&
+                      ((ldq * qesz) % qalign == 0) && (reinterpret_cast<uintptr_t>(Q) % qalign == 0);
     if (out_kind == kOutInt8) {
-        if (vec)
+        if (vec2)
             quantize_rows_kernel<kOutInt8, true><<<grid, kRowWarps * 32, 0, st>>>(
                 X, rows, cols, ldx, Q, ldq, scale, inv, dstatus);
         else
             quantize_rows_kernel<kOutInt8, false><<<grid, kRowWarps * 32, 0, st>>>(
                 X, rows, cols, ldx, Q, ldq, scale, inv, dstatus);
     } else {
-        if (vec)
+        if (vec2)
             quantize_rows_kernel<kOutHalfKMajor, true><<<grid, kRowWarps * 32, 0, st>>>(
                 X, rows, cols, ldx, Q, ldq, scale, inv, dstatus);
         else
@@ -304,20 +648,98 @@ cudaError_t launch_quantize_rows(const float *X, int64_t rows, int64_t cols, int
     return cudaGetLastError();
 }
 
+// Cluster shape of the single-pass column quantize: CS CTAs of R rows each
+// (R a multiple of 8, at most 1024), enough CTAs to cover the SMs twice.
+// Returns false when the columns are too long for one pass.
+static bool cols_cluster_shape(int64_t rows, int64_t cols, int &cs, int &R) {
+    const int64_t strips = (cols + kStripCols - 1) / kStripCols;
+    int64_t c = (2 * (int64_t)device_sm_count() + strips - 1) / strips;
+    const int64_t by_rows = (rows + 255) / 256;  // keep a CTA at or under 256 rows when possible
+    if (c < by_rows) c = by_rows;
+    if (c > 8) c = 8;
+    if (c < 1) c = 1;
+    int64_t r = (rows + c - 1) / c;
+    r = (r + 7) / 8 * 8;
+    if (r > 1024) return false;
+    cs = (int)c;
+    R = (int)r;
+    return true;
+}
+
+static size_t cols_cluster_smem(int R) {
+    return (size_t)R * kStripCols * 4 + (size_t)kStripCols * (R + 2) * 2 + 16;
+}
+
+template <int OUT>
+static cudaError_t launch_cols_cluster(const float *X, int64_t rows, int64_t cols, int64_t ldx,
+                                       int cs, int R, void *Q, int64_t ldq, float *scale,
+                                       float *inv, int32_t *dstatus, cudaStream_t st) {
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(quantize_cols_cluster_kernel<OUT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)cols_cluster_smem(1024));
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const int vec = (ldx % 4 == 0) && (reinterpret_cast<uintptr_t>(X) % 16 == 0);
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)((cols + kStripCols - 1) / kStripCols), (unsigned)cs, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = cols_cluster_smem(R);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)cs;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quantize_cols_cluster_kernel<OUT>, X, rows, cols, ldx, R, vec,
+                              Q, ldq, scale, inv, dstatus);
+}
+
 cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int64_t ldx,
                                  int out_kind, void *Q, int64_t ldq, float *scale, float *inv,
                                  uint32_t *partial, int32_t *dstatus, cudaStream_t st) {
-    const int nsplit = colmax_nsplit(rows);
+    int cs = 0, R = 0;
+    if (cols_cluster_shape(rows, cols, cs, R)) {
+        cudaError_t e = out_kind == kOutInt8
+                            ? launch_cols_cluster<kOutInt8>(X, rows, cols, ldx, cs, R, Q, ldq, scale,
+                                                            inv, dstatus, st)
+                            : launch_cols_cluster<kOutHalfKMajor>(X, rows, cols, ldx, cs, R, Q, ldq,
+                                                                  scale, inv, dstatus, st);
+        count_launches(1);
+        return e;
+    }
+    const int nsplit = colmax_nsplit(rows, cols);
     const int64_t rps = (rows + nsplit - 1) / nsplit;
-    dim3 g1((unsigned)((cols + 63) / 64), (unsigned)nsplit);
-    colmax_partial_kernel<<<g1, 256, 0, st>>>(X, rows, cols, ldx, rps, partial);
-    dim3 g2((unsigned)((cols + 63) / 64), (unsigned)((rows + 63) / 64));
-    if (out_kind == kOutInt8)
-        quantize_cols_kernel<kOutInt8><<<g2, 256, 0, st>>>(X, rows, cols, ldx, partial, nsplit, Q,
-                                                           ldq, scale, inv, dstatus);
-    else
-        quantize_cols_kernel<kOutHalfKMajor><<<g2, 256, 0, st>>>(
-            X, rows, cols, ldx, partial, nsplit, Q, ldq, scale, inv, dstatus);
+    const bool vec = (cols % 4 == 0) && (ldx % 4 == 0) &&
+                     (reinterpret_cast<uintptr_t>(X) % 16 == 0) &&
+                     (out_kind != kOutInt8 || ((ldq % 4 == 0) && reinterpret_cast<uintptr_t>(Q) % 4 == 0));
+    const int vw = vec ? 4 : 1;
+    const unsigned gx = (unsigned)((cols + 32 * vw - 1) / (32 * vw));
+    dim3 g1(gx, (unsigned)nsplit), g2(gx, (unsigned)((rows + 63) / 64));
+    if (vec) {
+        colmax_partial_kernel<4><<<g1, 256, 0, st>>>(X, rows, cols, ldx, rps, partial);
+        if (out_kind == kOutInt8)
+            quantize_cols_kernel<kOutInt8, 4><<<g2, 256, 0, st>>>(X, rows, cols, ldx, partial, nsplit,
+                                                                 Q, ldq, scale, inv, dstatus);
+        else
+            quantize_cols_kernel<kOutHalfKMajor, 4><<<g2, 256, 0, st>>>(
+                X, rows, cols, ldx, partial, nsplit, Q, ldq, scale, inv, dstatus);
+    } else {
+        colmax_partial_kernel<1><<<g1, 256, 0, st>>>(X, rows, cols, ldx, rps, partial);
+        if (out_kind == kOutInt8)
+            quantize_cols_kernel<kOutInt8, 1><<<g2, 256, 0, st>>>(X, rows, cols, ldx, partial, nsplit,
+                                                                 Q, ldq, scale, inv, dstatus);
+        else
+            quantize_cols_kernel<kOutHalfKMajor, 1><<<g2, 256, 0, st>>>(
+                X, rows, cols, ldx, partial, nsplit, Q, ldq, scale, inv, dstatus);
+    }
     count_launches(2);
     return cudaGetLastError();
 }
