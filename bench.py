@@ -281,13 +281,9 @@ def run_gpu(args, rank, world, local_rank):
     barrier()
     e2e_ms = statistics.mean(e2e_times) * 1e3
 
-    # ---- max over ranks
-    t_local = torch.tensor([ms_per_step, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
-    ms_max, e2e_max = float(t_local[0]), float(t_local[1])
-
-    # ---- probe agreement across replicas (the pages' cross-device check)
+    # ---- max over ranks, and the replicas' probe hashes (the pages' cross-device check)
+    from verifiable_quantize_rows_gb300.replicas import max_over_ranks, probe_hashes_agree
+    ms_max, e2e_max = max_over_ranks([ms_per_step, e2e_ms], device=dev)
     golden = None
     gpath = os.path.join(ROOT, "tests", "golden", "probe_hash.txt")
     if os.path.exists(gpath):
@@ -295,12 +291,7 @@ def run_gpu(args, rank, world, local_rank):
             p = line.split()
             if len(p) == 5 and p[:4] == [str(PROBE_SEED), *map(str, PROBE)]:
                 golden = p[4]
-    replicas_agree = True
-    if world > 1:
-        mine = torch.tensor(list(probe_out.cpu().tolist()), dtype=torch.int32, device=dev)
-        allh = [torch.empty_like(mine) for _ in range(world)]
-        dist.all_gather(allh, mine)
-        replicas_agree = all(torch.equal(allh[0], h) for h in allh)
+    replicas_agree, _ = probe_hashes_agree(bytes.fromhex(probe_hex), device=dev)
     torch.cuda.synchronize()
     dstat = int(dstatus.item())
 
