@@ -65,6 +65,7 @@ cudaError_t launch_i8_cols_to_half(const int8_t *Q, int64_t rows, int64_t cols, 
 // round_up(N, kBN) floats (mode 0).
 // The tile width (64, 128 or 256) the GEMM uses for an M x N problem.
 int gemm_tile_width(int64_t M, int64_t N, int sms);
+int gemm_cluster_size();
 cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int64_t N,
                            int64_t K, const float *sa, const float *sb, int relu, int mode,
                            void *out, int64_t ldo, int32_t *dstatus, cudaStream_t st);

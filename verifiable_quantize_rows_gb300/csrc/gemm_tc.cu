@@ -40,6 +40,7 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -82,24 +83,28 @@ struct Params {
     int M, N, K;
     int num_kb;        // k-blocks per tile
     int num_m, num_n;  // tiles
-    int num_tiles;
+    int num_mp;        // groups of CL m-tiles (one per cluster tile)
+    int num_gtiles;    // cluster tiles: num_mp * num_n
     const float *sa;
     const float *sb;
     void *out;
     int64_t ldo;
     int mode;       // 0: f32 epilogue, 1: int32 accumulators
     int relu;
-    int tma_store;  // 1: C/S rows are 16-byte aligned; store through tmap_c
+    int tma_store;  // 1: C's rows are 16-byte aligned; store through tmap_c
+    int cluster;    // 1, or 2: pairs of m-tiles share B through TMA multicast
     int32_t *dstatus;
 };
 
-__host__ __device__ __forceinline__ void tile_coords(const Params &p, int t, int &mb, int &nb) {
+// Cluster tile gt -> (m-group, n-tile), rastered in groups of kGroupM
+// m-groups so that concurrent tiles share operand rows and columns in L2.
+__host__ __device__ __forceinline__ void tile_coords(const Params &p, int gt, int &mp, int &nb) {
     const int per_group = kGroupM * p.num_n;
-    const int g = t / per_group;
+    const int g = gt / per_group;
     const int first_m = g * kGroupM;
-    const int gm = (p.num_m - first_m) < kGroupM ? (p.num_m - first_m) : kGroupM;
-    const int r = t - g * per_group;
-    mb = first_m + r % gm;
+    const int gm = (p.num_mp - first_m) < kGroupM ? (p.num_mp - first_m) : kGroupM;
+    const int r = gt - g * per_group;
+    mp = first_m + r % gm;
     nb = r / gm;
 }
 
@@ -149,7 +154,10 @@ __device__ __forceinline__ void emit_box(const Params &p, const CUtensorMap *tma
     }
 }
 
-template <int BN>
+// CL CTAs of a cluster take CL consecutive m-tiles of one n-tile and share
+// its B tile: each loads BN/CL rows of it and multicasts them to all, and a
+// stage is refilled only after every CTA's MMAs have finished with it.
+template <int BN, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
@@ -171,11 +179,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int num_chunks = (p.num_kb + kChunkBlocks - 1) / kChunkBlocks;
+    const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
+    const int cid = blockIdx.x / CL;
+    const int ncl = gridDim.x / CL;
+    constexpr uint16_t kMask = (uint16_t)((1u << CL) - 1u);
+    constexpr int kBoxB = BN / CL;  // B rows each CTA loads
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < K::kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], CL);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
@@ -192,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (CL > 1) cluster_sync_all();  // every CTA's barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem_base = *tmem_ptr;
 
@@ -206,9 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool issued[K::kStages];
             for (int s = 0; s < K::kStages; ++s) issued[s] = false, issued_parity[s] = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-                int mb, nb;
-                tile_coords(p, t, mb, nb);
+            for (int gt = cid; ok && gt < p.num_gtiles; gt += ncl) {
+                int mp, nb;
+                tile_coords(p, gt, mp, nb);
+                const int mb = mp * CL + rank;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
                         record_abort(abort_flag, p.dstatus);
@@ -219,13 +234,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t *sb_tile = sa_tile + kABytes;
                     mbar_arrive_expect_tx(&full[stage], K::kStageBytes);
                     tma_load_2d(&tmap_a, &full[stage], sa_tile, kb * kBK, mb * kBM);
-                    tma_load_2d(&tmap_b, &full[stage], sb_tile, kb * kBK, nb * BN);
+                    if (CL == 1)
+                        tma_load_2d(&tmap_b, &full[stage], sb_tile, kb * kBK, nb * BN);
+                    else
+                        tma_load_2d_mc(&tmap_b, &full[stage], sb_tile + rank * kBoxB * 128,
+                                       kb * kBK, nb * BN + rank * kBoxB, kMask);
                     issued[stage] = true;
                     issued_parity[stage] = phase;
                     if (++stage == K::kStages) stage = 0, phase ^= 1;
                 }
             }
-            // Never leave with a copy still landing in shared memory.
+            // Never leave with a copy still landing in shared memory, nor (in
+            // a cluster) with another CTA's MMA commit still due here.
             for (int s = 0; s < K::kStages; ++s)
                 if (issued[s] && !mbar_wait(&full[s], issued_parity[s], abort_flag)) {
                     const long long t0 = clock64();
@@ -233,6 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                            clock64() - t0 < kWaitLimitCycles) {
                     }
                 }
+            if (CL > 1)
+                for (int s = 0; s < K::kStages; ++s)
+                    if (issued[s]) {
+                        const long long t0 = clock64();
+                        while (!mbar_try_wait(&empty[s], issued_parity[s]) &&
+                               clock64() - t0 < kWaitLimitCycles) {
+                        }
+                    }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
@@ -242,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_iter = 0;
             bool ok = true;
             bool any_mma = false;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (int gt = cid; ok && gt < p.num_gtiles; gt += ncl) {
                 for (int c = 0; ok && c < num_chunks; ++c) {
                     const int kb0 = c * kChunkBlocks;
                     const int kb1 = min(p.num_kb, kb0 + kChunkBlocks);
@@ -273,7 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        K::kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
                         }
                         any_mma = true;
-                        mma_commit(&empty[stage]);
+                        if (CL == 1)
+                            mma_commit(&empty[stage]);
+                        else
+                            mma_commit_mc(&empty[stage], kMask);
                         if (++stage == K::kStages) stage = 0, phase ^= 1;
                     }
                     if (!ok) break;
@@ -299,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t acc_iter = 0;
         bool ok = true;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        for (int gt = cid; ok && gt < p.num_gtiles; gt += ncl) {
             // ---- drain every chunk into int32 sums
             uint32_t acc[K::kWarpCols];  // int32 bit patterns
             for (int c = 0; c < num_chunks; ++c) {
@@ -343,8 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
 
             // ---- final epilogue of the tile from the int32 sums
-            int mb, nb;
-            tile_coords(p, t, mb, nb);
+            int mp, nb;
+            tile_coords(p, gt, mp, nb);
+            const int mb = mp * CL + rank;
+            if (mb >= p.num_m) continue;  // the missing partner tile of an odd m count
             const int row0 = mb * kBM + q * 32;
             const int colh = nb * BN + h * K::kWarpCols;
             const float a = p.mode == 0 ? __ldg(p.sa + row0 + lane) : 0.0f;
@@ -373,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (CL > 1) cluster_sync_all();  // no CTA leaves while another may still signal it
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem_base, K::kTmemCols);
@@ -409,13 +443,13 @@ bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, size_t esz, const void
     return r == CUDA_SUCCESS;
 }
 
-template <int BN>
+template <int BN, int CL>
 cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tc, const __half *Bop,
                       int64_t N, int64_t K, const Params &p0, cudaStream_t st) {
     using C = Cfg<BN>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, CL>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)C::kSmemBytes);
         if (e != cudaSuccess) return e;
@@ -423,19 +457,51 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tc, const __half
     }
     CUtensorMap tb;
     if (!make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, Bop, (uint64_t)K, (uint64_t)N,
-                      (uint64_t)operand_ld(K), kBK, BN))
+                      (uint64_t)operand_ld(K), kBK, BN / CL))
         return cudaErrorInvalidValue;
     Params p = p0;
     p.num_n = (int)((N + BN - 1) / BN);
-    p.num_tiles = p.num_m * p.num_n;
+    p.num_mp = (p.num_m + CL - 1) / CL;
+    p.num_gtiles = p.num_mp * p.num_n;
     const int sms = device_sm_count();
-    const int grid = p.num_tiles < sms ? p.num_tiles : sms;
-    gemm_tc_kernel<BN><<<grid, kThreads, C::kSmemBytes, st>>>(ta, tb, tc, p);
+    const int clusters = p.num_gtiles < sms / CL ? p.num_gtiles : sms / CL;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)(clusters * CL), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = CL > 1 ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, CL>, ta, tb, tc, p);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
+}
+
+template <int BN>
+cudaError_t launch_width(const CUtensorMap &ta, const CUtensorMap &tc, const __half *Bop,
+                         int64_t N, int64_t K, const Params &p, cudaStream_t st) {
+    if (p.cluster == 2 && p.num_m >= 2) return launch_bn<BN, 2>(ta, tc, Bop, N, K, p, st);
+    return launch_bn<BN, 1>(ta, tc, Bop, N, K, p, st);
 }
 
 }  // namespace
+
+// Cluster size of the GEMM launch: 1 unless BSG_GEMM_CLUSTER=2 is set in the
+// environment, which makes pairs of m-tiles share each B tile through TMA
+// multicast (same results; measured no faster on GB300, so off by default).
+int gemm_cluster_size() {
+    static int cl = [] {
+        const char *e = getenv("BSG_GEMM_CLUSTER");
+        return (e && e[0] == '2' && e[1] == 0) ? 2 : 1;
+    }();
+    return cl;
+}
 
 // Tile width for an M x N problem on `sms` SMs: the one with the least
 // estimated time, rounds of tiles times the cost of one tile.  A tile of
@@ -492,11 +558,12 @@ cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int6
     p.mode = mode;
     p.relu = relu;
     p.tma_store = tma_store;
+    p.cluster = gemm_cluster_size();
     p.dstatus = dstatus;
     switch (gemm_tile_width(M, N, device_sm_count())) {
-        case 64: return launch_bn<64>(ta, tc, Bop, N, K, p, st);
-        case 128: return launch_bn<128>(ta, tc, Bop, N, K, p, st);
-        default: return launch_bn<256>(ta, tc, Bop, N, K, p, st);
+        case 64: return launch_width<64>(ta, tc, Bop, N, K, p, st);
+        case 128: return launch_width<128>(ta, tc, Bop, N, K, p, st);
+        default: return launch_width<256>(ta, tc, Bop, N, K, p, st);
     }
 }
 
