@@ -119,7 +119,16 @@ bsg_status bsg_epilogue(const int32_t *S, int64_t lds, const float *sa, const fl
  * column; all operands packed row-major.  `workspace`: at least
  * bsgemm_i8_workspace_size(M, N, K) bytes, 256-byte aligned, device memory;
  * its contents on return are unspecified.  Steps 1-3 of "The verified INT8
- * units". */
+ * units".
+ * The two operands are quantized at the same time: op(B) on a second stream
+ * that the library creates on its first such call on each device (one
+ * stream and two events, kept until the process exits), forked from
+ * `stream` and joined back into it with events, so the call is ordered on
+ * `stream` like any other and can be captured into a CUDA graph (make the
+ * first call on each device outside a capture).  If that stream cannot be
+ * created, the operands are quantized one after the other on `stream`.
+ * This applies to bsgemm_i8, bsgemm_i8_ex, bsgemm_i8_quantize and
+ * bsgemm_i8_host. */
 size_t bsgemm_i8_workspace_size(int64_t M, int64_t N, int64_t K);
 bsg_status bsgemm_i8(const float *A, const float *B, int64_t M, int64_t N, int64_t K, int relu,
                      float *C, void *workspace, size_t ws_bytes, int32_t *dstatus,
@@ -186,7 +195,8 @@ uint64_t bsg_launch_count(void);
  *     calls that may overlap on the GPU (other streams, other host threads)
  *     race on it and must be serialized by the caller.  Nothing in the array
  *     has to start at zero: each call writes every byte it reads.
- *   - It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine, and
+ *     creates no stream or event: every launch goes to `stream`.
  * The pages have no counterpart: this is a deployment variant. */
 #define BSG_NOALLOC_SCRATCH_BYTES (64u << 20)
 bsg_status bsgemm_i8_noalloc(const float *A, const float *B, int64_t M, int64_t N, int64_t K,

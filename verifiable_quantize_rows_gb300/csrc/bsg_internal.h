@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "bsgemm.h"
+
 namespace bsg {
 
 // Output encodings of the quantize kernels.
@@ -59,13 +61,14 @@ cudaError_t launch_i8_rows_to_half(const int8_t *Q, int64_t rows, int64_t cols, 
 cudaError_t launch_i8_cols_to_half(const int8_t *Q, int64_t rows, int64_t cols, int64_t ldq,
                                    __half *out, int64_t ldo, cudaStream_t st);
 
+// The tile width (64, 128 or 256) the GEMM uses for an M x N problem, and
+// the cluster size of its launch (1 or 2).
+int gemm_tile_width(int64_t M, int64_t N, int sms);
+int gemm_cluster_size();
 // The tensor-core GEMM.  Aop: M x ldk f16, Bop: N x ldk f16 (both K-major,
 // ldk = operand_ld(K)).  mode 0: C = epi(S, sa, sb) (+ReLU) as float;
 // mode 1: S stored as int32.  sa / sb must hold round_up(M, kBM) /
 // round_up(N, kBN) floats (mode 0).
-// The tile width (64, 128 or 256) the GEMM uses for an M x N problem.
-int gemm_tile_width(int64_t M, int64_t N, int sms);
-int gemm_cluster_size();
 cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int64_t N,
                            int64_t K, const float *sa, const float *sb, int relu, int mode,
                            void *out, int64_t ldo, int32_t *dstatus, cudaStream_t st);
@@ -78,6 +81,14 @@ cudaError_t launch_probe_fill(uint64_t seed, int64_t M, int64_t N, int64_t K, fl
                               float *B, cudaStream_t st);
 
 size_t hash_workspace_bytes(int64_t M, int64_t N);
+
+// The whole unit (quantize both operands, contract, epilogue) from a
+// workspace of bsgemm_i8_workspace_size(M, N, K) bytes.  `overlap`: quantize op(B)
+// on a second stream of this library beside op(A); false keeps every launch
+// on `st` and creates nothing.
+bsg_status run_unit(const float *A, int64_t lda, int transA, const float *B, int64_t ldb,
+                    int transB, int64_t M, int64_t N, int64_t K, int relu, float *C, int64_t ldc,
+                    void *ws, size_t ws_bytes, int32_t *dstatus, cudaStream_t st, bool overlap);
 cudaError_t launch_hash_f32(const float *C, int64_t M, int64_t N, int64_t ldc, uint8_t *out32,
                             void *ws, cudaStream_t st);
 

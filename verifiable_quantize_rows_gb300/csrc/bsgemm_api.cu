@@ -54,9 +54,11 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 //   Bop  f16 [N][ldk]
 //   sa   f32 [round_up(M, 128)]
 //   sb   f32 [round_up(N, 256)]
-//   partial column maxima (uint32) for the column quantize
+//   partial column maxima (uint32) of op(A), then of op(B), for the
+//   column quantizes that need two passes (separate, since the two
+//   operands may be quantized at the same time)
 struct UnitLayout {
-    size_t aop, bop, sa, sb, part, total;
+    size_t aop, bop, sa, sb, part, part_b, total;
 };
 
 UnitLayout unit_layout(int64_t M, int64_t N, int64_t K, int transA, int transB) {
@@ -72,10 +74,9 @@ UnitLayout unit_layout(int64_t M, int64_t N, int64_t K, int transA, int transB) 
     L.sb = off;
     off = align256(off + (size_t)round_up(N, kBN) * 4);
     L.part = off;
-    size_t part = 0;
-    if (transA) part = colmax_partial_bytes(K, M);
-    if (!transB) part = part > colmax_partial_bytes(K, N) ? part : colmax_partial_bytes(K, N);
-    off = align256(off + part);
+    if (transA) off = align256(off + colmax_partial_bytes(K, M));
+    L.part_b = off;
+    if (!transB) off = align256(off + colmax_partial_bytes(K, N));
     L.total = off;
     return L;
 }
@@ -103,11 +104,49 @@ bsg_status check_unit_args(const float *A, int64_t lda, int transA, const float 
     return BSG_OK;
 }
 
+// A second stream per device on which op(B) is quantized while op(A) is
+// quantized on the caller's stream: the two kernels are independent, and
+// the smaller one (usually the weight) is latency-bound, so running it beside
+// the larger one hides it.  It is forked from and joined back into the
+// caller's stream with two events, which also works while the caller's
+// stream is being captured into a CUDA graph (the side stream joins the
+// capture).  Created on the first call on each device and kept until the
+// process exits; one host thread at a time uses it.
+struct SideStream {
+    cudaStream_t st = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    bool tried = false;
+};
+std::mutex g_side_lock;
+SideStream g_side[64];
+
+// The side stream of the current device, or nullptr if it could not be
+// created (the operands are then quantized one after the other).  Called
+// with g_side_lock held.
+SideStream *side_stream() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    SideStream &s = g_side[dev];
+    if (!s.tried) {
+        s.tried = true;
+        int least = 0, greatest = 0;
+        cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        if (cudaStreamCreateWithPriority(&s.st, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+            cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            s.st = nullptr;
+        }
+    }
+    return s.st ? &s : nullptr;
+}
+
 // Step 1 into the workspace: op(A) per row, op(B) per column, as f16
-// K-major operands plus scales.
+// K-major operands plus scales.  With `overlap`, op(B) is quantized on the
+// side stream at the same time as op(A).
 bsg_status unit_quantize(const float *A, int64_t lda, int transA, const float *B, int64_t ldb,
                          int transB, int64_t M, int64_t N, int64_t K, void *ws, size_t ws_bytes,
-                         int32_t *dstatus, cudaStream_t st) {
+                         int32_t *dstatus, cudaStream_t st, bool overlap = true) {
     bsg_status s = check_unit_args(A, lda, transA, B, ldb, transB, M, N, K);
     if (s != BSG_OK) return s;
     const UnitLayout L = unit_layout(M, N, K, transA, transB);
@@ -119,22 +158,40 @@ bsg_status unit_quantize(const float *A, int64_t lda, int transA, const float *B
     __half *bop = at<__half>(ws, L.bop);
     float *sa = at<float>(ws, L.sa);
     float *sb = at<float>(ws, L.sb);
-    uint32_t *part = at<uint32_t>(ws, L.part);
-    cudaError_t e;
+    uint32_t *part_a = at<uint32_t>(ws, L.part);
+    uint32_t *part_b = at<uint32_t>(ws, L.part_b);
     // op(A) per row: a row quantize of A, or a column quantize of the stored K x M.
-    if (!transA)
-        e = launch_quantize_rows(A, M, K, lda, kOutHalfKMajor, aop, ldk, sa, nullptr, dstatus, st);
-    else
-        e = launch_quantize_cols(A, K, M, lda, kOutHalfKMajor, aop, ldk, sa, nullptr, part,
-                                 dstatus, st);
-    if (e != cudaSuccess) return BSG_ERR_CUDA;
+    auto quant_a = [&](cudaStream_t s) {
+        return !transA ? launch_quantize_rows(A, M, K, lda, kOutHalfKMajor, aop, ldk, sa, nullptr,
+                                              dstatus, s)
+                       : launch_quantize_cols(A, K, M, lda, kOutHalfKMajor, aop, ldk, sa, nullptr,
+                                              part_a, dstatus, s);
+    };
     // op(B) per column: a column quantize of B, or a row quantize of the stored N x K.
-    if (!transB)
-        e = launch_quantize_cols(B, K, N, ldb, kOutHalfKMajor, bop, ldk, sb, nullptr, part,
-                                 dstatus, st);
-    else
-        e = launch_quantize_rows(B, N, K, ldb, kOutHalfKMajor, bop, ldk, sb, nullptr, dstatus, st);
-    return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
+    auto quant_b = [&](cudaStream_t s) {
+        return !transB ? launch_quantize_cols(B, K, N, ldb, kOutHalfKMajor, bop, ldk, sb, nullptr,
+                                              part_b, dstatus, s)
+                       : launch_quantize_rows(B, N, K, ldb, kOutHalfKMajor, bop, ldk, sb, nullptr,
+                                              dstatus, s);
+    };
+    if (overlap) {
+        std::lock_guard<std::mutex> guard(g_side_lock);
+        SideStream *side = side_stream();
+        if (side) {
+            if (cudaEventRecord(side->fork, st) != cudaSuccess ||
+                cudaStreamWaitEvent(side->st, side->fork, 0) != cudaSuccess)
+                return BSG_ERR_CUDA;
+            const cudaError_t eb = quant_b(side->st);
+            const cudaError_t ea = quant_a(st);
+            // join even after a failed launch, so that no captured fork is left open
+            const cudaError_t ej = cudaEventRecord(side->join, side->st);
+            const cudaError_t ew = ej == cudaSuccess ? cudaStreamWaitEvent(st, side->join, 0) : ej;
+            return (ea == cudaSuccess && eb == cudaSuccess && ew == cudaSuccess) ? BSG_OK
+                                                                                 : BSG_ERR_CUDA;
+        }
+    }
+    if (quant_a(st) != cudaSuccess) return BSG_ERR_CUDA;
+    return quant_b(st) == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
 }
 
 // Steps 2-3 from the workspace: the tensor-core contraction with the fused
@@ -152,15 +209,25 @@ bsg_status unit_contract(int64_t M, int64_t N, int64_t K, int relu, float *C, in
                                     dstatus, st));
 }
 
-bsg_status unit(const float *A, int64_t lda, int transA, const float *B, int64_t ldb,
-                int transB, int64_t M, int64_t N, int64_t K, int relu, float *C, int64_t ldc,
-                void *ws, size_t ws_bytes, int32_t *dstatus, cudaStream_t st) {
+}  // namespace
+
+bsg_status run_unit(const float *A, int64_t lda, int transA, const float *B, int64_t ldb,
+                    int transB, int64_t M, int64_t N, int64_t K, int relu, float *C, int64_t ldc,
+                    void *ws, size_t ws_bytes, int32_t *dstatus, cudaStream_t st, bool overlap) {
     if (!C || ldc < N) return BSG_ERR_ARG;
-    bsg_status s = unit_quantize(A, lda, transA, B, ldb, transB, M, N, K, ws, ws_bytes, dstatus, st);
+    bsg_status s = unit_quantize(A, lda, transA, B, ldb, transB, M, N, K, ws, ws_bytes, dstatus,
+                                 st, overlap);
     if (s != BSG_OK) return s;
     return unit_contract(M, N, K, relu, C, ldc, ws, ws_bytes, dstatus, st);
 }
 
+namespace {
+bsg_status unit(const float *A, int64_t lda, int transA, const float *B, int64_t ldb,
+                int transB, int64_t M, int64_t N, int64_t K, int relu, float *C, int64_t ldc,
+                void *ws, size_t ws_bytes, int32_t *dstatus, cudaStream_t st) {
+    return run_unit(A, lda, transA, B, ldb, transB, M, N, K, relu, C, ldc, ws, ws_bytes, dstatus,
+                    st, true);
+}
 }  // namespace
 }  // namespace bsg
 

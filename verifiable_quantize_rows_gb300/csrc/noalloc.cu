@@ -14,6 +14,7 @@
 
 #include <mutex>
 
+#include "bsg_internal.h"
 #include "bsgemm.h"
 
 namespace {
@@ -57,6 +58,8 @@ extern "C" bsg_status bsgemm_i8_noalloc(const float *A, const float *B, int64_t 
     // Every byte of the scratch that the unit reads is written earlier in
     // the same call (operands, scales, partial maxima), so nothing needs
     // clearing between calls.
-    return bsgemm_i8(A, B, M, N, K, relu, C, scratch, (size_t)BSG_NOALLOC_SCRATCH_BYTES, dstatus,
-                     stream);
+    // overlap = false: the second quantize stream would be a created object
+    return bsg::run_unit(A, K, 0, B, N, 0, M, N, K, relu, C, N, scratch,
+                         (size_t)BSG_NOALLOC_SCRATCH_BYTES, dstatus,
+                         static_cast<cudaStream_t>(stream), false);
 }

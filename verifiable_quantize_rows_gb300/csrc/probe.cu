@@ -77,9 +77,12 @@ __device__ __forceinline__ uint32_t ror(uint32_t x, int n) { return __funnelshif
     } while (0)
 
 // The compression function F (RFC 7693 section 3.2): t is the byte count so
-// far, last_block / last_node the finalization flags.
-__device__ __forceinline__ void b2s_compress(uint32_t (&h)[8], const uint32_t (&m)[16], uint32_t t,
-                                             bool last_block, bool last_node) {
+// far, last_block / last_node the finalization flags.  Kept out of line: its
+// ten unrolled rounds are about 18 KB of code, and one copy per call site
+// (a leaf's four blocks, the tree levels) overflowed the instruction cache,
+// so that warps stalled on instruction fetch rather than on arithmetic.
+__device__ __noinline__ void b2s_compress(uint32_t (&h)[8], const uint32_t (&m)[16], uint32_t t,
+                                          bool last_block, bool last_node) {
     constexpr uint8_t S[10][16] = {
         {0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15},
         {14, 10, 4, 8, 9, 15, 13, 6, 1, 12, 0, 2, 11, 7, 5, 3},
@@ -145,15 +148,26 @@ __device__ void b2s_node(int W, WordFn word, uint64_t node_offset, uint32_t node
     }
 }
 
-// A full 64-word leaf from registers (the common case): 4 blocks.
-__device__ __forceinline__ void b2s_leaf64(const uint32_t (&w)[64], uint64_t node_offset,
+// A full 64-word leaf at a 16-byte aligned address (the common case): 4
+// blocks, each block's words loaded while the previous one is compressed.
+__device__ __forceinline__ void b2s_leaf64(const uint4 *src, uint64_t node_offset,
                                            bool last_node, uint32_t (&h)[8]) {
     b2s_node_init(h, node_offset, 0);
+    uint4 next[4];
 #pragma unroll
+    for (int j = 0; j < 4; ++j) next[j] = __ldg(src + j);
+#pragma unroll 1
     for (int blk = 0; blk < 4; ++blk) {
         uint32_t m[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) m[j] = w[blk * 16 + j];
+        for (int j = 0; j < 4; ++j) {
+            m[4 * j] = next[j].x; m[4 * j + 1] = next[j].y;
+            m[4 * j + 2] = next[j].z; m[4 * j + 3] = next[j].w;
+        }
+        if (blk < 3) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) next[j] = __ldg(src + 4 * (blk + 1) + j);
+        }
         b2s_compress(h, m, 64u * (blk + 1), blk == 3, last_node);
     }
 }
@@ -184,12 +198,13 @@ struct SmemWords {
 // LEAF: this block's level-0 inputs are leaves of C; otherwise they are the
 // digests in `in` at tree depth `depth0`.  The block reduces its THREADS
 // inputs through up to LEVELS levels (stopping once the whole tree has one
-// node) and writes its last node.
+// node) and writes its last node; the block that produces the root also
+// writes the digest's 32 bytes (its state words, little-endian) to out32.
 template <bool LEAF, int THREADS, int LEVELS>
 __global__ void __launch_bounds__(THREADS)
     hash_level_kernel(const float *__restrict__ C, int64_t M, int64_t N, int64_t ldc,
                       const uint32_t *__restrict__ in, int64_t count, uint32_t depth0,
-                      uint32_t *__restrict__ out) {
+                      uint32_t *__restrict__ out, uint8_t *__restrict__ out32) {
     static_assert((1 << (2 * LEVELS)) == THREADS, "THREADS must be 4^LEVELS");
     __shared__ uint32_t dig[2][THREADS][8];
     const int t = threadIdx.x;
@@ -202,21 +217,9 @@ __global__ void __launch_bounds__(THREADS)
             const int64_t first = idx * kLeafFloats;
             const int64_t left = nfloat - first;
             const bool last = idx == count - 1;
-            if (left >= kLeafFloats && ldc == N) {
-                uint32_t w[64];
-                const uint4 *src = reinterpret_cast<const uint4 *>(C + first);
-                const bool vec = (reinterpret_cast<uintptr_t>(C + first) & 15) == 0;
-                if (vec) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const uint4 u = __ldg(src + j);
-                        w[4 * j] = u.x; w[4 * j + 1] = u.y; w[4 * j + 2] = u.z; w[4 * j + 3] = u.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) w[j] = __float_as_uint(__ldg(C + first + j));
-                }
-                b2s_leaf64(w, (uint64_t)idx, last, h);
+            if (left >= kLeafFloats && ldc == N &&
+                (reinterpret_cast<uintptr_t>(C + first) & 15) == 0) {
+                b2s_leaf64(reinterpret_cast<const uint4 *>(C + first), (uint64_t)idx, last, h);
             } else {
                 const int W = (int)(left < kLeafFloats ? (left > 0 ? left : 0) : kLeafFloats);
                 LeafWords lw{C, first, N, ldc, ldc == N};
@@ -258,12 +261,7 @@ __global__ void __launch_bounds__(THREADS)
     }
     // This block's surviving node (index lbase at the final level).
     if (t < 8 && lbase < n) out[lbase * 8 + t] = dig[cur][0][t];
-}
-
-// The digest's bytes are its state words, little-endian.
-__global__ void digest_to_bytes_kernel(const uint32_t *__restrict__ d, uint8_t *__restrict__ out) {
-    const int t = threadIdx.x;
-    if (t < 32) out[t] = (uint8_t)(d[t >> 2] >> (8 * (t & 3)));
+    if (n == 1 && t < 32) out32[t] = (uint8_t)(dig[cur][0][t >> 2] >> (8 * (t & 3)));
 }
 
 
@@ -295,22 +293,21 @@ cudaError_t launch_hash_f32(const float *C, int64_t M, int64_t N, int64_t ldc, u
     const int64_t n1cap = (count + kLeafThreads - 1) / kLeafThreads;
     uint32_t *bufs[2] = {static_cast<uint32_t *>(ws), static_cast<uint32_t *>(ws) + n1cap * 8};
     int which = 0;
-    int nlaunch = 2;  // leaves + digest bytes
+    int nlaunch = 1;
     int64_t blocks = (count + kLeafThreads - 1) / kLeafThreads;
     hash_level_kernel<true, kLeafThreads, 3><<<(int)blocks, kLeafThreads, 0, st>>>(
-        C, M, N, ldc, nullptr, count, 0u, bufs[which]);
+        C, M, N, ldc, nullptr, count, 0u, bufs[which], out32);
     // tree depth reached inside the leaf blocks
     uint32_t depth = 0;
     for (int l = 0; l < 3 && count > 1; ++l) count = (count + 3) / 4, ++depth;
     while (count > 1) {
         blocks = (count + kNodeThreads - 1) / kNodeThreads;
         hash_level_kernel<false, kNodeThreads, 4><<<(int)blocks, kNodeThreads, 0, st>>>(
-            nullptr, 0, 0, 0, bufs[which], count, depth, bufs[which ^ 1]);
+            nullptr, 0, 0, 0, bufs[which], count, depth, bufs[which ^ 1], out32);
         which ^= 1;
         for (int l = 0; l < 4 && count > 1; ++l) count = (count + 3) / 4, ++depth;
         ++nlaunch;
     }
-    digest_to_bytes_kernel<<<1, 32, 0, st>>>(bufs[which], out32);
     count_launches(nlaunch);
     return cudaGetLastError();
 }
