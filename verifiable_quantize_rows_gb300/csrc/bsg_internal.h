@@ -62,9 +62,9 @@ cudaError_t launch_i8_cols_to_half(const int8_t *Q, int64_t rows, int64_t cols, 
                                    __half *out, int64_t ldo, cudaStream_t st);
 
 // The tile width (64, 128 or 256) the GEMM uses for an M x N problem, and
-// the cluster size of its launch (1 or 2).
+// whether it runs 256-row tiles on CTA pairs when M > 128.
 int gemm_tile_width(int64_t M, int64_t N, int sms);
-int gemm_cluster_size();
+bool gemm_pairs_enabled();
 // The tensor-core GEMM.  Aop: M x ldk f16, Bop: N x ldk f16 (both K-major,
 // ldk = operand_ld(K)).  mode 0: C = epi(S, sa, sb) (+ReLU) as float;
 // mode 1: S stored as int32.  sa / sb must hold round_up(M, kBM) /

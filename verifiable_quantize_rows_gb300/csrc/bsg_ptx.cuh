@@ -80,17 +80,6 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap *m, uint64_t *bar,
         : "memory");
 }
 
-// 2-D tiled load global -> shared of every CTA in `mask` (same shared
-// offset in each), completion counted on each destination CTA's `bar`.
-__device__ __forceinline__ void tma_load_2d_mc(const CUtensorMap *m, uint64_t *bar, void *dst,
-                                               int32_t x, int32_t y, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(m), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
-        : "memory");
-}
-
 // 2-D tiled store shared -> global (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, const void *src, int32_t x,
                                              int32_t y) {
@@ -106,6 +95,10 @@ __device__ __forceinline__ void bulk_commit() {
 // Wait until every committed bulk store has finished READING shared memory.
 __device__ __forceinline__ void bulk_wait_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until at most the most recent committed bulk store is still reading.
+__device__ __forceinline__ void bulk_wait_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // Wait until every committed bulk store has completed.
 __device__ __forceinline__ void bulk_wait0() {
@@ -158,15 +151,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
         : "memory");
 }
 
-// As mma_commit, arriving on `bar` (same shared offset) in every CTA of `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
-
 // Cluster-wide barrier (all threads of all CTAs of the cluster).
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
@@ -216,6 +200,110 @@ __device__ __forceinline__ uint64_t sdesc_k128(uint32_t smem_addr) {
 // 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
     return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// ------------------------------------------- CTA pairs (tcgen05 cta_group::2)
+// Two CTAs of a cluster whose ranks differ in bit 0 form a pair: one MMA,
+// issued by one thread of the even CTA, reads A's rows 0-127 and the first
+// half of B's rows from the even CTA's shared memory and the rest from the
+// odd CTA's at the same offsets, and writes rows 0-127 of D to the even CTA's
+// tensor memory and rows 128-255 to the odd CTA's.
+
+// The shared::cluster address of the variable at `p` in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+// Arrive on the mbarrier at shared::cluster address `bar` (any CTA of the
+// cluster), with the default (CTA-scope) release.  The GEMM's cross-CTA
+// arrivals order no generic memory operation: operand bytes are counted by
+// the TMA's own complete_tx, and tensor-memory reuse is ordered by the
+// tcgen05 fences around the barrier.  A cluster-scope release here, made on
+// every k-block, halved the pair kernel's throughput.
+__device__ __forceinline__ void mbar_arrive_cl(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_cl(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// try_wait / bounded wait on a barrier of this CTA that other CTAs of the
+// cluster arrive on (acquire at cluster scope).
+__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t *bar, uint32_t parity,
+                                             const volatile int *abort) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_cl(bar, parity)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitLimitCycles) return false;
+    }
+}
+
+// 2-D tiled load global -> this CTA's shared memory whose completion (bytes)
+// is counted on the mbarrier at shared::cluster address `bar`, which may be
+// the pair peer's.
+__device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap *m, uint32_t bar, void *dst,
+                                                 int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(m), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+// Tensor memory of a pair: one warp of EACH CTA executes these; the same
+// columns are allocated in both CTAs.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// The pair MMA (M = 256), issued by one thread of the even CTA.
+__device__ __forceinline__ void mma_f16_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` (same shared offset) in every CTA of `mask` when all
+// pair MMAs issued so far by this thread are done.
+__device__ __forceinline__ void mma_commit_pair_mc(uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(mask)
+        : "memory");
 }
 
 }  // namespace bsg

@@ -17,22 +17,33 @@
 // into chunks of 1024; each chunk's fp32 tile is converted to int32 and the
 // chunks are summed in int32, which is exact.
 //
-// Tiles are 128 x BN with BN in {64, 128, 256}, chosen per problem so that
-// the last wave of tiles leaves few SMs idle; one CTA per SM walks its tiles
-// round-robin (persistent).
+// Two kernels, one template:
+//   * PAIR (M > 128): a cluster of two CTAs on two SMs computes a 256 x BN
+//     tile with the pair MMA (tcgen05 cta_group::2, M = 256).  Each CTA
+//     loads 128 rows of A and BN/2 rows of B per k-block, so each SM takes
+//     in and its tensor core reads two thirds of what a 128 x BN tile per SM
+//     needs for the same multiply-adds.  With one CTA per SM the 128 x 256
+//     tile was bound by shared-memory traffic (TMA writes plus MMA reads),
+//     not by the tensor pipe; the pair also frees shared memory for two
+//     output staging buffers per epilogue warp.
+//   * single (M <= 128): one CTA computes a 128 x BN tile (cta_group::1).
+// BN in {64, 128, 256} is chosen per problem so that the last wave of tiles
+// leaves few SMs idle; CTAs (pairs) are persistent and walk their tiles
+// round-robin.
 //
 // Roles (one CTA per SM):
 //   warp 0      TMA producer: A and B k-blocks (64 wide, 128-byte swizzle)
-//               into a shared-memory ring (4 stages at BN 256, 6 below);
-//   warp 1      MMA issuer (one thread): 4 x tcgen05.mma (K = 16) per
-//               k-block into a tensor-memory accumulator, double-buffered
-//               (2 x BN columns) so the epilogue of one chunk or tile
-//               overlaps the next one's MMAs;
+//               into a shared-memory ring; in a pair both CTAs load and both
+//               count their bytes on the even CTA's barrier;
+//   warp 1      MMA issuer (one thread; in a pair, of the even CTA only):
+//               4 x tcgen05.mma (K = 16) per k-block into a tensor-memory
+//               accumulator, double-buffered (2 x BN columns) so the epilogue
+//               of one chunk or tile overlaps the next one's MMAs;
 //   warp 2      allocates / frees the tensor-memory columns;
-//   warps 4-11  epilogue: tcgen05.ld of each chunk into int32 registers
-//               (the tensor memory is released at once), then the f32
-//               epilogue, ReLU, staging in shared memory and TMA stores (or
-//               plain stores where C's rows are not 16-byte aligned).
+//   warps 4-11  epilogue: tcgen05.ld of each chunk into registers (the tensor
+//               memory is released at once), then the f32 epilogue, ReLU,
+//               staging in shared memory and TMA stores (or plain stores
+//               where C's rows are not 16-byte aligned).
 // Every mbarrier wait is bounded; on expiry the CTA records
 // BSG_DSTATUS_TIMEOUT, drains its copies and MMAs, frees tensor memory and
 // returns.
@@ -55,36 +66,42 @@ constexpr int kChunkBlocks = kChunkK / kBK;  // 16 k-blocks per exact chunk
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 128 + kEpiWarps * 32;
 constexpr uint32_t kABytes = kBM * kBK * 2;     // 16 KiB
-constexpr uint32_t kEpiBufBytes = 32 * 32 * 4;  // one 32 x 32 fp32 box per epilogue warp
-constexpr int kGroupM = 16;                     // tile raster: 16 m-tiles per group
+constexpr uint32_t kEpiBufBytes = 32 * 32 * 4;  // one 32 x 32 fp32 box
+constexpr int kGroupM = 16;                     // tile raster: 16 m-units per group
+constexpr uint32_t kMaxSmem = 232448;           // 227 KiB per CTA
 
-// Compile-time layout of one tile width.
-template <int BN>
+// Compile-time layout of one tile width and kernel kind.
+template <int BN, bool PAIR>
 struct Cfg {
     static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
-    static constexpr int kStages = BN == 256 ? 4 : 6;
-    static constexpr uint32_t kBBytes = BN * kBK * 2;
+    static constexpr int kBRows = PAIR ? BN / 2 : BN;  // B rows this CTA loads
+    static constexpr uint32_t kBBytes = kBRows * kBK * 2;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages =
+        PAIR ? (BN == 256 ? 5 : BN == 128 ? 6 : 8) : (BN == 256 ? 4 : BN == 128 ? 5 : 6);
+    static constexpr int kBoxes = (!PAIR && BN == 256) ? 1 : 2;  // staging boxes per warp
     static constexpr uint32_t kAccCols = BN;  // one accumulator buffer
     static constexpr uint32_t kTmemCols = 2 * BN;
     static constexpr int kWarpCols = BN / 2;  // columns per epilogue warp
     static constexpr int kPieces = kWarpCols / 32;
     static constexpr uint32_t kOffEpi = kStages * kStageBytes;
-    static constexpr uint32_t kOffBar = kOffEpi + kEpiWarps * kEpiBufBytes;
+    static constexpr uint32_t kOffBar = kOffEpi + kEpiWarps * kBoxes * kEpiBufBytes;
     // barriers: full[kStages], empty[kStages], tfull[2], tempty[2], drain
     static constexpr uint32_t kNumBars = 2 * kStages + 5;
     static constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
     static constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
     static constexpr uint32_t kSmemBytes = kOffAbort + 4 + 1024;  // + 1024-byte alignment slack
-    static constexpr uint32_t kIdesc = idesc_f16_f32(kBM, BN);
+    static constexpr uint32_t kIdesc = idesc_f16_f32(PAIR ? 2 * kBM : kBM, BN);
+    static_assert(kSmemBytes <= kMaxSmem, "shared memory");
+    static_assert(kStageBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms stay aligned");
 };
 
 struct Params {
     int M, N, K;
     int num_kb;        // k-blocks per tile
-    int num_m, num_n;  // tiles
-    int num_mp;        // groups of CL m-tiles (one per cluster tile)
-    int num_gtiles;    // cluster tiles: num_mp * num_n
+    int num_m, num_n;  // 128-row m-blocks, BN-wide n-tiles
+    int num_mu;        // m-units: m-blocks, or pairs of them (PAIR)
+    int num_units;     // tiles of the launch: num_mu * num_n
     const float *sa;
     const float *sb;
     void *out;
@@ -92,19 +109,18 @@ struct Params {
     int mode;       // 0: f32 epilogue, 1: int32 accumulators
     int relu;
     int tma_store;  // 1: C's rows are 16-byte aligned; store through tmap_c
-    int cluster;    // 1, or 2: pairs of m-tiles share B through TMA multicast
     int32_t *dstatus;
 };
 
-// Cluster tile gt -> (m-group, n-tile), rastered in groups of kGroupM
-// m-groups so that concurrent tiles share operand rows and columns in L2.
-__host__ __device__ __forceinline__ void tile_coords(const Params &p, int gt, int &mp, int &nb) {
+// Tile u -> (m-unit, n-tile), rastered in groups of kGroupM m-units so that
+// concurrent tiles share operand rows and columns in L2.
+__host__ __device__ __forceinline__ void tile_coords(const Params &p, int u, int &mu, int &nb) {
     const int per_group = kGroupM * p.num_n;
-    const int g = gt / per_group;
+    const int g = u / per_group;
     const int first_m = g * kGroupM;
-    const int gm = (p.num_mp - first_m) < kGroupM ? (p.num_mp - first_m) : kGroupM;
-    const int r = gt - g * per_group;
-    mp = first_m + r % gm;
+    const int gm = (p.num_mu - first_m) < kGroupM ? (p.num_mu - first_m) : kGroupM;
+    const int r = u - g * per_group;
+    mu = first_m + r % gm;
     nb = r / gm;
 }
 
@@ -113,23 +129,61 @@ __device__ __forceinline__ void record_abort(volatile int *abort_flag, int32_t *
     if (dstatus) atomicOr(dstatus, 2);
 }
 
+// Bounded wait on one of this CTA's barriers; PAIR barriers may be arrived
+// on from the other CTA, so they are acquired at cluster scope.
+template <bool PAIR>
+__device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort) {
+    return PAIR ? mbar_wait_cl(bar, parity, abort) : mbar_wait(bar, parity, abort);
+}
+template <bool PAIR>
+__device__ __forceinline__ bool bar_try_wait(uint64_t *bar, uint32_t parity) {
+    return PAIR ? mbar_try_wait_cl(bar, parity) : mbar_try_wait(bar, parity);
+}
+
 // Epilogue value of one accumulator: f32(S) * a * b, each step RN; ReLU maps
 // everything that is not > 0 (including -0) to +0.
-__device__ __forceinline__ float epi_value(int32_t s, float a, float b, int relu) {
-    const float c = __fmul_rn(__fmul_rn(__int2float_rn(s), a), b);
+__device__ __forceinline__ float epi_value_f(float s, float a, float b, int relu) {
+    const float c = __fmul_rn(__fmul_rn(s, a), b);
     return relu ? (c > 0.0f ? c : 0.0f) : c;
 }
 
-// Write one thread's 32 values (row `lane` of a 32 x 32 box) into the
-// swizzled staging box and store it, or store directly to global memory.
+// The epilogue of 32 consecutive sums of one row, in place.  F32: v holds
+// f32(S) bit patterns (+0 added to map -0 to +0); otherwise int32 S.
+template <bool F32>
+__device__ __forceinline__ void epi_piece(uint32_t (&v)[32], const float4 *sbv, float a,
+                                          int relu) {
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 bb = __ldg(sbv + j4);
+        const float bj[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t x = v[4 * j4 + u];
+            const float sv = F32 ? __fadd_rn(__uint_as_float(x), 0.0f) : __int2float_rn((int32_t)x);
+            v[4 * j4 + u] = __float_as_uint(epi_value_f(sv, a, bj[u], relu));
+        }
+    }
+}
+
+// Write one thread's 32 values (row `lane` of a 32 x 32 box) into the next
+// of the warp's NBOX swizzled staging boxes and store it with the TMA, or
+// store directly to global memory.  `nstored` counts the warp's TMA stores;
+// a box is rewritten only after the store that last used it has read it.
+template <int NBOX>
 __device__ __forceinline__ void emit_box(const Params &p, const CUtensorMap *tmap_c,
-                                         uint8_t *box, const uint32_t (&v)[32], int row0,
-                                         int col0, int lane, bool &box_busy) {
+                                         uint8_t *boxes, const uint32_t (&v)[32], int row0,
+                                         int col0, int lane, int &nstored) {
     if (p.tma_store) {
-        if (box_busy) {
-            if (lane == 0) bulk_wait_read0();
+        if (nstored >= NBOX) {
+            if (lane == 0) {
+                if (NBOX == 1)
+                    bulk_wait_read0();
+                else
+                    bulk_wait_read1();
+            }
             __syncwarp();
         }
+        uint8_t *box = boxes + (nstored % NBOX) * kEpiBufBytes;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const uint32_t off = lane * 128 + ((j ^ (lane & 7)) << 4);
@@ -142,7 +196,7 @@ __device__ __forceinline__ void emit_box(const Params &p, const CUtensorMap *tma
             tma_store_2d(tmap_c, box, col0, row0);
             bulk_commit();
         }
-        box_busy = true;
+        ++nstored;
     } else {
         const int row = row0 + lane;
         if (row < p.M) {
@@ -154,15 +208,12 @@ __device__ __forceinline__ void emit_box(const Params &p, const CUtensorMap *tma
     }
 }
 
-// CL CTAs of a cluster take CL consecutive m-tiles of one n-tile and share
-// its B tile: each loads BN/CL rows of it and multicasts them to all, and a
-// stage is refilled only after every CTA's MMAs have finished with it.
-template <int BN, int CL>
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c, const Params p) {
-    using K = Cfg<BN>;
+    using K = Cfg<BN, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -179,20 +230,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int num_chunks = (p.num_kb + kChunkBlocks - 1) / kChunkBlocks;
-    const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
-    const int cid = blockIdx.x / CL;
-    const int ncl = gridDim.x / CL;
-    constexpr uint16_t kMask = (uint16_t)((1u << CL) - 1u);
-    constexpr int kBoxB = BN / CL;  // B rows each CTA loads
+    const int rank = PAIR ? (int)cluster_ctarank() : 0;  // 0: the pair's MMA-issuing CTA
+    const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int nunits = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    constexpr uint16_t kPairMask = 0x3;  // cluster ranks 0 and 1
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < K::kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], CL);
+            mbar_init(&full[s], PAIR ? 2 : 1);  // PAIR: both CTAs' producers
+            mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], kEpiWarps);
+            mbar_init(&tempty[b], PAIR ? 2 * kEpiWarps : kEpiWarps);  // PAIR: both epilogues
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -200,12 +250,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_async_shared();
     }
     if (warp == 2) {
-        tmem_alloc(tmem_ptr, K::kTmemCols);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(tmem_ptr, K::kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_ptr, K::kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
-    if (CL > 1) cluster_sync_all();  // every CTA's barriers exist before any multicast
+    if (PAIR) cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_ptr;
 
@@ -220,63 +275,69 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool issued[K::kStages];
             for (int s = 0; s < K::kStages; ++s) issued[s] = false, issued_parity[s] = 0;
             bool ok = true;
-            for (int gt = cid; ok && gt < p.num_gtiles; gt += ncl) {
-                int mp, nb;
-                tile_coords(p, gt, mp, nb);
-                const int mb = mp * CL + rank;
+            for (int u = unit0; ok && u < p.num_units; u += nunits) {
+                int mu, nb;
+                tile_coords(p, u, mu, nb);
+                const int mb = PAIR ? 2 * mu + rank : mu;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+                    if (!bar_wait<PAIR>(&empty[stage], phase ^ 1, abort_flag)) {
                         record_abort(abort_flag, p.dstatus);
                         ok = false;
                         break;
                     }
                     uint8_t *sa_tile = smem + stage * K::kStageBytes;
                     uint8_t *sb_tile = sa_tile + kABytes;
-                    mbar_arrive_expect_tx(&full[stage], K::kStageBytes);
-                    tma_load_2d(&tmap_a, &full[stage], sa_tile, kb * kBK, mb * kBM);
-                    if (CL == 1)
+                    if (PAIR) {
+                        // the even CTA's full barrier, where both CTAs count their bytes
+                        const uint32_t fb = cluster_addr(&full[stage], 0);
+                        mbar_arrive_expect_tx_cl(fb, K::kStageBytes);
+                        tma_load_2d_pair(&tmap_a, fb, sa_tile, kb * kBK, mb * kBM);
+                        tma_load_2d_pair(&tmap_b, fb, sb_tile, kb * kBK, nb * BN + rank * K::kBRows);
+                    } else {
+                        mbar_arrive_expect_tx(&full[stage], K::kStageBytes);
+                        tma_load_2d(&tmap_a, &full[stage], sa_tile, kb * kBK, mb * kBM);
                         tma_load_2d(&tmap_b, &full[stage], sb_tile, kb * kBK, nb * BN);
-                    else
-                        tma_load_2d_mc(&tmap_b, &full[stage], sb_tile + rank * kBoxB * 128,
-                                       kb * kBK, nb * BN + rank * kBoxB, kMask);
+                    }
                     issued[stage] = true;
                     issued_parity[stage] = phase;
                     if (++stage == K::kStages) stage = 0, phase ^= 1;
                 }
             }
-            // Never leave with a copy still landing in shared memory, nor (in
-            // a cluster) with another CTA's MMA commit still due here.
-            for (int s = 0; s < K::kStages; ++s)
-                if (issued[s] && !mbar_wait(&full[s], issued_parity[s], abort_flag)) {
-                    const long long t0 = clock64();
-                    while (!mbar_try_wait(&full[s], issued_parity[s]) &&
-                           clock64() - t0 < kWaitLimitCycles) {
+            // Never leave with a copy still landing in shared memory (the
+            // even CTA's full barriers count both CTAs' copies), nor, in a
+            // pair, with an MMA commit still due to arrive here.
+            if (!PAIR || rank == 0)
+                for (int s = 0; s < K::kStages; ++s)
+                    if (issued[s] && !bar_wait<PAIR>(&full[s], issued_parity[s], abort_flag)) {
+                        const long long t0 = clock64();
+                        while (!bar_try_wait<PAIR>(&full[s], issued_parity[s]) &&
+                               clock64() - t0 < kWaitLimitCycles) {
+                        }
                     }
-                }
-            if (CL > 1)
+            if (PAIR)
                 for (int s = 0; s < K::kStages; ++s)
                     if (issued[s]) {
                         const long long t0 = clock64();
-                        while (!mbar_try_wait(&empty[s], issued_parity[s]) &&
+                        while (!bar_try_wait<PAIR>(&empty[s], issued_parity[s]) &&
                                clock64() - t0 < kWaitLimitCycles) {
                         }
                     }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t acc_iter = 0;
             bool ok = true;
             bool any_mma = false;
-            for (int gt = cid; ok && gt < p.num_gtiles; gt += ncl) {
+            for (int u = unit0; ok && u < p.num_units; u += nunits) {
                 for (int c = 0; ok && c < num_chunks; ++c) {
                     const int kb0 = c * kChunkBlocks;
                     const int kb1 = min(p.num_kb, kb0 + kChunkBlocks);
                     const uint32_t b = acc_iter & 1;
                     const uint32_t acc_phase = (acc_iter >> 1) & 1;
-                    if (!mbar_wait(&tempty[b], acc_phase ^ 1, abort_flag)) {
+                    if (!bar_wait<PAIR>(&tempty[b], acc_phase ^ 1, abort_flag)) {
                         record_abort(abort_flag, p.dstatus);
                         ok = false;
                         break;
@@ -284,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + b * K::kAccCols;
                     for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                        if (!bar_wait<PAIR>(&full[stage], phase, abort_flag)) {
                             record_abort(abort_flag, p.dstatus);
                             ok = false;
                             break;
@@ -297,24 +358,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int k = 0; k < kBK / 16; ++k) {
                             // advance 16 f16 = 32 bytes along K inside the swizzle atom
-                            mma_f16_ss(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k),
-                                       K::kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                            const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
+                            if (PAIR)
+                                mma_f16_ss_pair(d_tmem, adesc + (uint64_t)(2 * k),
+                                                bdesc + (uint64_t)(2 * k), K::kIdesc, accum);
+                            else
+                                mma_f16_ss(d_tmem, adesc + (uint64_t)(2 * k),
+                                           bdesc + (uint64_t)(2 * k), K::kIdesc, accum);
                         }
                         any_mma = true;
-                        if (CL == 1)
-                            mma_commit(&empty[stage]);
+                        if (PAIR)
+                            mma_commit_pair_mc(&empty[stage], kPairMask);
                         else
-                            mma_commit_mc(&empty[stage], kMask);
+                            mma_commit(&empty[stage]);
                         if (++stage == K::kStages) stage = 0, phase ^= 1;
                     }
                     if (!ok) break;
-                    mma_commit(&tfull[b]);
+                    if (PAIR)
+                        mma_commit_pair_mc(&tfull[b], kPairMask);
+                    else
+                        mma_commit(&tfull[b]);
                     ++acc_iter;
                 }
             }
             if (!ok && any_mma) {
                 // drain: wait until every MMA issued so far has finished
-                mma_commit(drain);
+                if (PAIR)
+                    mma_commit_pair_mc(drain, 0x1);
+                else
+                    mma_commit(drain);
                 const long long t0 = clock64();
                 while (!mbar_try_wait(drain, 0) && clock64() - t0 < kWaitLimitCycles) {
                 }
@@ -325,19 +397,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;         // tensor-memory lane quadrant
         const int h = (warp - 4) >> 2;  // column half of the tile
         const int ew = warp - 4;        // epilogue warp index
-        uint8_t *box = smem + K::kOffEpi + ew * kEpiBufBytes;
-        bool box_busy = false;
+        uint8_t *boxes = smem + K::kOffEpi + ew * K::kBoxes * kEpiBufBytes;
+        int nstored = 0;
         uint32_t acc_iter = 0;
         bool ok = true;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        for (int gt = cid; ok && gt < p.num_gtiles; gt += ncl) {
-            // ---- drain every chunk into int32 sums
-            uint32_t acc[K::kWarpCols];  // int32 bit patterns
+        // With a single chunk (K <= 1024) the fp32 accumulator already is
+        // f32(S): S is an integer below 2^24 in magnitude, held exactly.  The
+        // f32 epilogue then needs no conversion (float->int and back run at a
+        // fraction of the ALU rate); adding +0 turns a -0 sum (all products
+        // -0) into f32(0) = +0.
+        const bool f32_sums = num_chunks == 1 && p.mode == 0;
+        for (int u = unit0; ok && u < p.num_units; u += nunits) {
+            // ---- drain every chunk into int32 sums (or, f32_sums, f32(S))
+            uint32_t acc[K::kWarpCols];  // int32 or f32 bit patterns
             for (int c = 0; c < num_chunks; ++c) {
                 const uint32_t b = acc_iter & 1;
                 const uint32_t acc_phase = (acc_iter >> 1) & 1;
                 // warp-uniform: every lane must agree before the .sync.aligned loads
-                if (!__all_sync(0xffffffffu, mbar_wait(&tfull[b], acc_phase, abort_flag))) {
+                if (!__all_sync(0xffffffffu, bar_wait<PAIR>(&tfull[b], acc_phase, abort_flag))) {
                     if (lane == 0) record_abort(abort_flag, p.dstatus);
                     ok = false;
                     break;
@@ -350,9 +428,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld16(tbase + piece * 16,
                                   *reinterpret_cast<uint32_t(*)[16]>(&acc[piece * 16]));
                     tmem_ld_wait();
+                    if (!f32_sums) {
 #pragma unroll
-                    for (int j = 0; j < K::kWarpCols; ++j)
-                        acc[j] = (uint32_t)__float2int_rn(__uint_as_float(acc[j]));
+                        for (int j = 0; j < K::kWarpCols; ++j)
+                            acc[j] = (uint32_t)__float2int_rn(__uint_as_float(acc[j]));
+                    }
                 } else {
 #pragma unroll
                     for (int piece = 0; piece < K::kWarpCols / 16; ++piece) {
@@ -368,16 +448,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the accumulator buffer is free again
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[b]);
+                if (lane == 0) {
+                    if (PAIR)  // the even CTA's barrier: both epilogues release
+                        mbar_arrive_cl(cluster_addr(&tempty[b], 0));
+                    else
+                        mbar_arrive(&tempty[b]);
+                }
                 ++acc_iter;
             }
             if (!ok) break;
 
-            // ---- final epilogue of the tile from the int32 sums
-            int mp, nb;
-            tile_coords(p, gt, mp, nb);
-            const int mb = mp * CL + rank;
-            if (mb >= p.num_m) continue;  // the missing partner tile of an odd m count
+            // ---- final epilogue of the tile from the sums
+            int mu, nb;
+            tile_coords(p, u, mu, nb);
+            const int mb = PAIR ? 2 * mu + rank : mu;
+            if (mb >= p.num_m) continue;  // the odd CTA of a pair past the last m-block
             const int row0 = mb * kBM + q * 32;
             const int colh = nb * BN + h * K::kWarpCols;
             const float a = p.mode == 0 ? __ldg(p.sa + row0 + lane) : 0.0f;
@@ -386,18 +471,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t(&v)[32] = *reinterpret_cast<uint32_t(*)[32]>(&acc[piece * 32]);
                 const int col0 = colh + piece * 32;
                 if (p.mode == 0) {
-                    // in place: the int32 sums become the output bits
+                    // in place: the sums become the output bits
                     const float4 *sbv = reinterpret_cast<const float4 *>(p.sb + col0);
-#pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 bb = __ldg(sbv + j4);
-                        v[4 * j4 + 0] = __float_as_uint(epi_value((int32_t)v[4 * j4 + 0], a, bb.x, p.relu));
-                        v[4 * j4 + 1] = __float_as_uint(epi_value((int32_t)v[4 * j4 + 1], a, bb.y, p.relu));
-                        v[4 * j4 + 2] = __float_as_uint(epi_value((int32_t)v[4 * j4 + 2], a, bb.z, p.relu));
-                        v[4 * j4 + 3] = __float_as_uint(epi_value((int32_t)v[4 * j4 + 3], a, bb.w, p.relu));
-                    }
+                    if (f32_sums)
+                        epi_piece<true>(v, sbv, a, p.relu);
+                    else
+                        epi_piece<false>(v, sbv, a, p.relu);
                 }
-                emit_box(p, &tmap_c, box, v, row0, col0, lane, box_busy);
+                emit_box<K::kBoxes>(p, &tmap_c, boxes, v, row0, col0, lane, nstored);
             }
         }
         if (p.tma_store && lane == 0) bulk_wait0();
@@ -406,10 +487,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (CL > 1) cluster_sync_all();  // no CTA leaves while another may still signal it
+    if (PAIR) cluster_sync_all();  // neither CTA leaves while the other may still signal it
     if (warp == 2) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, K::kTmemCols);
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, K::kTmemCols);
+        else
+            tmem_dealloc(tmem_base, K::kTmemCols);
     }
 }
 
@@ -443,80 +527,100 @@ bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, size_t esz, const void
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, int CL>
+template <int BN, bool PAIR>
 cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tc, const __half *Bop,
                       int64_t N, int64_t K, const Params &p0, cudaStream_t st) {
-    using C = Cfg<BN>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, CL>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)C::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    CUtensorMap tb;
-    if (!make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, Bop, (uint64_t)K, (uint64_t)N,
-                      (uint64_t)operand_ld(K), kBK, BN / CL))
-        return cudaErrorInvalidValue;
-    Params p = p0;
-    p.num_n = (int)((N + BN - 1) / BN);
-    p.num_mp = (p.num_m + CL - 1) / CL;
-    p.num_gtiles = p.num_mp * p.num_n;
+    using C = Cfg<BN, PAIR>;
+    // per device: the shared-memory attribute, and how many CTAs (pairs)
+    // can be resident at once -- a pair needs two free SMs of one GPC, so
+    // fewer than half the SMs may host pairs
+    static bool ready[64] = {false};
+    static int max_units[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const int sms = device_sm_count();
-    const int clusters = p.num_gtiles < sms / CL ? p.num_gtiles : sms / CL;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3((unsigned)(clusters * CL), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = CL > 1 ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, CL>, ta, tb, tc, p);
+    cfg.numAttrs = PAIR ? 1 : 0;
+    if (!ready[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, PAIR>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        int units = PAIR ? sms / 2 : sms;
+        if (PAIR) {
+            cfg.gridDim = dim3((unsigned)(2 * units), 1, 1);
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, PAIR>, &cfg) == cudaSuccess &&
+                n > 0 && n < units)
+                units = n;
+            cudaGetLastError();
+        }
+        max_units[dev] = units;
+        ready[dev] = true;
+    }
+    CUtensorMap tb;
+    if (!make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, Bop, (uint64_t)K, (uint64_t)N,
+                      (uint64_t)operand_ld(K), kBK, C::kBRows))
+        return cudaErrorInvalidValue;
+    Params p = p0;
+    p.num_n = (int)((N + BN - 1) / BN);
+    p.num_mu = PAIR ? (p.num_m + 1) / 2 : p.num_m;
+    p.num_units = p.num_mu * p.num_n;
+    const int units = p.num_units < max_units[dev] ? p.num_units : max_units[dev];
+    cfg.gridDim = dim3((unsigned)(units * (PAIR ? 2 : 1)), 1, 1);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, PAIR>, ta, tb, tc, p);
     count_launches(1);
     return e;
 }
 
 template <int BN>
 cudaError_t launch_width(const CUtensorMap &ta, const CUtensorMap &tc, const __half *Bop,
-                         int64_t N, int64_t K, const Params &p, cudaStream_t st) {
-    if (p.cluster == 2 && p.num_m >= 2) return launch_bn<BN, 2>(ta, tc, Bop, N, K, p, st);
-    return launch_bn<BN, 1>(ta, tc, Bop, N, K, p, st);
+                         int64_t N, int64_t K, const Params &p, bool pair, cudaStream_t st) {
+    if (pair) return launch_bn<BN, true>(ta, tc, Bop, N, K, p, st);
+    return launch_bn<BN, false>(ta, tc, Bop, N, K, p, st);
 }
 
 }  // namespace
 
-// Cluster size of the GEMM launch: 1 unless BSG_GEMM_CLUSTER=2 is set in the
-// environment, which makes pairs of m-tiles share each B tile through TMA
-// multicast (same results; measured no faster on GB300, so off by default).
-int gemm_cluster_size() {
-    static int cl = [] {
-        const char *e = getenv("BSG_GEMM_CLUSTER");
-        return (e && e[0] == '2' && e[1] == 0) ? 2 : 1;
+// CTA pairs are used whenever M spans two or more 128-row blocks, unless
+// BSG_GEMM_PAIR=0 is set in the environment (the single-CTA kernel then runs
+// every shape; same results, for comparison).
+bool gemm_pairs_enabled() {
+    static const bool on = [] {
+        const char *e = getenv("BSG_GEMM_PAIR");
+        return !(e && e[0] == '0' && e[1] == 0);
     }();
-    return cl;
+    return on;
 }
 
 // Tile width for an M x N problem on `sms` SMs: the one with the least
-// estimated time, rounds of tiles times the cost of one tile.  A tile of
-// width BN costs BN/256 of a 256-wide one, times a penalty for the narrower
-// MMAs (which read more shared memory per multiply-add) and for the fixed
-// per-tile epilogue work.
+// estimated time, rounds of tiles times the cost of one tile.  Tiles are
+// 256 rows on CTA pairs (sms / 2 of them) when M > 128, else 128 rows on
+// single CTAs.  A tile of width BN costs BN/256 of a 256-wide one, times a
+// penalty for the narrower MMAs (which read more shared memory per
+// multiply-add) and for the fixed per-tile epilogue work.
 int gemm_tile_width(int64_t M, int64_t N, int sms) {
     const int widths[3] = {256, 128, 64};
     const double penalty[3] = {1.0, 1.37, 2.64};  // measured: 8192^3 at each width
     const int64_t num_m = (M + kBM - 1) / kBM;
+    const bool pair = num_m >= 2 && gemm_pairs_enabled();
+    const int64_t num_mu = pair ? (num_m + 1) / 2 : num_m;
+    const int64_t units = pair ? (sms / 2 > 0 ? sms / 2 : 1) : sms;
     int best = 256;
     double best_cost = 1e300;
     for (int i = 0; i < 3; ++i) {
-        const int64_t tiles = num_m * ((N + widths[i] - 1) / widths[i]);
-        const int64_t rounds = (tiles + sms - 1) / sms;
+        const int64_t tiles = num_mu * ((N + widths[i] - 1) / widths[i]);
+        const int64_t rounds = (tiles + units - 1) / units;
         const double cost = (double)rounds * widths[i] / 256.0 * penalty[i];
         if (cost < best_cost * 0.999) {
             best_cost = cost;
@@ -558,12 +662,12 @@ cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int6
     p.mode = mode;
     p.relu = relu;
     p.tma_store = tma_store;
-    p.cluster = gemm_cluster_size();
     p.dstatus = dstatus;
+    const bool pair = p.num_m >= 2 && gemm_pairs_enabled();
     switch (gemm_tile_width(M, N, device_sm_count())) {
-        case 64: return launch_width<64>(ta, tc, Bop, N, K, p, st);
-        case 128: return launch_width<128>(ta, tc, Bop, N, K, p, st);
-        default: return launch_width<256>(ta, tc, Bop, N, K, p, st);
+        case 64: return launch_width<64>(ta, tc, Bop, N, K, p, pair, st);
+        case 128: return launch_width<128>(ta, tc, Bop, N, K, p, pair, st);
+        default: return launch_width<256>(ta, tc, Bop, N, K, p, pair, st);
     }
 }
 
