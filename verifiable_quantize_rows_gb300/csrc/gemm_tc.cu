@@ -611,7 +611,7 @@ bool gemm_pairs_enabled() {
 // multiply-add) and for the fixed per-tile epilogue work.
 int gemm_tile_width(int64_t M, int64_t N, int sms) {
     const int widths[3] = {256, 128, 64};
-    const double penalty[3] = {1.0, 1.37, 2.64};  // measured: 8192^3 at each width
+    const double penalty[3] = {1.0, 1.65, 3.24};  // measured: 8192^3 at each width (pairs)
     const int64_t num_m = (M + kBM - 1) / kBM;
     const bool pair = num_m >= 2 && gemm_pairs_enabled();
     const int64_t num_mu = pair ? (num_m + 1) / 2 : num_m;
