@@ -167,10 +167,11 @@ bsg_status bsgemm_i8_contract(int64_t M, int64_t N, int64_t K, int relu, float *
 bsg_status bsg_selftest_scales(uint32_t first_bits, uint32_t last_bits,
                                uint64_t *mismatches_host);
 
-/* The output tile width (64, 128 or 256 columns; tiles are 128 rows) the
- * GEMM kernel uses for an M x N problem on `sms` SMs: the width with the
- * fewest idle SMs in the last wave, weighted by the narrower tiles' lower
- * MMA efficiency.  Host-only; -1 on bad arguments.  No counterpart in the
+/* The output tile width (64, 128, 192 or 256 columns) the GEMM kernel uses
+ * for an M x N problem on `sms` SMs: the width with the fewest idle SMs in
+ * the last wave, weighted by the narrower tiles' lower MMA efficiency.
+ * Tiles are 256 rows on pairs of SMs (sms / 2 of them) when M > 128, else
+ * 128 rows on single SMs.  Host-only; -1 on bad arguments.  No counterpart in the
  * pages: it documents this library's schedule. */
 int bsg_gemm_tile_width(int64_t M, int64_t N, int sms);
 

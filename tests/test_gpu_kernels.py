@@ -1,0 +1,74 @@
+"""Every GEMM kernel instantiation against the oracle, bitwise.
+
+The library picks one of eight tensor-core kernels per problem: a 128-row
+tile on one SM or a 256-row tile on a pair of SMs (M > 128), each at tile
+width 64, 128, 192 or 256.  The workloads exercise only the choices the
+schedule makes for them, so these tests force each kernel in turn (the
+BSG_GEMM_PAIR and BSG_GEMM_BN environment switches, read on every call) on
+ragged shapes -- partial m-blocks, a pair whose second CTA has no rows,
+partial n-tiles including N in (192, 256], one and several exact 1024-deep
+K chunks -- and compare C (and the int32 accumulators) with the oracle.
+
+Rule: "Verification -- why you can trust the numbers", section "The verified
+INT8 units": the result is defined independently of tiling, so every
+schedule must reproduce the oracle bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import assert_bits_equal, dev, host
+from verifiable_quantize_rows_gb300 import inputs
+import verifiable_quantize_rows_gb300 as bsg
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(300, 200, 100), (129, 257, 1025), (520, 383, 2100), (256, 256, 64), (640, 250, 960),
+          (100, 700, 1030)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("bn", [64, 128, 192, 256])
+@pytest.mark.parametrize("pair", [True, False], ids=["pair", "single"])
+def test_forced_kernel_matches_oracle(orc, monkeypatch, shape, bn, pair):
+    monkeypatch.setenv("BSG_GEMM_BN", str(bn))
+    monkeypatch.setenv("BSG_GEMM_PAIR", "1" if pair else "0")
+    M, N, K = shape
+    relu = (M + bn) % 2 == 1
+    A = inputs.normal((M, K), 1.0, M * 31 + K).numpy()
+    B = inputs.normal((K, N), 1.0, N * 17 + K).numpy()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    C = bsg.bsgemm_i8(dev(A), dev(B), relu=relu, dstatus=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    Co, _ = orc.bsgemm_i8(A, B, relu)
+    assert_bits_equal(host(C), Co, f"{shape} bn={bn} pair={pair} relu={relu}")
+
+
+@pytest.mark.parametrize("bn", [64, 128, 192, 256])
+@pytest.mark.parametrize("pair", [True, False], ids=["pair", "single"])
+def test_forced_kernel_int32_accumulators(orc, monkeypatch, bn, pair):
+    monkeypatch.setenv("BSG_GEMM_BN", str(bn))
+    monkeypatch.setenv("BSG_GEMM_PAIR", "1" if pair else "0")
+    M, N, K = 390, 230, 2200
+    rng = np.random.default_rng(bn + 7 * pair)
+    Aq = rng.integers(-127, 128, (M, K), dtype=np.int64).astype(np.int8)
+    Bq = rng.integers(-127, 128, (K, N), dtype=np.int64).astype(np.int8)
+    S = bsg.gemm_s32(dev(Aq), dev(Bq))
+    torch.cuda.synchronize()
+    want, _ = orc.gemm_s32(Aq, Bq)
+    assert_bits_equal(host(S), want, f"S bn={bn} pair={pair}")
+
+
+def test_switches_are_read_per_call(orc, monkeypatch):
+    """The same inputs through two different kernels give the same bits."""
+    M, N, K = 512, 384, 1500
+    A = inputs.uniform((M, K), -1, 1, 5).numpy()
+    B = inputs.uniform((K, N), -1, 1, 6).numpy()
+    outs = []
+    for bn, pair in ((256, "1"), (64, "0")):
+        monkeypatch.setenv("BSG_GEMM_BN", str(bn))
+        monkeypatch.setenv("BSG_GEMM_PAIR", pair)
+        outs.append(host(bsg.bsgemm_i8(dev(A), dev(B))))
+    torch.cuda.synchronize()
+    assert_bits_equal(outs[0], outs[1], "256/pair vs 64/single")

@@ -16,8 +16,9 @@ enum QuantOut : int {
     kOutHalfKMajor = 1,  // f16-encoded int8 in the GEMM's K-major operand layout
 };
 
-// GEMM tile: 128 x (64, 128 or 256) output per CTA, K in blocks of 64.
-// kBN is the widest tile; per-column arrays are padded to it.
+// GEMM tile: 128 x (64, 128, 192 or 256) output per CTA, K in blocks of 64.
+// kBN is the widest tile; per-column arrays hold round_up(N, kBN) + kBN
+// entries so that any tile width's last tile stays inside them.
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
@@ -61,14 +62,14 @@ cudaError_t launch_i8_rows_to_half(const int8_t *Q, int64_t rows, int64_t cols, 
 cudaError_t launch_i8_cols_to_half(const int8_t *Q, int64_t rows, int64_t cols, int64_t ldq,
                                    __half *out, int64_t ldo, cudaStream_t st);
 
-// The tile width (64, 128 or 256) the GEMM uses for an M x N problem, and
+// The tile width (64, 128, 192 or 256) the GEMM uses for an M x N problem, and
 // whether it runs 256-row tiles on CTA pairs when M > 128.
 int gemm_tile_width(int64_t M, int64_t N, int sms);
 bool gemm_pairs_enabled();
 // The tensor-core GEMM.  Aop: M x ldk f16, Bop: N x ldk f16 (both K-major,
 // ldk = operand_ld(K)).  mode 0: C = epi(S, sa, sb) (+ReLU) as float;
 // mode 1: S stored as int32.  sa / sb must hold round_up(M, kBM) /
-// round_up(N, kBN) floats (mode 0).
+// round_up(N, kBN) + kBN floats (mode 0).
 cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int64_t N,
                            int64_t K, const float *sa, const float *sb, int relu, int mode,
                            void *out, int64_t ldo, int32_t *dstatus, cudaStream_t st);

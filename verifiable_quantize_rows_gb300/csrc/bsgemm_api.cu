@@ -53,7 +53,8 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 //   Aop  f16 [M][ldk]        (ldk = K rounded up to 64)
 //   Bop  f16 [N][ldk]
 //   sa   f32 [round_up(M, 128)]
-//   sb   f32 [round_up(N, 256)]
+//   sb   f32 [round_up(N, 256) + 256] (a tile of any width may read its
+//        whole last tile of scales; entries past N are never used)
 //   partial column maxima (uint32) of op(A), then of op(B), for the
 //   column quantizes that need two passes (separate, since the two
 //   operands may be quantized at the same time)
@@ -72,7 +73,7 @@ UnitLayout unit_layout(int64_t M, int64_t N, int64_t K, int transA, int transB) 
     L.sa = off;
     off = align256(off + (size_t)round_up(M, kBM) * 4);
     L.sb = off;
-    off = align256(off + (size_t)round_up(N, kBN) * 4);
+    off = align256(off + (size_t)(round_up(N, kBN) + kBN) * 4);
     L.part = off;
     if (transA) off = align256(off + colmax_partial_bytes(K, M));
     L.part_b = off;

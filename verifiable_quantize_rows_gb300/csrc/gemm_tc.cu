@@ -27,7 +27,7 @@
 //     not by the tensor pipe; the pair also frees shared memory for two
 //     output staging buffers per epilogue warp.
 //   * single (M <= 128): one CTA computes a 128 x BN tile (cta_group::1).
-// BN in {64, 128, 256} is chosen per problem so that the last wave of tiles
+// BN in {64, 128, 192, 256} is chosen per problem so that the last wave of tiles
 // leaves few SMs idle; CTAs (pairs) are persistent and walk their tiles
 // round-robin.
 //
@@ -73,15 +73,17 @@ constexpr uint32_t kMaxSmem = 232448;           // 227 KiB per CTA
 // Compile-time layout of one tile width and kernel kind.
 template <int BN, bool PAIR>
 struct Cfg {
-    static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
+    static_assert(BN == 64 || BN == 128 || BN == 192 || BN == 256, "tile width");
     static constexpr int kBRows = PAIR ? BN / 2 : BN;  // B rows this CTA loads
     static constexpr uint32_t kBBytes = kBRows * kBK * 2;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages =
-        PAIR ? (BN == 256 ? 5 : BN == 128 ? 6 : 8) : (BN == 256 ? 4 : BN == 128 ? 5 : 6);
+    static constexpr int kStages = PAIR ? (BN >= 192 ? 5 : BN == 128 ? 6 : 8)
+                                        : (BN >= 192 ? 4 : BN == 128 ? 5 : 6);
     static constexpr int kBoxes = (!PAIR && BN == 256) ? 1 : 2;  // staging boxes per warp
-    static constexpr uint32_t kAccCols = BN;  // one accumulator buffer
-    static constexpr uint32_t kTmemCols = 2 * BN;
+    // one accumulator buffer (192 wide tiles keep 256-column buffers, so
+    // both start at a multiple of 256 and the allocation is a power of 2)
+    static constexpr uint32_t kAccCols = BN == 192 ? 256 : BN;
+    static constexpr uint32_t kTmemCols = 2 * kAccCols;
     static constexpr int kWarpCols = BN / 2;  // columns per epilogue warp
     static constexpr int kPieces = kWarpCols / 32;
     static constexpr uint32_t kOffEpi = kStages * kStageBytes;
@@ -594,13 +596,20 @@ cudaError_t launch_width(const CUtensorMap &ta, const CUtensorMap &tc, const __h
 
 // CTA pairs are used whenever M spans two or more 128-row blocks, unless
 // BSG_GEMM_PAIR=0 is set in the environment (the single-CTA kernel then runs
-// every shape; same results, for comparison).
+// every shape; same results).  Read on every call, like BSG_GEMM_BN below,
+// so that tests can run each kernel on the same inputs.
 bool gemm_pairs_enabled() {
-    static const bool on = [] {
-        const char *e = getenv("BSG_GEMM_PAIR");
-        return !(e && e[0] == '0' && e[1] == 0);
-    }();
-    return on;
+    const char *e = getenv("BSG_GEMM_PAIR");
+    return !(e && e[0] == '0' && e[1] == 0);
+}
+
+// BSG_GEMM_BN=64|128|192|256 forces the tile width (same results); anything
+// else, or nothing, leaves the choice to gemm_tile_width.
+static int forced_tile_width() {
+    const char *e = getenv("BSG_GEMM_BN");
+    if (!e) return 0;
+    const int v = atoi(e);
+    return (v == 64 || v == 128 || v == 192 || v == 256) ? v : 0;
 }
 
 // Tile width for an M x N problem on `sms` SMs: the one with the least
@@ -610,15 +619,15 @@ bool gemm_pairs_enabled() {
 // penalty for the narrower MMAs (which read more shared memory per
 // multiply-add) and for the fixed per-tile epilogue work.
 int gemm_tile_width(int64_t M, int64_t N, int sms) {
-    const int widths[3] = {256, 128, 64};
-    const double penalty[3] = {1.0, 1.65, 3.24};  // measured: 8192^3 at each width (pairs)
+    const int widths[4] = {256, 192, 128, 64};
+    const double penalty[4] = {1.0, 1.15, 1.65, 3.24};  // measured: 8192^3 at each width (pairs)
     const int64_t num_m = (M + kBM - 1) / kBM;
     const bool pair = num_m >= 2 && gemm_pairs_enabled();
     const int64_t num_mu = pair ? (num_m + 1) / 2 : num_m;
     const int64_t units = pair ? (sms / 2 > 0 ? sms / 2 : 1) : sms;
     int best = 256;
     double best_cost = 1e300;
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 4; ++i) {
         const int64_t tiles = num_mu * ((N + widths[i] - 1) / widths[i]);
         const int64_t rounds = (tiles + units - 1) / units;
         const double cost = (double)rounds * widths[i] / 256.0 * penalty[i];
@@ -664,9 +673,11 @@ cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int6
     p.tma_store = tma_store;
     p.dstatus = dstatus;
     const bool pair = p.num_m >= 2 && gemm_pairs_enabled();
-    switch (gemm_tile_width(M, N, device_sm_count())) {
+    const int forced = forced_tile_width();
+    switch (forced ? forced : gemm_tile_width(M, N, device_sm_count())) {
         case 64: return launch_width<64>(ta, tc, Bop, N, K, p, pair, st);
         case 128: return launch_width<128>(ta, tc, Bop, N, K, p, pair, st);
+        case 192: return launch_width<192>(ta, tc, Bop, N, K, p, pair, st);
         default: return launch_width<256>(ta, tc, Bop, N, K, p, pair, st);
     }
 }
