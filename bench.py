@@ -32,6 +32,10 @@ WORKLOAD = "gpt2_small_linears_M8192_qkv_fc_proj+probe1024"
 PROBE = (1024, 1024, 1024)
 PROBE_SEED = 0
 L2_FLUSH_BYTES = 256 << 20
+STAGE_REPEAT = 8          # launches per stage graph for the per-kernel durations
+GEMM_SOURCES = ("verifiable_quantize_rows_gb300/csrc/gemm_tc.cu",
+                "verifiable_quantize_rows_gb300/csrc/bsg_ptx.cuh")
+GEMM_PROFILE = "profiles/gemm_tc_gpt2_linears.md"
 
 
 def env_int(name, default):
@@ -58,6 +62,34 @@ def config_dict(n_gpus):
         "l2": "flushed between timed steps (256 MiB write); inputs resident in HBM",
         "parallelism": f"replicas x{n_gpus} (weak: each GPU runs the full step)",
     }
+
+
+def gemm_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in GEMM_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per GEMM launch from the committed ncu summary, if it was
+    taken on the current GEMM source (else None: the counters are stale)."""
+    p = os.path.join(ROOT, GEMM_PROFILE)
+    if not os.path.exists(p):
+        return None
+    src, per = None, {}
+    with open(p) as f:
+        for line in f:
+            parts = line.strip().strip("`").split()
+            if len(parts) == 2 and parts[0] == "source-sha256:":
+                src = parts[1]
+            elif len(parts) == 3 and parts[0] == "dram-bytes-per-launch":
+                per[parts[1].rstrip(":")] = int(parts[2])
+    if src != gemm_source_hash() or not per:
+        return None
+    return per
 
 
 def load_peaks():
@@ -194,11 +226,34 @@ def run_gpu(args, rank, world, local_rank):
         else:
             stage_probe()
 
+    # Per-kernel launch durations: each stage is captured STAGE_REPEAT times
+    # back to back in one graph, timed with events around the replay and
+    # divided by the repeat count (a one-launch graph would add the graph's
+    # own launch latency to every number).  Quantize stages rotate over
+    # STAGE_REPEAT copies of their inputs, so that every launch reads A and B
+    # from HBM as in the step; GEMM stages re-run on the operands their
+    # quantize stage wrote, which sit in L2 as they do in the step.
+    R = STAGE_REPEAT
+    for L in lin:
+        L["copies"] = [(L["A"].clone(), L["B"].clone()) for _ in range(R - 1)] + [(L["A"], L["B"])]
+
+    def stage_quantize_r(L):
+        for A_, B_ in L["copies"]:
+            bsg.bsgemm_i8_quantize(A_, B_, L["ws"], dstatus=dstatus)
+
+    def stage_contract_r(L):
+        for _ in range(R):
+            stage_contract(L)
+
+    def stage_probe_r():
+        for _ in range(R):
+            stage_probe()
+
     stages = []
     for L in lin:
-        stages.append(("quantize_" + L["name"], (lambda L=L: stage_quantize(L))))
-        stages.append(("gemm_" + L["name"], (lambda L=L: stage_contract(L))))
-    stages.append(("probe", stage_probe))
+        stages.append(("quantize_" + L["name"], (lambda L=L: stage_quantize_r(L))))
+        stages.append(("gemm_" + L["name"], (lambda L=L: stage_contract_r(L))))
+    stages.append(("probe", stage_probe_r))
 
     def barrier():
         if world > 1:
@@ -232,8 +287,9 @@ def run_gpu(args, rank, world, local_rank):
     # ---- timed region: device-resident inputs, L2 flushed between steps
     ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(g_stages) + 1)]
-           for _ in range(args.steps)]
+    stage_steps = max(10, min(args.steps, 50))
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(len(g_stages))] for _ in range(stage_steps)]
     clocks = ClockSampler(gpu_selector(local_rank))
     clocks.start()
     time.sleep(0.3)
@@ -245,20 +301,22 @@ def run_gpu(args, rank, world, local_rank):
         ev_step[s][0].record(stream)
         g_step.replay()
         ev_step[s][1].record(stream)
-    for s in range(args.steps):
-        flush.zero_()
-        evs[s][0].record(stream)
-        for k, (_, g) in enumerate(g_stages):
+    for s in range(stage_steps):
+        for k, (name, g) in enumerate(g_stages):
+            if not name.startswith("gemm_"):   # a GEMM reads what its quantize just wrote
+                flush.zero_()
+            e0, e1 = evs[s][k]
+            e0.record(stream)
             g.replay()
-            evs[s][k + 1].record(stream)
+            e1.record(stream)
     torch.cuda.synchronize()
     barrier()
     wall = time.perf_counter() - wall0
-    launches = (launches_step + launches_stages) * args.steps
+    launches = launches_step * args.steps + launches_stages * stage_steps
     clk = clocks.stop()
 
     step_ms_list = [a.elapsed_time(b) for a, b in ev_step]
-    stage_ms = [[ev[k].elapsed_time(ev[k + 1]) for k in range(len(g_stages))] for ev in evs]
+    stage_ms = [[a.elapsed_time(b) / R for a, b in row] for row in evs]
     ms_per_step = statistics.mean(step_ms_list)
     probe_hex = bytes(probe_out.cpu().tolist()).hex()
     # ---- end-to-end through the host-buffer entry point (copies inside)
@@ -300,6 +358,12 @@ def run_gpu(args, rank, world, local_rank):
 
     ops = step_ops()
     peaks, peak_kind = load_peaks()
+    prof = profiled_traffic()
+    traffic = (round(sum(prof[L["name"]] for L in lin) / len(lin))
+               if prof and all(L["name"] in prof for L in lin) else None)
+    # f16 operands read once, f32 C written once
+    algo_bytes = round(sum(2 * (L["M"] + L["N"]) * L["K"] + 4 * L["M"] * L["N"] for L in lin)
+                       / len(lin))
     # dominant kernel: the tensor-core contraction (one launch per linear),
     # timed per stage graph in the second half of the timed region
     gemm_ms = [statistics.mean(sm[2 * i + 1] for sm in stage_ms) for i in range(len(lin))]
@@ -336,7 +400,12 @@ def run_gpu(args, rank, world, local_rank):
             "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4),
             "peak_source": f"{peak_kind} bf16 burst (f16 dense rate = bf16 nominal)",
-            "traffic": None,
+            "traffic": traffic,
+            "traffic_note": ("DRAM bytes read + written per GEMM launch (mean of the three "
+                             "linears) from the committed ncu summary " + GEMM_PROFILE +
+                             ", taken on this GEMM source; null if the source has changed "
+                             "since"),
+            "algorithmic_bytes": algo_bytes,
             "per_gemm_ms": {L["name"]: round(g, 4) for L, g in zip(lin, gemm_ms)},
         },
         "quantize": {
@@ -359,8 +428,10 @@ def run_gpu(args, rank, world, local_rank):
         "gpu_launches": launches,
         "wall_s_timed": round(wall, 4),
         "timing": ("value/ms_per_step: the whole step replayed as one CUDA graph, CUDA events "
-                   "around each replay; roofline/quantize/probe: the same stages replayed as "
-                   "separate graphs with events between them, in the same timed region"),
+                   "around each replay, L2 flushed before each; roofline/quantize/probe: per "
+                   f"launch, each stage captured {R}x back to back in one graph and timed with "
+                   f"events around its replay / {R}, quantize over {R} input copies (reads from "
+                   "HBM), GEMM on the operands its quantize wrote (in L2, as in the step)"),
         "probe_overlap": bool(args.probe_overlap),
         "stage_sum_ms": round(statistics.mean(sum(x) for x in stage_ms), 4),
         "probe_hash": probe_hex,

@@ -52,6 +52,15 @@ cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int
                                  int out_kind, void *Q, int64_t ldq, float *scale, float *inv,
                                  uint32_t *partial, int32_t *dstatus, cudaStream_t st);
 
+// Both operands of the unit in one launch: A (M x K, lda) per row into Aop
+// (M x ldk f16) and sa, B (K x N, ldb) per column into Bop (N x ldk f16,
+// transposed) and sb.  cudaErrorNotSupported (nothing launched) when the
+// layout or size is outside the fused kernel's range.
+cudaError_t launch_quantize_ab(const float *A, int64_t M, int64_t K, int64_t lda,
+                               const float *B, int64_t N, int64_t ldb, __half *Aop,
+                               __half *Bop, int64_t ldk, float *sa, float *sb,
+                               int32_t *dstatus, cudaStream_t st);
+
 // Device check of the scale derivation over absmax bit patterns [first, last].
 cudaError_t launch_selftest_scales(uint32_t first, uint32_t last, unsigned long long *bad,
                                    cudaStream_t st);

@@ -175,6 +175,13 @@ bsg_status unit_quantize(const float *A, int64_t lda, int transA, const float *B
                        : launch_quantize_rows(B, N, K, ldb, kOutHalfKMajor, bop, ldk, sb, nullptr,
                                               dstatus, s);
     };
+    if (!transA && !transB) {
+        // the common layout: one launch for both operands
+        const cudaError_t ef = launch_quantize_ab(A, M, K, lda, B, N, ldb, aop, bop, ldk, sa, sb,
+                                                  dstatus, st);
+        if (ef == cudaSuccess) return BSG_OK;
+        if (ef != cudaErrorNotSupported) return BSG_ERR_CUDA;
+    }
     if (overlap) {
         std::lock_guard<std::mutex> guard(g_side_lock);
         SideStream *side = side_stream();

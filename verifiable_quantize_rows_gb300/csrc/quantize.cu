@@ -339,18 +339,19 @@ __global__ void __launch_bounds__(256)
 // once, reduced (shuffles, then shared memory across the row's warps) and
 // quantized from registers.  8 warps per block: 8 / WPR rows per block.
 template <int OUT, int WPR, int RV>
-__global__ void __launch_bounds__(256)
-    quantize_rows_wide_kernel(const float *__restrict__ X, int64_t rows, int64_t cols,
-                              int64_t ldx, void *__restrict__ Q, int64_t ldq,
-                              float *__restrict__ scale, float *__restrict__ inv,
-                              int32_t *__restrict__ dstatus) {
+__device__ __forceinline__ void rows_wide_block(int64_t blk, const float *__restrict__ X,
+                                                int64_t rows, int64_t cols, int64_t ldx,
+                                                void *__restrict__ Q, int64_t ldq,
+                                                float *__restrict__ scale,
+                                                float *__restrict__ inv,
+                                                int32_t *__restrict__ dstatus) {
     constexpr int RPB = 8 / WPR;
     __shared__ uint32_t red[8];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int rloc = warp / WPR;
     const int wr = warp % WPR;
-    const int64_t r = (int64_t)blockIdx.x * RPB + rloc;
+    const int64_t r = blk * RPB + rloc;
     const bool live = r < rows;
     const int64_t c4n = cols / 4;
     const float4 *xr = reinterpret_cast<const float4 *>(X + (live ? r : 0) * ldx);
@@ -389,6 +390,16 @@ __global__ void __launch_bounds__(256)
             store4<OUT>(Q, r * ldq + 4 * c4, quant(v[i].x, iv), quant(v[i].y, iv), quant(v[i].z, iv),
                         quant(v[i].w, iv));
     }
+}
+
+template <int OUT, int WPR, int RV>
+__global__ void __launch_bounds__(256)
+    quantize_rows_wide_kernel(const float *__restrict__ X, int64_t rows, int64_t cols,
+                              int64_t ldx, void *__restrict__ Q, int64_t ldq,
+                              float *__restrict__ scale, float *__restrict__ inv,
+                              int32_t *__restrict__ dstatus) {
+    rows_wide_block<OUT, WPR, RV>((int64_t)blockIdx.x, X, rows, cols, ldx, Q, ldq, scale, inv,
+                                  dstatus);
 }
 
 // Columns, single pass: a cluster of CS CTAs shares a strip of 32 columns;
@@ -490,6 +501,144 @@ __global__ void __launch_bounds__(256)
         }
     }
     cluster.sync();  // no CTA leaves while another may still read its maxima
+}
+
+// Both operands of the unit in one launch, for the common layout (A stored
+// M x K, quantized per row; B stored K x N, quantized per column, written
+// transposed).  The column work is latency-bound (a small matrix, a max
+// before any output) and the row work bandwidth-bound, so they share the
+// launch: clusters of CS CTAs each take one 32-column strip of B and come
+// first in launch order, and the row blocks of A fill the rest of the grid
+// (grid (strips + row clusters, CS), cluster (1, CS, 1); row clusters do
+// not interact).  A strip CTA holds its (at most 256) rows of the strip in
+// registers -- one read, all loads in flight at once -- reduces its partial
+// column maxima, combines them across the cluster through distributed
+// shared memory, quantizes from registers and writes the strip transposed
+// (Q[col][row], f16) through shared memory, each store a whole 128-byte row
+// segment.
+constexpr int kStripRows = 256;  // rows of a strip per CTA: 8 per thread
+
+__device__ __forceinline__ void cols_strip_block(const float *__restrict__ X, int64_t rows,
+                                                 int64_t cols, int64_t ldx, int R, int64_t strip,
+                                                 __half *__restrict__ Q, int64_t ldq,
+                                                 float *__restrict__ scale,
+                                                 int32_t *__restrict__ dstatus) {
+    __shared__ uint32_t red[32][33];  // [row phase][column] partial maxima
+    __shared__ uint32_t part[kStripCols];
+    __shared__ float s_inv[kStripCols];
+    __shared__ __align__(16) __half ts[kStripCols][kStripRows + 2];  // [column][row]
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int cs = (int)cluster.num_blocks();
+    const int t = threadIdx.x;
+    const int c4 = t & 7;   // float4 column group of the strip
+    const int rs = t >> 3;  // row phase, 0..31
+    const int64_t c0 = strip * kStripCols;
+    const int64_t r0 = (int64_t)rank * R;
+    const int64_t left = rows - r0;
+    const int nr = left <= 0 ? 0 : (left < R ? (int)left : R);  // R <= kStripRows
+    const int64_t col = c0 + 4 * c4;
+    const bool full4 = col + 3 < cols;
+
+    float4 v[kStripRows / 32];
+#pragma unroll
+    for (int i = 0; i < kStripRows / 32; ++i) {
+        const int r = rs + 32 * i;
+        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < nr) {
+            const float *src = X + (r0 + r) * ldx + col;
+            if (full4) {
+                v[i] = __ldg(reinterpret_cast<const float4 *>(src));
+            } else {
+                if (col < cols) v[i].x = __ldg(src);
+                if (col + 1 < cols) v[i].y = __ldg(src + 1);
+                if (col + 2 < cols) v[i].z = __ldg(src + 2);
+            }
+        }
+    }
+    uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
+#pragma unroll
+    for (int i = 0; i < kStripRows / 32; ++i) {
+        m0 = max(m0, absbits(v[i].x));
+        m1 = max(m1, absbits(v[i].y));
+        m2 = max(m2, absbits(v[i].z));
+        m3 = max(m3, absbits(v[i].w));
+    }
+    red[rs][4 * c4 + 0] = m0;
+    red[rs][4 * c4 + 1] = m1;
+    red[rs][4 * c4 + 2] = m2;
+    red[rs][4 * c4 + 3] = m3;
+    __syncthreads();
+    if (t < kStripCols) {
+        uint32_t mm = 0;
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i) mm = max(mm, red[i][t]);
+        part[t] = mm;
+    }
+    cluster.sync();  // every CTA's partial maxima are visible cluster-wide
+    if (t < kStripCols) {
+        uint32_t mm = 0;
+        for (int k = 0; k < cs; ++k) mm = max(mm, *cluster.map_shared_rank(&part[t], k));
+        float sc, iv;
+        scale_from_max(mm, sc, iv);
+        s_inv[t] = iv;
+        if (rank == 0 && c0 + t < cols) {
+            scale[c0 + t] = sc;
+            if (mm >= kNonfiniteBits && dstatus) atomicOr(dstatus, 1);
+        }
+    }
+    __syncthreads();
+    const float i0 = s_inv[4 * c4], i1 = s_inv[4 * c4 + 1], i2 = s_inv[4 * c4 + 2],
+                i3 = s_inv[4 * c4 + 3];
+#pragma unroll
+    for (int i = 0; i < kStripRows / 32; ++i) {
+        const int r = rs + 32 * i;
+        ts[4 * c4 + 0][r] = __float2half_rn(quant(v[i].x, i0));
+        ts[4 * c4 + 1][r] = __float2half_rn(quant(v[i].y, i1));
+        ts[4 * c4 + 2][r] = __float2half_rn(quant(v[i].z, i2));
+        ts[4 * c4 + 3][r] = __float2half_rn(quant(v[i].w, i3));
+    }
+    __syncthreads();
+    // 32 output rows (columns of X), nr halves each from row r0: one warp
+    // per output row at a time, 4-byte pairs, 128 bytes per store
+    const int w = t >> 5, lane = t & 31;
+    for (int n = w; n < kStripCols; n += 8) {
+        if (c0 + n >= cols) continue;
+        __half *dst = Q + (c0 + n) * ldq + r0;
+#pragma unroll
+        for (int k2 = 2 * lane; k2 < kStripRows; k2 += 64) {
+            if (k2 + 1 < nr)
+                *reinterpret_cast<__half2 *>(dst + k2) = *reinterpret_cast<const __half2 *>(&ts[n][k2]);
+            else if (k2 < nr)
+                dst[k2] = ts[n][k2];
+        }
+    }
+    cluster.sync();  // no CTA leaves while another may still read its maxima
+}
+
+template <int WPR, int RV>
+__global__ void __launch_bounds__(256)
+    quantize_ab_kernel(const float *__restrict__ A, int64_t M, int64_t K, int64_t lda,
+                       __half *__restrict__ Aop, float *__restrict__ sa,
+                       const float *__restrict__ B, int64_t N, int64_t ldb,
+                       __half *__restrict__ Bop, float *__restrict__ sb, int64_t ldk, int R,
+                       int strips, int32_t *__restrict__ dstatus) {
+    if ((int)blockIdx.x < strips) {
+        cols_strip_block(B, K, N, ldb, R, (int64_t)blockIdx.x, Bop, ldk, sb, dstatus);
+    } else {
+        const int64_t blk = (int64_t)(blockIdx.x - strips) * gridDim.y + blockIdx.y;
+        rows_wide_block<kOutHalfKMajor, WPR, RV>(blk, A, M, K, lda, Aop, ldk, sa, nullptr,
+                                                 dstatus);
+    }
+}
+
+// The strip CTAs alone, for a column quantize that is not fused with a row
+// quantize: grid (strips, CS), cluster (1, CS, 1).
+__global__ void __launch_bounds__(256)
+    quantize_cols_strip_kernel(const float *__restrict__ X, int64_t rows, int64_t cols,
+                               int64_t ldx, int R, __half *__restrict__ Q, int64_t ldq,
+                               float *__restrict__ scale, int32_t *__restrict__ dstatus) {
+    cols_strip_block(X, rows, cols, ldx, R, (int64_t)blockIdx.x, Q, ldq, scale, dstatus);
 }
 
 __global__ void i8_rows_to_half_kernel(const int8_t *__restrict__ Q, int64_t rows, int64_t cols,
@@ -702,10 +851,113 @@ static cudaError_t launch_cols_cluster(const float *X, int64_t rows, int64_t col
                               Q, ldq, scale, inv, dstatus);
 }
 
+// Cluster size and rows per CTA of the register-resident strip kernels:
+// CTAs of at most 256 rows, clusters of at most `max_cs` CTAs.
+static bool strip_shape(int64_t rows, int max_cs, int &cs, int &R) {
+    if (rows < 1 || rows > (int64_t)max_cs * kStripRows) return false;
+    cs = (int)((rows + kStripRows - 1) / kStripRows);
+    R = (int)round_up((rows + cs - 1) / cs, 8);
+    return true;
+}
+
+static cudaError_t allow_big_clusters(const void *kernel, bool *ready) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!ready[dev]) {  // clusters of up to 16 CTAs
+        const cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        ready[dev] = true;
+    }
+    return cudaSuccess;
+}
+
+template <int WPR, int RV>
+static cudaError_t launch_ab(const float *A, int64_t M, int64_t K, int64_t lda, __half *Aop,
+                             float *sa, const float *B, int64_t N, int64_t ldb, __half *Bop,
+                             float *sb, int64_t ldk, int cs, int R, int32_t *dstatus,
+                             cudaStream_t st) {
+    constexpr int RPB = 8 / WPR;
+    const int64_t strips = (N + kStripCols - 1) / kStripCols;
+    const int64_t row_blocks = (M + RPB - 1) / RPB;
+    const int64_t row_clusters = (row_blocks + cs - 1) / cs;
+    if (strips + row_clusters > 0x7fffffff) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)(strips + row_clusters), (unsigned)cs, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)cs;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quantize_ab_kernel<WPR, RV>, A, M, K, lda, Aop, sa, B, N, ldb,
+                              Bop, sb, ldk, R, (int)strips, dstatus);
+}
+
+cudaError_t launch_quantize_ab(const float *A, int64_t M, int64_t K, int64_t lda,
+                               const float *B, int64_t N, int64_t ldb, __half *Aop,
+                               __half *Bop, int64_t ldk, float *sa, float *sb,
+                               int32_t *dstatus, cudaStream_t st) {
+    const bool vecA = (K % 4 == 0) && (lda % 4 == 0) &&
+                      (reinterpret_cast<uintptr_t>(A) % 16 == 0) && ((ldk * 2) % 8 == 0) &&
+                      (reinterpret_cast<uintptr_t>(Aop) % 8 == 0);
+    const int layout = vecA ? row_layout(K) : -1;
+    const bool vecB = (ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(B) % 16 == 0) &&
+                      (ldk % 2 == 0) && (reinterpret_cast<uintptr_t>(Bop) % 4 == 0);
+    // Strip CTAs of at most 256 rows, at most 8 to a cluster (K <= 2048):
+    // every row block of the grid is launched in a cluster of the same size,
+    // and larger clusters (with the strip CTAs' registers) slowed the row
+    // blocks down more than the fusion saved.
+    int cs = 0, R = 0;
+    if (layout < 0 || !vecB || !strip_shape(K, 8, cs, R)) return cudaErrorNotSupported;
+    cudaError_t e = cudaErrorNotSupported;
+    switch (layout) {
+        case 0: e = launch_ab<1, 2>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, st); break;
+        case 1: e = launch_ab<1, 4>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, st); break;
+        case 2: e = launch_ab<1, 6>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, st); break;
+        case 3: e = launch_ab<1, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, st); break;
+        case 4: e = launch_ab<2, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, st); break;
+        case 5: e = launch_ab<4, 6>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, st); break;
+        case 6: e = launch_ab<4, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, st); break;
+        default: return cudaErrorNotSupported;  // rows longer than 4096: not fused
+    }
+    count_launches(1);
+    return e;
+}
+
 cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int64_t ldx,
                                  int out_kind, void *Q, int64_t ldq, float *scale, float *inv,
                                  uint32_t *partial, int32_t *dstatus, cudaStream_t st) {
     int cs = 0, R = 0;
+    // the GEMM's transposed f16 operand, no inv wanted, 16-byte rows: strip CTAs
+    if (out_kind == kOutHalfKMajor && !inv && ldx % 4 == 0 &&
+        reinterpret_cast<uintptr_t>(X) % 16 == 0 && ldq % 2 == 0 &&
+        reinterpret_cast<uintptr_t>(Q) % 4 == 0 && strip_shape(rows, 16, cs, R)) {
+        static bool ready[64] = {false};
+        cudaError_t e = allow_big_clusters((const void *)quantize_cols_strip_kernel, ready);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3((unsigned)((cols + kStripCols - 1) / kStripCols), (unsigned)cs, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = (unsigned)cs;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, quantize_cols_strip_kernel, X, rows, cols, ldx, R,
+                               static_cast<__half *>(Q), ldq, scale, dstatus);
+        count_launches(1);
+        return e;
+    }
     if (cols_cluster_shape(rows, cols, cs, R)) {
         cudaError_t e = out_kind == kOutInt8
                             ? launch_cols_cluster<kOutInt8>(X, rows, cols, ldx, cs, R, Q, ldq, scale,
