@@ -58,7 +58,8 @@ typedef enum {
     BSG_ERR_CUDA = 4,        /* a CUDA call or launch failed */
     BSG_ERR_NONFINITE = 5,   /* only as a host-side summary; see BSG_DSTATUS_NONFINITE */
     BSG_ERR_TIMEOUT = 6,     /* only as a host-side summary; see BSG_DSTATUS_TIMEOUT */
-    BSG_ERR_UNSUPPORTED = 7  /* the current device is not sm_103 */
+    BSG_ERR_UNSUPPORTED = 7, /* the current device is not sm_103 */
+    BSG_ERR_SELFTEST = 8     /* bsg_selftest found a wrong result */
 } bsg_status;
 
 #define BSG_MAX_K 133144
@@ -202,6 +203,38 @@ uint64_t bsg_launch_count(void);
 #define BSG_NOALLOC_SCRATCH_BYTES (64u << 20)
 bsg_status bsgemm_i8_noalloc(const float *A, const float *B, int64_t M, int64_t N, int64_t K,
                              int relu, float *C, int32_t *dstatus, void *stream);
+
+/* ---- verification of live results ----------------------------------------- */
+
+/* The live audit ("Verification -- why you can trust the numbers", section
+ * "Layer 2: the live audit"): `nsamples` cells of C, chosen by SplitMix64
+ * seeded with `seed` (output 2s gives sample s's row mod M, output 2s+1 its
+ * column mod N), are recomputed on the CUDA cores by a path that shares no
+ * kernel with bsgemm_i8 -- the cell's row of A and column of B read from the
+ * f32 inputs, scales from the f64 definition, int64 dot product, f32
+ * epilogue -- and every cell whose bits differ from C adds 1 to *mismatches
+ * (DEVICE uint32, not cleared by the call).  Cells whose row or column holds
+ * Inf or NaN are skipped.  A (M x K, lda >= K), B (K x N, ldb >= N), C (M x N,
+ * ldc >= N): the inputs and output of one bsgemm_i8(A, B, relu) call,
+ * row-major device memory.  `cells` (DEVICE int64[2 * nsamples], may be NULL)
+ * receives the sampled (row, column) pairs.  1 <= nsamples <= 1 << 24.
+ * Asynchronous on `stream`. */
+bsg_status bsg_audit(const float *A, int64_t lda, const float *B, int64_t ldb, const float *C,
+                     int64_t ldc, int64_t M, int64_t N, int64_t K, int relu, uint64_t seed,
+                     int nsamples, uint32_t *mismatches, int64_t *cells, void *stream);
+
+/* The init gate ("Layer 1: exact init gates"): runs the probe (seed 0,
+ * 1024^3) through the live kernels, compares its hash with the known answer
+ * the CPU oracle computes for it, and audits 4096 cells of that GEMM with
+ * bsg_audit.  Returns BSG_OK when both agree, BSG_ERR_SELFTEST when either
+ * does not (other codes for argument or CUDA errors).  `workspace`: DEVICE
+ * memory of bsg_selftest_workspace_size() bytes, 256-byte aligned.
+ * *audit_mismatches_host and *hash_ok_host (each may be NULL) receive the
+ * audit's mismatch count and 1 if the hash matched.  Synchronous (default
+ * stream). */
+size_t bsg_selftest_workspace_size(void);
+bsg_status bsg_selftest(void *workspace, size_t ws_bytes, uint32_t *audit_mismatches_host,
+                        int *hash_ok_host);
 
 /* bsgemm_i8 on HOST buffers (packed row-major; pinned memory gives
  * asynchronous copies): copies A and B to the device, runs the unit, copies

@@ -19,7 +19,8 @@ def test_header_declares_the_boundary():
     names = bsg.exported_symbols()
     for required in ("bsg_quantize_rows", "bsg_quantize_cols", "bsg_gemm_s32", "bsg_epilogue",
                      "bsgemm_i8", "bsgemm_i8_ex", "bsgemm_i8_host", "bsg_hash_f32",
-                     "bsg_probe_hash", "bsg_probe_hash_async", "bsg_status_str"):
+                     "bsg_probe_hash", "bsg_probe_hash_async", "bsg_status_str", "bsg_audit",
+                     "bsg_selftest"):
         assert required in names
 
 
@@ -30,7 +31,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings_and_version(lib):
     assert lib.bsg_version() >= 100
-    for code in range(8):
+    for code in range(9):
         assert lib.bsg_status_str(code).startswith(b"BSG_")
 
 
@@ -65,8 +66,34 @@ def test_argument_errors_without_gpu(lib):
                             None) == 1
     assert lib.bsg_hash_f32(dummy, 2, 2, 2, None, dummy, 1 << 20, None) == 1
     assert lib.bsg_probe_hash(0, 4, 4, 4, None, dummy, 1 << 20, None) == 1
+    # audit: null mismatch counter, ldc < N, no samples, K over the limit
+    assert lib.bsg_audit(dummy, 4, dummy, 4, dummy, 4, 4, 4, 4, 0, 0, 8, None, None, None) == 1
+    assert lib.bsg_audit(dummy, 4, dummy, 4, dummy, 3, 4, 4, 4, 0, 0, 8, dummy, None, None) == 1
+    assert lib.bsg_audit(dummy, 4, dummy, 4, dummy, 4, 4, 4, 4, 0, 0, 0, dummy, None, None) == 1
+    assert lib.bsg_audit(dummy, bsg.MAX_K + 1, dummy, 4, dummy, 4, 4, 4, bsg.MAX_K + 1, 0, 0, 8,
+                         dummy, None, None) == 2
+    # self-test: missing or small workspace
+    assert lib.bsg_selftest(None, 0, None, None) == 3
+    assert lib.bsg_selftest(dummy, 16, None, None) == 3
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         bsg.load(str(tmp_path / "missing.so"))
+
+
+def test_selftest_known_answer_is_the_oracle_golden():
+    """The self-test's compiled-in probe hash equals the value the oracle
+    wrote to tests/golden/probe_hash.txt for seed 0 at 1024^3."""
+    import re
+    here = os.path.dirname(os.path.abspath(__file__))
+    src = open(os.path.join(here, "..", "verifiable_quantize_rows_gb300", "csrc",
+                            "bsgemm_api.cu")).read()
+    body = re.search(r"kProbeKnownAnswer\[32\] = \{(.*?)\};", src, re.S).group(1)
+    compiled = bytes(int(x, 16) for x in re.findall(r"0x([0-9a-f]{2})", body)).hex()
+    golden = None
+    for line in open(os.path.join(here, "golden", "probe_hash.txt")):
+        p = line.split()
+        if len(p) == 5 and p[:4] == ["0", "1024", "1024", "1024"]:
+            golden = p[4]
+    assert golden is not None and compiled == golden

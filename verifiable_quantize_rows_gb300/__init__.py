@@ -76,6 +76,10 @@ def _declare(lib):
         "bsg_probe_hash_async": ([ctypes.c_uint64, _i64, _i64, _i64, _vp, _vp, _sz, _vp, _vp],
                                  _i32),
         "bsg_probe_hash": ([ctypes.c_uint64, _i64, _i64, _i64, _vp, _vp, _sz, _vp], _i32),
+        "bsg_audit": ([_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _i64, _i32, ctypes.c_uint64,
+                       _i32, _vp, _vp, _vp], _i32),
+        "bsg_selftest_workspace_size": ([], _sz),
+        "bsg_selftest": ([_vp, _sz, _vp, _vp], _i32),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -344,6 +348,41 @@ def hash_f32(C, stream=None, workspace=None) -> bytes:
     _check(lib.bsg_hash_f32(_ptr(C), M, N, N, _ptr(out), wp, wn, _stream_ptr(stream)),
            "bsg_hash_f32")
     return bytes(out.cpu().tolist())
+
+
+def audit(A, B, C, relu=False, seed: int = 0, nsamples: int = 256, mismatches=None,
+          cells=None, stream=None):
+    """Live audit of C = bsgemm_i8(A, B, relu): `nsamples` seeded cells
+    recomputed on the CUDA cores; mismatches are added to the device uint32
+    tensor `mismatches` (a fresh zero one if None), which is returned.
+    `cells` (int64, 2 * nsamples elements, or None) receives the sampled
+    (row, column) pairs."""
+    torch = _torch()
+    _need(A, torch.float32, "A")
+    _need(B, torch.float32, "B")
+    _need(C, torch.float32, "C")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2 or tuple(C.shape) != (M, N):
+        raise ValueError("shapes differ")
+    if mismatches is None:
+        mismatches = torch.zeros(1, dtype=torch.int32, device=A.device)
+    if cells is not None and (cells.dtype != torch.int64 or cells.numel() < 2 * nsamples):
+        raise ValueError("cells must be an int64 tensor of 2 * nsamples elements")
+    _check(load().bsg_audit(_ptr(A), K, _ptr(B), N, _ptr(C), N, M, N, K, int(bool(relu)),
+                            ctypes.c_uint64(seed), int(nsamples), _ptr(mismatches), _ptr(cells),
+                            _stream_ptr(stream)), "bsg_audit")
+    return mismatches
+
+
+def selftest(workspace=None):
+    """The init gate: (status, audit mismatches, hash matched).  Synchronous."""
+    lib = load()
+    wp, wn = _ws(workspace, lib.bsg_selftest_workspace_size())
+    mis = ctypes.c_uint32(0)
+    ok = ctypes.c_int(0)
+    st = lib.bsg_selftest(wp, wn, ctypes.byref(mis), ctypes.byref(ok))
+    return int(st), int(mis.value), bool(ok.value)
 
 
 def probe_hash_async(seed: int, M: int = 1024, N: int = 1024, K: int = 1024, out=None,

@@ -61,6 +61,12 @@ cudaError_t launch_quantize_ab(const float *A, int64_t M, int64_t K, int64_t lda
                                __half *Bop, int64_t ldk, float *sa, float *sb,
                                int32_t *dstatus, cudaStream_t st);
 
+// The live audit: `nsamples` seeded cells of C recomputed on the CUDA cores
+// from the f32 inputs; mismatching cells are counted into *mismatches.
+cudaError_t launch_audit(const float *A, int64_t lda, const float *B, int64_t ldb, const float *C,
+                         int64_t ldc, int64_t M, int64_t N, int64_t K, int relu, uint64_t seed,
+                         int nsamples, uint32_t *mismatches, int64_t *cells, cudaStream_t st);
+
 // Device check of the scale derivation over absmax bit patterns [first, last].
 cudaError_t launch_selftest_scales(uint32_t first, uint32_t last, unsigned long long *bad,
                                    cudaStream_t st);

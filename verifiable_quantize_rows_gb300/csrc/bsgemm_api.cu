@@ -253,6 +253,7 @@ const char *bsg_status_str(bsg_status s) {
         case BSG_ERR_NONFINITE: return "BSG_ERR_NONFINITE: non-finite input";
         case BSG_ERR_TIMEOUT: return "BSG_ERR_TIMEOUT: a bounded device wait expired";
         case BSG_ERR_UNSUPPORTED: return "BSG_ERR_UNSUPPORTED: device is not sm_103";
+        case BSG_ERR_SELFTEST: return "BSG_ERR_SELFTEST: the self-test found a wrong result";
     }
     return "unknown bsg_status";
 }
@@ -510,6 +511,59 @@ bsg_status bsg_probe_hash(uint64_t seed, int64_t M, int64_t N, int64_t K, uint8_
     if (hstat & BSG_DSTATUS_TIMEOUT) return BSG_ERR_TIMEOUT;
     if (hstat & BSG_DSTATUS_NONFINITE) return BSG_ERR_NONFINITE;
     return BSG_OK;
+}
+
+bsg_status bsg_audit(const float *A, int64_t lda, const float *B, int64_t ldb, const float *C,
+                     int64_t ldc, int64_t M, int64_t N, int64_t K, int relu, uint64_t seed,
+                     int nsamples, uint32_t *mismatches, int64_t *cells, void *stream) {
+    if (!A || !B || !C || !mismatches || !dims_ok(M, N, K)) return BSG_ERR_ARG;
+    if (lda < K || ldb < N || ldc < N || nsamples < 1 || nsamples > (1 << 24)) return BSG_ERR_ARG;
+    if (K > BSG_MAX_K) return BSG_ERR_K_TOO_LARGE;
+    bsg_status s = check_device();
+    if (s != BSG_OK) return s;
+    return from_cuda(launch_audit(A, lda, B, ldb, C, ldc, M, N, K, relu, seed, nsamples,
+                                  mismatches, cells, static_cast<cudaStream_t>(stream)));
+}
+
+// The probe hash of seed 0 at M = N = K = 1024, as the CPU oracle computes it
+// (its SplitMix64 inputs, its quantize, exact contraction and epilogue, its
+// BLAKE2s tree): the self-test's known answer.
+static const uint8_t kProbeKnownAnswer[32] = {
+    0xdd, 0x11, 0x9c, 0x18, 0x51, 0xaf, 0x87, 0x41, 0xe7, 0x50, 0xdd, 0x2a, 0x3f, 0x14, 0xa0, 0x42,
+    0x72, 0x4f, 0x6c, 0xce, 0xd2, 0x6e, 0xd2, 0x08, 0xf6, 0xfc, 0x07, 0xd8, 0xdd, 0xc9, 0x41, 0xe8};
+static const int64_t kSelftestN = 1024;
+static const int kSelftestSamples = 4096;
+
+size_t bsg_selftest_workspace_size(void) {
+    return bsg_probe_workspace_size(kSelftestN, kSelftestN, kSelftestN) + 256;
+}
+
+bsg_status bsg_selftest(void *workspace, size_t ws_bytes, uint32_t *audit_mismatches_host,
+                        int *hash_ok_host) {
+    const size_t pws = bsg_probe_workspace_size(kSelftestN, kSelftestN, kSelftestN);
+    if (!ws_ok(workspace, ws_bytes, pws + 256)) return BSG_ERR_WORKSPACE;
+    bsg_status s = check_device();
+    if (s != BSG_OK) return s;
+    uint8_t digest[32];
+    s = bsg_probe_hash(0, kSelftestN, kSelftestN, kSelftestN, digest, workspace, pws, nullptr);
+    if (s != BSG_OK) return s;
+    int hash_ok = memcmp(digest, kProbeKnownAnswer, 32) == 0;
+    // audit the probe's GEMM, whose A, B and C are still in the probe workspace
+    size_t offs[6];
+    probe_parts(kSelftestN, kSelftestN, kSelftestN, offs);
+    uint32_t *dmis = at<uint32_t>(workspace, pws);
+    if (cudaMemsetAsync(dmis, 0, sizeof(uint32_t), nullptr) != cudaSuccess) return BSG_ERR_CUDA;
+    if (launch_audit(at<float>(workspace, offs[0]), kSelftestN, at<float>(workspace, offs[1]),
+                     kSelftestN, at<float>(workspace, offs[2]), kSelftestN, kSelftestN,
+                     kSelftestN, kSelftestN, 0, 0x5eed, kSelftestSamples, dmis, nullptr,
+                     nullptr) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    uint32_t mis = 0;
+    if (cudaMemcpy(&mis, dmis, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    if (audit_mismatches_host) *audit_mismatches_host = mis;
+    if (hash_ok_host) *hash_ok_host = hash_ok;
+    return (hash_ok && mis == 0) ? BSG_OK : BSG_ERR_SELFTEST;
 }
 
 }  // extern "C"
