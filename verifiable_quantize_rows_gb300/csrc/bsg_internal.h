@@ -41,9 +41,11 @@ int device_sm_count();
 // Host-side count of kernel launches made by this library.
 void count_launches(int n);
 
+// zero2 (may be NULL): two words zeroed by the launch (a GEMM tile counter).
 cudaError_t launch_quantize_rows(const float *X, int64_t rows, int64_t cols, int64_t ldx,
                                  int out_kind, void *Q, int64_t ldq, float *scale, float *inv,
-                                 int32_t *dstatus, cudaStream_t st);
+                                 int32_t *dstatus, cudaStream_t st,
+                                 unsigned int *zero2 = nullptr);
 
 // Columns: a partial-max pass over row slices, then a quantize pass.
 // kOutInt8 keeps X's layout (Q is rows x cols); kOutHalfKMajor writes the
@@ -59,7 +61,7 @@ cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int
 cudaError_t launch_quantize_ab(const float *A, int64_t M, int64_t K, int64_t lda,
                                const float *B, int64_t N, int64_t ldb, __half *Aop,
                                __half *Bop, int64_t ldk, float *sa, float *sb,
-                               int32_t *dstatus, cudaStream_t st);
+                               int32_t *dstatus, unsigned int *zero2, cudaStream_t st);
 
 // The live audit: `nsamples` seeded cells of C recomputed on the CUDA cores
 // from the f32 inputs; mismatching cells are counted into *mismatches.
@@ -84,10 +86,14 @@ bool gemm_pairs_enabled();
 // The tensor-core GEMM.  Aop: M x ldk f16, Bop: N x ldk f16 (both K-major,
 // ldk = operand_ld(K)).  mode 0: C = epi(S, sa, sb) (+ReLU) as float;
 // mode 1: S stored as int32.  sa / sb must hold round_up(M, kBM) /
-// round_up(N, kBN) + kBN floats (mode 0).
+// round_up(N, kBN) + kBN floats (mode 0).  `ticket`: two unsigned ints of
+// device memory, the tile counter: zero before the first launch on it (the
+// quantize step that fills a unit workspace zeroes it), and zero again after
+// every launch that completes.
 cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int64_t N,
                            int64_t K, const float *sa, const float *sb, int relu, int mode,
-                           void *out, int64_t ldo, int32_t *dstatus, cudaStream_t st);
+                           void *out, int64_t ldo, int32_t *dstatus, unsigned int *ticket,
+                           cudaStream_t st);
 
 cudaError_t launch_epilogue(const int32_t *S, int64_t lds, const float *sa, const float *sb,
                             int64_t M, int64_t N, int relu, float *C, int64_t ldc,

@@ -231,6 +231,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_cl(uint32_t bar, uint32_t 
                  : "memory");
 }
 
+// Arrive on a barrier of another CTA of the cluster, releasing this thread's
+// prior writes (including shared::cluster stores into that CTA) cluster-wide.
+__device__ __forceinline__ void mbar_arrive_release_cl(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32-bit store to shared::cluster address `addr` (any CTA of the cluster).
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // try_wait / bounded wait on a barrier of this CTA that other CTAs of the
 // cluster arrive on (acquire at cluster scope).
 __device__ __forceinline__ bool mbar_try_wait_cl(uint64_t *bar, uint32_t parity) {

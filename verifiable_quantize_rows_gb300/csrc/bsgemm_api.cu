@@ -55,11 +55,12 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 //   sa   f32 [round_up(M, 128)]
 //   sb   f32 [round_up(N, 256) + 256] (a tile of any width may read its
 //        whole last tile of scales; entries past N are never used)
+//   the GEMM's tile counter (one uint32 in 256 bytes)
 //   partial column maxima (uint32) of op(A), then of op(B), for the
 //   column quantizes that need two passes (separate, since the two
 //   operands may be quantized at the same time)
 struct UnitLayout {
-    size_t aop, bop, sa, sb, part, part_b, total;
+    size_t aop, bop, sa, sb, ticket, part, part_b, total;
 };
 
 UnitLayout unit_layout(int64_t M, int64_t N, int64_t K, int transA, int transB) {
@@ -74,6 +75,8 @@ UnitLayout unit_layout(int64_t M, int64_t N, int64_t K, int transA, int transB) 
     off = align256(off + (size_t)round_up(M, kBM) * 4);
     L.sb = off;
     off = align256(off + (size_t)(round_up(N, kBN) + kBN) * 4);
+    L.ticket = off;  // the GEMM's tile counter
+    off += 256;
     L.part = off;
     if (transA) off = align256(off + colmax_partial_bytes(K, M));
     L.part_b = off;
@@ -161,10 +164,16 @@ bsg_status unit_quantize(const float *A, int64_t lda, int transA, const float *B
     float *sb = at<float>(ws, L.sb);
     uint32_t *part_a = at<uint32_t>(ws, L.part);
     uint32_t *part_b = at<uint32_t>(ws, L.part_b);
+    // The GEMM claims tiles from a counter in the workspace that must start
+    // at zero: the quantize launch of op(A) zeroes it (the GEMM sets it back
+    // to zero whenever it completes).
+    unsigned int *ticket = at<unsigned int>(ws, L.ticket);
+    if (transA && cudaMemsetAsync(ticket, 0, 2 * sizeof(unsigned int), st) != cudaSuccess)
+        return BSG_ERR_CUDA;
     // op(A) per row: a row quantize of A, or a column quantize of the stored K x M.
     auto quant_a = [&](cudaStream_t s) {
         return !transA ? launch_quantize_rows(A, M, K, lda, kOutHalfKMajor, aop, ldk, sa, nullptr,
-                                              dstatus, s)
+                                              dstatus, s, ticket)
                        : launch_quantize_cols(A, K, M, lda, kOutHalfKMajor, aop, ldk, sa, nullptr,
                                               part_a, dstatus, s);
     };
@@ -178,7 +187,7 @@ bsg_status unit_quantize(const float *A, int64_t lda, int transA, const float *B
     if (!transA && !transB) {
         // the common layout: one launch for both operands
         const cudaError_t ef = launch_quantize_ab(A, M, K, lda, B, N, ldb, aop, bop, ldk, sa, sb,
-                                                  dstatus, st);
+                                                  dstatus, ticket, st);
         if (ef == cudaSuccess) return BSG_OK;
         if (ef != cudaErrorNotSupported) return BSG_ERR_CUDA;
     }
@@ -214,7 +223,7 @@ bsg_status unit_contract(int64_t M, int64_t N, int64_t K, int relu, float *C, in
     if (s != BSG_OK) return s;
     return from_cuda(launch_gemm_tc(at<__half>(ws, L.aop), at<__half>(ws, L.bop), M, N, K,
                                     at<float>(ws, L.sa), at<float>(ws, L.sb), relu, 0, C, ldc,
-                                    dstatus, st));
+                                    dstatus, at<unsigned int>(ws, L.ticket), st));
 }
 
 }  // namespace
@@ -291,7 +300,7 @@ bsg_status bsg_quantize_cols(const float *X, int64_t rows, int64_t cols, int64_t
 size_t bsg_gemm_s32_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (!dims_ok(M, N, K)) return 0;
     const int64_t ldk = operand_ld(K);
-    return align256((size_t)M * ldk * 2) + align256((size_t)N * ldk * 2);
+    return align256((size_t)M * ldk * 2) + align256((size_t)N * ldk * 2) + 256;  // + tile counter
 }
 
 bsg_status bsg_gemm_s32(const int8_t *Aq, int64_t lda, const int8_t *Bq, int64_t ldb, int64_t M,
@@ -308,8 +317,11 @@ bsg_status bsg_gemm_s32(const int8_t *Aq, int64_t lda, const int8_t *Bq, int64_t
     __half *bop = at<__half>(workspace, align256((size_t)M * ldk * 2));
     if (launch_i8_rows_to_half(Aq, M, K, lda, aop, ldk, st) != cudaSuccess) return BSG_ERR_CUDA;
     if (launch_i8_cols_to_half(Bq, K, N, ldb, bop, ldk, st) != cudaSuccess) return BSG_ERR_CUDA;
+    unsigned int *ticket =
+        at<unsigned int>(workspace, align256((size_t)M * ldk * 2) + align256((size_t)N * ldk * 2));
+    if (cudaMemsetAsync(ticket, 0, 2 * sizeof(unsigned int), st) != cudaSuccess) return BSG_ERR_CUDA;
     return from_cuda(
-        launch_gemm_tc(aop, bop, M, N, K, nullptr, nullptr, 0, 1, S, lds, dstatus, st));
+        launch_gemm_tc(aop, bop, M, N, K, nullptr, nullptr, 0, 1, S, lds, dstatus, ticket, st));
 }
 
 bsg_status bsg_epilogue(const int32_t *S, int64_t lds, const float *sa, const float *sb,

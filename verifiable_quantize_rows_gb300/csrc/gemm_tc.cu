@@ -28,8 +28,9 @@
 //     output staging buffers per epilogue warp.
 //   * single (M <= 128): one CTA computes a 128 x BN tile (cta_group::1).
 // BN in {64, 128, 192, 256} is chosen per problem so that the last wave of tiles
-// leaves few SMs idle; CTAs (pairs) are persistent and walk their tiles
-// round-robin.
+// leaves few SMs idle; CTAs (pairs) are persistent, and after the first wave
+// they claim tiles dynamically, so that a CTA that starts late, its SM busy
+// with other work, takes fewer tiles instead of holding up the launch.
 //
 // Roles (one CTA per SM):
 //   warp 0      TMA producer: A and B k-blocks (64 wide, 128-byte swizzle)
@@ -40,6 +41,10 @@
 //               accumulator, double-buffered (2 x BN columns) so the epilogue
 //               of one chunk or tile overlaps the next one's MMAs;
 //   warp 2      allocates / frees the tensor-memory columns;
+//   warp 3      tile scheduler (one thread; in a pair, of the even CTA only):
+//               the first tile of each CTA (pair) is its index, later tiles
+//               are claimed from a counter, and each index is handed to every
+//               role of both CTAs through a small shared-memory queue;
 //   warps 4-11  epilogue: tcgen05.ld of each chunk into registers (the tensor
 //               memory is released at once), then the f32 epilogue, ReLU,
 //               staging in shared memory and TMA stores (or plain stores
@@ -68,6 +73,7 @@ constexpr int kThreads = 128 + kEpiWarps * 32;
 constexpr uint32_t kABytes = kBM * kBK * 2;     // 16 KiB
 constexpr uint32_t kEpiBufBytes = 32 * 32 * 4;  // one 32 x 32 fp32 box
 constexpr int kGroupM = 16;                     // tile raster: 16 m-units per group
+constexpr int kTileQ = 2;                       // depth of the tile-index queue
 constexpr uint32_t kMaxSmem = 232448;           // 227 KiB per CTA
 
 // Compile-time layout of one tile width and kernel kind.
@@ -90,9 +96,11 @@ struct Cfg {
     static constexpr int kPieces = kWarpCols / 32;
     static constexpr uint32_t kOffEpi = kStages * kStageBytes;
     static constexpr uint32_t kOffBar = kOffEpi + kEpiWarps * kBoxes * kEpiBufBytes;
-    // barriers: full[kStages], empty[kStages], tfull[2], tempty[2], drain
-    static constexpr uint32_t kNumBars = 2 * kStages + 5;
-    static constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
+    // barriers: full[kStages], empty[kStages], tfull[2], tempty[2], drain,
+    // qfull[kTileQ], qempty[kTileQ]; then the tile-index queue
+    static constexpr uint32_t kNumBars = 2 * kStages + 5 + 2 * kTileQ;
+    static constexpr uint32_t kOffTileQ = kOffBar + kNumBars * 8;
+    static constexpr uint32_t kOffTmemPtr = kOffTileQ + kTileQ * 4;
     static constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
     static constexpr uint32_t kSmemBytes = kOffAbort + 4 + 1024;  // + 1024-byte alignment slack
     static constexpr uint32_t kIdesc = idesc_f16_f32(PAIR ? 2 * kBM : kBM, BN);
@@ -114,6 +122,10 @@ struct Params {
     int relu;
     int tma_store;  // 1: C's rows are 16-byte aligned; store through tmap_c
     int32_t *dstatus;
+    // ticket[0]: tiles claimed beyond the first wave; ticket[1]: CTAs (pairs)
+    // done claiming.  Zero at launch; the last CTA to finish claiming sets
+    // both back to zero for the next launch.
+    unsigned int *ticket;
 };
 
 // Tile u -> (m-unit, n-tile), rastered in groups of kGroupM m-units so that
@@ -228,6 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *tfull = bars + 2 * K::kStages;
     uint64_t *tempty = bars + 2 * K::kStages + 2;
     uint64_t *drain = bars + 2 * K::kStages + 4;
+    uint64_t *qfull = bars + 2 * K::kStages + 5;
+    uint64_t *qempty = qfull + kTileQ;
+    volatile int *tileq = reinterpret_cast<volatile int *>(smem + K::kOffTileQ);
     uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + K::kOffTmemPtr);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K::kOffAbort);
 
@@ -235,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int num_chunks = (p.num_kb + kChunkBlocks - 1) / kChunkBlocks;
     const int rank = PAIR ? (int)cluster_ctarank() : 0;  // 0: the pair's MMA-issuing CTA
-    const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // first tile
     const int nunits = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
     constexpr uint16_t kPairMask = 0x3;  // cluster ranks 0 and 1
 
@@ -249,6 +264,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&tempty[b], PAIR ? 2 * kEpiWarps : kEpiWarps);  // PAIR: both epilogues
         }
         mbar_init(drain, 1);
+        for (int q = 0; q < kTileQ; ++q) {
+            mbar_init(&qfull[q], 1);
+            // readers of a queue slot: the producer, the MMA thread and the
+            // epilogue warps of this CTA, and in a pair the odd CTA's producer
+            // and epilogue warps
+            mbar_init(&qempty[q], PAIR ? 2 * (1 + kEpiWarps) + 1 : 2 + kEpiWarps);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         fence_async_shared();
@@ -279,9 +301,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool issued[K::kStages];
             for (int s = 0; s < K::kStages; ++s) issued[s] = false, issued_parity[s] = 0;
             bool ok = true;
-            for (int u = unit0; ok && u < p.num_units; u += nunits) {
+            for (uint32_t t = 0; ok; ++t) {
+                const int slot = (int)(t % kTileQ);
+                const uint32_t qph = (t / kTileQ) & 1;
+                if (!bar_wait<PAIR>(&qfull[slot], qph, abort_flag)) {
+                    record_abort(abort_flag, p.dstatus);
+                    ok = false;
+                    break;
+                }
+                const int tile = tileq[slot];
+                if (PAIR)
+                    mbar_arrive_cl(cluster_addr(&qempty[slot], 0));
+                else
+                    mbar_arrive(&qempty[slot]);
+                if (tile < 0) break;  // no tiles left
                 int mu, nb;
-                tile_coords(p, u, mu, nb);
+                tile_coords(p, tile, mu, nb);
                 const int mb = PAIR ? 2 * mu + rank : mu;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!bar_wait<PAIR>(&empty[stage], phase ^ 1, abort_flag)) {
@@ -327,6 +362,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
         }
+    } else if (warp == 3) {
+        // ------------------------------------------------ tile scheduler
+        // (one thread of the even CTA) The first wave is static (tile = unit
+        // index); later tiles are claimed from the launch's counter, so that
+        // a CTA that starts late (its SM busy with other work) takes fewer of
+        // them.  Each tile index goes into a 2-deep queue read by every role
+        // of both CTAs; claiming and publishing here keeps the latency of the
+        // atomic and of the cluster-scope release off the operand path.
+        if (lane == 0 && rank == 0) {
+            for (uint32_t t = 0;; ++t) {
+                const int slot = (int)(t % kTileQ);
+                const uint32_t qph = (t / kTileQ) & 1;
+                if (!bar_wait<PAIR>(&qempty[slot], qph ^ 1, abort_flag)) {
+                    record_abort(abort_flag, p.dstatus);
+                    break;
+                }
+                const unsigned int u = t == 0 ? (unsigned int)unit0
+                                              : (unsigned int)nunits + atomicAdd(&p.ticket[0], 1u);
+                const int tile = u < (unsigned int)p.num_units ? (int)u : -1;
+                tileq[slot] = tile;
+                if (PAIR) {
+                    st_cluster_u32(cluster_addr(const_cast<int *>(&tileq[slot]), 1),
+                                   (uint32_t)tile);
+                    mbar_arrive_release_cl(cluster_addr(&qfull[slot], 1));
+                }
+                mbar_arrive(&qfull[slot]);
+                if (tile < 0) break;
+            }
+            // The last CTA (pair) to stop claiming resets the counter for the
+            // next launch; every CTA counts itself once, also after an abort.
+            __threadfence();  // this CTA's last claim lands before its "done"
+            if (atomicAdd(&p.ticket[1], 1u) == (unsigned int)nunits - 1u) {
+                __threadfence();  // every claim of this launch is in before the reset
+                atomicExch(&p.ticket[0], 0u);
+                atomicExch(&p.ticket[1], 0u);
+            }
+        }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0 && rank == 0) {
@@ -335,7 +407,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_iter = 0;
             bool ok = true;
             bool any_mma = false;
-            for (int u = unit0; ok && u < p.num_units; u += nunits) {
+            for (uint32_t t = 0; ok; ++t) {
+                const int slot = (int)(t % kTileQ);
+                const uint32_t qph = (t / kTileQ) & 1;
+                if (!bar_wait<PAIR>(&qfull[slot], qph, abort_flag)) {
+                    record_abort(abort_flag, p.dstatus);
+                    ok = false;
+                    break;
+                }
+                const int tile = tileq[slot];
+                mbar_arrive(&qempty[slot]);
+                if (tile < 0) break;
                 for (int c = 0; ok && c < num_chunks; ++c) {
                     const int kb0 = c * kChunkBlocks;
                     const int kb1 = min(p.num_kb, kb0 + kChunkBlocks);
@@ -412,7 +494,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         // fraction of the ALU rate); adding +0 turns a -0 sum (all products
         // -0) into f32(0) = +0.
         const bool f32_sums = num_chunks == 1 && p.mode == 0;
-        for (int u = unit0; ok && u < p.num_units; u += nunits) {
+        for (uint32_t t = 0; ok; ++t) {
+            const int slot = (int)(t % kTileQ);
+            const uint32_t qph = (t / kTileQ) & 1;
+            if (!__all_sync(0xffffffffu, bar_wait<PAIR>(&qfull[slot], qph, abort_flag))) {
+                if (lane == 0) record_abort(abort_flag, p.dstatus);
+                ok = false;
+                break;
+            }
+            const int tile = tileq[slot];
+            __syncwarp();
+            if (lane == 0) {
+                if (PAIR)
+                    mbar_arrive_cl(cluster_addr(&qempty[slot], 0));
+                else
+                    mbar_arrive(&qempty[slot]);
+            }
+            if (tile < 0) break;
             // ---- drain every chunk into int32 sums (or, f32_sums, f32(S))
             uint32_t acc[K::kWarpCols];  // int32 or f32 bit patterns
             for (int c = 0; c < num_chunks; ++c) {
@@ -464,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // ---- final epilogue of the tile from the sums
             int mu, nb;
-            tile_coords(p, u, mu, nb);
+            tile_coords(p, tile, mu, nb);
             const int mb = PAIR ? 2 * mu + rank : mu;
             if (mb >= p.num_m) continue;  // the odd CTA of a pair past the last m-block
             const int row0 = mb * kBM + q * 32;
@@ -643,7 +741,8 @@ int gemm_tile_width(int64_t M, int64_t N, int sms) {
 
 cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int64_t N,
                            int64_t K, const float *sa, const float *sb, int relu, int mode,
-                           void *out, int64_t ldo, int32_t *dstatus, cudaStream_t st) {
+                           void *out, int64_t ldo, int32_t *dstatus, unsigned int *ticket,
+                           cudaStream_t st) {
     CUtensorMap ta, tc;
     if (!make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, Aop, (uint64_t)K, (uint64_t)M,
                       (uint64_t)operand_ld(K), kBK, kBM))
@@ -674,6 +773,7 @@ cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int6
     p.relu = relu;
     p.tma_store = tma_store;
     p.dstatus = dstatus;
+    p.ticket = ticket;
     const bool pair = p.num_m >= 2 && gemm_pairs_enabled();
     const int forced = forced_tile_width();
     switch (forced ? forced : gemm_tile_width(M, N, device_sm_count())) {

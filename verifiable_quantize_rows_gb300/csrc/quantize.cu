@@ -392,12 +392,15 @@ __device__ __forceinline__ void rows_wide_block(int64_t blk, const float *__rest
     }
 }
 
+// zero2 (may be NULL): two words set to zero by one thread -- the tile
+// counter of the GEMM that reads this launch's output.
 template <int OUT, int WPR, int RV>
 __global__ void __launch_bounds__(256)
     quantize_rows_wide_kernel(const float *__restrict__ X, int64_t rows, int64_t cols,
                               int64_t ldx, void *__restrict__ Q, int64_t ldq,
                               float *__restrict__ scale, float *__restrict__ inv,
-                              int32_t *__restrict__ dstatus) {
+                              int32_t *__restrict__ dstatus, unsigned int *__restrict__ zero2) {
+    if (zero2 && blockIdx.x == 0 && threadIdx.x == 0) zero2[0] = zero2[1] = 0u;
     rows_wide_block<OUT, WPR, RV>((int64_t)blockIdx.x, X, rows, cols, ldx, Q, ldq, scale, inv,
                                   dstatus);
 }
@@ -622,7 +625,9 @@ __global__ void __launch_bounds__(256)
                        __half *__restrict__ Aop, float *__restrict__ sa,
                        const float *__restrict__ B, int64_t N, int64_t ldb,
                        __half *__restrict__ Bop, float *__restrict__ sb, int64_t ldk, int R,
-                       int strips, int32_t *__restrict__ dstatus) {
+                       int strips, int32_t *__restrict__ dstatus, unsigned int *__restrict__ zero2) {
+    if (zero2 && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        zero2[0] = zero2[1] = 0u;  // the GEMM's tile counter
     if ((int)blockIdx.x < strips) {
         cols_strip_block(B, K, N, ldb, R, (int64_t)blockIdx.x, Bop, ldk, sb, dstatus);
     } else {
@@ -723,11 +728,11 @@ static int grid_for(int64_t work, int per_block) {
 template <int OUT, int WPR, int RV>
 static void launch_rows_wide(const float *X, int64_t rows, int64_t cols, int64_t ldx, void *Q,
                              int64_t ldq, float *scale, float *inv, int32_t *dstatus,
-                             cudaStream_t st) {
+                             unsigned int *zero2, cudaStream_t st) {
     constexpr int RPB = 8 / WPR;
     const int64_t blocks = (rows + RPB - 1) / RPB;
     quantize_rows_wide_kernel<OUT, WPR, RV><<<(unsigned)blocks, 256, 0, st>>>(
-        X, rows, cols, ldx, Q, ldq, scale, inv, dstatus);
+        X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2);
 }
 
 // Smallest single-pass layout (warps per row, float4 per lane) that holds a
@@ -742,24 +747,24 @@ static int row_layout(int64_t cols) {
 template <int OUT>
 static bool dispatch_rows_wide(int layout, const float *X, int64_t rows, int64_t cols,
                                int64_t ldx, void *Q, int64_t ldq, float *scale, float *inv,
-                               int32_t *dstatus, cudaStream_t st) {
+                               int32_t *dstatus, unsigned int *zero2, cudaStream_t st) {
     switch (layout) {
-        case 0: launch_rows_wide<OUT, 1, 2>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
-        case 1: launch_rows_wide<OUT, 1, 4>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
-        case 2: launch_rows_wide<OUT, 1, 6>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
-        case 3: launch_rows_wide<OUT, 1, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
-        case 4: launch_rows_wide<OUT, 2, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
-        case 5: launch_rows_wide<OUT, 4, 6>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
-        case 6: launch_rows_wide<OUT, 4, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
-        case 7: launch_rows_wide<OUT, 8, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
-        case 8: launch_rows_wide<OUT, 8, 16>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st); return true;
+        case 0: launch_rows_wide<OUT, 1, 2>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
+        case 1: launch_rows_wide<OUT, 1, 4>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
+        case 2: launch_rows_wide<OUT, 1, 6>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
+        case 3: launch_rows_wide<OUT, 1, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
+        case 4: launch_rows_wide<OUT, 2, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
+        case 5: launch_rows_wide<OUT, 4, 6>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
+        case 6: launch_rows_wide<OUT, 4, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
+        case 7: launch_rows_wide<OUT, 8, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
+        case 8: launch_rows_wide<OUT, 8, 16>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
     }
     return false;
 }
 
 cudaError_t launch_quantize_rows(const float *X, int64_t rows, int64_t cols, int64_t ldx,
                                  int out_kind, void *Q, int64_t ldq, float *scale, float *inv,
-                                 int32_t *dstatus, cudaStream_t st) {
+                                 int32_t *dstatus, cudaStream_t st, unsigned int *zero2) {
     const size_t qalign = out_kind == kOutInt8 ? 4 : 8;
     const size_t qesz = out_kind == kOutInt8 ? 1 : 2;
     const bool vec = (cols % 4 == 0) && (ldx % 4 == 0) &&
@@ -768,13 +773,16 @@ cudaError_t launch_quantize_rows(const float *X, int64_t rows, int64_t cols, int
     const int layout = vec ? row_layout(cols) : -1;
     if (layout >= 0) {
         if (out_kind == kOutInt8)
-            dispatch_rows_wide<kOutInt8>(layout, X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, st);
+            dispatch_rows_wide<kOutInt8>(layout, X, rows, cols, ldx, Q, ldq, scale, inv, dstatus,
+                                         zero2, st);
         else
             dispatch_rows_wide<kOutHalfKMajor>(layout, X, rows, cols, ldx, Q, ldq, scale, inv, dstatus,
-                                              st);
+                                              zero2, st);
         count_launches(1);
         return cudaGetLastError();
     }
+    if (zero2 && cudaMemsetAsync(zero2, 0, 2 * sizeof(unsigned int), st) != cudaSuccess)
+        return cudaErrorInvalidValue;
     const int grid = grid_for(rows, kRowWarps);
     const bool vec2 = (ldx % 4 == 0) && (reinterpret_cast<uintptr_t>(X) % 16 == 0) &&
                       ((ldq * qesz) % qalign == 0) && (reinterpret_cast<uintptr_t>(Q) % qalign == 0);
@@ -876,7 +884,7 @@ template <int WPR, int RV>
 static cudaError_t launch_ab(const float *A, int64_t M, int64_t K, int64_t lda, __half *Aop,
                              float *sa, const float *B, int64_t N, int64_t ldb, __half *Bop,
                              float *sb, int64_t ldk, int cs, int R, int32_t *dstatus,
-                             cudaStream_t st) {
+                             unsigned int *zero2, cudaStream_t st) {
     constexpr int RPB = 8 / WPR;
     const int64_t strips = (N + kStripCols - 1) / kStripCols;
     const int64_t row_blocks = (M + RPB - 1) / RPB;
@@ -896,13 +904,13 @@ static cudaError_t launch_ab(const float *A, int64_t M, int64_t K, int64_t lda, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, quantize_ab_kernel<WPR, RV>, A, M, K, lda, Aop, sa, B, N, ldb,
-                              Bop, sb, ldk, R, (int)strips, dstatus);
+                              Bop, sb, ldk, R, (int)strips, dstatus, zero2);
 }
 
 cudaError_t launch_quantize_ab(const float *A, int64_t M, int64_t K, int64_t lda,
                                const float *B, int64_t N, int64_t ldb, __half *Aop,
                                __half *Bop, int64_t ldk, float *sa, float *sb,
-                               int32_t *dstatus, cudaStream_t st) {
+                               int32_t *dstatus, unsigned int *zero2, cudaStream_t st) {
     const bool vecA = (K % 4 == 0) && (lda % 4 == 0) &&
                       (reinterpret_cast<uintptr_t>(A) % 16 == 0) && ((ldk * 2) % 8 == 0) &&
                       (reinterpret_cast<uintptr_t>(Aop) % 8 == 0);
@@ -917,13 +925,13 @@ cudaError_t launch_quantize_ab(const float *A, int64_t M, int64_t K, int64_t lda
     if (layout < 0 || !vecB || !strip_shape(K, 8, cs, R)) return cudaErrorNotSupported;
     cudaError_t e = cudaErrorNotSupported;
     switch (layout) {
-        case 0: e = launch_ab<1, 2>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, st); break;
-        case 1: e = launch_ab<1, 4>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, st); break;
-        case 2: e = launch_ab<1, 6>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, st); break;
-        case 3: e = launch_ab<1, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, st); break;
-        case 4: e = launch_ab<2, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, st); break;
-        case 5: e = launch_ab<4, 6>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, st); break;
-        case 6: e = launch_ab<4, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, st); break;
+        case 0: e = launch_ab<1, 2>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, st); break;
+        case 1: e = launch_ab<1, 4>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, st); break;
+        case 2: e = launch_ab<1, 6>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, st); break;
+        case 3: e = launch_ab<1, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, st); break;
+        case 4: e = launch_ab<2, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, st); break;
+        case 5: e = launch_ab<4, 6>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, st); break;
+        case 6: e = launch_ab<4, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, st); break;
         default: return cudaErrorNotSupported;  // rows longer than 4096: not fused
     }
     count_launches(1);
