@@ -86,14 +86,15 @@ bool gemm_pairs_enabled();
 // The tensor-core GEMM.  Aop: M x ldk f16, Bop: N x ldk f16 (both K-major,
 // ldk = operand_ld(K)).  mode 0: C = epi(S, sa, sb) (+ReLU) as float;
 // mode 1: S stored as int32.  sa / sb must hold round_up(M, kBM) /
-// round_up(N, kBN) + kBN floats (mode 0).  `ticket`: two unsigned ints of
+// round_up(N, kBN) + kBN floats (mode 0).  `tile_width` 64/128/192/256
+// fixes the tile width, 0 leaves it to gemm_tile_width.  `ticket`: two unsigned ints of
 // device memory, the tile counter: zero before the first launch on it (the
 // quantize step that fills a unit workspace zeroes it), and zero again after
 // every launch that completes.
 cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int64_t N,
                            int64_t K, const float *sa, const float *sb, int relu, int mode,
                            void *out, int64_t ldo, int32_t *dstatus, unsigned int *ticket,
-                           cudaStream_t st);
+                           cudaStream_t st, int tile_width = 0);
 
 cudaError_t launch_epilogue(const int32_t *S, int64_t lds, const float *sa, const float *sb,
                             int64_t M, int64_t N, int relu, float *C, int64_t ldc,

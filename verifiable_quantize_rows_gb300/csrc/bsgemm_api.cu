@@ -214,7 +214,8 @@ bsg_status unit_quantize(const float *A, int64_t lda, int transA, const float *B
 // Steps 2-3 from the workspace: the tensor-core contraction with the fused
 // epilogue.
 bsg_status unit_contract(int64_t M, int64_t N, int64_t K, int relu, float *C, int64_t ldc,
-                         void *ws, size_t ws_bytes, int32_t *dstatus, cudaStream_t st) {
+                         void *ws, size_t ws_bytes, int32_t *dstatus, cudaStream_t st,
+                         int tile_width = 0) {
     if (!C || !dims_ok(M, N, K) || ldc < N) return BSG_ERR_ARG;
     if (K > BSG_MAX_K) return BSG_ERR_K_TOO_LARGE;
     const UnitLayout L = unit_layout(M, N, K, 0, 0);
@@ -223,7 +224,7 @@ bsg_status unit_contract(int64_t M, int64_t N, int64_t K, int relu, float *C, in
     if (s != BSG_OK) return s;
     return from_cuda(launch_gemm_tc(at<__half>(ws, L.aop), at<__half>(ws, L.bop), M, N, K,
                                     at<float>(ws, L.sa), at<float>(ws, L.sb), relu, 0, C, ldc,
-                                    dstatus, at<unsigned int>(ws, L.ticket), st));
+                                    dstatus, at<unsigned int>(ws, L.ticket), st, tile_width));
 }
 
 }  // namespace
@@ -497,8 +498,12 @@ bsg_status bsg_probe_hash_async(uint64_t seed, int64_t M, int64_t N, int64_t K, 
     float *B = at<float>(workspace, offs[1]);
     float *C = at<float>(workspace, offs[2]);
     if (launch_probe_fill(seed, M, N, K, A, B, st) != cudaSuccess) return BSG_ERR_CUDA;
-    s = unit(A, K, 0, B, N, 0, M, N, K, 0, C, N, at<void>(workspace, offs[3]),
-             offs[4] - offs[3], dstatus, st);
+    // The probe runs beside other work: the widest tiles keep its GEMM on
+    // the fewest SMs (1024^3: 16 pair tiles on 32 SMs), the same results.
+    void *uws = at<void>(workspace, offs[3]);
+    s = unit_quantize(A, K, 0, B, N, 0, M, N, K, uws, offs[4] - offs[3], dstatus, st);
+    if (s != BSG_OK) return s;
+    s = unit_contract(M, N, K, 0, C, N, uws, offs[4] - offs[3], dstatus, st, 256);
     if (s != BSG_OK) return s;
     return from_cuda(launch_hash_f32(C, M, N, N, out32, at<void>(workspace, offs[4]), st));
 }

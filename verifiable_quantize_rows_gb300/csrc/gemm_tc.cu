@@ -742,7 +742,7 @@ int gemm_tile_width(int64_t M, int64_t N, int sms) {
 cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int64_t N,
                            int64_t K, const float *sa, const float *sb, int relu, int mode,
                            void *out, int64_t ldo, int32_t *dstatus, unsigned int *ticket,
-                           cudaStream_t st) {
+                           cudaStream_t st, int tile_width) {
     CUtensorMap ta, tc;
     if (!make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, Aop, (uint64_t)K, (uint64_t)M,
                       (uint64_t)operand_ld(K), kBK, kBM))
@@ -776,7 +776,7 @@ cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int6
     p.ticket = ticket;
     const bool pair = p.num_m >= 2 && gemm_pairs_enabled();
     const int forced = forced_tile_width();
-    switch (forced ? forced : gemm_tile_width(M, N, device_sm_count())) {
+    switch (forced ? forced : tile_width ? tile_width : gemm_tile_width(M, N, device_sm_count())) {
         case 64: return launch_width<64>(ta, tc, Bop, N, K, p, pair, st);
         case 128: return launch_width<128>(ta, tc, Bop, N, K, p, pair, st);
         case 192: return launch_width<192>(ta, tc, Bop, N, K, p, pair, st);

@@ -172,10 +172,15 @@ __device__ __forceinline__ void b2s_leaf64(const uint4 *src, uint64_t node_offse
     }
 }
 
-// Leaves are hashed 64 to a block (3 tree levels inside the block) so that
-// every SM takes part; higher levels 256 to a block (4 levels).
-constexpr int kLeafThreads = 64;
+// Leaves are hashed 1024 to a block (5 tree levels inside the block; a
+// 1024 x 1024 output is 16 blocks), higher levels 256 to a block (4
+// levels).  The hash is latency-bound (a chain of compressions), so few,
+// full blocks are as fast as many small ones and leave most SMs to other
+// work running beside the probe.
+constexpr int kLeafThreads = 1024;
+constexpr int kLeafLevels = 5;
 constexpr int kNodeThreads = 256;
+constexpr int kNodeLevels = 4;
 constexpr int kLeafFloats = 64;  // 256-byte leaves
 
 struct LeafWords {
@@ -206,7 +211,9 @@ __global__ void __launch_bounds__(THREADS)
                       const uint32_t *__restrict__ in, int64_t count, uint32_t depth0,
                       uint32_t *__restrict__ out, uint8_t *__restrict__ out32) {
     static_assert((1 << (2 * LEVELS)) == THREADS, "THREADS must be 4^LEVELS");
-    __shared__ uint32_t dig[2][THREADS][8];
+    // two digest buffers of THREADS x 8 words, dynamic shared memory
+    extern __shared__ uint32_t dig_raw[];
+    uint32_t(*dig)[THREADS][8] = reinterpret_cast<uint32_t(*)[THREADS][8]>(dig_raw);
     const int t = threadIdx.x;
     const int64_t base = (int64_t)blockIdx.x * THREADS;
     const int64_t idx = base + t;
@@ -294,18 +301,31 @@ cudaError_t launch_hash_f32(const float *C, int64_t M, int64_t N, int64_t ldc, u
     uint32_t *bufs[2] = {static_cast<uint32_t *>(ws), static_cast<uint32_t *>(ws) + n1cap * 8};
     int which = 0;
     int nlaunch = 1;
+    constexpr size_t kLeafSmem = 2 * kLeafThreads * 8 * sizeof(uint32_t);  // 64 KiB
+    constexpr size_t kNodeSmem = 2 * kNodeThreads * 8 * sizeof(uint32_t);
+    static bool ready[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!ready[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            hash_level_kernel<true, kLeafThreads, kLeafLevels>,
+            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLeafSmem);
+        if (e != cudaSuccess) return e;
+        ready[dev] = true;
+    }
     int64_t blocks = (count + kLeafThreads - 1) / kLeafThreads;
-    hash_level_kernel<true, kLeafThreads, 3><<<(int)blocks, kLeafThreads, 0, st>>>(
+    hash_level_kernel<true, kLeafThreads, kLeafLevels><<<(int)blocks, kLeafThreads, kLeafSmem, st>>>(
         C, M, N, ldc, nullptr, count, 0u, bufs[which], out32);
     // tree depth reached inside the leaf blocks
     uint32_t depth = 0;
-    for (int l = 0; l < 3 && count > 1; ++l) count = (count + 3) / 4, ++depth;
+    for (int l = 0; l < kLeafLevels && count > 1; ++l) count = (count + 3) / 4, ++depth;
     while (count > 1) {
         blocks = (count + kNodeThreads - 1) / kNodeThreads;
-        hash_level_kernel<false, kNodeThreads, 4><<<(int)blocks, kNodeThreads, 0, st>>>(
-            nullptr, 0, 0, 0, bufs[which], count, depth, bufs[which ^ 1], out32);
+        hash_level_kernel<false, kNodeThreads, kNodeLevels>
+            <<<(int)blocks, kNodeThreads, kNodeSmem, st>>>(nullptr, 0, 0, 0, bufs[which], count,
+                                                          depth, bufs[which ^ 1], out32);
         which ^= 1;
-        for (int l = 0; l < 4 && count > 1; ++l) count = (count + 3) / 4, ++depth;
+        for (int l = 0; l < kNodeLevels && count > 1; ++l) count = (count + 3) / 4, ++depth;
         ++nlaunch;
     }
     count_launches(nlaunch);
