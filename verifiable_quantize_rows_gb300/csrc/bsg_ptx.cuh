@@ -202,6 +202,20 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
     return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// ----------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it in the stream is still running; it must execute
+// griddep_wait() before touching anything that kernel writes (or reads, if it
+// overwrites it).  Without that launch attribute the wait returns at once.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// This block is done with its part: the next kernel in the stream may be
+// scheduled once every block of this grid has said so (or exited).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------- CTA pairs (tcgen05 cta_group::2)
 // Two CTAs of a cluster whose ranks differ in bit 0 form a pair: one MMA,
 // issued by one thread of the even CTA, reads A's rows 0-127 and the first

@@ -289,6 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (PAIR) cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_ptr;
+    // everything above overlaps the end of the previous kernel in the stream
+    // (programmatic launch); the operands, scales and tile counter it wrote
+    // are read only from here on
+    griddep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -587,6 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     }
 
+    griddep_launch_dependents();
     tc_fence_before();
     __syncthreads();
     if (PAIR) cluster_sync_all();  // neither CTA leaves while the other may still signal it
@@ -646,13 +651,15 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tc, const __half
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = PAIR ? 1 : 0;
+    cfg.numAttrs = PAIR ? 2 : 1;
     if (!ready[dev]) {
         cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, PAIR>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -19,6 +19,7 @@
 #include <string.h>
 
 #include "bsg_internal.h"
+#include "bsg_ptx.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -400,9 +401,11 @@ __global__ void __launch_bounds__(256)
                               int64_t ldx, void *__restrict__ Q, int64_t ldq,
                               float *__restrict__ scale, float *__restrict__ inv,
                               int32_t *__restrict__ dstatus, unsigned int *__restrict__ zero2) {
+    griddep_wait();  // programmatic launch: the previous kernel is done from here on
     if (zero2 && blockIdx.x == 0 && threadIdx.x == 0) zero2[0] = zero2[1] = 0u;
     rows_wide_block<OUT, WPR, RV>((int64_t)blockIdx.x, X, rows, cols, ldx, Q, ldq, scale, inv,
                                   dstatus);
+    griddep_launch_dependents();
 }
 
 // Columns, single pass: a cluster of CS CTAs shares a strip of 32 columns;
@@ -626,6 +629,7 @@ __global__ void __launch_bounds__(256)
                        const float *__restrict__ B, int64_t N, int64_t ldb,
                        __half *__restrict__ Bop, float *__restrict__ sb, int64_t ldk, int R,
                        int strips, int32_t *__restrict__ dstatus, unsigned int *__restrict__ zero2) {
+    griddep_wait();  // programmatic launch: the previous kernel is done from here on
     if (zero2 && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
         zero2[0] = zero2[1] = 0u;  // the GEMM's tile counter
     if ((int)blockIdx.x < strips) {
@@ -635,6 +639,7 @@ __global__ void __launch_bounds__(256)
         rows_wide_block<kOutHalfKMajor, WPR, RV>(blk, A, M, K, lda, Aop, ldk, sa, nullptr,
                                                  dstatus);
     }
+    griddep_launch_dependents();
 }
 
 // The strip CTAs alone, for a column quantize that is not fused with a row
@@ -643,7 +648,9 @@ __global__ void __launch_bounds__(256)
     quantize_cols_strip_kernel(const float *__restrict__ X, int64_t rows, int64_t cols,
                                int64_t ldx, int R, __half *__restrict__ Q, int64_t ldq,
                                float *__restrict__ scale, int32_t *__restrict__ dstatus) {
+    griddep_wait();  // programmatic launch: the previous kernel is done from here on
     cols_strip_block(X, rows, cols, ldx, R, (int64_t)blockIdx.x, Q, ldq, scale, dstatus);
+    griddep_launch_dependents();
 }
 
 __global__ void i8_rows_to_half_kernel(const int8_t *__restrict__ Q, int64_t rows, int64_t cols,
@@ -731,8 +738,18 @@ static void launch_rows_wide(const float *X, int64_t rows, int64_t cols, int64_t
                              unsigned int *zero2, cudaStream_t st) {
     constexpr int RPB = 8 / WPR;
     const int64_t blocks = (rows + RPB - 1) / RPB;
-    quantize_rows_wide_kernel<OUT, WPR, RV><<<(unsigned)blocks, 256, 0, st>>>(
-        X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2);
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, quantize_rows_wide_kernel<OUT, WPR, RV>, X, rows, cols, ldx, Q, ldq,
+                       scale, inv, dstatus, zero2);
 }
 
 // Smallest single-pass layout (warps per row, float4 per lane) that holds a
@@ -896,13 +913,15 @@ static cudaError_t launch_ab(const float *A, int64_t M, int64_t K, int64_t lda, 
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = (unsigned)cs;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, quantize_ab_kernel<WPR, RV>, A, M, K, lda, Aop, sa, B, N, ldb,
                               Bop, sb, ldk, R, (int)strips, dstatus, zero2);
 }
@@ -954,13 +973,15 @@ cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int
         cfg.gridDim = dim3((unsigned)((cols + kStripCols - 1) / kStripCols), (unsigned)cs, 1);
         cfg.blockDim = dim3(256, 1, 1);
         cfg.stream = st;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 1;
         attr[0].val.clusterDim.y = (unsigned)cs;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
         e = cudaLaunchKernelEx(&cfg, quantize_cols_strip_kernel, X, rows, cols, ldx, R,
                                static_cast<__half *>(Q), ldq, scale, dstatus);
         count_launches(1);
