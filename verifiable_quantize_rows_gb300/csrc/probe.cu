@@ -278,7 +278,10 @@ cudaError_t launch_probe_fill(uint64_t seed, int64_t M, int64_t N, int64_t K, fl
                               float *B, cudaStream_t st) {
     const int64_t total = M * K + K * N;
     const int64_t blocks = (total + 255) / 256;
-    const int64_t cap = (int64_t)device_sm_count() * 16;
+    // half the SMs, one block each: the fill is ALU work that runs beside
+    // other kernels in the probe's use, and a block on every SM would hold
+    // each of them back
+    const int64_t cap = (int64_t)device_sm_count() / 2 > 0 ? (int64_t)device_sm_count() / 2 : 1;
     probe_fill_kernel<<<(int)(blocks < cap ? blocks : cap), 256, 0, st>>>(seed, M * K, K * N, A, B);
     count_launches(1);
     return cudaGetLastError();
