@@ -106,6 +106,13 @@ def _declare(lib):
     lib.orc_probe_value.restype = ctypes.c_float
     lib.orc_probe_inputs.argtypes = [ctypes.c_uint64, _i64, _i64, _i64, _F32P, _F32P]
     lib.orc_probe_hash.argtypes = [ctypes.c_uint64, _i64, _i64, _i64, _U8P]
+    lib.orc_pow2_ceil.argtypes = [ctypes.c_float]
+    lib.orc_pow2_ceil.restype = ctypes.c_float
+    lib.orc_wquant_cols.argtypes = [_F32P, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _I8P,
+                                    _i64, _F32P]
+    lib.orc_wquant_cols.restype = ctypes.c_int
+    lib.orc_pack_int4.argtypes = [_I8P, _i64, _i64, _i64, _U8P, _i64]
+    lib.orc_wdequant_cols.argtypes = [_I8P, _i64, _i64, _i64, _F32P, _F32P, _i64]
     for name in ("orc_quantize_rows", "orc_quantize_cols", "orc_gemm_s32", "orc_epilogue",
                  "orc_bsgemm_i8", "orc_bsgemm_cells", "orc_hash_f32", "orc_probe_hash"):
         getattr(lib, name).restype = ctypes.c_int
@@ -258,3 +265,30 @@ class Oracle:
         out = np.zeros(32, np.uint8)
         st = self.lib.orc_probe_hash(seed, M, N, K, out)
         return out.tobytes(), st
+
+    # -- presk weight storage ("Precision" manual, "Integer weights") ------
+    def pow2_ceil(self, s: float) -> float:
+        return float(self.lib.orc_pow2_ceil(s))
+
+    def wquant_cols(self, W, bits: int = 8, pow2: bool = False):
+        """Codes (K x N int8), per-column scales and status."""
+        W = _c(W, np.float32)
+        K, N = W.shape
+        Q = np.zeros((K, N), np.int8)
+        sc = np.zeros(N, np.float32)
+        st = self.lib.orc_wquant_cols(W, K, N, N, int(bits), int(bool(pow2)), Q, N, sc)
+        return Q, sc, st
+
+    def pack_int4(self, Q):
+        Q = _c(Q, np.int8)
+        K, N = Q.shape
+        P = np.zeros((K, (N + 1) // 2), np.uint8)
+        self.lib.orc_pack_int4(Q, K, N, N, P, (N + 1) // 2)
+        return P
+
+    def wdequant_cols(self, Q, scale):
+        Q = _c(Q, np.int8)
+        K, N = Q.shape
+        out = np.zeros((K, N), np.float32)
+        self.lib.orc_wdequant_cols(Q, K, N, N, _c(scale, np.float32), out, N)
+        return out

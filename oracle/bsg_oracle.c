@@ -464,3 +464,86 @@ int orc_probe_hash(uint64_t seed, int64_t M, int64_t N, int64_t K, uint8_t out[3
     free(A); free(B); free(C);
     return st;
 }
+
+/* ------------------------------------------------------------------------ */
+/* [P] "Precision" manual (docs.presk-lang.org/presk_manual/precision), */
+/* section "Integer weights": weights stored as int8 or int4 with one scale */
+/* per channel -- per index of every axis other than the contracted one, so */
+/* for a K x N weight contracted over K, one scale per column j:            */
+/*   s_j = max_k |W[k][j]| / (2^(b-1) - 1), rounded to f32;                  */
+/*   "pow2": s_j rounded up to a power of two instead (q*s then exact);      */
+/*   an all-zero channel gets s = 0 and stores zeros;                        */
+/*   q = round to nearest of w / s;  the stored weight means f32(q * s).     */
+/* Readings (the page leaves them open):                                    */
+/*   P1  "round to nearest" is IEEE's: the integer nearest the exact        */
+/*       quotient w/s, ties to even;                                        */
+/*   P2  a channel whose scale rounds to zero (absmax below ~127 * 2^-150)  */
+/*       is stored like an all-zero one: s = 0, q = 0;                       */
+/*   P3  "rounds each scale up to a power of two" is the smallest power of   */
+/*       two >= the absmax scale;                                            */
+/*   P4  int4 codes are 4-bit two's complement, packed two to a byte along   */
+/*       each row of the K x N code matrix: column 2i in bits 0-3 of byte i, */
+/*       column 2i+1 in bits 4-7 (a last odd column leaves bits 4-7 zero).   */
+/* ------------------------------------------------------------------------ */
+
+/* The smallest power of two >= s (s >= 0 finite); 0 stays 0.  Reading P3. */
+float orc_pow2_ceil(float s) {
+    if (s == 0.0f) return 0.0f;
+    int e;
+    const float f = frexpf(s, &e); /* s = f * 2^e, f in [0.5, 1) */
+    if (f == 0.5f) return s;       /* already a power of two */
+    return ldexpf(1.0f, e);        /* 2^e, the next power of two above s */
+}
+
+/* The nearest integer to the exact quotient w / s, ties to even (P1).  The */
+/* f64 quotient of two f32 values is within 2^-53 relative of the exact one, */
+/* while a quotient that is not exactly k + 1/2 is at least ~2^-25 from it,  */
+/* so rounding the f64 quotient gives the same integer.                     */
+static long orc_round_quotient(float w, float s) {
+    return lrint((double)w / (double)s); /* default mode: to nearest, ties to even */
+}
+
+/* W (K x N, row stride ldw) -> codes Q (K x N int8, row stride ldq) and  */
+/* per-column scales.  bits: 8 or 4.  pow2: 0 or 1.                       */
+int orc_wquant_cols(const float *W, int64_t K, int64_t N, int64_t ldw, int bits, int pow2,
+                    int8_t *Q, int64_t ldq, float *scale) {
+    if ((bits != 8 && bits != 4) || K < 1 || N < 1 || ldw < N || ldq < N) return ORC_ERR_ARG;
+    const float qmax = bits == 8 ? 127.0f : 7.0f;
+    int status = ORC_OK;
+    for (int64_t j = 0; j < N; ++j) {
+        float m;
+        if (!absmax_strided(W + j, K, ldw, &m)) status = ORC_ERR_NONFINITE;
+        float s = m / qmax; /* one IEEE f32 division: the exact quotient rounded to f32 */
+        if (pow2) s = orc_pow2_ceil(s);
+        scale[j] = s;
+        for (int64_t k = 0; k < K; ++k) {
+            long q = 0;
+            if (s != 0.0f && isfinite(s)) q = orc_round_quotient(W[k * ldw + j], s);
+            if (q < -(long)qmax || q > (long)qmax) {
+                /* only reachable with non-finite input */
+                if (status == ORC_OK) status = ORC_ERR_RANGE;
+                q = q < 0 ? -(long)qmax : (long)qmax;
+            }
+            Q[k * ldq + j] = (int8_t)q;
+        }
+    }
+    return status;
+}
+
+/* Pack int4 codes (K x N, row stride ldq, each in [-7, 7]) two to a byte */
+/* along rows (P4): P is K x ceil(N/2) bytes, row stride ldp.             */
+void orc_pack_int4(const int8_t *Q, int64_t K, int64_t N, int64_t ldq, uint8_t *P, int64_t ldp) {
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t i = 0; i < (N + 1) / 2; ++i) {
+            const uint8_t lo = (uint8_t)(Q[k * ldq + 2 * i] & 0x0f);
+            const uint8_t hi = 2 * i + 1 < N ? (uint8_t)(Q[k * ldq + 2 * i + 1] & 0x0f) : 0;
+            P[k * ldp + i] = (uint8_t)(lo | (hi << 4));
+        }
+}
+
+/* The stored weights: What[k][j] = f32(q * s_j), one rounding. */
+void orc_wdequant_cols(const int8_t *Q, int64_t K, int64_t N, int64_t ldq, const float *scale,
+                       float *What, int64_t ldo) {
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t j = 0; j < N; ++j) What[k * ldo + j] = (float)Q[k * ldq + j] * scale[j];
+}

@@ -69,6 +69,16 @@ MUTANTS = {
                                "orc_splitmix64(seed, (uint64_t)(e + 1))")],
     "probe_value_offset": [("int32_t v = (int32_t)(z >> 40) - (1 << 23);",
                             "int32_t v = (int32_t)(z >> 40) - (1 << 22);")],
+    "wquant_round_half_up": [("return lrint((double)w / (double)s);",
+                              "return (long)floor((double)w / (double)s + 0.5);")],
+    "wquant_divide_by_2_pow_b": [("float s = m / qmax;", "float s = m / (qmax + 1.0f);")],
+    "wquant_pow2_rounds_down": [("return ldexpf(1.0f, e);        /* 2^e",
+                                 "return ldexpf(1.0f, e - 1);    /* 2^e")],
+    "wquant_zero_channel_floored": [("float s = m / qmax;", "float s = fmaxf(m / qmax, 1e-8f);")],
+    "int4_nibbles_swapped": [("P[k * ldp + i] = (uint8_t)(lo | (hi << 4));",
+                              "P[k * ldp + i] = (uint8_t)(hi | (lo << 4));")],
+    "wdequant_next_channel_scale": [("What[k * ldo + j] = (float)Q[k * ldq + j] * scale[j];",
+                                     "What[k * ldo + j] = (float)Q[k * ldq + j] * scale[(j + 1) % N];")],
 }
 
 
@@ -184,8 +194,39 @@ def pin_probe(o):
         assert B.reshape(-1)[e] == np.float32(((z >> 40) - 2 ** 23) / 2 ** 23)
 
 
+def pin_wquant(o):
+    from fractions import Fraction
+    from test_oracle_wquant import columns, frac, rne, bits
+    for b, p in ((8, False), (4, True)):
+        W = columns(13, 9, b)
+        Q, s, _ = o.wquant_cols(W, b, p)
+        qmax = 2 ** (b - 1) - 1
+        What = o.wdequant_cols(Q, s)
+        for j in range(W.shape[1]):
+            m = max(abs(frac(w)) for w in W[:, j])
+            sa = R.decode(R.from_fraction(m / qmax, F32), F32).fraction()
+            want = sa
+            if p and sa:
+                want = Fraction(1)
+                while want < sa:
+                    want *= 2
+                while want / 2 >= sa:
+                    want /= 2
+            assert frac(s[j]) == want
+            for k in range(W.shape[0]):
+                q = 0 if want == 0 else rne(frac(W[k, j]) / want)
+                assert int(Q[k, j]) == q
+                assert bits(What[k, j]) == R.from_fraction(q * want, F32)
+    Q4, _, _ = o.wquant_cols(np.float32([[3.0], [1.25], [0.75], [-1.25]]), 4, True)
+    assert [int(v) for v in Q4[:, 0]] == [6, 2, 2, -2]
+    P = o.pack_int4(np.array([[1, -1, 7]], np.int8))
+    assert P[0, 0] == 0xF1 and P[0, 1] == 0x07
+
+
+F32 = R.BINARY32
+
 BATTERY = [pin_quantize_referee, pin_epilogue_referee, pin_bruteforce, pin_unit_scales,
-           pin_int32_range, pin_zero_row, pin_hash, pin_probe]
+           pin_int32_range, pin_zero_row, pin_hash, pin_probe, pin_wquant]
 
 
 def run_battery(o):
