@@ -204,6 +204,33 @@ uint64_t bsg_launch_count(void);
 bsg_status bsgemm_i8_noalloc(const float *A, const float *B, int64_t M, int64_t N, int64_t K,
                              int relu, float *C, int32_t *dstatus, void *stream);
 
+/* ---- weight storage as int8 / int4 codes ------------------------------------ */
+
+/* The weight storage of the presk "Precision" manual, section "Integer
+ * weights": a K x N weight W contracted over K is stored as codes with one
+ * scale per column j,
+ *   s_j = max_k |W[k][j]| / (2^(bits-1) - 1) rounded to f32 (bits = 8 or 4),
+ * or, with pow2 != 0, that scale rounded up to the smallest power of two >=
+ * it (q * s is then exact); an all-zero column, or one whose scale rounds to
+ * zero, gets s = 0 and stores zeros; the codes are q = W / s rounded to the
+ * nearest integer, ties to even.  W: DEVICE f32, row-major, ldw >= N.
+ * bits = 8: Q is K x N int8 (ldq >= N).  bits = 4: Q is K rows of ceil(N/2)
+ * bytes (ldq >= ceil(N/2)), 4-bit two's complement codes, column 2i in bits
+ * 0-3 of byte i and column 2i+1 in bits 4-7 (zero past the last column).
+ * scale: DEVICE f32[N].  Inf or NaN in W sets BSG_DSTATUS_NONFINITE in
+ * *dstatus (may be NULL); the codes and scales of such columns are then
+ * unspecified.  Asynchronous.  These are the pages' stored-weight semantics
+ * for a presk realization, a different scheme from the block-scaled unit's
+ * floor(x * inv + 0.5) codes. */
+bsg_status bsg_wquant_cols(const float *W, int64_t K, int64_t N, int64_t ldw, int bits, int pow2,
+                           void *Q, int64_t ldq, float *scale, int32_t *dstatus, void *stream);
+
+/* The stored weights: W_hat[k][j] = f32(q[k][j] * s_j), one rounding (exact
+ * with pow2 scales).  Q and bits as written by bsg_wquant_cols; W_hat: DEVICE
+ * f32 K x N, ldo >= N.  Asynchronous. */
+bsg_status bsg_wdequant_cols(const void *Q, int64_t K, int64_t N, int64_t ldq, int bits,
+                             const float *scale, float *W_hat, int64_t ldo, void *stream);
+
 /* ---- verification of live results ----------------------------------------- */
 
 /* The live audit ("Verification -- why you can trust the numbers", section

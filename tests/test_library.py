@@ -72,6 +72,10 @@ def test_argument_errors_without_gpu(lib):
     assert lib.bsg_audit(dummy, 4, dummy, 4, dummy, 4, 4, 4, 4, 0, 0, 0, dummy, None, None) == 1
     assert lib.bsg_audit(dummy, bsg.MAX_K + 1, dummy, 4, dummy, 4, 4, 4, bsg.MAX_K + 1, 0, 0, 8,
                          dummy, None, None) == 2
+    # weight storage: bits other than 8/4, ldq too small for the packed int4 rows
+    assert lib.bsg_wquant_cols(dummy, 4, 4, 4, 6, 0, dummy, 4, dummy, None, None) == 1
+    assert lib.bsg_wquant_cols(dummy, 4, 5, 5, 4, 0, dummy, 2, dummy, None, None) == 1
+    assert lib.bsg_wdequant_cols(dummy, 4, 4, 4, 8, dummy, dummy, 3, None) == 1
     # self-test: missing or small workspace
     assert lib.bsg_selftest(None, 0, None, None) == 3
     assert lib.bsg_selftest(dummy, 16, None, None) == 3

@@ -80,6 +80,8 @@ def _declare(lib):
                        _i32, _vp, _vp, _vp], _i32),
         "bsg_selftest_workspace_size": ([], _sz),
         "bsg_selftest": ([_vp, _sz, _vp, _vp], _i32),
+        "bsg_wquant_cols": ([_vp, _i64, _i64, _i64, _i32, _i32, _vp, _i64, _vp, _vp, _vp], _i32),
+        "bsg_wdequant_cols": ([_vp, _i64, _i64, _i64, _i32, _vp, _vp, _i64, _vp], _i32),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -373,6 +375,34 @@ def audit(A, B, C, relu=False, seed: int = 0, nsamples: int = 256, mismatches=No
                             ctypes.c_uint64(seed), int(nsamples), _ptr(mismatches), _ptr(cells),
                             _stream_ptr(stream)), "bsg_audit")
     return mismatches
+
+
+def wquant_cols(W, bits: int = 8, pow2: bool = False, dstatus=None, stream=None):
+    """Weight storage codes of a K x N f32 weight (per-column scales):
+    (Q, scale).  bits 8: Q int8 K x N; bits 4: Q uint8 K x ceil(N/2), two
+    4-bit codes per byte."""
+    torch = _torch()
+    _need(W, torch.float32, "W")
+    K, N = W.shape
+    if bits == 8:
+        Q = torch.empty((K, N), dtype=torch.int8, device=W.device)
+    else:
+        Q = torch.empty((K, (N + 1) // 2), dtype=torch.uint8, device=W.device)
+    sc = torch.empty(N, dtype=torch.float32, device=W.device)
+    _check(load().bsg_wquant_cols(_ptr(W), K, N, N, int(bits), int(bool(pow2)), _ptr(Q),
+                                  Q.shape[1], _ptr(sc), _ptr(dstatus), _stream_ptr(stream)),
+           "bsg_wquant_cols")
+    return Q, sc
+
+
+def wdequant_cols(Q, scale, N: int, bits: int = 8, stream=None):
+    """The stored weights f32(q * s) (K x N f32)."""
+    torch = _torch()
+    K = Q.shape[0]
+    out = torch.empty((K, N), dtype=torch.float32, device=Q.device)
+    _check(load().bsg_wdequant_cols(_ptr(Q), K, N, Q.shape[1], int(bits), _ptr(scale),
+                                    _ptr(out), N, _stream_ptr(stream)), "bsg_wdequant_cols")
+    return out
 
 
 def selftest(workspace=None):

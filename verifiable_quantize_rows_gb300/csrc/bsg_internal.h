@@ -69,6 +69,13 @@ cudaError_t launch_audit(const float *A, int64_t lda, const float *B, int64_t ld
                          int64_t ldc, int64_t M, int64_t N, int64_t K, int relu, uint64_t seed,
                          int nsamples, uint32_t *mismatches, int64_t *cells, cudaStream_t st);
 
+// Weight storage as int8 / int4 codes with per-column scales, and back.
+cudaError_t launch_wquant_cols(const float *W, int64_t K, int64_t N, int64_t ldw, int bits,
+                               int pow2, void *Q, int64_t ldq, float *scale, int32_t *dstatus,
+                               cudaStream_t st);
+cudaError_t launch_wdequant_cols(const void *Q, int64_t K, int64_t N, int64_t ldq, int bits,
+                                 const float *scale, float *out, int64_t ldo, cudaStream_t st);
+
 // Device check of the scale derivation over absmax bit patterns [first, last].
 cudaError_t launch_selftest_scales(uint32_t first, uint32_t last, unsigned long long *bad,
                                    cudaStream_t st);

@@ -583,4 +583,27 @@ bsg_status bsg_selftest(void *workspace, size_t ws_bytes, uint32_t *audit_mismat
     return (hash_ok && mis == 0) ? BSG_OK : BSG_ERR_SELFTEST;
 }
 
+bsg_status bsg_wquant_cols(const float *W, int64_t K, int64_t N, int64_t ldw, int bits, int pow2,
+                           void *Q, int64_t ldq, float *scale, int32_t *dstatus, void *stream) {
+    if (!W || !Q || !scale || K < 1 || N < 1 || ldw < N || (bits != 8 && bits != 4) ||
+        (pow2 != 0 && pow2 != 1))
+        return BSG_ERR_ARG;
+    if (ldq < (bits == 8 ? N : (N + 1) / 2)) return BSG_ERR_ARG;
+    bsg_status s = check_device();
+    if (s != BSG_OK) return s;
+    return from_cuda(launch_wquant_cols(W, K, N, ldw, bits, pow2, Q, ldq, scale, dstatus,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+bsg_status bsg_wdequant_cols(const void *Q, int64_t K, int64_t N, int64_t ldq, int bits,
+                             const float *scale, float *W_hat, int64_t ldo, void *stream) {
+    if (!Q || !scale || !W_hat || K < 1 || N < 1 || ldo < N || (bits != 8 && bits != 4))
+        return BSG_ERR_ARG;
+    if (ldq < (bits == 8 ? N : (N + 1) / 2)) return BSG_ERR_ARG;
+    bsg_status s = check_device();
+    if (s != BSG_OK) return s;
+    return from_cuda(launch_wdequant_cols(Q, K, N, ldq, bits, scale, W_hat, ldo,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"
