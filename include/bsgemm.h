@@ -265,7 +265,12 @@ bsg_status bsg_selftest(void *workspace, size_t ws_bytes, uint32_t *audit_mismat
 
 /* bsgemm_i8 on HOST buffers (packed row-major; pinned memory gives
  * asynchronous copies): copies A and B to the device, runs the unit, copies
- * C back, and synchronizes `stream` before returning.  `workspace`: device
+ * C back, and synchronizes `stream` before returning.  A moves in row chunks
+ * on a copy stream of the library's own and C comes back chunk by chunk on
+ * another, so that uploads, the kernels (on `stream`) and downloads overlap
+ * (the two copy streams are created on the first call on each device and
+ * kept until the process exits); the result does not depend on the
+ * chunking.  `workspace`: device
  * memory of at least bsgemm_i8_host_workspace_size(M, N, K) bytes.
  * *dstatus_host (may be NULL) receives the device status bits. */
 size_t bsgemm_i8_host_workspace_size(int64_t M, int64_t N, int64_t K);

@@ -119,3 +119,23 @@ def test_host_buffer_entry_point(orc):
     assert st == 0
     Co, _ = orc.bsgemm_i8(A, B, True)
     assert_bits_equal(C.numpy(), Co, "host entry point")
+
+
+@pytest.mark.parametrize("M,N,K", [(3000, 257, 1100), (8192, 2304, 768), (100, 33, 65),
+                                   (2049, 64, 3072)])
+def test_host_buffer_entry_point_chunked(orc, M, N, K):
+    """The host entry point moves A in row chunks and overlaps copies with the
+    kernels: ragged chunk counts and a last partial chunk give the same bits."""
+    A = inputs.gpt2_activations(M, K, M + K).numpy()
+    B = inputs.gpt2_weights(K, N, N).numpy()
+    Ah = torch.from_numpy(A).pin_memory()
+    Bh = torch.from_numpy(B).pin_memory()
+    C, st = bsg.bsgemm_i8_host(Ah, Bh, relu=False)
+    assert st == 0
+    if M * N * K <= 3000 * 257 * 1100:
+        Co, _ = orc.bsgemm_i8(A, B, False)
+        assert_bits_equal(C.numpy(), Co, f"host {M}x{N}x{K}")
+    else:
+        Cd = bsg.bsgemm_i8(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda())
+        torch.cuda.synchronize()
+        assert_bits_equal(C.numpy(), Cd.cpu().numpy(), "host vs device entry point")

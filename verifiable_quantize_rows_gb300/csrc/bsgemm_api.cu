@@ -408,6 +408,53 @@ size_t bsgemm_i8_host_workspace_size(int64_t M, int64_t N, int64_t K) {
     return host_prefix(M, N, K) + bsgemm_i8_workspace_size(M, N, K);
 }
 
+}  // extern "C"
+
+namespace bsg {
+namespace {
+
+// Copy streams of the host-buffer entry point, one pair per device: uploads
+// on one, downloads on the other, so that both directions of the link and the
+// kernels on the caller's stream run at once.  Created on the first call on
+// each device and kept until the process exits; one host thread at a time
+// uses them (the entry point is synchronous).
+constexpr int kHostChunks = 8;
+struct HostPipe {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, b_in = nullptr, done = nullptr;
+    cudaEvent_t a_in[kHostChunks] = {}, c_ready[kHostChunks] = {};
+    bool tried = false;
+};
+std::mutex g_host_lock;
+HostPipe g_host[64];
+
+HostPipe *host_pipe() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    HostPipe &h = g_host[dev];
+    if (!h.tried) {
+        h.tried = true;
+        bool ok = cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&h.b_in, cudaEventDisableTiming) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&h.done, cudaEventDisableTiming) == cudaSuccess;
+        for (int c = 0; ok && c < kHostChunks; ++c)
+            ok = cudaEventCreateWithFlags(&h.a_in[c], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&h.c_ready[c], cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) {
+            cudaGetLastError();
+            h.in = nullptr;
+        }
+    }
+    return h.in ? &h : nullptr;
+}
+
+}  // namespace
+}  // namespace bsg
+
+extern "C" {
+
 bsg_status bsgemm_i8_host(const float *A_host, const float *B_host, int64_t M, int64_t N,
                           int64_t K, int relu, float *C_host, void *workspace, size_t ws_bytes,
                           int32_t *dstatus_host, void *stream) {
@@ -428,17 +475,65 @@ bsg_status bsgemm_i8_host(const float *A_host, const float *B_host, int64_t M, i
     int32_t *dstat = at<int32_t>(workspace, off);
     off += 256;
     void *uws = at<void>(workspace, off);
-    if (cudaMemsetAsync(dstat, 0, sizeof(int32_t), st) != cudaSuccess) return BSG_ERR_CUDA;
-    if (cudaMemcpyAsync(dA, A_host, (size_t)M * K * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemcpyAsync(dB, B_host, (size_t)K * N * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    const UnitLayout L = unit_layout(M, N, K, 0, 0);
+    const int64_t ldk = operand_ld(K);
+    __half *aop = at<__half>(uws, L.aop);
+    __half *bop = at<__half>(uws, L.bop);
+    float *sa = at<float>(uws, L.sa);
+    float *sb = at<float>(uws, L.sb);
+    unsigned int *ticket = at<unsigned int>(uws, L.ticket);
+    uint32_t *part_b = at<uint32_t>(uws, L.part_b);
+
+    std::lock_guard<std::mutex> guard(g_host_lock);
+    HostPipe *h = host_pipe();
+    if (!h) return BSG_ERR_CUDA;
+    // A in row chunks of a multiple of 256 rows (the GEMM's pair tile): the
+    // upload of chunk c+1 and the download of chunk c-1 overlap the quantize
+    // and GEMM of chunk c.  Per-row quantize and the GEMM's tiling do not
+    // depend on the chunking, so neither does any bit of C.
+    int64_t rows = (M + kHostChunks - 1) / kHostChunks;
+    rows = (rows + 255) / 256 * 256;
+    const int nchunks = (int)((M + rows - 1) / rows);
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    if (!ok(cudaEventRecord(h->start, st)) || !ok(cudaStreamWaitEvent(h->in, h->start, 0)) ||
+        !ok(cudaStreamWaitEvent(h->out, h->start, 0)) ||
+        !ok(cudaMemsetAsync(dstat, 0, sizeof(int32_t), st)))
         return BSG_ERR_CUDA;
-    s = unit(dA, K, 0, dB, N, 0, M, N, K, relu, dC, N, uws, ws_bytes - off, dstat, st);
-    if (s != BSG_OK) return s;
+    // uploads: B, then A chunk by chunk
+    if (!ok(cudaMemcpyAsync(dB, B_host, (size_t)K * N * 4, cudaMemcpyHostToDevice, h->in)) ||
+        !ok(cudaEventRecord(h->b_in, h->in)))
+        return BSG_ERR_CUDA;
+    for (int c = 0; c < nchunks; ++c) {
+        const int64_t r0 = c * rows, mc = M - r0 < rows ? M - r0 : rows;
+        if (!ok(cudaMemcpyAsync(dA + r0 * K, A_host + r0 * K, (size_t)(mc * K) * 4,
+                                cudaMemcpyHostToDevice, h->in)) ||
+            !ok(cudaEventRecord(h->a_in[c], h->in)))
+            return BSG_ERR_CUDA;
+    }
+    // kernels on the caller's stream: B per column once, then per chunk the
+    // rows of A and the GEMM of those rows; downloads follow each chunk
+    if (!ok(cudaStreamWaitEvent(st, h->b_in, 0)) ||
+        !ok(launch_quantize_cols(dB, K, N, N, kOutHalfKMajor, bop, ldk, sb, nullptr, part_b, dstat,
+                                 st)))
+        return BSG_ERR_CUDA;
+    for (int c = 0; c < nchunks; ++c) {
+        const int64_t r0 = c * rows, mc = M - r0 < rows ? M - r0 : rows;
+        if (!ok(cudaStreamWaitEvent(st, h->a_in[c], 0)) ||
+            !ok(launch_quantize_rows(dA + r0 * K, mc, K, K, kOutHalfKMajor, aop + r0 * ldk, ldk,
+                                     sa + r0, nullptr, dstat, st, ticket)) ||
+            !ok(launch_gemm_tc(aop + r0 * ldk, bop, mc, N, K, sa + r0, sb, relu, 0, dC + r0 * N, N,
+                               dstat, ticket, st)) ||
+            !ok(cudaEventRecord(h->c_ready[c], st)) ||
+            !ok(cudaStreamWaitEvent(h->out, h->c_ready[c], 0)) ||
+            !ok(cudaMemcpyAsync(C_host + r0 * N, dC + r0 * N, (size_t)(mc * N) * 4,
+                                cudaMemcpyDeviceToHost, h->out)))
+            return BSG_ERR_CUDA;
+    }
     int32_t hstat = 0;
-    if (cudaMemcpyAsync(C_host, dC, (size_t)M * N * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaMemcpyAsync(&hstat, dstat, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    if (!ok(cudaMemcpyAsync(&hstat, dstat, sizeof(int32_t), cudaMemcpyDeviceToHost, h->out)) ||
+        !ok(cudaEventRecord(h->done, h->out)) || !ok(cudaStreamWaitEvent(st, h->done, 0)) ||
+        !ok(cudaStreamSynchronize(st)))
         return BSG_ERR_CUDA;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return BSG_ERR_CUDA;
     if (dstatus_host) *dstatus_host = hstat;
     return BSG_OK;
 }
