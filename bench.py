@@ -470,11 +470,17 @@ def cpu_baseline(budget_s=12.0):
     ops, t = oracle_sample_step(orc, 256)
     rows = int(min(8192, max(256, 256 * budget_s / max(t, 1e-3))))
     rows = max(256, (rows // 256) * 256)
-    ops, t = oracle_sample_step(orc, rows)
-    return {"value": round(ops / t / 1e12, 6), "unit": "TOPS", "cores": orc.num_threads(),
-            "kind": "oracle",
+    # repeat the sample until about budget_s of CPU work (when even the whole
+    # workload takes less)
+    total_ops, total_t, reps = 0, 0.0, 0
+    while total_t < 0.8 * budget_s or reps == 0:
+        ops, t = oracle_sample_step(orc, rows)
+        total_ops, total_t, reps = total_ops + ops, total_t + t, reps + 1
+    return {"value": round(total_ops / total_t / 1e12, 6), "unit": "TOPS",
+            "cores": orc.num_threads(), "kind": "oracle",
             "sample": f"each GPT-2 linear on its first {rows} of 8192 rows (full N, K) plus the "
-                      f"full 1024^3 probe; {ops / 1e9:.1f} G ops in {t:.1f} s"}
+                      f"full 1024^3 probe, {reps}x: {total_ops / 1e9:.1f} G ops in "
+                      f"{total_t:.1f} s"}
 
 
 def run_reference(args, rank, world):
