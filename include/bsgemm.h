@@ -146,6 +146,33 @@ bsg_status bsgemm_i8_ex(const float *A, int64_t lda, int transA, const float *B,
                         int64_t ldc, void *workspace, size_t ws_bytes, int32_t *dstatus,
                         void *stream);
 
+/* Several units in one GEMM launch (at most BSG_MAX_GROUP): each item is the
+ * argument list of bsgemm_i8_ex, with its own workspace of
+ * bsgemm_i8_workspace_size(M, N, K) bytes.  Every item's operands are
+ * quantized as in bsgemm_i8_ex; then ONE tensor-core launch computes all the
+ * products, its CTAs sharing the tiles of all items (one tail wave instead of
+ * one per item) -- for instance the three GEMMs of a training step's linear
+ * layer (forward X.W, grad-input dY.W^T, grad-weight X^T.dY).  The C of each
+ * item is bit for bit what bsgemm_i8_ex gives it.  Items must not overlap in
+ * C or workspace.  The pages have no grouped call; their units run one
+ * product at a time. */
+#define BSG_MAX_GROUP 3
+typedef struct {
+    const float *A;
+    int64_t lda;
+    int transA;
+    const float *B;
+    int64_t ldb;
+    int transB;
+    int64_t M, N, K;
+    int relu;
+    float *C;
+    int64_t ldc;
+    void *workspace;
+    size_t ws_bytes;
+} bsg_gemm_item;
+bsg_status bsgemm_i8_group(const bsg_gemm_item *items, int count, int32_t *dstatus, void *stream);
+
 /* The unit in two stages over one workspace (bsgemm_i8 is the pair):
  * bsgemm_i8_quantize runs step 1 -- op(A) per row and op(B) per column into
  * the workspace's f16 operands and scales (arguments as bsgemm_i8_ex) -- and

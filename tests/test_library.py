@@ -76,6 +76,11 @@ def test_argument_errors_without_gpu(lib):
     assert lib.bsg_wquant_cols(dummy, 4, 4, 4, 6, 0, dummy, 4, dummy, None, None) == 1
     assert lib.bsg_wquant_cols(dummy, 4, 5, 5, 4, 0, dummy, 2, dummy, None, None) == 1
     assert lib.bsg_wdequant_cols(dummy, 4, 4, 4, 8, dummy, dummy, 3, None) == 1
+    # grouped call: no items, too many items
+    assert lib.bsgemm_i8_group(None, 1, None, None) == 1
+    items = (bsg.GemmItem * 4)()
+    assert lib.bsgemm_i8_group(items, 4, None, None) == 1
+    assert lib.bsgemm_i8_group(items, 0, None, None) == 1
     # self-test: missing or small workspace
     assert lib.bsg_selftest(None, 0, None, None) == 3
     assert lib.bsg_selftest(dummy, 16, None, None) == 3

@@ -46,6 +46,15 @@ _lib = None
 _i64, _vp, _sz, _i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
 
 
+class GemmItem(ctypes.Structure):
+    """One item of bsgemm_i8_group (the C struct bsg_gemm_item)."""
+    _fields_ = [("A", ctypes.c_void_p), ("lda", ctypes.c_int64), ("transA", ctypes.c_int),
+                ("B", ctypes.c_void_p), ("ldb", ctypes.c_int64), ("transB", ctypes.c_int),
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("relu", ctypes.c_int), ("C", ctypes.c_void_p), ("ldc", ctypes.c_int64),
+                ("workspace", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t)]
+
+
 def _declare(lib):
     sigs = {
         "bsg_status_str": ([_i32], ctypes.c_char_p),
@@ -80,6 +89,7 @@ def _declare(lib):
                        _i32, _vp, _vp, _vp], _i32),
         "bsg_selftest_workspace_size": ([], _sz),
         "bsg_selftest": ([_vp, _sz, _vp, _vp], _i32),
+        "bsgemm_i8_group": ([ctypes.POINTER(GemmItem), _i32, _vp, _vp], _i32),
         "bsg_wquant_cols": ([_vp, _i64, _i64, _i64, _i32, _i32, _vp, _i64, _vp, _vp, _vp], _i32),
         "bsg_wdequant_cols": ([_vp, _i64, _i64, _i64, _i32, _vp, _vp, _i64, _vp], _i32),
     }
@@ -375,6 +385,40 @@ def audit(A, B, C, relu=False, seed: int = 0, nsamples: int = 256, mismatches=No
                             ctypes.c_uint64(seed), int(nsamples), _ptr(mismatches), _ptr(cells),
                             _stream_ptr(stream)), "bsg_audit")
     return mismatches
+
+
+def bsgemm_i8_group(items, dstatus=None, stream=None, workspace=None):
+    """Several units in one GEMM launch.  `items`: up to 3 tuples
+    (A, B, transA, transB, relu) of CUDA float32 tensors as for bsgemm_i8_ex
+    (A stored M x K, or K x M with transA; B stored K x N, or N x K with
+    transB).  Returns the list of C tensors."""
+    torch = _torch()
+    lib = load()
+    n = len(items)
+    arr = (GemmItem * n)()
+    dims, outs, offs = [], [], []
+    total = 0
+    for A, B, tA, tB, relu in items:
+        _need(A, torch.float32, "A")
+        _need(B, torch.float32, "B")
+        M, K = (A.shape[1], A.shape[0]) if tA else (A.shape[0], A.shape[1])
+        N = B.shape[0] if tB else B.shape[1]
+        dims.append((M, N, K))
+        offs.append(total)
+        total += (lib.bsgemm_i8_workspace_size(M, N, K) + 255) // 256 * 256
+    # one workspace carved into the items' parts (the library's default one
+    # unless `workspace` is given), kept alive beyond this call
+    wp, wn = _ws(workspace, total)
+    base = wp.value
+    for i, ((A, B, tA, tB, relu), (M, N, K)) in enumerate(zip(items, dims)):
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+        outs.append(C)
+        size = lib.bsgemm_i8_workspace_size(M, N, K)
+        arr[i] = GemmItem(A.data_ptr(), A.shape[1], int(bool(tA)), B.data_ptr(), B.shape[1],
+                          int(bool(tB)), M, N, K, int(bool(relu)), C.data_ptr(), N,
+                          base + offs[i], size)
+    _check(lib.bsgemm_i8_group(arr, n, _ptr(dstatus), _stream_ptr(stream)), "bsgemm_i8_group")
+    return outs
 
 
 def wquant_cols(W, bits: int = 8, pow2: bool = False, dstatus=None, stream=None):

@@ -86,9 +86,11 @@ cudaError_t launch_i8_rows_to_half(const int8_t *Q, int64_t rows, int64_t cols, 
 cudaError_t launch_i8_cols_to_half(const int8_t *Q, int64_t rows, int64_t cols, int64_t ldq,
                                    __half *out, int64_t ldo, cudaStream_t st);
 
-// The tile width (64, 128, 192 or 256) the GEMM uses for an M x N problem, and
-// whether it runs 256-row tiles on CTA pairs when M > 128.
+// The tile width (64, 128, 192 or 256) the GEMM uses for an M x N problem (or
+// a launch of n of them), and whether it runs 256-row tiles on CTA pairs
+// when M > 128.
 int gemm_tile_width(int64_t M, int64_t N, int sms);
+int gemm_group_tile_width(const int64_t *M, const int64_t *N, int n, int sms);
 bool gemm_pairs_enabled();
 // The tensor-core GEMM.  Aop: M x ldk f16, Bop: N x ldk f16 (both K-major,
 // ldk = operand_ld(K)).  mode 0: C = epi(S, sa, sb) (+ReLU) as float;
@@ -98,6 +100,20 @@ bool gemm_pairs_enabled();
 // device memory, the tile counter: zero before the first launch on it (the
 // quantize step that fills a unit workspace zeroes it), and zero again after
 // every launch that completes.
+// One GEMM of a grouped launch (the arguments of launch_gemm_tc).
+struct GemmJob {
+    const __half *Aop, *Bop;
+    int64_t M, N, K;
+    const float *sa, *sb;
+    int relu;
+    void *out;
+    int64_t ldo;
+};
+// Up to 3 GEMMs in one launch: their tiles form one list that the launch's
+// CTAs share (one tail instead of three).  Same mode, status word and tile
+// counter for all.
+cudaError_t launch_gemm_tc_group(const GemmJob *jobs, int n, int mode, int32_t *dstatus,
+                                 unsigned int *ticket, cudaStream_t st, int tile_width = 0);
 cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int64_t N,
                            int64_t K, const float *sa, const float *sb, int relu, int mode,
                            void *out, int64_t ldo, int32_t *dstatus, unsigned int *ticket,

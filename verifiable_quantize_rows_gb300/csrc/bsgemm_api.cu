@@ -358,6 +358,47 @@ bsg_status bsgemm_i8_ex(const float *A, int64_t lda, int transA, const float *B,
                 dstatus, static_cast<cudaStream_t>(stream));
 }
 
+bsg_status bsgemm_i8_group(const bsg_gemm_item *items, int count, int32_t *dstatus,
+                           void *stream) {
+    if (!items || count < 1 || count > BSG_MAX_GROUP) return BSG_ERR_ARG;
+    for (int i = 0; i < count; ++i) {
+        const bsg_gemm_item &it = items[i];
+        if ((it.transA != 0 && it.transA != 1) || (it.transB != 0 && it.transB != 1))
+            return BSG_ERR_ARG;
+        bsg_status s = check_unit_args(it.A, it.lda, it.transA, it.B, it.ldb, it.transB, it.M,
+                                       it.N, it.K);
+        if (s != BSG_OK) return s;
+        if (!it.C || it.ldc < it.N || (it.relu != 0 && it.relu != 1)) return BSG_ERR_ARG;
+        if (!ws_ok(it.workspace, it.ws_bytes, bsgemm_i8_workspace_size(it.M, it.N, it.K)))
+            return BSG_ERR_WORKSPACE;
+    }
+    bsg_status s = check_device();
+    if (s != BSG_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    GemmJob jobs[BSG_MAX_GROUP];
+    for (int i = 0; i < count; ++i) {
+        const bsg_gemm_item &it = items[i];
+        s = unit_quantize(it.A, it.lda, it.transA, it.B, it.ldb, it.transB, it.M, it.N, it.K,
+                          it.workspace, it.ws_bytes, dstatus, st);
+        if (s != BSG_OK) return s;
+        const UnitLayout L = unit_layout(it.M, it.N, it.K, 0, 0);
+        jobs[i].Aop = at<__half>(it.workspace, L.aop);
+        jobs[i].Bop = at<__half>(it.workspace, L.bop);
+        jobs[i].M = it.M;
+        jobs[i].N = it.N;
+        jobs[i].K = it.K;
+        jobs[i].sa = at<float>(it.workspace, L.sa);
+        jobs[i].sb = at<float>(it.workspace, L.sb);
+        jobs[i].relu = it.relu;
+        jobs[i].out = it.C;
+        jobs[i].ldo = it.ldc;
+    }
+    // the tile counter of the first item's workspace (its quantize zeroed it)
+    const UnitLayout L0 = unit_layout(items[0].M, items[0].N, items[0].K, 0, 0);
+    return from_cuda(launch_gemm_tc_group(jobs, count, 0, dstatus,
+                                          at<unsigned int>(items[0].workspace, L0.ticket), st));
+}
+
 bsg_status bsgemm_i8_quantize(const float *A, int64_t lda, int transA, const float *B,
                               int64_t ldb, int transB, int64_t M, int64_t N, int64_t K,
                               void *workspace, size_t ws_bytes, int32_t *dstatus, void *stream) {

@@ -108,19 +108,29 @@ struct Cfg {
     static_assert(kStageBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms stay aligned");
 };
 
-struct Params {
+constexpr int kMaxGroup = 3;  // GEMMs per launch
+
+// One GEMM of a launch.
+struct Prob {
     int M, N, K;
     int num_kb;        // k-blocks per tile
     int num_m, num_n;  // 128-row m-blocks, BN-wide n-tiles
     int num_mu;        // m-units: m-blocks, or pairs of them (PAIR)
-    int num_units;     // tiles of the launch: num_mu * num_n
+    int unit0;         // index of this GEMM's first tile in the launch
     const float *sa;
     const float *sb;
     void *out;
     int64_t ldo;
-    int mode;       // 0: f32 epilogue, 1: int32 accumulators
     int relu;
-    int tma_store;  // 1: C's rows are 16-byte aligned; store through tmap_c
+    int tma_store;  // 1: C's rows are 16-byte aligned; store through its tensor map
+};
+
+template <int NP>  // GEMMs the launch was compiled for (1, or kMaxGroup)
+struct Params {
+    Prob prob[NP];
+    int nprob;
+    int num_units;  // tiles of the launch, all GEMMs
+    int mode;       // 0: f32 epilogue, 1: int32 accumulators
     int32_t *dstatus;
     // ticket[0]: tiles claimed beyond the first wave; ticket[1]: CTAs (pairs)
     // done claiming.  Zero at launch; the last CTA to finish claiming sets
@@ -128,16 +138,31 @@ struct Params {
     unsigned int *ticket;
 };
 
-// Tile u -> (m-unit, n-tile), rastered in groups of kGroupM m-units so that
-// concurrent tiles share operand rows and columns in L2.
-__host__ __device__ __forceinline__ void tile_coords(const Params &p, int u, int &mu, int &nb) {
-    const int per_group = kGroupM * p.num_n;
+// The tensor maps of every GEMM: operands A and B (f16, K-major) and C.
+template <int NP>
+struct Maps {
+    CUtensorMap a[NP], b[NP], c[NP];
+};
+
+// Tile u of the launch -> its GEMM (returned) and (m-unit, n-tile) there,
+// rastered in groups of kGroupM m-units so that concurrent tiles share
+// operand rows and columns in L2.  With NP = 1 the GEMM is a constant, so
+// that a single GEMM's parameters are read at fixed offsets.
+template <int NP>
+__device__ __forceinline__ int tile_coords(const Params<NP> &p, int u, int &mu, int &nb) {
+    int pi = 0;
+    if (NP > 1)
+        while (pi + 1 < p.nprob && u >= p.prob[pi + 1].unit0) ++pi;
+    const Prob &q = p.prob[pi];
+    u -= q.unit0;
+    const int per_group = kGroupM * q.num_n;
     const int g = u / per_group;
     const int first_m = g * kGroupM;
-    const int gm = (p.num_mu - first_m) < kGroupM ? (p.num_mu - first_m) : kGroupM;
+    const int gm = (q.num_mu - first_m) < kGroupM ? (q.num_mu - first_m) : kGroupM;
     const int r = u - g * per_group;
     mu = first_m + r % gm;
     nb = r / gm;
+    return pi;
 }
 
 __device__ __forceinline__ void record_abort(volatile int *abort_flag, int32_t *dstatus) {
@@ -186,7 +211,7 @@ __device__ __forceinline__ void epi_piece(uint32_t (&v)[32], const float4 *sbv, 
 // store directly to global memory.  `nstored` counts the warp's TMA stores;
 // a box is rewritten only after the store that last used it has read it.
 template <int NBOX>
-__device__ __forceinline__ void emit_box(const Params &p, const CUtensorMap *tmap_c,
+__device__ __forceinline__ void emit_box(const Prob &p, const CUtensorMap *tmap_c,
                                          uint8_t *boxes, const uint32_t (&v)[32], int row0,
                                          int col0, int lane, int &nstored) {
     if (p.tma_store) {
@@ -224,11 +249,9 @@ __device__ __forceinline__ void emit_box(const Params &p, const CUtensorMap *tma
     }
 }
 
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, int NP>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                   const __grid_constant__ CUtensorMap tmap_b,
-                   const __grid_constant__ CUtensorMap tmap_c, const Params p) {
+    gemm_tc_kernel(const __grid_constant__ Maps<NP> maps, const __grid_constant__ Params<NP> p) {
     using K = Cfg<BN, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -248,7 +271,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int num_chunks = (p.num_kb + kChunkBlocks - 1) / kChunkBlocks;
     const int rank = PAIR ? (int)cluster_ctarank() : 0;  // 0: the pair's MMA-issuing CTA
     const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // first tile
     const int nunits = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
@@ -297,8 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            prefetch_tmap(&tmap_a);
-            prefetch_tmap(&tmap_b);
+            for (int i = 0; i < p.nprob; ++i) {
+                prefetch_tmap(&maps.a[i]);
+                prefetch_tmap(&maps.b[i]);
+            }
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_parity[K::kStages];
@@ -320,9 +344,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(&qempty[slot]);
                 if (tile < 0) break;  // no tiles left
                 int mu, nb;
-                tile_coords(p, tile, mu, nb);
+                const int pi = tile_coords(p, tile, mu, nb);
+                const CUtensorMap *tma = &maps.a[pi];
+                const CUtensorMap *tmb = &maps.b[pi];
                 const int mb = PAIR ? 2 * mu + rank : mu;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                const int num_kb = p.prob[pi].num_kb;
+                for (int kb = 0; kb < num_kb; ++kb) {
                     if (!bar_wait<PAIR>(&empty[stage], phase ^ 1, abort_flag)) {
                         record_abort(abort_flag, p.dstatus);
                         ok = false;
@@ -334,12 +361,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // the even CTA's full barrier, where both CTAs count their bytes
                         const uint32_t fb = cluster_addr(&full[stage], 0);
                         mbar_arrive_expect_tx_cl(fb, K::kStageBytes);
-                        tma_load_2d_pair(&tmap_a, fb, sa_tile, kb * kBK, mb * kBM);
-                        tma_load_2d_pair(&tmap_b, fb, sb_tile, kb * kBK, nb * BN + rank * K::kBRows);
+                        tma_load_2d_pair(tma, fb, sa_tile, kb * kBK, mb * kBM);
+                        tma_load_2d_pair(tmb, fb, sb_tile, kb * kBK, nb * BN + rank * K::kBRows);
                     } else {
                         mbar_arrive_expect_tx(&full[stage], K::kStageBytes);
-                        tma_load_2d(&tmap_a, &full[stage], sa_tile, kb * kBK, mb * kBM);
-                        tma_load_2d(&tmap_b, &full[stage], sb_tile, kb * kBK, nb * BN);
+                        tma_load_2d(tma, &full[stage], sa_tile, kb * kBK, mb * kBM);
+                        tma_load_2d(tmb, &full[stage], sb_tile, kb * kBK, nb * BN);
                     }
                     issued[stage] = true;
                     issued_parity[stage] = phase;
@@ -422,9 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int tile = tileq[slot];
                 mbar_arrive(&qempty[slot]);
                 if (tile < 0) break;
+                int mu, nb;
+                const int num_kb = p.prob[tile_coords(p, tile, mu, nb)].num_kb;
+                const int num_chunks = (num_kb + kChunkBlocks - 1) / kChunkBlocks;
                 for (int c = 0; ok && c < num_chunks; ++c) {
                     const int kb0 = c * kChunkBlocks;
-                    const int kb1 = min(p.num_kb, kb0 + kChunkBlocks);
+                    const int kb1 = min(num_kb, kb0 + kChunkBlocks);
                     const uint32_t b = acc_iter & 1;
                     const uint32_t acc_phase = (acc_iter >> 1) & 1;
                     if (!bar_wait<PAIR>(&tempty[b], acc_phase ^ 1, abort_flag)) {
@@ -492,12 +522,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t acc_iter = 0;
         bool ok = true;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        // With a single chunk (K <= 1024) the fp32 accumulator already is
-        // f32(S): S is an integer below 2^24 in magnitude, held exactly.  The
-        // f32 epilogue then needs no conversion (float->int and back run at a
-        // fraction of the ALU rate); adding +0 turns a -0 sum (all products
-        // -0) into f32(0) = +0.
-        const bool f32_sums = num_chunks == 1 && p.mode == 0;
         for (uint32_t t = 0; ok; ++t) {
             const int slot = (int)(t % kTileQ);
             const uint32_t qph = (t / kTileQ) & 1;
@@ -515,6 +539,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(&qempty[slot]);
             }
             if (tile < 0) break;
+            int mu, nb;
+            const int pi = tile_coords(p, tile, mu, nb);
+            const Prob &pr = p.prob[pi];
+            const int num_chunks = (pr.num_kb + kChunkBlocks - 1) / kChunkBlocks;
+            // With a single chunk (K <= 1024) the fp32 accumulator already is
+            // f32(S): S is an integer below 2^24 in magnitude, held exactly.
+            // The f32 epilogue then needs no conversion (float->int and back
+            // run at a fraction of the ALU rate); adding +0 turns a -0 sum
+            // (all products -0) into f32(0) = +0.
+            const bool f32_sums = num_chunks == 1 && p.mode == 0;
             // ---- drain every chunk into int32 sums (or, f32_sums, f32(S))
             uint32_t acc[K::kWarpCols];  // int32 or f32 bit patterns
             for (int c = 0; c < num_chunks; ++c) {
@@ -565,29 +599,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
 
             // ---- final epilogue of the tile from the sums
-            int mu, nb;
-            tile_coords(p, tile, mu, nb);
             const int mb = PAIR ? 2 * mu + rank : mu;
-            if (mb >= p.num_m) continue;  // the odd CTA of a pair past the last m-block
+            if (mb >= pr.num_m) continue;  // the odd CTA of a pair past the last m-block
             const int row0 = mb * kBM + q * 32;
             const int colh = nb * BN + h * K::kWarpCols;
-            const float a = p.mode == 0 ? __ldg(p.sa + row0 + lane) : 0.0f;
+            const float a = p.mode == 0 ? __ldg(pr.sa + row0 + lane) : 0.0f;
 #pragma unroll
             for (int piece = 0; piece < K::kPieces; ++piece) {
                 uint32_t(&v)[32] = *reinterpret_cast<uint32_t(*)[32]>(&acc[piece * 32]);
                 const int col0 = colh + piece * 32;
                 if (p.mode == 0) {
                     // in place: the sums become the output bits
-                    const float4 *sbv = reinterpret_cast<const float4 *>(p.sb + col0);
+                    const float4 *sbv = reinterpret_cast<const float4 *>(pr.sb + col0);
                     if (f32_sums)
-                        epi_piece<true>(v, sbv, a, p.relu);
+                        epi_piece<true>(v, sbv, a, pr.relu);
                     else
-                        epi_piece<false>(v, sbv, a, p.relu);
+                        epi_piece<false>(v, sbv, a, pr.relu);
                 }
-                emit_box<K::kBoxes>(p, &tmap_c, boxes, v, row0, col0, lane, nstored);
+                emit_box<K::kBoxes>(pr, &maps.c[pi], boxes, v, row0, col0, lane, nstored);
             }
         }
-        if (p.tma_store && lane == 0) bulk_wait0();
+        if (lane == 0) bulk_wait0();
         __syncwarp();
     }
 
@@ -634,9 +666,8 @@ bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, size_t esz, const void
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool PAIR>
-cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tc, const __half *Bop,
-                      int64_t N, int64_t K, const Params &p0, cudaStream_t st) {
+template <int BN, bool PAIR, int NP>
+cudaError_t launch_bn(Maps<NP> &maps, Params<NP> &p, const GemmJob *jobs, cudaStream_t st) {
     using C = Cfg<BN, PAIR>;
     // per device: the shared-memory attribute, and how many CTAs (pairs)
     // can be resident at once -- a pair needs two free SMs of one GPC, so
@@ -661,7 +692,7 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tc, const __half
     cfg.attrs = attr;
     cfg.numAttrs = PAIR ? 2 : 1;
     if (!ready[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, PAIR>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, PAIR, NP>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)C::kSmemBytes);
         if (e != cudaSuccess) return e;
@@ -669,7 +700,7 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tc, const __half
         if (PAIR) {
             cfg.gridDim = dim3((unsigned)(2 * units), 1, 1);
             int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, PAIR>, &cfg) == cudaSuccess &&
+            if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, PAIR, NP>, &cfg) == cudaSuccess &&
                 n > 0 && n < units)
                 units = n;
             cudaGetLastError();
@@ -677,26 +708,33 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tc, const __half
         max_units[dev] = units;
         ready[dev] = true;
     }
-    CUtensorMap tb;
-    if (!make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, Bop, (uint64_t)K, (uint64_t)N,
-                      (uint64_t)operand_ld(K), kBK, C::kBRows))
-        return cudaErrorInvalidValue;
-    Params p = p0;
-    p.num_n = (int)((N + BN - 1) / BN);
-    p.num_mu = PAIR ? (p.num_m + 1) / 2 : p.num_m;
-    p.num_units = p.num_mu * p.num_n;
+    // per GEMM: B's tensor map (its box depends on the tile width) and the
+    // GEMM's tiles, numbered after the previous GEMMs' tiles
+    int units_total = 0;
+    for (int i = 0; i < p.nprob; ++i) {
+        const GemmJob &j = jobs[i];
+        if (!make_tmap_2d(&maps.b[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, j.Bop, (uint64_t)j.K,
+                          (uint64_t)j.N, (uint64_t)operand_ld(j.K), kBK, C::kBRows))
+            return cudaErrorInvalidValue;
+        Prob &q = p.prob[i];
+        q.num_n = (int)((j.N + BN - 1) / BN);
+        q.num_mu = PAIR ? (q.num_m + 1) / 2 : q.num_m;
+        q.unit0 = units_total;
+        units_total += q.num_mu * q.num_n;
+    }
+    p.num_units = units_total;
     const int units = p.num_units < max_units[dev] ? p.num_units : max_units[dev];
     cfg.gridDim = dim3((unsigned)(units * (PAIR ? 2 : 1)), 1, 1);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, PAIR>, ta, tb, tc, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, PAIR, NP>, maps, p);
     count_launches(1);
     return e;
 }
 
-template <int BN>
-cudaError_t launch_width(const CUtensorMap &ta, const CUtensorMap &tc, const __half *Bop,
-                         int64_t N, int64_t K, const Params &p, bool pair, cudaStream_t st) {
-    if (pair) return launch_bn<BN, true>(ta, tc, Bop, N, K, p, st);
-    return launch_bn<BN, false>(ta, tc, Bop, N, K, p, st);
+template <int BN, int NP>
+cudaError_t launch_width(Maps<NP> &maps, Params<NP> &p, const GemmJob *jobs, bool pair,
+                         cudaStream_t st) {
+    if (pair) return launch_bn<BN, true, NP>(maps, p, jobs, st);
+    return launch_bn<BN, false, NP>(maps, p, jobs, st);
 }
 
 }  // namespace
@@ -719,76 +757,118 @@ static int forced_tile_width() {
     return (v == 64 || v == 128 || v == 192 || v == 256) ? v : 0;
 }
 
-// Tile width for an M x N problem on `sms` SMs: the one with the least
-// estimated time, rounds of tiles times the cost of one tile.  Tiles are
-// 256 rows on CTA pairs (sms / 2 of them) when M > 128, else 128 rows on
-// single CTAs.  A tile of width BN costs BN/256 of a 256-wide one, times a
-// penalty for the narrower MMAs (which read more shared memory per
-// multiply-add) and for the fixed per-tile epilogue work.
-int gemm_tile_width(int64_t M, int64_t N, int sms) {
+// Tile width for a launch of n GEMMs (M[i] x N[i]) on `sms` SMs: the one
+// with the least estimated time, rounds of tiles (all GEMMs together) times
+// the cost of one tile.  Tiles are 256 rows on CTA pairs (sms / 2 of them)
+// when some M > 128, else 128 rows on single CTAs.  A tile of width BN costs
+// BN/256 of a 256-wide one, times a penalty for the narrower MMAs (which
+// read more shared memory per multiply-add) and for the fixed per-tile
+// epilogue work.
+int gemm_group_tile_width(const int64_t *M, const int64_t *N, int n, int sms) {
     const int widths[4] = {256, 192, 128, 64};
     const double penalty[4] = {1.0, 1.27, 1.65, 3.24};  // measured: 8192^3 at each width (pairs)
-    const int64_t num_m = (M + kBM - 1) / kBM;
-    const bool pair = num_m >= 2 && gemm_pairs_enabled();
-    const int64_t num_mu = pair ? (num_m + 1) / 2 : num_m;
+    int64_t max_m = 0;
+    for (int i = 0; i < n; ++i) max_m = M[i] > max_m ? M[i] : max_m;
+    const bool pair = (max_m + kBM - 1) / kBM >= 2 && gemm_pairs_enabled();
     const int64_t units = pair ? (sms / 2 > 0 ? sms / 2 : 1) : sms;
     int best = 256;
     double best_cost = 1e300;
-    for (int i = 0; i < 4; ++i) {
-        const int64_t tiles = num_mu * ((N + widths[i] - 1) / widths[i]);
+    for (int w = 0; w < 4; ++w) {
+        int64_t tiles = 0;
+        for (int i = 0; i < n; ++i) {
+            const int64_t num_m = (M[i] + kBM - 1) / kBM;
+            const int64_t num_mu = pair ? (num_m + 1) / 2 : num_m;
+            tiles += num_mu * ((N[i] + widths[w] - 1) / widths[w]);
+        }
         const int64_t rounds = (tiles + units - 1) / units;
-        const double cost = (double)rounds * widths[i] / 256.0 * penalty[i];
+        const double cost = (double)rounds * widths[w] / 256.0 * penalty[w];
         if (cost < best_cost * 0.999) {
             best_cost = cost;
-            best = widths[i];
+            best = widths[w];
         }
     }
     return best;
+}
+
+int gemm_tile_width(int64_t M, int64_t N, int sms) { return gemm_group_tile_width(&M, &N, 1, sms); }
+
+template <int NP>
+cudaError_t launch_group_np(const GemmJob *jobs, int n, int mode, int32_t *dstatus,
+                            unsigned int *ticket, cudaStream_t st, int tile_width) {
+    Maps<NP> maps;
+    memset(&maps, 0, sizeof(maps));
+    Params<NP> p;
+    memset(&p, 0, sizeof(p));
+    p.nprob = n;
+    p.mode = mode;
+    p.dstatus = dstatus;
+    p.ticket = ticket;
+    int64_t Ms[kMaxGroup], Ns[kMaxGroup];
+    int max_m = 0;
+    for (int i = 0; i < n; ++i) {
+        const GemmJob &j = jobs[i];
+        if (!make_tmap_2d(&maps.a[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, j.Aop, (uint64_t)j.K,
+                          (uint64_t)j.M, (uint64_t)operand_ld(j.K), kBK, kBM))
+            return cudaErrorInvalidValue;
+        const bool aligned =
+            ((j.ldo * 4) % 16 == 0) && (reinterpret_cast<uintptr_t>(j.out) % 16 == 0);
+        Prob &q = p.prob[i];
+        q.tma_store = aligned && make_tmap_2d(&maps.c[i],
+                                              mode == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                        : CU_TENSOR_MAP_DATA_TYPE_INT32,
+                                              4, j.out, (uint64_t)j.N, (uint64_t)j.M,
+                                              (uint64_t)j.ldo, 32, 32)
+                          ? 1
+                          : 0;
+        q.M = (int)j.M;
+        q.N = (int)j.N;
+        q.K = (int)j.K;
+        q.num_kb = (int)((j.K + kBK - 1) / kBK);
+        q.num_m = (int)((j.M + kBM - 1) / kBM);
+        q.sa = j.sa;
+        q.sb = j.sb;
+        q.out = j.out;
+        q.ldo = j.ldo;
+        q.relu = j.relu;
+        Ms[i] = j.M;
+        Ns[i] = j.N;
+        max_m = q.num_m > max_m ? q.num_m : max_m;
+    }
+    const bool pair = max_m >= 2 && gemm_pairs_enabled();
+    const int forced = forced_tile_width();
+    switch (forced ? forced
+                   : tile_width ? tile_width : gemm_group_tile_width(Ms, Ns, n, device_sm_count())) {
+        case 64: return launch_width<64, NP>(maps, p, jobs, pair, st);
+        case 128: return launch_width<128, NP>(maps, p, jobs, pair, st);
+        case 192: return launch_width<192, NP>(maps, p, jobs, pair, st);
+        default: return launch_width<256, NP>(maps, p, jobs, pair, st);
+    }
+}
+
+cudaError_t launch_gemm_tc_group(const GemmJob *jobs, int n, int mode, int32_t *dstatus,
+                                 unsigned int *ticket, cudaStream_t st, int tile_width) {
+    if (n < 1 || n > kMaxGroup) return cudaErrorInvalidValue;
+    // a single GEMM gets the kernel compiled for one
+    if (n == 1) return launch_group_np<1>(jobs, n, mode, dstatus, ticket, st, tile_width);
+    return launch_group_np<kMaxGroup>(jobs, n, mode, dstatus, ticket, st, tile_width);
 }
 
 cudaError_t launch_gemm_tc(const __half *Aop, const __half *Bop, int64_t M, int64_t N,
                            int64_t K, const float *sa, const float *sb, int relu, int mode,
                            void *out, int64_t ldo, int32_t *dstatus, unsigned int *ticket,
                            cudaStream_t st, int tile_width) {
-    CUtensorMap ta, tc;
-    if (!make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, Aop, (uint64_t)K, (uint64_t)M,
-                      (uint64_t)operand_ld(K), kBK, kBM))
-        return cudaErrorInvalidValue;
-    const bool aligned = ((ldo * 4) % 16 == 0) && (reinterpret_cast<uintptr_t>(out) % 16 == 0);
-    int tma_store = 0;
-    memset(&tc, 0, sizeof(tc));
-    if (aligned) {
-        tma_store = make_tmap_2d(&tc,
-                                 mode == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                           : CU_TENSOR_MAP_DATA_TYPE_INT32,
-                                 4, out, (uint64_t)N, (uint64_t)M, (uint64_t)ldo, 32, 32)
-                        ? 1
-                        : 0;
-    }
-    Params p;
-    memset(&p, 0, sizeof(p));
-    p.M = (int)M;
-    p.N = (int)N;
-    p.K = (int)K;
-    p.num_kb = (int)((K + kBK - 1) / kBK);
-    p.num_m = (int)((M + kBM - 1) / kBM);
-    p.sa = sa;
-    p.sb = sb;
-    p.out = out;
-    p.ldo = ldo;
-    p.mode = mode;
-    p.relu = relu;
-    p.tma_store = tma_store;
-    p.dstatus = dstatus;
-    p.ticket = ticket;
-    const bool pair = p.num_m >= 2 && gemm_pairs_enabled();
-    const int forced = forced_tile_width();
-    switch (forced ? forced : tile_width ? tile_width : gemm_tile_width(M, N, device_sm_count())) {
-        case 64: return launch_width<64>(ta, tc, Bop, N, K, p, pair, st);
-        case 128: return launch_width<128>(ta, tc, Bop, N, K, p, pair, st);
-        case 192: return launch_width<192>(ta, tc, Bop, N, K, p, pair, st);
-        default: return launch_width<256>(ta, tc, Bop, N, K, p, pair, st);
-    }
+    GemmJob j;
+    j.Aop = Aop;
+    j.Bop = Bop;
+    j.M = M;
+    j.N = N;
+    j.K = K;
+    j.sa = sa;
+    j.sb = sb;
+    j.relu = relu;
+    j.out = out;
+    j.ldo = ldo;
+    return launch_gemm_tc_group(&j, 1, mode, dstatus, ticket, st, tile_width);
 }
 
 }  // namespace bsg
