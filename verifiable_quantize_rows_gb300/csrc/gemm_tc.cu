@@ -189,20 +189,18 @@ __device__ __forceinline__ float epi_value_f(float s, float a, float b, int relu
 }
 
 // The epilogue of 32 consecutive sums of one row, in place.  F32: v holds
-// f32(S) bit patterns (+0 added to map -0 to +0); otherwise int32 S.
+// f32(S) bit patterns (+0 added to map -0 to +0); otherwise int32 S.  Lane j
+// holds the column scale of column j of the piece in `bl`; the scales reach
+// every lane by shuffles (they were loaded before the tile's sums were ready,
+// so no global-memory latency sits between the sums and the stores).
 template <bool F32>
-__device__ __forceinline__ void epi_piece(uint32_t (&v)[32], const float4 *sbv, float a,
-                                          int relu) {
+__device__ __forceinline__ void epi_piece(uint32_t (&v)[32], float bl, float a, int relu) {
 #pragma unroll
-    for (int j4 = 0; j4 < 8; ++j4) {
-        const float4 bb = __ldg(sbv + j4);
-        const float bj[4] = {bb.x, bb.y, bb.z, bb.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const uint32_t x = v[4 * j4 + u];
-            const float sv = F32 ? __fadd_rn(__uint_as_float(x), 0.0f) : __int2float_rn((int32_t)x);
-            v[4 * j4 + u] = __float_as_uint(epi_value_f(sv, a, bj[u], relu));
-        }
+    for (int j = 0; j < 32; ++j) {
+        const float bj = __shfl_sync(0xffffffffu, bl, j);
+        const uint32_t x = v[j];
+        const float sv = F32 ? __fadd_rn(__uint_as_float(x), 0.0f) : __int2float_rn((int32_t)x);
+        v[j] = __float_as_uint(epi_value_f(sv, a, bj, relu));
     }
 }
 
@@ -543,6 +541,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int pi = tile_coords(p, tile, mu, nb);
             const Prob &pr = p.prob[pi];
             const int num_chunks = (pr.num_kb + kChunkBlocks - 1) / kChunkBlocks;
+            const int mb = PAIR ? 2 * mu + rank : mu;
+            const bool rows_here = mb < pr.num_m;  // false: the odd CTA of a pair past the last m-block
+            const int row0 = mb * kBM + q * 32;
+            const int colh = nb * BN + h * K::kWarpCols;
+            // The scales of this warp's rows and columns, loaded now so that
+            // their latency overlaps the wait for the tile's sums (the scale
+            // arrays are padded past M and N, like the tiles).
+            float a = 0.0f;
+            float bl[K::kPieces];
+#pragma unroll
+            for (int piece = 0; piece < K::kPieces; ++piece) bl[piece] = 0.0f;
+            if (p.mode == 0 && rows_here) {
+                a = __ldg(pr.sa + row0 + lane);
+#pragma unroll
+                for (int piece = 0; piece < K::kPieces; ++piece)
+                    bl[piece] = __ldg(pr.sb + colh + piece * 32 + lane);
+            }
             // With a single chunk (K <= 1024) the fp32 accumulator already is
             // f32(S): S is an integer below 2^24 in magnitude, held exactly.
             // The f32 epilogue then needs no conversion (float->int and back
@@ -599,22 +614,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
 
             // ---- final epilogue of the tile from the sums
-            const int mb = PAIR ? 2 * mu + rank : mu;
-            if (mb >= pr.num_m) continue;  // the odd CTA of a pair past the last m-block
-            const int row0 = mb * kBM + q * 32;
-            const int colh = nb * BN + h * K::kWarpCols;
-            const float a = p.mode == 0 ? __ldg(pr.sa + row0 + lane) : 0.0f;
+            if (!rows_here) continue;
 #pragma unroll
             for (int piece = 0; piece < K::kPieces; ++piece) {
                 uint32_t(&v)[32] = *reinterpret_cast<uint32_t(*)[32]>(&acc[piece * 32]);
                 const int col0 = colh + piece * 32;
                 if (p.mode == 0) {
                     // in place: the sums become the output bits
-                    const float4 *sbv = reinterpret_cast<const float4 *>(pr.sb + col0);
                     if (f32_sums)
-                        epi_piece<true>(v, sbv, a, pr.relu);
+                        epi_piece<true>(v, bl[piece], a, pr.relu);
                     else
-                        epi_piece<false>(v, sbv, a, pr.relu);
+                        epi_piece<false>(v, bl[piece], a, pr.relu);
                 }
                 emit_box<K::kBoxes>(pr, &maps.c[pi], boxes, v, row0, col0, lane, nstored);
             }
