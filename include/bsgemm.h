@@ -305,6 +305,31 @@ bsg_status bsgemm_i8_host(const float *A_host, const float *B_host, int64_t M, i
                           int64_t K, int relu, float *C_host, void *workspace, size_t ws_bytes,
                           int32_t *dstatus_host, void *stream);
 
+/* Several independent units on host buffers in one call (at most
+ * BSG_MAX_HOST_BATCH): each item is the argument list of bsgemm_i8_host.
+ * The items' copies and kernels are pipelined across items: item i+1 uploads
+ * while item i computes and downloads, so both directions of the host link
+ * stay busy for the whole batch, where back-to-back bsgemm_i8_host calls
+ * drain the pipeline at every call.  Each C is bit for bit what
+ * bsgemm_i8_host gives it.  Items may share A or B, but no two items may
+ * overlap in workspace or in C (BSG_ERR_ARG); an item's A and B must not
+ * overlap another item's C.  Synchronizes `stream` before returning;
+ * *dstatus_host (may be NULL) receives the OR of every item's device status
+ * bits.  The pages run one unit at a time; this call has no counterpart
+ * there. */
+#define BSG_MAX_HOST_BATCH 16
+typedef struct {
+    const float *A_host;
+    const float *B_host;
+    int64_t M, N, K;
+    int relu;
+    float *C_host;
+    void *workspace;
+    size_t ws_bytes;
+} bsg_host_item;
+bsg_status bsgemm_i8_host_batch(const bsg_host_item *items, int n, int32_t *dstatus_host,
+                                void *stream);
+
 /* ---- the probe --------------------------------------------------------------------- */
 
 /* 32-byte hash of an M x N float matrix (leading dimension ldc >= N): the

@@ -139,3 +139,49 @@ def test_host_buffer_entry_point_chunked(orc, M, N, K):
         Cd = bsg.bsgemm_i8(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda())
         torch.cuda.synchronize()
         assert_bits_equal(C.numpy(), Cd.cpu().numpy(), "host vs device entry point")
+
+
+def test_host_batch_matches_the_oracle(orc):
+    """Several units in one pipelined host call: each C is the oracle's, the
+    items sharing one B and differing in shape, chunk count and ReLU."""
+    shapes = [(700, 130, 1100, True), (2600, 257, 768, False), (64, 33, 65, True),
+              (1300, 130, 1100, False)]
+    data = []
+    for i, (M, N, K, relu) in enumerate(shapes):
+        A = inputs.gpt2_activations(M, K, 60 + i).numpy()
+        B = inputs.gpt2_weights(K, N, 70 + i).numpy()
+        data.append((A, B, relu))
+    # items 0 and 3 share B (read-only inputs may be shared)
+    data[3] = (data[3][0], data[0][1], data[3][2])
+    items = [(torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory(), relu)
+             for A, B, relu in data]
+    outs, st = bsg.bsgemm_i8_host_batch(items)
+    assert st == 0
+    for i, ((A, B, relu), C) in enumerate(zip(data, outs)):
+        Co, _ = orc.bsgemm_i8(A, B, relu)
+        assert_bits_equal(C.numpy(), Co, f"batch item {i}")
+
+
+def test_host_batch_gpt2_linears_equal_device_entry_point():
+    """The three GPT-2-small linears at M = 8192 in one batch, as the
+    end-to-end measurement runs them: bit for bit the device entry point."""
+    items, dev_out = [], []
+    for name, M, N, K, relu, seed in inputs.GPT2_LINEARS:
+        A, B, _ = inputs.gpt2_linear_inputs(name)
+        items.append((A.pin_memory(), B.pin_memory(), relu))
+        dev_out.append(bsg.bsgemm_i8(A.cuda(), B.cuda(), relu=relu))
+    outs, st = bsg.bsgemm_i8_host_batch(items)
+    torch.cuda.synchronize()
+    assert st == 0
+    for (name, *_), C, Cd in zip(inputs.GPT2_LINEARS, outs, dev_out):
+        assert_bits_equal(C.numpy(), Cd.cpu().numpy(), f"batch {name}")
+
+
+def test_host_batch_reports_nonfinite_input():
+    A0 = inputs.normal((300, 200), 1.0, 1)
+    A1 = inputs.normal((300, 200), 1.0, 2)
+    A1[7, 9] = float("inf")
+    B = inputs.normal((200, 100), 1.0, 3)
+    items = [(A0.pin_memory(), B.pin_memory(), False), (A1.pin_memory(), B.pin_memory(), False)]
+    outs, st = bsg.bsgemm_i8_host_batch(items)
+    assert st == bsg.DSTATUS_NONFINITE

@@ -18,7 +18,7 @@ def lib():
 def test_header_declares_the_boundary():
     names = bsg.exported_symbols()
     for required in ("bsg_quantize_rows", "bsg_quantize_cols", "bsg_gemm_s32", "bsg_epilogue",
-                     "bsgemm_i8", "bsgemm_i8_ex", "bsgemm_i8_host", "bsg_hash_f32",
+                     "bsgemm_i8", "bsgemm_i8_ex", "bsgemm_i8_host", "bsgemm_i8_host_batch", "bsg_hash_f32",
                      "bsg_probe_hash", "bsg_probe_hash_async", "bsg_status_str", "bsg_audit",
                      "bsg_selftest"):
         assert required in names
@@ -81,6 +81,26 @@ def test_argument_errors_without_gpu(lib):
     items = (bsg.GemmItem * 4)()
     assert lib.bsgemm_i8_group(items, 4, None, None) == 1
     assert lib.bsgemm_i8_group(items, 0, None, None) == 1
+    # host batch: no items, too many, a null buffer, shared workspace or C,
+    # a too-small workspace
+    assert lib.bsgemm_i8_host_batch(None, 1, None, None) == 1
+    hitems = (bsg.HostItem * 17)()
+    assert lib.bsgemm_i8_host_batch(hitems, 0, None, None) == 1
+    assert lib.bsgemm_i8_host_batch(hitems, 17, None, None) == 1
+    big = 1 << 30
+    for i in range(2):
+        hitems[i] = bsg.HostItem(256, 256, 4, 4, 4, 0, 4096 + 1024 * i, (1 << 20) + i * big, big)
+    hitems[1].workspace = (1 << 20) + big - 256          # overlaps item 0's workspace
+    assert lib.bsgemm_i8_host_batch(hitems, 2, None, None) == 1
+    hitems[1].workspace = (1 << 20) + big
+    hitems[1].C_host = 4096 + 32                            # overlaps item 0's C (64 bytes)
+    assert lib.bsgemm_i8_host_batch(hitems, 2, None, None) == 1
+    hitems[1].C_host = 4096 + 64
+    hitems[1].A_host = None
+    assert lib.bsgemm_i8_host_batch(hitems, 2, None, None) == 1
+    hitems[1].A_host = 256
+    hitems[1].ws_bytes = 64
+    assert lib.bsgemm_i8_host_batch(hitems, 2, None, None) == 3
     # self-test: missing or small workspace
     assert lib.bsg_selftest(None, 0, None, None) == 3
     assert lib.bsg_selftest(dummy, 16, None, None) == 3

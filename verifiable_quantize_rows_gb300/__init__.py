@@ -55,6 +55,14 @@ class GemmItem(ctypes.Structure):
                 ("workspace", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t)]
 
 
+class HostItem(ctypes.Structure):
+    """One item of bsgemm_i8_host_batch (the C struct bsg_host_item)."""
+    _fields_ = [("A_host", ctypes.c_void_p), ("B_host", ctypes.c_void_p),
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("relu", ctypes.c_int), ("C_host", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t)]
+
+
 def _declare(lib):
     sigs = {
         "bsg_status_str": ([_i32], ctypes.c_char_p),
@@ -79,6 +87,7 @@ def _declare(lib):
         "bsg_selftest_scales": ([ctypes.c_uint32, ctypes.c_uint32, _vp], _i32),
         "bsgemm_i8_host_workspace_size": ([_i64, _i64, _i64], _sz),
         "bsgemm_i8_host": ([_vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _sz, _vp, _vp], _i32),
+        "bsgemm_i8_host_batch": ([ctypes.POINTER(HostItem), _i32, _vp, _vp], _i32),
         "bsg_hash_f32_workspace_size": ([_i64, _i64], _sz),
         "bsg_hash_f32": ([_vp, _i64, _i64, _i64, _vp, _vp, _sz, _vp], _i32),
         "bsg_probe_workspace_size": ([_i64, _i64, _i64], _sz),
@@ -347,6 +356,44 @@ def bsgemm_i8_host(A, B, relu: bool = False, out=None, stream=None, workspace=No
     _check(lib.bsgemm_i8_host(_ptr(A), _ptr(B), M, N, K, int(bool(relu)), _ptr(C), wp, wn,
                               ctypes.byref(st), _stream_ptr(stream)), "bsgemm_i8_host")
     return C, st.value
+
+
+def bsgemm_i8_host_batch(items, stream=None, workspace=None):
+    """Several independent units on HOST float32 tensors in one pipelined
+    call.  `items`: tuples (A, B, relu) or (A, B, relu, out) of contiguous
+    host tensors (pinned for asynchronous copies).  Returns (list of C on the
+    host, OR of the device status bits).  Synchronizes the stream."""
+    torch = _torch()
+    lib = load()
+    n = len(items)
+    arr = (HostItem * n)()
+    dims, offs, outs = [], [], []
+    total = 0
+    for it in items:
+        A, B = it[0], it[1]
+        for name, t in (("A", A), ("B", B)):
+            if t.dtype != torch.float32 or t.is_cuda or t.dim() != 2 or not t.is_contiguous():
+                raise TypeError(f"{name} must be a contiguous 2-D float32 host tensor")
+        M, K = A.shape
+        K2, N = B.shape
+        if K != K2:
+            raise ValueError("inner dimensions differ")
+        dims.append((M, N, K))
+        offs.append(total)
+        total += (lib.bsgemm_i8_host_workspace_size(M, N, K) + 255) // 256 * 256
+    # one device workspace carved into the items' parts, kept beyond the call
+    wp, wn = _ws(workspace, total)
+    base = wp.value
+    for i, (it, (M, N, K)) in enumerate(zip(items, dims)):
+        C = it[3] if len(it) > 3 and it[3] is not None else torch.empty(
+            (M, N), dtype=torch.float32, pin_memory=True)
+        outs.append(C)
+        arr[i] = HostItem(it[0].data_ptr(), it[1].data_ptr(), M, N, K, int(bool(it[2])),
+                          C.data_ptr(), base + offs[i], lib.bsgemm_i8_host_workspace_size(M, N, K))
+    st = ctypes.c_int32(0)
+    _check(lib.bsgemm_i8_host_batch(arr, n, ctypes.byref(st), _stream_ptr(stream)),
+           "bsgemm_i8_host_batch")
+    return outs, st.value
 
 
 def hash_f32(C, stream=None, workspace=None) -> bytes:

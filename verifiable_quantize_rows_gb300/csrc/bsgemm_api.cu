@@ -491,31 +491,34 @@ HostPipe *host_pipe() {
     return h.in ? &h : nullptr;
 }
 
-}  // namespace
-}  // namespace bsg
+bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return na && nb && pa < pb + nb && pb < pa + na;
+}
 
-extern "C" {
+// Byte offset of the status word inside a host-entry workspace.
+size_t host_status_offset(int64_t M, int64_t N, int64_t K) {
+    return align256((size_t)M * K * 4) + align256((size_t)K * N * 4) + align256((size_t)M * N * 4);
+}
 
-bsg_status bsgemm_i8_host(const float *A_host, const float *B_host, int64_t M, int64_t N,
-                          int64_t K, int relu, float *C_host, void *workspace, size_t ws_bytes,
-                          int32_t *dstatus_host, void *stream) {
-    if (!A_host || !B_host || !C_host || !dims_ok(M, N, K)) return BSG_ERR_ARG;
-    if (K > BSG_MAX_K) return BSG_ERR_K_TOO_LARGE;
-    if (!ws_ok(workspace, ws_bytes, bsgemm_i8_host_workspace_size(M, N, K)))
-        return BSG_ERR_WORKSPACE;
-    bsg_status s = check_device();
-    if (s != BSG_OK) return s;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+// One unit on host buffers, enqueued: B and then A in row chunks upload on
+// h->in; on `st`, B is quantized per column once, then per chunk the rows of
+// A and the GEMM of those rows; each chunk of C downloads on h->out as soon
+// as its GEMM is done.  A chunk is a multiple of 256 rows (the GEMM's pair
+// tile).  Per-row quantize and the GEMM's tiling do not depend on the
+// chunking, so neither does any bit of C.  The events of `h` are re-recorded
+// per item; every wait is enqueued right after the record it pairs with.
+cudaError_t host_enqueue(const bsg_host_item &it, int32_t *dstat, cudaStream_t st, HostPipe *h) {
+    const int64_t M = it.M, N = it.N, K = it.K;
     size_t off = 0;
-    float *dA = at<float>(workspace, off);
+    float *dA = at<float>(it.workspace, off);
     off += align256((size_t)M * K * 4);
-    float *dB = at<float>(workspace, off);
+    float *dB = at<float>(it.workspace, off);
     off += align256((size_t)K * N * 4);
-    float *dC = at<float>(workspace, off);
+    float *dC = at<float>(it.workspace, off);
     off += align256((size_t)M * N * 4);
-    int32_t *dstat = at<int32_t>(workspace, off);
-    off += 256;
-    void *uws = at<void>(workspace, off);
+    off += 256;  // the status word
+    void *uws = at<void>(it.workspace, off);
     const UnitLayout L = unit_layout(M, N, K, 0, 0);
     const int64_t ldk = operand_ld(K);
     __half *aop = at<__half>(uws, L.aop);
@@ -524,52 +527,94 @@ bsg_status bsgemm_i8_host(const float *A_host, const float *B_host, int64_t M, i
     float *sb = at<float>(uws, L.sb);
     unsigned int *ticket = at<unsigned int>(uws, L.ticket);
     uint32_t *part_b = at<uint32_t>(uws, L.part_b);
+    int64_t rows = (M + kHostChunks - 1) / kHostChunks;
+    rows = (rows + 255) / 256 * 256;
+    const int nchunks = (int)((M + rows - 1) / rows);
+    cudaError_t e;
+#define BSG_TRY(x)                         \
+    if ((e = (x)) != cudaSuccess) return e;
+    BSG_TRY(cudaMemcpyAsync(dB, it.B_host, (size_t)K * N * 4, cudaMemcpyHostToDevice, h->in));
+    BSG_TRY(cudaEventRecord(h->b_in, h->in));
+    for (int c = 0; c < nchunks; ++c) {
+        const int64_t r0 = c * rows, mc = M - r0 < rows ? M - r0 : rows;
+        BSG_TRY(cudaMemcpyAsync(dA + r0 * K, it.A_host + r0 * K, (size_t)(mc * K) * 4,
+                                cudaMemcpyHostToDevice, h->in));
+        BSG_TRY(cudaEventRecord(h->a_in[c], h->in));
+    }
+    BSG_TRY(cudaStreamWaitEvent(st, h->b_in, 0));
+    BSG_TRY(launch_quantize_cols(dB, K, N, N, kOutHalfKMajor, bop, ldk, sb, nullptr, part_b, dstat,
+                                 st));
+    for (int c = 0; c < nchunks; ++c) {
+        const int64_t r0 = c * rows, mc = M - r0 < rows ? M - r0 : rows;
+        BSG_TRY(cudaStreamWaitEvent(st, h->a_in[c], 0));
+        BSG_TRY(launch_quantize_rows(dA + r0 * K, mc, K, K, kOutHalfKMajor, aop + r0 * ldk, ldk,
+                                     sa + r0, nullptr, dstat, st, ticket));
+        BSG_TRY(launch_gemm_tc(aop + r0 * ldk, bop, mc, N, K, sa + r0, sb, it.relu, 0, dC + r0 * N,
+                               N, dstat, ticket, st));
+        BSG_TRY(cudaEventRecord(h->c_ready[c], st));
+        BSG_TRY(cudaStreamWaitEvent(h->out, h->c_ready[c], 0));
+        BSG_TRY(cudaMemcpyAsync(it.C_host + r0 * N, dC + r0 * N, (size_t)(mc * N) * 4,
+                                cudaMemcpyDeviceToHost, h->out));
+    }
+#undef BSG_TRY
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace bsg
+
+extern "C" {
+
+bsg_status bsgemm_i8_host(const float *A_host, const float *B_host, int64_t M, int64_t N,
+                          int64_t K, int relu, float *C_host, void *workspace, size_t ws_bytes,
+                          int32_t *dstatus_host, void *stream) {
+    const bsg_host_item item = {A_host, B_host, M, N, K, relu, C_host, workspace, ws_bytes};
+    return bsgemm_i8_host_batch(&item, 1, dstatus_host, stream);
+}
+
+bsg_status bsgemm_i8_host_batch(const bsg_host_item *items, int n, int32_t *dstatus_host,
+                                void *stream) {
+    if (!items || n < 1 || n > BSG_MAX_HOST_BATCH) return BSG_ERR_ARG;
+    for (int i = 0; i < n; ++i) {
+        const bsg_host_item &it = items[i];
+        if (!it.A_host || !it.B_host || !it.C_host || !dims_ok(it.M, it.N, it.K))
+            return BSG_ERR_ARG;
+        if (it.K > BSG_MAX_K) return BSG_ERR_K_TOO_LARGE;
+    }
+    // no two items may share device workspace or C (their copies and kernels
+    // are in flight together)
+    for (int i = 0; i < n; ++i)
+        for (int j = 0; j < i; ++j) {
+            const bsg_host_item &a = items[i], &b = items[j];
+            if (ranges_overlap(a.workspace, a.ws_bytes, b.workspace, b.ws_bytes) ||
+                ranges_overlap(a.C_host, (size_t)(a.M * a.N) * 4, b.C_host,
+                               (size_t)(b.M * b.N) * 4))
+                return BSG_ERR_ARG;
+        }
+    for (int i = 0; i < n; ++i)
+        if (!ws_ok(items[i].workspace, items[i].ws_bytes,
+                   bsgemm_i8_host_workspace_size(items[i].M, items[i].N, items[i].K)))
+            return BSG_ERR_WORKSPACE;
+    bsg_status s = check_device();
+    if (s != BSG_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    // every item's kernels report into the first item's status word
+    int32_t *dstat = at<int32_t>(items[0].workspace, host_status_offset(items[0].M, items[0].N,
+                                                                         items[0].K));
 
     std::lock_guard<std::mutex> guard(g_host_lock);
     HostPipe *h = host_pipe();
     if (!h) return BSG_ERR_CUDA;
-    // A in row chunks of a multiple of 256 rows (the GEMM's pair tile): the
-    // upload of chunk c+1 and the download of chunk c-1 overlap the quantize
-    // and GEMM of chunk c.  Per-row quantize and the GEMM's tiling do not
-    // depend on the chunking, so neither does any bit of C.
-    int64_t rows = (M + kHostChunks - 1) / kHostChunks;
-    rows = (rows + 255) / 256 * 256;
-    const int nchunks = (int)((M + rows - 1) / rows);
-    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    // One fork for the whole batch: the copy streams start after the work
+    // already on `stream`, then run ahead of it -- item i+1 uploads while
+    // item i computes and downloads.
     if (!ok(cudaEventRecord(h->start, st)) || !ok(cudaStreamWaitEvent(h->in, h->start, 0)) ||
         !ok(cudaStreamWaitEvent(h->out, h->start, 0)) ||
         !ok(cudaMemsetAsync(dstat, 0, sizeof(int32_t), st)))
         return BSG_ERR_CUDA;
-    // uploads: B, then A chunk by chunk
-    if (!ok(cudaMemcpyAsync(dB, B_host, (size_t)K * N * 4, cudaMemcpyHostToDevice, h->in)) ||
-        !ok(cudaEventRecord(h->b_in, h->in)))
-        return BSG_ERR_CUDA;
-    for (int c = 0; c < nchunks; ++c) {
-        const int64_t r0 = c * rows, mc = M - r0 < rows ? M - r0 : rows;
-        if (!ok(cudaMemcpyAsync(dA + r0 * K, A_host + r0 * K, (size_t)(mc * K) * 4,
-                                cudaMemcpyHostToDevice, h->in)) ||
-            !ok(cudaEventRecord(h->a_in[c], h->in)))
-            return BSG_ERR_CUDA;
-    }
-    // kernels on the caller's stream: B per column once, then per chunk the
-    // rows of A and the GEMM of those rows; downloads follow each chunk
-    if (!ok(cudaStreamWaitEvent(st, h->b_in, 0)) ||
-        !ok(launch_quantize_cols(dB, K, N, N, kOutHalfKMajor, bop, ldk, sb, nullptr, part_b, dstat,
-                                 st)))
-        return BSG_ERR_CUDA;
-    for (int c = 0; c < nchunks; ++c) {
-        const int64_t r0 = c * rows, mc = M - r0 < rows ? M - r0 : rows;
-        if (!ok(cudaStreamWaitEvent(st, h->a_in[c], 0)) ||
-            !ok(launch_quantize_rows(dA + r0 * K, mc, K, K, kOutHalfKMajor, aop + r0 * ldk, ldk,
-                                     sa + r0, nullptr, dstat, st, ticket)) ||
-            !ok(launch_gemm_tc(aop + r0 * ldk, bop, mc, N, K, sa + r0, sb, relu, 0, dC + r0 * N, N,
-                               dstat, ticket, st)) ||
-            !ok(cudaEventRecord(h->c_ready[c], st)) ||
-            !ok(cudaStreamWaitEvent(h->out, h->c_ready[c], 0)) ||
-            !ok(cudaMemcpyAsync(C_host + r0 * N, dC + r0 * N, (size_t)(mc * N) * 4,
-                                cudaMemcpyDeviceToHost, h->out)))
-            return BSG_ERR_CUDA;
-    }
+    for (int i = 0; i < n; ++i)
+        if (!ok(host_enqueue(items[i], dstat, st, h))) return BSG_ERR_CUDA;
     int32_t hstat = 0;
     if (!ok(cudaMemcpyAsync(&hstat, dstat, sizeof(int32_t), cudaMemcpyDeviceToHost, h->out)) ||
         !ok(cudaEventRecord(h->done, h->out)) || !ok(cudaStreamWaitEvent(st, h->done, 0)) ||
