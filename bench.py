@@ -24,6 +24,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -476,43 +478,67 @@ def run_gpu(args, rank, world, local_rank):
 
 
 # -------------------------------------------------------------- CPU oracle
-def oracle_sample_step(orc, rows):
-    """The oracle on the step's workload with each linear cut to `rows`
-    rows of A (the probe at full size); returns (ops, seconds)."""
+def oracle_inputs():
+    """The step's inputs for the oracle, generated once (the same seeded
+    tensors the GPU arm uses)."""
     from verifiable_quantize_rows_gb300 import inputs
-    ops = 0
-    t = 0.0
+    out = []
     for name, M, N, K, relu, seed in inputs.GPT2_LINEARS:
         A, B, _ = inputs.gpt2_linear_inputs(name)
-        a = A[:rows].numpy()
-        b = B.numpy()
+        out.append((A.numpy(), B.numpy(), relu))
+    return out
+
+
+PARTS = ("qkv", "fc", "proj", "probe")
+
+
+def oracle_part(orc, data, part, rows):
+    """Part `part` of the step on the oracle: a GPT-2 linear on the first
+    `rows` rows of its A (full N, K), or (part 3) the probe with M = `rows`
+    (N = K = 1024, hash included).  Returns (ops, seconds)."""
+    if part < 3:
+        A, B, relu = data[part]
+        a = np.ascontiguousarray(A[:rows])
         t0 = time.perf_counter()
-        orc.bsgemm_i8(a, b, relu)
-        t += time.perf_counter() - t0
-        ops += 2 * a.shape[0] * N * K
+        orc.bsgemm_i8(a, B, relu)
+        return 2 * a.shape[0] * B.shape[1] * B.shape[0], time.perf_counter() - t0
     t0 = time.perf_counter()
-    orc.probe_hash(PROBE_SEED, *PROBE)
-    t += time.perf_counter() - t0
-    ops += 2 * PROBE[0] * PROBE[1] * PROBE[2]
-    return ops, t
+    orc.probe_hash(PROBE_SEED, rows, PROBE[1], PROBE[2])
+    return 2 * rows * PROBE[1] * PROBE[2], time.perf_counter() - t0
+
+
+def sample_rows(orc, data, seconds):
+    """Rows per part for about `seconds` of oracle work each, scaled from a
+    256-row calibration run of every part."""
+    rows = []
+    for part in range(len(PARTS)):
+        _, t = oracle_part(orc, data, part, 256)
+        cap = 8192 if part < 3 else PROBE[0]
+        rows.append(max(8, int(min(cap, max(8, 256 * seconds / max(t, 1e-3)))) // 8 * 8))
+    return rows
+
+
+def sample_text(rows):
+    return (f"qkv, fc, proj on their first {rows[0]}, {rows[1]}, {rows[2]} of 8192 rows "
+            f"(full N, K) and the probe at M = {rows[3]} of 1024 (N = K = 1024, hash included)")
 
 
 def cpu_baseline(budget_s=12.0):
     import oracle
     orc = oracle.load()
-    ops, t = oracle_sample_step(orc, 256)
-    rows = int(min(8192, max(256, 256 * budget_s / max(t, 1e-3))))
-    rows = max(256, (rows // 256) * 256)
-    # repeat the sample until about budget_s of CPU work (when even the whole
-    # workload takes less)
+    data = oracle_inputs()
+    rows = sample_rows(orc, data, budget_s / len(PARTS))
+    # repeat the four parts until about budget_s of CPU work (when even the
+    # whole workload takes less)
     total_ops, total_t, reps = 0, 0.0, 0
     while total_t < 0.8 * budget_s or reps == 0:
-        ops, t = oracle_sample_step(orc, rows)
-        total_ops, total_t, reps = total_ops + ops, total_t + t, reps + 1
+        for part in range(len(PARTS)):
+            ops, t = oracle_part(orc, data, part, rows[part])
+            total_ops, total_t = total_ops + ops, total_t + t
+        reps += 1
     return {"value": round(total_ops / total_t / 1e12, 6), "unit": "TOPS",
             "cores": orc.num_threads(), "kind": "oracle",
-            "sample": f"each GPT-2 linear on its first {rows} of 8192 rows (full N, K) plus the "
-                      f"full 1024^3 probe, {reps}x: {total_ops / 1e9:.1f} G ops in "
+            "sample": f"{sample_text(rows)}, {reps}x: {total_ops / 1e9:.1f} G ops in "
                       f"{total_t:.1f} s"}
 
 
@@ -521,21 +547,23 @@ def run_reference(args, rank, world):
         return None
     import oracle
     orc = oracle.load()
-    _, t = oracle_sample_step(orc, 256)
-    total_budget = 150.0
-    per_step = max(1.0, min(10.0, total_budget / max(1, args.steps + args.warmup)))
-    rows = int(min(8192, max(256, 256 * per_step / max(t, 1e-3))))
-    rows = max(256, (rows // 256) * 256)
-    for _ in range(args.warmup):
-        oracle_sample_step(orc, rows)
-    times, ops = [], 0
-    for _ in range(args.steps):
-        ops, t = oracle_sample_step(orc, rows)
-        times.append(t)
-    ms = statistics.mean(times) * 1e3
-    value = ops / (ms * 1e-3) / 1e12
-    sample = (f"each GPT-2 linear on its first {rows} of 8192 rows (full N, K) plus the full "
-              f"1024^3 probe, {ops / 1e9:.1f} G ops per step")
+    data = oracle_inputs()
+    # About two minutes of oracle work for the whole run, whatever K and W
+    # are: step i runs part i mod 4 of the workload (qkv, fc, proj, probe),
+    # each on a row sample sized to the per-step budget.
+    total_budget = 120.0
+    per_step = min(10.0, total_budget / max(1, args.steps + args.warmup))
+    rows = sample_rows(orc, data, per_step)
+    for i in range(args.warmup):
+        oracle_part(orc, data, i % len(PARTS), rows[i % len(PARTS)])
+    total_ops, total_t = 0, 0.0
+    for i in range(args.steps):
+        ops, t = oracle_part(orc, data, i % len(PARTS), rows[i % len(PARTS)])
+        total_ops, total_t = total_ops + ops, total_t + t
+    value = total_ops / total_t / 1e12
+    ms = total_t / max(1, args.steps) * 1e3
+    sample = (f"step i runs part i mod 4 of the step: {sample_text(rows)}; "
+              f"{total_ops / 1e9:.2f} G ops in {total_t:.1f} s over {args.steps} steps")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TOPS",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
