@@ -477,6 +477,100 @@ def run_gpu(args, rank, world, local_rank):
     return line
 
 
+# -------------------------------------------------------------- config sweep
+def run_configs(args):
+    """Device time of the unit on every workload of the measurement plan
+    (inputs resident in HBM, L2 flushed between timed replays): one JSON line
+    per workload.  Each timing is a graph of R back-to-back calls, replayed
+    10 times; the median replay / R is reported."""
+    import torch
+    import verifiable_quantize_rows_gb300 as bsg
+    from verifiable_quantize_rows_gb300 import inputs
+    dev = torch.device("cuda", 0)
+    peaks, _ = load_peaks()
+    tc_peak = float(peaks.get("bf16_tflops", 1900.0))
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    dstatus = torch.zeros(1, dtype=torch.int32, device=dev)
+    capture = torch.cuda.Stream(device=dev)
+
+    def timed(fn, target_us=400.0):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(); fn(); e1.record(); torch.cuda.synchronize()
+        R = int(max(1, min(8, target_us // max(e0.elapsed_time(e1) * 1e3, 1.0))))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=capture):
+            for _ in range(R):
+                fn()
+        g.replay()
+        ts = []
+        for _ in range(10):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(); g.replay(); b.record(); torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3 / R)
+        return statistics.median(ts)
+
+    def unit_line(name, A, B, relu=False):
+        M, K = A.shape
+        N = B.shape[1]
+        ws = bsg.Workspace(dev)
+        ws.get(bsg.workspace_size(M, N, K))
+        C = torch.empty(M, N, device=dev)
+        q_us = timed(lambda: bsg.bsgemm_i8_quantize(A, B, ws, dstatus=dstatus))
+        g_us = timed(lambda: bsg.bsgemm_i8_contract(M, N, K, C, ws, relu=relu, dstatus=dstatus))
+        u_us = timed(lambda: bsg.bsgemm_i8(A, B, relu=relu, out=C, dstatus=dstatus, workspace=ws))
+        ops = 2 * M * N * K
+        qbytes = 6 * (M * K + K * N)
+        return {"config": name, "M": M, "N": N, "K": K, "relu": relu,
+                "unit_us": round(u_us, 2), "unit_tops": round(ops / u_us / 1e6, 1),
+                "gemm_us": round(g_us, 2), "gemm_tflops": round(ops / g_us / 1e6, 1),
+                "gemm_frac_of_measured_bf16": round(ops / g_us / 1e6 / tc_peak, 3),
+                "quantize_us": round(q_us, 2), "quantize_gbs": round(qbytes / q_us / 1e3, 1),
+                "quantize_frac_of_measured_hbm": round(qbytes / q_us / 1e3 / hbm_peak, 3)}
+
+    lines = []
+    lines.append(unit_line("c0 256^3", inputs.normal((256, 256), 1.0, 0).to(dev),
+                           inputs.normal((256, 256), 1.0, 1).to(dev)))
+    for name, M, N, K, relu, seed in inputs.GPT2_LINEARS:
+        A, B, _ = inputs.gpt2_linear_inputs(name)
+        lines.append(unit_line("c1 " + name, A.to(dev), B.to(dev), relu))
+    lines.append(unit_line("c2 lm head", inputs.gpt2_activations(8192, 768, 4).to(dev),
+                           inputs.gpt2_weights(768, 50304, 4).to(dev)))
+    pws = bsg.Workspace(dev)
+    pws.get(bsg.load().bsg_probe_workspace_size(*PROBE))
+    pout = torch.empty(32, dtype=torch.uint8, device=dev)
+    p_us = timed(lambda: bsg.probe_hash_async(PROBE_SEED, *PROBE, out=pout, dstatus=dstatus,
+                                              workspace=pws))
+    lines.append({"config": "c2 probe 1024^3 (fill, unit, hash)", "unit_us": round(p_us, 2),
+                  "unit_tops": round(2 * 1024 ** 3 / p_us / 1e6, 1)})
+    X, W, dY = (t.to(dev) for t in inputs.train_trio())
+    trio = [(X, W, False, False, False), (dY, W, False, True, False), (X, dY, True, False, False)]
+    gws = bsg.Workspace(dev)
+    g_us = timed(lambda: bsg.bsgemm_i8_group(trio, dstatus=dstatus, workspace=gws))
+    s_us = timed(lambda: [bsg.bsgemm_i8_ex(A, B, transA=tA, transB=tB, relu=r, dstatus=dstatus)
+                          for A, B, tA, tB, r in trio])
+    ops = 3 * 2 * 8192 * 3072 * 768
+    lines.append({"config": "c3 training trio 8192x3072x768", "grouped_us": round(g_us, 1),
+                  "grouped_tops": round(ops / g_us / 1e6, 1), "separate_us": round(s_us, 1),
+                  "separate_tops": round(ops / s_us / 1e6, 1)})
+    del X, W, dY, trio
+    for n in (4096, 8192, 16384):
+        lines.append(unit_line(f"c4 {n}^3", inputs.uniform((n, n), -1, 1, 7).to(dev),
+                               inputs.uniform((n, n), -1, 1, 8).to(dev)))
+        torch.cuda.empty_cache()
+    lines.append(unit_line("c4 ragged", inputs.uniform((4097, 8191), -1, 1, 9).to(dev),
+                           inputs.uniform((8191, 12289), -1, 1, 10).to(dev)))
+    lines.append(unit_line("c4 adversarial 4096^3", inputs.adversarial(4096, 4096, 11).to(dev),
+                           inputs.adversarial(4096, 4096, 12, along_rows=False).to(dev)))
+    torch.cuda.synchronize()
+    if int(dstatus.item()) & ~1:  # the adversarial mix sets the non-finite bit by design
+        raise RuntimeError(f"device status {int(dstatus.item())}")
+    return lines
+
+
 # -------------------------------------------------------------- CPU oracle
 def oracle_inputs():
     """The step's inputs for the oracle, generated once (the same seeded
@@ -585,6 +679,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--probe-overlap", type=int, default=1,
                     help="1: the probe runs on a side stream alongside the linears")
+    ap.add_argument("--configs", action="store_true",
+                    help="time the unit on every workload of the measurement plan instead "
+                         "(one JSON line each)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -592,6 +689,11 @@ def main():
     world = env_int("WORLD_SIZE", 1)
     rank = env_int("RANK", 0)
     local_rank = env_int("LOCAL_RANK", 0)
+
+    if args.configs:
+        for line in run_configs(args):
+            print(json.dumps(line), flush=True)
+        return
 
     if args.impl == "reference":
         line = run_reference(args, rank, world)

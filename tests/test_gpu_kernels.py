@@ -72,3 +72,30 @@ def test_switches_are_read_per_call(orc, monkeypatch):
         outs.append(host(bsg.bsgemm_i8(dev(A), dev(B))))
     torch.cuda.synchronize()
     assert_bits_equal(outs[0], outs[1], "256/pair vs 64/single")
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 300, 4097), (130, 129, 5000), (40, 257, 8191),
+                                   (33, 1000, 9000)], ids=lambda v: str(v))
+def test_long_columns_two_pass_operand(orc, M, N, K):
+    """Columns longer than the strip kernel's 4096 rows go through the
+    two-pass column quantize into the f16 operand (a transposing tile);
+    B's columns carry the adversarial kinds, K is odd or ragged."""
+    A = inputs.normal((M, K), 1.0, M + K).numpy()
+    B = inputs.adversarial(N, K, N + K, along_rows=False).numpy()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    C = bsg.bsgemm_i8(dev(A), dev(B), dstatus=st)
+    torch.cuda.synchronize()
+    Co, _ = orc.bsgemm_i8(A, B, False)
+    assert_bits_equal(host(C), Co, f"{M}x{N}x{K}")
+
+
+def test_long_columns_transposed_a(orc):
+    """op(A) = A^T of a stored K x M matrix with K > 4096: A's per-row
+    quantize of op(A) is a column quantize of the stored matrix."""
+    M, N, K = 200, 96, 6000
+    At = inputs.gpt2_activations(K, M, 17).numpy()     # stored K x M
+    B = inputs.gpt2_weights(K, N, 18).numpy()
+    C = bsg.bsgemm_i8_ex(dev(At), dev(B), transA=True)
+    torch.cuda.synchronize()
+    Co, _ = orc.bsgemm_i8(np.ascontiguousarray(At.T), B, False)
+    assert_bits_equal(host(C), Co, "transA K=6000")

@@ -653,6 +653,80 @@ __global__ void __launch_bounds__(256)
     griddep_launch_dependents();
 }
 
+// Column quantize, pass 2, into the GEMM's K-major f16 operand (Q[col][row]):
+// a tile of 64 rows x 128 columns.  Each thread quantizes 32 consecutive rows
+// of one column -- the lanes of a warp take consecutive columns, so each row
+// load is one 128-byte line -- and stores them as f16 pairs into a [128][66]
+// tile whose 33-word row stride puts the 32 lanes' stores in 32 distinct
+// banks.  Each warp then copies whole output rows (one column of X, 64
+// halves) from the tile to Q, 128 bytes per store.  Loads are scalar, so X
+// may have any alignment and stride.
+constexpr int kT16Cols = 128;
+constexpr int kT16Rows = 64;
+
+__global__ void __launch_bounds__(256)
+    quantize_cols_t16_kernel(const float *__restrict__ X, int64_t rows, int64_t cols, int64_t ldx,
+                             const uint32_t *__restrict__ partial, int nsplit,
+                             __half *__restrict__ Q, int64_t ldq, float *__restrict__ scale,
+                             float *__restrict__ inv, int32_t *__restrict__ dstatus) {
+    __shared__ float s_inv[kT16Cols];
+    __shared__ __align__(16) __half tile[kT16Cols][kT16Rows + 2];
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int64_t c0 = (int64_t)blockIdx.x * kT16Cols;
+    const int64_t r0 = (int64_t)blockIdx.y * kT16Rows;
+    if (t < kT16Cols) {
+        const int64_t col = c0 + t;
+        float iv = 0.f;
+        if (col < cols) {
+            uint32_t mm[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mm[u] = 0;
+            for (int s = 0; s < nsplit; s += 8) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (s + u < nsplit) mm[u] = max(mm[u], partial[(int64_t)(s + u) * cols + col]);
+            }
+            const uint32_t m = max(max(max(mm[0], mm[1]), max(mm[2], mm[3])),
+                                   max(max(mm[4], mm[5]), max(mm[6], mm[7])));
+            float sc;
+            scale_from_max(m, sc, iv);
+            if (blockIdx.y == 0) {
+                scale[col] = sc;
+                if (inv) inv[col] = iv;
+                if (m >= kNonfiniteBits && dstatus) atomicOr(dstatus, 1);
+            }
+        }
+        s_inv[t] = iv;
+    }
+    __syncthreads();
+    const int cj = 32 * (w & 3) + lane;  // tile column = output row of the tile
+    const int rh = 32 * (w >> 2);        // this thread's first row in the tile
+    const int64_t col = c0 + cj;
+    const float iv = s_inv[cj];
+    float x[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        const int64_t row = r0 + rh + k;
+        x[k] = (row < rows && col < cols) ? __ldg(X + row * ldx + col) : 0.f;
+    }
+#pragma unroll
+    for (int k2 = 0; k2 < 16; ++k2)
+        *reinterpret_cast<__half2 *>(&tile[cj][rh + 2 * k2]) =
+            __floats2half2_rn(quant(x[2 * k2], iv), quant(x[2 * k2 + 1], iv));
+    __syncthreads();
+    const int64_t nr = rows - r0 < kT16Rows ? rows - r0 : kT16Rows;  // valid halves per row
+    const int e = 2 * lane;
+    for (int j = w; j < kT16Cols; j += 8) {
+        const int64_t orow = c0 + j;
+        if (orow >= cols) break;
+        __half *dst = Q + orow * ldq + r0 + e;
+        if (e + 1 < nr)
+            *reinterpret_cast<__half2 *>(dst) = *reinterpret_cast<const __half2 *>(&tile[j][e]);
+        else if (e < nr)
+            dst[0] = tile[j][e];
+    }
+}
+
 __global__ void i8_rows_to_half_kernel(const int8_t *__restrict__ Q, int64_t rows, int64_t cols,
                                        int64_t ldq, __half *__restrict__ out, int64_t ldo) {
     const int64_t total = rows * cols;
@@ -987,7 +1061,10 @@ cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int
         count_launches(1);
         return e;
     }
-    if (cols_cluster_shape(rows, cols, cs, R)) {
+    // the GEMM's f16 operand beyond the strip kernel's rows: two passes, the
+    // second through the conflict-free transposing tile (one CTA per SM with
+    // ~200 KB of shared memory made the single-pass cluster kernel slower)
+    if (out_kind != kOutHalfKMajor && cols_cluster_shape(rows, cols, cs, R)) {
         cudaError_t e = out_kind == kOutInt8
                             ? launch_cols_cluster<kOutInt8>(X, rows, cols, ldx, cs, R, Q, ldq, scale,
                                                             inv, dstatus, st)
@@ -1004,6 +1081,20 @@ cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int
     const int vw = vec ? 4 : 1;
     const unsigned gx = (unsigned)((cols + 32 * vw - 1) / (32 * vw));
     dim3 g1(gx, (unsigned)nsplit), g2(gx, (unsigned)((rows + 63) / 64));
+    if (out_kind == kOutHalfKMajor) {
+        if (reinterpret_cast<uintptr_t>(Q) % 4 != 0 || ldq % 2 != 0) return cudaErrorInvalidValue;
+        if (vec)
+            colmax_partial_kernel<4><<<g1, 256, 0, st>>>(X, rows, cols, ldx, rps, partial);
+        else
+            colmax_partial_kernel<1><<<g1, 256, 0, st>>>(X, rows, cols, ldx, rps, partial);
+        const dim3 g3((unsigned)((cols + kT16Cols - 1) / kT16Cols),
+                      (unsigned)((rows + kT16Rows - 1) / kT16Rows));
+        quantize_cols_t16_kernel<<<g3, 256, 0, st>>>(X, rows, cols, ldx, partial, nsplit,
+                                                     static_cast<__half *>(Q), ldq, scale, inv,
+                                                     dstatus);
+        count_launches(2);
+        return cudaGetLastError();
+    }
     if (vec) {
         colmax_partial_kernel<4><<<g1, 256, 0, st>>>(X, rows, cols, ldx, rps, partial);
         if (out_kind == kOutInt8)
