@@ -132,7 +132,23 @@ __global__ void __launch_bounds__(kRowWarps * 32)
                 }
             }
         }
-        for (int64_t c = 4 * c4n + lane; c < cols; c += 32) m = max(m, absbits(__ldg(xr + c)));
+        int64_t c0 = 4 * c4n + lane;
+        if (!VEC) {
+            // unaligned rows: scalar loads, eight in flight per lane
+            uint32_t m1 = 0;
+            for (; c0 + 224 < cols; c0 += 256) {
+                float a[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) a[u] = __ldg(xr + c0 + 32 * u);
+#pragma unroll
+                for (int u = 0; u < 8; u += 2) {
+                    m = max(m, absbits(a[u]));
+                    m1 = max(m1, absbits(a[u + 1]));
+                }
+            }
+            m = max(m, m1);
+        }
+        for (int64_t c = c0; c < cols; c += 32) m = max(m, absbits(__ldg(xr + c)));
         m = __reduce_max_sync(0xffffffffu, m);
 
         float sc = 0.f, iv = 0.f;
@@ -162,7 +178,17 @@ __global__ void __launch_bounds__(kRowWarps * 32)
                 }
             }
         }
-        for (int64_t c = 4 * c4n + lane; c < cols; c += 32)
+        int64_t cq = 4 * c4n + lane;
+        if (!VEC) {
+            for (; cq + 224 < cols; cq += 256) {
+                float a[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) a[u] = __ldg(xr + cq + 32 * u);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) store1<OUT>(Q, qrow + cq + 32 * u, quant(a[u], iv));
+            }
+        }
+        for (int64_t c = cq; c < cols; c += 32)
             store1<OUT>(Q, qrow + c, quant(__ldg(xr + c), iv));
     }
 }
@@ -210,12 +236,13 @@ __global__ void __launch_bounds__(256)
                 m[VW > 3 ? 3 : 0] = max(m[VW > 3 ? 3 : 0], absbits(t.w));
             }
         } else {
-            for (; r + 3 * kColRows < r1; r += 4 * kColRows) {
-                float t[4];
+            // scalar columns: sixteen row loads in flight per thread
+            for (; r + 15 * kColRows < r1; r += 16 * kColRows) {
+                float t[16];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) t[u] = __ldg(X + (r + u * kColRows) * ldx + col);
+                for (int u = 0; u < 16; ++u) t[u] = __ldg(X + (r + u * kColRows) * ldx + col);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) m[0] = max(m[0], absbits(t[u]));
+                for (int u = 0; u < 16; ++u) m[0] = max(m[0], absbits(t[u]));
             }
             for (; r < r1; r += kColRows) m[0] = max(m[0], absbits(__ldg(X + r * ldx + col)));
         }
