@@ -28,7 +28,7 @@ def _matrix(kind, rows, cols, seed):
 
 SHAPES = [(1, 1), (3, 5), (17, 13), (64, 768), (129, 1000), (300, 1024), (37, 1025),
           (8, 3072), (5, 5003), (1000, 33), (9, 16384), (2, 20000), (8200, 40), (16, 252),
-          (2048, 96)]
+          (2048, 96), (5000, 257)]
 
 
 @pytest.mark.parametrize("kind", ["normal", "gpt2", "adversarial", "uniform"])

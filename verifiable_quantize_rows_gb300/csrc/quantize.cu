@@ -1088,10 +1088,13 @@ cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int
         count_launches(1);
         return e;
     }
-    // the GEMM's f16 operand beyond the strip kernel's rows: two passes, the
-    // second through the conflict-free transposing tile (one CTA per SM with
-    // ~200 KB of shared memory made the single-pass cluster kernel slower)
-    if (out_kind != kOutHalfKMajor && cols_cluster_shape(rows, cols, cs, R)) {
+    // Single pass in clusters only for columns of at most 3072 rows (int8 in
+    // X's layout): beyond, two passes measured faster (8192 rows 108 against
+    // 191 us, 4096 rows 30 against 35 us), the cluster kernel's CTAs holding
+    // up to ~200 KB of shared memory, one per SM.  The GEMM's f16 operand past
+    // the strip kernel's rows always takes two passes, the second through the
+    // conflict-free transposing tile.
+    if (out_kind != kOutHalfKMajor && rows <= 3072 && cols_cluster_shape(rows, cols, cs, R)) {
         cudaError_t e = out_kind == kOutInt8
                             ? launch_cols_cluster<kOutInt8>(X, rows, cols, ldx, cs, R, Q, ldq, scale,
                                                             inv, dstatus, st)
