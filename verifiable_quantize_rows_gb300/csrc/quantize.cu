@@ -731,10 +731,17 @@ __global__ void __launch_bounds__(256)
     const int64_t col = c0 + cj;
     const float iv = s_inv[cj];
     float x[32];
+    if (col < cols && r0 + rh + 32 <= rows) {
+        // the common case: 32 rows in range, the address stepped by ldx
+        const float *xp = X + (r0 + rh) * ldx + col;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-        const int64_t row = r0 + rh + k;
-        x[k] = (row < rows && col < cols) ? __ldg(X + row * ldx + col) : 0.f;
+        for (int k = 0; k < 32; ++k) x[k] = __ldg(xp + k * ldx);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const int64_t row = r0 + rh + k;
+            x[k] = (row < rows && col < cols) ? __ldg(X + row * ldx + col) : 0.f;
+        }
     }
 #pragma unroll
     for (int k2 = 0; k2 < 16; ++k2)
@@ -742,15 +749,14 @@ __global__ void __launch_bounds__(256)
             __floats2half2_rn(quant(x[2 * k2], iv), quant(x[2 * k2 + 1], iv));
     __syncthreads();
     const int64_t nr = rows - r0 < kT16Rows ? rows - r0 : kT16Rows;  // valid halves per row
+    const int jmax = cols - c0 < kT16Cols ? (int)(cols - c0) : kT16Cols;
     const int e = 2 * lane;
-    for (int j = w; j < kT16Cols; j += 8) {
-        const int64_t orow = c0 + j;
-        if (orow >= cols) break;
-        __half *dst = Q + orow * ldq + r0 + e;
-        if (e + 1 < nr)
+    __half *dst = Q + (c0 + w) * ldq + r0 + e;
+    if (e + 1 < nr) {
+        for (int j = w; j < jmax; j += 8, dst += 8 * ldq)
             *reinterpret_cast<__half2 *>(dst) = *reinterpret_cast<const __half2 *>(&tile[j][e]);
-        else if (e < nr)
-            dst[0] = tile[j][e];
+    } else if (e < nr) {
+        for (int j = w; j < jmax; j += 8, dst += 8 * ldq) dst[0] = tile[j][e];
     }
 }
 
