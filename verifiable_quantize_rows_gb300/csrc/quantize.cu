@@ -11,8 +11,12 @@
 // Memory plan: rows are read once with 128-bit loads (the row stays in
 // registers when it is short), absmax by a warp-shuffle max of |x| bit
 // patterns (non-negative floats order like their bits; Inf/NaN show up as
-// >= 0x7f800000).  Columns take a partial-max pass over row slices and a
-// quantize pass over 64 x 64 tiles that also transposes for the GEMM.
+// >= 0x7f800000).  Columns of up to 4096 rows are read once too: a strip of
+// 32 columns sits in the registers of a cluster of CTAs, which exchange
+// their partial maxima through distributed shared memory (fused with the
+// row quantize of A in one launch when K <= 2048).  Longer columns take a
+// partial-max pass over row slices, then a quantize pass whose tiles also
+// transpose B into the GEMM's K-major operand.
 #include <cooperative_groups.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
