@@ -24,13 +24,14 @@
 //     in and its tensor core reads two thirds of what a 128 x BN tile per SM
 //     needs for the same multiply-adds.  With one CTA per SM the 128 x 256
 //     tile was bound by shared-memory traffic (TMA writes plus MMA reads),
-//     not by the tensor pipe; the pair also frees shared memory for two
-//     output staging buffers per epilogue warp.
+//     not by the tensor pipe; the pair also frees shared memory for a deeper
+//     operand ring (6 stages at the widest tiles) beside the output staging.
 //   * single (M <= 128): one CTA computes a 128 x BN tile (cta_group::1).
 // BN in {64, 128, 192, 256} is chosen per problem so that the last wave of tiles
 // leaves few SMs idle; CTAs (pairs) are persistent, and after the first wave
 // they claim tiles dynamically, so that a CTA that starts late, its SM busy
-// with other work, takes fewer tiles instead of holding up the launch.
+// with other work, takes fewer tiles (only its first, static tile waits for
+// it).
 //
 // Roles (one CTA per SM):
 //   warp 0      TMA producer: A and B k-blocks (64 wide, 128-byte swizzle)
