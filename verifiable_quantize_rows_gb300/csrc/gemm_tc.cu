@@ -341,7 +341,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_cl(cluster_addr(&qempty[slot], 0));
                 else
                     mbar_arrive(&qempty[slot]);
-                if (tile < 0) break;  // no tiles left
+                if (tile < 0) {
+                    // no tiles left for this CTA: the next kernel may be placed
+                    // on SMs as the grid drains (it waits for this grid's
+                    // completion before it touches memory)
+                    griddep_launch_dependents();
+                    break;
+                }
                 int mu, nb;
                 const int pi = tile_coords(p, tile, mu, nb);
                 const CUtensorMap *tma = &maps.a[pi];

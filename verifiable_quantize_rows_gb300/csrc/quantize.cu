@@ -433,10 +433,12 @@ __global__ void __launch_bounds__(256)
                               float *__restrict__ scale, float *__restrict__ inv,
                               int32_t *__restrict__ dstatus, unsigned int *__restrict__ zero2) {
     griddep_wait();  // programmatic launch: the previous kernel is done from here on
+    // the next kernel may be placed on SMs as this one drains; it waits for
+    // this grid's completion before it touches memory
+    griddep_launch_dependents();
     if (zero2 && blockIdx.x == 0 && threadIdx.x == 0) zero2[0] = zero2[1] = 0u;
     rows_wide_block<OUT, WPR, RV>((int64_t)blockIdx.x, X, rows, cols, ldx, Q, ldq, scale, inv,
                                   dstatus);
-    griddep_launch_dependents();
 }
 
 // Columns, single pass: a cluster of CS CTAs shares a strip of 32 columns;
@@ -661,6 +663,7 @@ __global__ void __launch_bounds__(256)
                        __half *__restrict__ Bop, float *__restrict__ sb, int64_t ldk, int R,
                        int strips, int32_t *__restrict__ dstatus, unsigned int *__restrict__ zero2) {
     griddep_wait();  // programmatic launch: the previous kernel is done from here on
+    griddep_launch_dependents();  // see quantize_rows_wide_kernel
     if (zero2 && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
         zero2[0] = zero2[1] = 0u;  // the GEMM's tile counter
     if ((int)blockIdx.x < strips) {
@@ -670,7 +673,6 @@ __global__ void __launch_bounds__(256)
         rows_wide_block<kOutHalfKMajor, WPR, RV>(blk, A, M, K, lda, Aop, ldk, sa, nullptr,
                                                  dstatus);
     }
-    griddep_launch_dependents();
 }
 
 // The strip CTAs alone, for a column quantize that is not fused with a row
@@ -680,8 +682,8 @@ __global__ void __launch_bounds__(256)
                                int64_t ldx, int R, __half *__restrict__ Q, int64_t ldq,
                                float *__restrict__ scale, int32_t *__restrict__ dstatus) {
     griddep_wait();  // programmatic launch: the previous kernel is done from here on
+    griddep_launch_dependents();  // see quantize_rows_wide_kernel
     cols_strip_block(X, rows, cols, ldx, R, (int64_t)blockIdx.x, Q, ldq, scale, dstatus);
-    griddep_launch_dependents();
 }
 
 // Column quantize, pass 2, into the GEMM's K-major f16 operand (Q[col][row]):
