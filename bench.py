@@ -66,20 +66,28 @@ def config_dict(n_gpus):
     }
 
 
-def gemm_source_hash():
-    """Hash of the GEMM's code: its sources with comments and blank lines
-    removed, so that an edit of comments alone keeps the profiled counters."""
+def code_digest(texts):
+    """SHA-256 (16 hex digits) of C/C++ sources with comments and blank lines
+    removed: an edit of comments alone keeps the digest."""
     import hashlib
     import re
     h = hashlib.sha256()
-    for rel in GEMM_SOURCES:
-        with open(os.path.join(ROOT, rel)) as f:
-            text = f.read()
+    for text in texts:
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
         lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
         h.update("\n".join(lines).encode())
     return h.hexdigest()[:16]
+
+
+def gemm_source_hash():
+    """Digest of the GEMM's code (see code_digest), as recorded in the
+    committed ncu summary."""
+    texts = []
+    for rel in GEMM_SOURCES:
+        with open(os.path.join(ROOT, rel)) as f:
+            texts.append(f.read())
+    return code_digest(texts)
 
 
 def profiled_traffic():
