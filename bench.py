@@ -127,7 +127,11 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+        # the raw samples: a temporary file unless BSG_CLOCKS_DIR names a
+        # folder to keep them in
+        import tempfile
+        folder = os.environ.get("BSG_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(folder, f"bsg_clocks_gpu{index}.csv")
 
     def start(self):
         try:
