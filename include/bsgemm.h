@@ -307,10 +307,13 @@ bsg_status bsgemm_i8_host(const float *A_host, const float *B_host, int64_t M, i
 
 /* Several independent units on host buffers in one call (at most
  * BSG_MAX_HOST_BATCH): each item is the argument list of bsgemm_i8_host.
- * The items' copies and kernels are pipelined across items: item i+1 uploads
- * while item i computes and downloads, so both directions of the host link
- * stay busy for the whole batch, where back-to-back bsgemm_i8_host calls
- * drain the pipeline at every call.  Each C is bit for bit what
+ * The items' copies and kernels are pipelined across items: one item uploads
+ * while the previous one computes and downloads, so both directions of the
+ * host link stay busy for the whole batch, where back-to-back bsgemm_i8_host
+ * calls drain the pipeline at every call.  The library picks the order of
+ * the items (Johnson's rule for the two stages, upload then download:
+ * download-heavy items first by increasing upload, then the rest by
+ * decreasing download).  Each C is bit for bit what
  * bsgemm_i8_host gives it.  Items may share A or B, but no two items may
  * overlap in workspace or in C (BSG_ERR_ARG); an item's A and B must not
  * overlap another item's C.  Synchronizes `stream` before returning;

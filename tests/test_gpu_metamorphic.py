@@ -185,3 +185,20 @@ def test_host_batch_reports_nonfinite_input():
     items = [(A0.pin_memory(), B.pin_memory(), False), (A1.pin_memory(), B.pin_memory(), False)]
     outs, st = bsg.bsgemm_i8_host_batch(items)
     assert st == bsg.DSTATUS_NONFINITE
+
+
+def test_host_batch_order_does_not_change_results():
+    """The batch call reorders its items for the host link; each C still
+    belongs to its own item, bit for bit."""
+    data = []
+    for i, (M, N, K) in enumerate([(2100, 64, 3000), (700, 900, 256), (1500, 1200, 300)]):
+        A = inputs.gpt2_activations(M, K, 90 + i)
+        B = inputs.gpt2_weights(K, N, 95 + i)
+        data.append((A.pin_memory(), B.pin_memory(), i == 1))
+    fwd, _ = bsg.bsgemm_i8_host_batch(data)
+    rev, _ = bsg.bsgemm_i8_host_batch(list(reversed(data)))
+    for i, C in enumerate(fwd):
+        Cd = bsg.bsgemm_i8(data[i][0].cuda(), data[i][1].cuda(), relu=data[i][2])
+        torch.cuda.synchronize()
+        assert_bits_equal(C.numpy(), Cd.cpu().numpy(), f"item {i}")
+        assert_bits_equal(rev[len(data) - 1 - i].numpy(), C.numpy(), f"reversed item {i}")

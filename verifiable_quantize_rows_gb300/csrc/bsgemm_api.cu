@@ -4,6 +4,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -616,8 +617,21 @@ bsg_status bsgemm_i8_host_batch(const bsg_host_item *items, int n, int32_t *dsta
         !ok(cudaStreamWaitEvent(h->out, h->start, 0)) ||
         !ok(cudaMemsetAsync(dstat, 0, sizeof(int32_t), st)))
         return BSG_ERR_CUDA;
-    for (int i = 0; i < n; ++i)
-        if (!ok(host_enqueue(items[i], dstat, st, h))) return BSG_ERR_CUDA;
+    // Items are independent, so they may run in any order: Johnson's rule for
+    // a two-stage flow (upload, then download) minimises the makespan.
+    // Items that download more than they upload go first, by increasing
+    // upload; the others follow, by decreasing download.
+    int order[BSG_MAX_HOST_BATCH];
+    for (int i = 0; i < n; ++i) order[i] = i;
+    auto up = [&](int i) { return (items[i].M + items[i].N) * items[i].K; };
+    auto down = [&](int i) { return items[i].M * items[i].N; };
+    std::stable_sort(order, order + n, [&](int a, int b) {
+        const bool fa = up(a) < down(a), fb = up(b) < down(b);
+        if (fa != fb) return fa;
+        return fa ? up(a) < up(b) : down(a) > down(b);
+    });
+    for (int k = 0; k < n; ++k)
+        if (!ok(host_enqueue(items[order[k]], dstat, st, h))) return BSG_ERR_CUDA;
     int32_t hstat = 0;
     if (!ok(cudaMemcpyAsync(&hstat, dstat, sizeof(int32_t), cudaMemcpyDeviceToHost, h->out)) ||
         !ok(cudaEventRecord(h->done, h->out)) || !ok(cudaStreamWaitEvent(st, h->done, 0)) ||
