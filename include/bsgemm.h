@@ -208,22 +208,26 @@ int bsg_gemm_tile_width(int64_t M, int64_t N, int sms);
 uint64_t bsg_launch_count(void);
 
 /* bsgemm_i8 for callers that cannot allocate device memory -- a framework
- * that owns every device allocation and lends none to extensions, code that
- * must not call cudaMalloc while a stream is being captured, an embedding
- * where the library may not touch the allocator.  It takes no workspace: its
- * scratch is a device array compiled into the library, BSG_NOALLOC_SCRATCH_BYTES
- * (64 MiB) long, which every GPU that loads the library holds until the
- * process exits.  Arguments and results are those of bsgemm_i8.
- *   - Problems whose bsgemm_i8_workspace_size(M, N, K) exceeds the array are
+ * that owns every device allocation and lends none to extensions, or an
+ * embedding where the library may not touch the allocator (a plug-in in
+ * someone else's process, a loop that forbids allocation after start-up).
+ * It takes no workspace: its scratch is a device array compiled into the
+ * library, BSG_NOALLOC_SCRATCH_BYTES (64 MiB) long, which every GPU that
+ * loads the library holds until the process exits.  Arguments and results
+ * are those of bsgemm_i8 (A and B as stored, never transposed).
+ *   - Problems whose unit workspace for that layout exceeds the array are
  *     rejected with BSG_ERR_WORKSPACE before anything is launched (the GPT-2
  *     linears fit; an 8192 x 50304 x 768 LM head does not).
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, once per device, that device current): make the
- *     first call on each device before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.  The address is looked up
+ *     again if the device's context has been replaced (cudaDeviceReset).
  *   - All calls share the one array and each leaves its contents behind:
  *     calls that may overlap on the GPU (other streams, other host threads)
  *     race on it and must be serialized by the caller.  Nothing in the array
- *     has to start at zero: each call writes every byte it reads.
+ *     has to start at zero: what a call reads is written earlier in the same
+ *     call, except column scales past N, which the epilogue loads for whole
+ *     tiles but applies to no stored column.
  *   - It calls no cudaMalloc, cudaFree or other allocating routine, and
  *     creates no stream or event: every launch goes to `stream`.
  * The pages have no counterpart: this is a deployment variant. */

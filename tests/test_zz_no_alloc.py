@@ -1,14 +1,17 @@
 """bsgemm_i8_noalloc: the unit for callers that cannot allocate device
-memory (a framework that owns every allocation and lends none, code running
-while a stream is captured into a CUDA graph, an embedding that may not touch
-the allocator).  Its scratch is a device array compiled into the library, so
-it takes no workspace.
+memory -- a framework that owns every device allocation and lends none to
+extensions, or an embedding where the library may not touch the allocator.
+Its scratch is a device array compiled into the library, so it takes no
+workspace.
 
-Checked through the C ABI: on two calls in a row, with different inputs, its
-output is bit-identical to bsgemm_i8's on a caller-provided workspace (the
-tolerance of every parity test here: bitwise); problems too large for the
-array are rejected before anything runs.  This file is collected last so a
-run that stops at the first failure has already run every other test.
+Checked through the C ABI, on calls in a row with different inputs: its
+output is bit-identical to the CPU oracle's and to bsgemm_i8's on a
+caller-provided workspace (the tolerance of every parity test here:
+bitwise).  The calls cover the fused quantize launch (K = 768), the separate
+row and column quantizes (K = 3072) and the two-pass column quantize whose
+partial maxima live in the shared array (K > 4096).  Problems too large for
+the array are rejected before anything runs.  This file is collected last so
+a run that stops at the first failure has already run every other test.
 """
 import ctypes
 
@@ -16,6 +19,7 @@ import numpy as np
 import pytest
 import torch
 
+from gpu_util import assert_bits_equal
 import verifiable_quantize_rows_gb300 as bsg
 from verifiable_quantize_rows_gb300 import inputs
 
@@ -43,19 +47,27 @@ def _noalloc(fn, A, B, relu):
     return C, int(st.item())
 
 
-def test_noalloc_matches_workspace_entry_point_on_two_calls():
+CALLS = [
+    ("fc", 8192, 3072, 768, True, 2),
+    ("proj", 8192, 768, 3072, False, 3),
+    ("long columns", 256, 320, 5000, False, 21),
+]
+
+
+def test_noalloc_matches_oracle_and_workspace_entry_point_on_calls_in_a_row(orc):
     fn = _entry()
-    calls = [("fc", 8192, 3072, 768, True, 2), ("proj", 8192, 768, 3072, False, 3)]
-    for name, M, N, K, relu, seed in calls:
-        A = inputs.gpt2_activations(M, K, seed).cuda()
-        B = inputs.gpt2_weights(K, N, seed).cuda()
-        want = bsg.bsgemm_i8(A, B, relu=relu)
-        torch.cuda.synchronize()
-        got, st = _noalloc(fn, A, B, relu)
+    for name, M, N, K, relu, seed in CALLS:
+        A = inputs.gpt2_activations(M, K, seed)
+        B = inputs.gpt2_weights(K, N, seed)
+        Ad, Bd = A.cuda(), B.cuda()
+        got, st = _noalloc(fn, Ad, Bd, relu)
         assert st == 0
-        g = got.cpu().numpy().view(np.uint32)
-        w = want.cpu().numpy().view(np.uint32)
-        assert np.array_equal(g, w), f"{name}: {(g != w).sum()} cells differ"
+        want = bsg.bsgemm_i8(Ad, Bd, relu=relu)
+        torch.cuda.synchronize()
+        Co, _ = orc.bsgemm_i8(A.numpy(), B.numpy(), relu)
+        g = got.cpu().numpy()
+        assert_bits_equal(g, Co, f"{name}: noalloc vs oracle")
+        assert_bits_equal(g, want.cpu().numpy(), f"{name}: noalloc vs bsgemm_i8")
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():

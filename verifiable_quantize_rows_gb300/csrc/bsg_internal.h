@@ -47,6 +47,10 @@ cudaError_t launch_quantize_rows(const float *X, int64_t rows, int64_t cols, int
                                  int32_t *dstatus, cudaStream_t st,
                                  unsigned int *zero2 = nullptr);
 
+// Bytes of the unit workspace for one operand layout (transA / transB as in
+// bsgemm_i8_ex); bsgemm_i8_workspace_size is the largest over the layouts.
+size_t unit_workspace_bytes(int64_t M, int64_t N, int64_t K, int transA, int transB);
+
 // Columns: a partial-max pass over row slices, then a quantize pass.
 // kOutInt8 keeps X's layout (Q is rows x cols); kOutHalfKMajor writes the
 // transpose (Q is cols x ldq, each row a column of X).

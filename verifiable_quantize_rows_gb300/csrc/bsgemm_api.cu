@@ -230,6 +230,11 @@ bsg_status unit_contract(int64_t M, int64_t N, int64_t K, int relu, float *C, in
 
 }  // namespace
 
+size_t unit_workspace_bytes(int64_t M, int64_t N, int64_t K, int transA, int transB) {
+    if (!dims_ok(M, N, K)) return 0;
+    return unit_layout(M, N, K, transA, transB).total;
+}
+
 bsg_status run_unit(const float *A, int64_t lda, int transA, const float *B, int64_t ldb,
                     int transB, int64_t M, int64_t N, int64_t K, int relu, float *C, int64_t ldc,
                     void *ws, size_t ws_bytes, int32_t *dstatus, cudaStream_t st, bool overlap) {
