@@ -1,18 +1,23 @@
 """Benchmark of the bit-exact block-scaled int8 GEMM on GB300.
 
-One step = one pass of the whole hot path over one batch: the three
-GPT-2-small linears at M = 8192 tokens -- QKV (K 768 -> N 2304), fc
-(768 -> 3072, fused ReLU), proj (3072 -> 768) -- each a full bsgemm_i8
-(per-row quantize of A, per-column quantize of B, exact int8 contraction on
-the tensor cores, f32 epilogue), plus the step's probe hash (the seeded
-1024^3 GEMM hashed to 32 bytes).  Throughput counts 2*M*N*K operations per
-GEMM.  Inputs are synthetic (seeded, GPT-2-small-shaped), resident in HBM
-before the timed region; L2 is flushed between timed steps.
+One step = one pass of the whole hot path over one batch of the large and
+adversarial GEMMs: 4096^3, 8192^3 and 16384^3 with U(-1, 1) values, and the
+ragged 4097 x 12289 x 8191 whose rows of A and columns of B mix the
+adversarial cases (all-zero and -0 vectors, exact quantize ties, subnormals,
+1e30 and 1e-30 magnitudes) -- each a full bsgemm_i8 (per-row quantize of A,
+per-column quantize of B, exact int8 contraction on the tensor cores, f32
+epilogue) -- plus the step's probe hash (the seeded 1024^3 GEMM hashed to 32
+bytes) on a side stream.  Throughput counts 2*M*N*K operations per GEMM.
+Inputs are synthetic (seeded), resident in HBM before the timed region; L2
+is flushed between timed steps.  The GPT-2-small linears at M = 8192 (QKV,
+fc + ReLU, proj, with the probe) are measured the same way and reported
+under "gpt2_linears".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
 Prints one JSON line.  `--impl reference` times the CPU oracle on a bounded
-sample of the same workload on this host's cores.
+sample of the same workload on this host's cores.  `--configs` times the unit
+on every workload of the measurement plan instead (one line each).
 """
 from __future__ import annotations
 
@@ -30,14 +35,68 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "bit-exact block-scaled int8 GEMM TOPS and % of GB300 dense INT8 peak"
-WORKLOAD = "gpt2_small_linears_M8192_qkv_fc_proj+probe1024"
+WORKLOAD = "large_gemms_4096^3+8192^3+16384^3+ragged_4097x12289x8191_adversarial+probe1024"
+SMALL_WORKLOAD = "gpt2_small_linears_M8192_qkv_fc_proj+probe1024"
 PROBE = (1024, 1024, 1024)
 PROBE_SEED = 0
 L2_FLUSH_BYTES = 256 << 20
-STAGE_REPEAT = 8          # launches per stage graph for the per-kernel durations
 GEMM_SOURCES = ("verifiable_quantize_rows_gb300/csrc/gemm_tc.cu",
                 "verifiable_quantize_rows_gb300/csrc/bsg_ptx.cuh")
-GEMM_PROFILE = "profiles/gemm_tc_gpt2_linears.md"
+GEMM_PROFILE = "profiles/gemm_tc_large_gemms.md"
+SMALL_GEMM_PROFILE = "profiles/gemm_tc_gpt2_linears.md"
+HBM_NOMINAL_GBS = 8000.0
+# The INT8 tensor figure NVIDIA publishes for the GB300 NVL72 rack, 23 POPS
+# over 72 GPUs.  Blackwell Ultra cut INT8 tensor throughput far below its
+# 16-bit rate, and CUDA 13.0's ptxas has no int8 tensor-core MMA for sm_103a
+# at all, so the exact contraction runs on the 16-bit pipe; the fraction of
+# this figure is reported because the metric names it.
+INT8_DATASHEET_TOPS = 23000.0 / 72
+INT8_DATASHEET_SOURCE = ("NVIDIA GB300 NVL72 specifications: INT8 Tensor Core 23 POPS for 72 "
+                         "GPUs (quoted without network access here; per GPU 319.4 TOPS)")
+MMA_CEILING_ITERS = 8192
+
+
+def unit_list(kind):
+    """(name, M, N, K, relu, loader) of the step's GEMMs."""
+    from verifiable_quantize_rows_gb300 import inputs
+    if kind == "large":
+        return [(n, M, N, K, r, (lambda n=n: inputs.large_gemm_inputs(n)[:2]))
+                for n, M, N, K, r, _ in inputs.LARGE_GEMMS]
+    return [(n, M, N, K, r, (lambda n=n: inputs.gpt2_linear_inputs(n)[:2]))
+            for n, M, N, K, r, _ in inputs.GPT2_LINEARS]
+
+
+def step_ops(kind="large"):
+    ops = sum(2 * M * N * K for _, M, N, K, _, _ in unit_list(kind))
+    return ops + 2 * PROBE[0] * PROBE[1] * PROBE[2]
+
+
+def quant_algo_bytes(M, N, K):
+    """Quantize's algorithmic bytes for one unit: 4 B read + 1 B int8 code
+    written per element of A and B, and 4 B per scale."""
+    return 5 * (M * K + K * N) + 4 * (M + N)
+
+
+def config_dict(n_gpus, kind="large"):
+    if kind == "large":
+        workload = WORKLOAD
+        vals = ("squares U(-1,1) (A seed 6/7/8, B seed+1); ragged A rows / B columns: the "
+                "adversarial mix (a third of the vectors all-zero, -0, exact ties, subnormal, "
+                "subnormal-mixed, 1e30, 1e-30, negative-max, spike; the rest U(-1,1)), seeded")
+        l2 = "flushed between timed steps (256 MiB write); inputs resident in HBM, larger than L2"
+    else:
+        workload = SMALL_WORKLOAD
+        vals = "activations N(0,1) with 0.1% x20 outliers, weights N(0,0.02), seeded"
+        l2 = "flushed between timed steps (256 MiB write); inputs resident in HBM"
+    return {
+        "workload": workload,
+        "gemms": [{"name": n, "M": M, "N": N, "K": K, "relu": r}
+                  for n, M, N, K, r, _ in unit_list(kind)]
+                 + [{"name": "probe", "M": PROBE[0], "N": PROBE[1], "K": PROBE[2], "relu": False}],
+        "inputs": vals,
+        "l2": l2,
+        "parallelism": f"replicas x{n_gpus} (weak: each GPU runs the full step)",
+    }
 
 
 def env_int(name, default):
@@ -45,25 +104,6 @@ def env_int(name, default):
         return int(os.environ.get(name, default))
     except ValueError:
         return default
-
-
-def step_ops():
-    from verifiable_quantize_rows_gb300 import inputs
-    ops = sum(2 * M * N * K for _, M, N, K, _, _ in inputs.GPT2_LINEARS)
-    return ops + 2 * PROBE[0] * PROBE[1] * PROBE[2]
-
-
-def config_dict(n_gpus):
-    from verifiable_quantize_rows_gb300 import inputs
-    return {
-        "workload": WORKLOAD,
-        "gemms": [{"name": n, "M": M, "N": N, "K": K, "relu": r}
-                  for n, M, N, K, r, _ in inputs.GPT2_LINEARS]
-                 + [{"name": "probe", "M": PROBE[0], "N": PROBE[1], "K": PROBE[2], "relu": False}],
-        "inputs": "activations N(0,1) with 0.1% x20 outliers, weights N(0,0.02), seeded",
-        "l2": "flushed between timed steps (256 MiB write); inputs resident in HBM",
-        "parallelism": f"replicas x{n_gpus} (weak: each GPU runs the full step)",
-    }
 
 
 def code_digest(texts):
@@ -90,13 +130,13 @@ def gemm_source_hash():
     return code_digest(texts)
 
 
-def profiled_traffic():
-    """DRAM bytes per GEMM launch from the committed ncu summary, if it was
-    taken on the current GEMM source (else None: the counters are stale)."""
-    p = os.path.join(ROOT, GEMM_PROFILE)
-    if not os.path.exists(p):
-        return None
+def parse_profile(profile):
+    """(source digest, {gemm name: DRAM bytes per launch}) recorded in a
+    committed ncu summary, or (None, {}) if there is none."""
+    p = os.path.join(ROOT, profile)
     src, per = None, {}
+    if not os.path.exists(p):
+        return src, per
     with open(p) as f:
         for line in f:
             parts = line.strip().strip("`").split()
@@ -104,6 +144,13 @@ def profiled_traffic():
                 src = parts[1]
             elif len(parts) == 3 and parts[0] == "dram-bytes-per-launch":
                 per[parts[1].rstrip(":")] = int(parts[2])
+    return src, per
+
+
+def profiled_traffic(profile=GEMM_PROFILE):
+    """DRAM bytes per GEMM launch from a committed ncu summary, if it was
+    taken on the current GEMM source (else None: the counters are stale)."""
+    src, per = parse_profile(profile)
     if src != gemm_source_hash() or not per:
         return None
     return per
@@ -187,144 +234,128 @@ def gpu_selector(local_rank):
 
 
 # -------------------------------------------------------------- GPU arm
-def run_gpu(args, rank, world, local_rank):
-    import torch
-    import torch.distributed as dist
+class Workload:
+    """Device-resident inputs, outputs and workspaces of one step's GEMMs,
+    with the step and its per-stage graphs."""
 
-    import verifiable_quantize_rows_gb300 as bsg
-    from verifiable_quantize_rows_gb300 import build as bsg_build
-    from verifiable_quantize_rows_gb300 import inputs
+    def __init__(self, kind, dev, lib, side, dstatus, probe_out, probe_ws, with_host):
+        import torch
+        import verifiable_quantize_rows_gb300 as bsg
+        self.kind = kind
+        self.dev = dev
+        self.side = side
+        self.dstatus = dstatus
+        self.probe_out = probe_out
+        self.probe_ws = probe_ws
+        self.units = []
+        for name, M, N, K, relu, load in unit_list(kind):
+            A, B = load()
+            ws = bsg.Workspace(dev)
+            ws.get(lib.bsgemm_i8_workspace_size(M, N, K))
+            u = dict(name=name, M=M, N=N, K=K, relu=relu, A=A.to(dev), B=B.to(dev),
+                     C=torch.empty(M, N, device=dev), ws=ws)
+            if with_host:
+                u.update(Ah=A.pin_memory(), Bh=B.pin_memory(),
+                         Ch=torch.empty(M, N, pin_memory=True))
+            del A, B
+            # Small inputs are timed per stage over 8 copies so that every
+            # quantize launch reads them from HBM as in the step; large ones
+            # (beyond L2) repeat on the same copy, twice.
+            in_bytes = 4 * (M * K + K * N)
+            if in_bytes <= (256 << 20):
+                u["copies"] = [(u["A"].clone(), u["B"].clone()) for _ in range(7)] + [(u["A"], u["B"])]
+            else:
+                u["copies"] = [(u["A"], u["B"])] * 2
+            self.units.append(u)
 
-    if not os.path.exists(bsg.LIB_PATH):
-        bsg_build.build()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    stream = torch.cuda.current_stream()
-    lib = bsg.load()
+    # ---- the step
+    def quantize(self, u, A=None, B=None):
+        import verifiable_quantize_rows_gb300 as bsg
+        bsg.bsgemm_i8_quantize(u["A"] if A is None else A, u["B"] if B is None else B, u["ws"],
+                               dstatus=self.dstatus)
 
-    # resident inputs and outputs
-    lin = []
-    for name, M, N, K, relu, seed in inputs.GPT2_LINEARS:
-        A, B, _ = inputs.gpt2_linear_inputs(name)
-        ws = bsg.Workspace(dev)
-        ws.get(lib.bsgemm_i8_workspace_size(M, N, K))
-        lin.append(dict(name=name, M=M, N=N, K=K, relu=relu, A=A.to(dev), B=B.to(dev),
-                        C=torch.empty(M, N, device=dev), ws=ws, Ah=A.pin_memory(),
-                        Bh=B.pin_memory(), Ch=torch.empty(M, N, pin_memory=True)))
-    pws = bsg.Workspace(dev)
-    pws.get(lib.bsg_probe_workspace_size(*PROBE))
-    probe_out = torch.empty(32, dtype=torch.uint8, device=dev)
-    dstatus = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    host_ws = bsg.Workspace(dev)
-    host_ws.get(sum((lib.bsgemm_i8_host_workspace_size(L["M"], L["N"], L["K"]) + 255) // 256 * 256
-                    for L in lin))
+    def contract(self, u):
+        import verifiable_quantize_rows_gb300 as bsg
+        bsg.bsgemm_i8_contract(u["M"], u["N"], u["K"], u["C"], u["ws"], relu=u["relu"],
+                               dstatus=self.dstatus)
 
-    side = torch.cuda.Stream(device=dev)
+    def probe(self):
+        import verifiable_quantize_rows_gb300 as bsg
+        bsg.probe_hash_async(PROBE_SEED, *PROBE, out=self.probe_out, dstatus=self.dstatus,
+                             workspace=self.probe_ws)
 
-    def stage_quantize(L):
-        bsg.bsgemm_i8_quantize(L["A"], L["B"], L["ws"], dstatus=dstatus)
-
-    def stage_contract(L):
-        bsg.bsgemm_i8_contract(L["M"], L["N"], L["K"], L["C"], L["ws"], relu=L["relu"],
-                               dstatus=dstatus)
-
-    def stage_probe():
-        bsg.probe_hash_async(PROBE_SEED, *PROBE, out=probe_out, dstatus=dstatus, workspace=pws)
-
-    def step_body():
+    def step(self):
         """One step on the current stream; the probe runs on a side stream
-        forked from it and joined at the end, so it overlaps the linears."""
+        forked from it and joined at the end, so it overlaps the GEMMs."""
+        import torch
         cur = torch.cuda.current_stream()
-        if args.probe_overlap:
-            side.wait_stream(cur)
-            with torch.cuda.stream(side):
-                stage_probe()
-        for L in lin:
-            stage_quantize(L)
-            stage_contract(L)
-        if args.probe_overlap:
-            cur.wait_stream(side)
-        else:
-            stage_probe()
+        self.side.wait_stream(cur)
+        with torch.cuda.stream(self.side):
+            self.probe()
+        for u in self.units:
+            self.quantize(u)
+            self.contract(u)
+        cur.wait_stream(self.side)
 
-    # Per-kernel launch durations: each stage is captured STAGE_REPEAT times
-    # back to back in one graph, timed with events around the replay and
-    # divided by the repeat count (a one-launch graph would add the graph's
-    # own launch latency to every number).  Quantize stages rotate over
-    # STAGE_REPEAT copies of their inputs, so that every launch reads A and B
-    # from HBM as in the step; GEMM stages re-run on the operands their
-    # quantize stage wrote, which sit in L2 as they do in the step.
-    R = STAGE_REPEAT
-    for L in lin:
-        L["copies"] = [(L["A"].clone(), L["B"].clone()) for _ in range(R - 1)] + [(L["A"], L["B"])]
+    def stages(self):
+        """(name, fn, repeat) per stage: each is captured `repeat` times back
+        to back in one graph and timed per launch."""
+        out = []
+        for u in self.units:
+            out.append(("quantize_" + u["name"],
+                        (lambda u=u: [self.quantize(u, A_, B_) for A_, B_ in u["copies"]]),
+                        len(u["copies"])))
+            reps = len(u["copies"])
+            out.append(("gemm_" + u["name"], (lambda u=u, r=reps: [self.contract(u)
+                                                                    for _ in range(r)]), reps))
+        out.append(("probe", lambda: [self.probe() for _ in range(4)], 4))
+        return out
 
-    def stage_quantize_r(L):
-        for A_, B_ in L["copies"]:
-            bsg.bsgemm_i8_quantize(A_, B_, L["ws"], dstatus=dstatus)
 
-    def stage_contract_r(L):
-        for _ in range(R):
-            stage_contract(L)
-
-    def stage_probe_r():
-        for _ in range(R):
-            stage_probe()
-
-    stages = []
-    for L in lin:
-        stages.append(("quantize_" + L["name"], (lambda L=L: stage_quantize_r(L))))
-        stages.append(("gemm_" + L["name"], (lambda L=L: stage_contract_r(L))))
-    stages.append(("probe", stage_probe_r))
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    # warm up eagerly (first calls set kernel attributes), then capture graphs
-    for _ in range(args.warmup):
-        step_body()
+def time_workload(W, steps, warmup, flush, stream, barrier, stage_steps):
+    """Time W's step (graph replays, L2 flushed before each) and each stage
+    (per launch).  Returns step times (ms), stage times (ms per launch, one
+    row per stage round) and the number of this library's kernel launches."""
+    import torch
+    import verifiable_quantize_rows_gb300 as bsg
+    dev = W.dev
+    for _ in range(warmup):           # eager first calls set kernel attributes
+        W.step()
     torch.cuda.synchronize()
     capture = torch.cuda.Stream(device=dev)
     n0 = bsg.launch_count()
     g_step = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step, stream=capture):
-        step_body()
+        W.step()
     launches_step = bsg.launch_count() - n0
     g_stages = []
     launches_stages = 0
-    for name, fn in stages:
+    for name, fn, reps in W.stages():
         g = torch.cuda.CUDAGraph()
         n0 = bsg.launch_count()
         with torch.cuda.graph(g, stream=capture):
             fn()
         launches_stages += bsg.launch_count() - n0
-        g_stages.append((name, g))
-    for _ in range(args.warmup):
+        g_stages.append((name, g, reps))
+    for _ in range(warmup):
         g_step.replay()
-        for _, g in g_stages:
+        for _, g, _ in g_stages:
             g.replay()
     torch.cuda.synchronize()
 
-    # ---- timed region: device-resident inputs, L2 flushed between steps
-    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-    stage_steps = max(10, min(args.steps, 50))
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(len(g_stages))] for _ in range(stage_steps)]
-    clocks = ClockSampler(gpu_selector(local_rank))
-    clocks.start()
-    time.sleep(0.3)
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+    ev_step = [(ev(), ev()) for _ in range(steps)]
+    evs = [[(ev(), ev()) for _ in g_stages] for _ in range(stage_steps)]
     barrier()
     torch.cuda.synchronize()
-    wall0 = time.perf_counter()
-    for s in range(args.steps):
+    for s in range(steps):
         flush.zero_()                      # L2 flush, outside the timed pair
         ev_step[s][0].record(stream)
         g_step.replay()
         ev_step[s][1].record(stream)
     for s in range(stage_steps):
-        for k, (name, g) in enumerate(g_stages):
+        for k, (name, g, _) in enumerate(g_stages):
             if not name.startswith("gemm_"):   # a GEMM reads what its quantize just wrote
                 flush.zero_()
             e0, e1 = evs[s][k]
@@ -333,18 +364,130 @@ def run_gpu(args, rank, world, local_rank):
             e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    wall = time.perf_counter() - wall0
-    launches = launches_step * args.steps + launches_stages * stage_steps
-    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev_step]
+    stage_ms = {name: [evs[s][k][0].elapsed_time(evs[s][k][1]) / reps for s in range(stage_steps)]
+                for k, (name, _, reps) in enumerate(g_stages)}
+    launches = launches_step * steps + launches_stages * stage_steps
+    del g_step, g_stages
+    return step_ms, stage_ms, launches
 
-    step_ms_list = [a.elapsed_time(b) for a, b in ev_step]
-    stage_ms = [[a.elapsed_time(b) / R for a, b in row] for row in evs]
-    ms_per_step = statistics.mean(step_ms_list)
+
+def mma_ceiling(stream, dstatus, reps=5):
+    """TFLOP/s of the tensor-pipe ceiling kernel (median of `reps` launches)."""
+    import torch
+    import verifiable_quantize_rows_gb300 as bsg
+    bsg.mma_ceiling(MMA_CEILING_ITERS, dstatus=dstatus)
+    torch.cuda.synchronize()
+    ts, flops = [], 0.0
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        flops = bsg.mma_ceiling(MMA_CEILING_ITERS, dstatus=dstatus)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return flops / (statistics.median(ts) * 1e-3) / 1e12
+
+
+def summarize(W, step_ms, stage_ms, peaks, peak_kind, ms_max, world, profile):
+    """Roofline of the GEMM (dominant kernel) and quantize figures."""
+    units = W.units
+    mean = statistics.mean
+    gemm_ms = [mean(stage_ms["gemm_" + u["name"]]) for u in units]
+    quant_ms = [mean(stage_ms["quantize_" + u["name"]]) for u in units]
+    gemm_ops = [2 * u["M"] * u["N"] * u["K"] for u in units]
+    achieved = sum(gemm_ops) / (sum(gemm_ms) * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    peak_sus = float(peaks.get("bf16_tflops_sustained", 1700.0))
+    prof = profiled_traffic(profile)
+    traffic = (round(sum(prof[u["name"]] for u in units) / len(units))
+               if prof and all(u["name"] in prof for u in units) else None)
+    algo_bytes = round(sum(2 * (u["M"] + u["N"]) * u["K"] + 4 * u["M"] * u["N"] for u in units)
+                       / len(units))
+    qbytes = [quant_algo_bytes(u["M"], u["N"], u["K"]) for u in units]
+    f16_extra = [2 * (u["M"] * u["K"] + u["K"] * u["N"]) for u in units]
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    q_gbs = sum(qbytes) / (sum(quant_ms) * 1e-3) / 1e9
+    roof = {
+        "bound": "tensor",
+        "kernel": "gemm_tc_kernel (tcgen05 kind::f16, exact int8 contraction + epilogue)",
+        "achieved": round(achieved, 2),
+        "peak": peak,
+        "unit": "TFLOP/s",
+        "frac": round(achieved / peak, 4),
+        "peak_source": f"{peak_kind} bf16 burst (f16 dense rate = bf16 nominal)",
+        "frac_of_sustained": round(achieved / peak_sus, 4),
+        "traffic": traffic,
+        "traffic_note": ("DRAM bytes read + written per GEMM launch (mean over the step's "
+                         "GEMMs) from the committed ncu summary " + profile + ", taken on this "
+                         "GEMM source; null if the source has changed since"),
+        "algorithmic_bytes": algo_bytes,
+        "per_gemm_ms": {u["name"]: round(g, 4) for u, g in zip(units, gemm_ms)},
+        "per_gemm_frac": {u["name"]: round(o / (g * 1e-3) / 1e12 / peak, 4)
+                          for u, o, g in zip(units, gemm_ops, gemm_ms)},
+    }
+    quant = {
+        "bound": "hbm",
+        "achieved_gbs": round(q_gbs, 1),
+        "peak_gbs": hbm,
+        "frac": round(q_gbs / hbm, 4),
+        "frac_of_nominal_8tbs": round(q_gbs / HBM_NOMINAL_GBS, 4),
+        "bytes": "4 B read + 1 B int8 code per element of A and B + 4 B per scale",
+        "f16_operand_extra_bytes": sum(f16_extra),
+        "achieved_gbs_incl_f16_operand": round((sum(qbytes) + sum(f16_extra))
+                                               / (sum(quant_ms) * 1e-3) / 1e9, 1),
+        "per_gemm_ms": {u["name"]: round(q, 4) for u, q in zip(units, quant_ms)},
+        "per_gemm_frac": {u["name"]: round(b / (q * 1e-3) / 1e9 / hbm, 4)
+                          for u, b, q in zip(units, qbytes, quant_ms)},
+    }
+    return roof, quant, mean(stage_ms["probe"])
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import verifiable_quantize_rows_gb300 as bsg
+    from verifiable_quantize_rows_gb300 import build as bsg_build
+    from verifiable_quantize_rows_gb300.replicas import max_over_ranks, probe_hashes_agree
+
+    if not os.path.exists(bsg.LIB_PATH):
+        bsg_build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    lib = bsg.load()
+    side = torch.cuda.Stream(device=dev)
+    pws = bsg.Workspace(dev)
+    pws.get(lib.bsg_probe_workspace_size(*PROBE))
+    probe_out = torch.empty(32, dtype=torch.uint8, device=dev)
+    dstatus = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    W = Workload("large", dev, lib, side, dstatus, probe_out, pws, with_host=True)
+    clocks = ClockSampler(gpu_selector(local_rank))
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    step_ms, stage_ms, launches = time_workload(W, args.steps, args.warmup, flush, stream,
+                                                barrier, stage_steps=5)
+    wall = time.perf_counter() - wall0
+    ceiling = mma_ceiling(stream, dstatus)
+    clk = clocks.stop()
+    ms_per_step = statistics.mean(step_ms)
     probe_hex = bytes(probe_out.cpu().tolist()).hex()
-    # ---- end-to-end through the host-buffer entry points (copies inside):
-    # the probe starts on a side stream (device work only), the three linears
-    # run as one pipelined batch call (bound by the host link), then the
-    # probe's 32-byte hash is read back to the host
+
+    # ---- end to end through the host-buffer entry points (copies inside):
+    # the probe starts on a side stream, the GEMMs run as one pipelined
+    # bsgemm_i8_host_batch call (bound by the host link), then the probe's
+    # 32-byte hash is read back to the host
+    host_ws = bsg.Workspace(dev)
+    host_ws.get(sum((lib.bsgemm_i8_host_workspace_size(u["M"], u["N"], u["K"]) + 255) // 256 * 256
+                    for u in W.units))
     e2e_hash = torch.empty(32, dtype=torch.uint8, device=dev)
     e2e_hash_host = torch.empty(32, dtype=torch.uint8, pin_memory=True)
 
@@ -352,28 +495,21 @@ def run_gpu(args, rank, world, local_rank):
         side.wait_stream(torch.cuda.current_stream())
         bsg.probe_hash_async(PROBE_SEED, *PROBE, out=e2e_hash, stream=side, dstatus=dstatus,
                              workspace=pws)
-        _, st = bsg.bsgemm_i8_host_batch([(L["Ah"], L["Bh"], L["relu"], L["Ch"]) for L in lin],
-                                         workspace=host_ws)
-        if st:
+        _, st = bsg.bsgemm_i8_host_batch([(u["Ah"], u["Bh"], u["relu"], u["Ch"])
+                                          for u in W.units], workspace=host_ws)
+        if st & ~1:
             raise RuntimeError(f"device status {st} in the end-to-end step")
         with torch.cuda.stream(side):
             e2e_hash_host.copy_(e2e_hash, non_blocking=True)
         side.synchronize()
         return bytes(e2e_hash_host.tolist())
 
-    def e2e_step_calls():
-        """The same work as one bsgemm_i8_host call per linear (for comparison)."""
-        for L in lin:
-            bsg.bsgemm_i8_host(L["Ah"], L["Bh"], relu=L["relu"], out=L["Ch"], workspace=host_ws)
-        return bsg.probe_hash(PROBE_SEED, *PROBE, workspace=pws)
-
-    for _ in range(max(1, args.warmup // 2)):
-        e2e_step()
+    e2e_steps = max(3, min(args.steps, 10))
+    e2e_step()
     torch.cuda.synchronize()
     barrier()
-    e2e_times = []
-    e2e_hex = ""
-    for _ in range(args.steps):
+    e2e_times, e2e_hex = [], ""
+    for _ in range(e2e_steps):
         flush.zero_()
         torch.cuda.synchronize()
         t = time.perf_counter()
@@ -381,18 +517,30 @@ def run_gpu(args, rank, world, local_rank):
         e2e_times.append(time.perf_counter() - t)
     barrier()
     e2e_ms = statistics.mean(e2e_times) * 1e3
-    calls_times = []
-    for _ in range(min(args.steps, 50)):
-        flush.zero_()
-        torch.cuda.synchronize()
-        t = time.perf_counter()
-        e2e_step_calls()
-        calls_times.append(time.perf_counter() - t)
-    e2e_calls_ms = statistics.mean(calls_times) * 1e3
-
-    # ---- max over ranks, and the replicas' probe hashes (the pages' cross-device check)
-    from verifiable_quantize_rows_gb300.replicas import max_over_ranks, probe_hashes_agree
+    h2d = sum(4 * (u["M"] * u["K"] + u["K"] * u["N"]) for u in W.units)
+    d2h = sum(4 * u["M"] * u["N"] for u in W.units) + 32
+    peaks, peak_kind = load_peaks()
     ms_max, e2e_max = max_over_ranks([ms_per_step, e2e_ms], device=dev)
+    roof, quant, probe_ms = summarize(W, step_ms, stage_ms, peaks, peak_kind, ms_max, world,
+                                      GEMM_PROFILE)
+    dstat_large = int(dstatus.item())
+    del W, host_ws
+    torch.cuda.empty_cache()
+
+    # ---- the GPT-2-small linears, the same way (reported beside the headline)
+    dstatus.zero_()
+    Ws = Workload("small", dev, lib, side, dstatus, probe_out, pws, with_host=False)
+    s_steps = max(10, min(args.steps * 4, 400))
+    s_step_ms, s_stage_ms, s_launches = time_workload(Ws, s_steps, args.warmup, flush, stream,
+                                                      barrier, stage_steps=20)
+    s_ms = statistics.mean(s_step_ms)
+    (s_ms_max,) = max_over_ranks([s_ms], device=dev)
+    s_roof, s_quant, _ = summarize(Ws, s_step_ms, s_stage_ms, peaks, peak_kind, s_ms_max, world,
+                                   SMALL_GEMM_PROFILE)
+    dstat_small = int(dstatus.item())
+    del Ws
+    torch.cuda.empty_cache()
+
     golden = None
     gpath = os.path.join(ROOT, "tests", "golden", "probe_hash.txt")
     if os.path.exists(gpath):
@@ -401,35 +549,27 @@ def run_gpu(args, rank, world, local_rank):
             if len(p) == 5 and p[:4] == [str(PROBE_SEED), *map(str, PROBE)]:
                 golden = p[4]
     replicas_agree, _ = probe_hashes_agree(bytes.fromhex(probe_hex), device=dev)
-    torch.cuda.synchronize()
-    dstat = int(dstatus.item())
-
     if rank != 0:
         return None
+    return build_line(args, world, ms_max, roof, quant, probe_ms, ceiling, clk, launches,
+                      s_launches, s_steps, wall, e2e_max, e2e_steps, h2d, d2h, golden, e2e_hex,
+                      probe_hex, replicas_agree, dstat_large, dstat_small, s_ms_max, s_roof,
+                      s_quant)
 
-    ops = step_ops()
-    peaks, peak_kind = load_peaks()
-    prof = profiled_traffic()
-    traffic = (round(sum(prof[L["name"]] for L in lin) / len(lin))
-               if prof and all(L["name"] in prof for L in lin) else None)
-    # f16 operands read once, f32 C written once
-    algo_bytes = round(sum(2 * (L["M"] + L["N"]) * L["K"] + 4 * L["M"] * L["N"] for L in lin)
-                       / len(lin))
-    # dominant kernel: the tensor-core contraction (one launch per linear),
-    # timed per stage graph in the second half of the timed region
-    gemm_ms = [statistics.mean(sm[2 * i + 1] for sm in stage_ms) for i in range(len(lin))]
-    quant_ms = [statistics.mean(sm[2 * i] for sm in stage_ms) for i in range(len(lin))]
-    probe_ms = statistics.mean(sm[-1] for sm in stage_ms)
-    gemm_ops = [2 * L["M"] * L["N"] * L["K"] for L in lin]
-    achieved = sum(gemm_ops) / (sum(gemm_ms) * 1e-3) / 1e12      # TFLOP/s (f16 pipe)
-    peak = float(peaks.get("bf16_tflops", 1900.0))
-    quant_bytes = [4 * (L["M"] * L["K"] + L["K"] * L["N"]) + 2 * (L["M"] * L["K"] + L["K"] * L["N"])
-                   for L in lin]
-    quant_gbs = sum(quant_bytes) / (sum(quant_ms) * 1e-3) / 1e9
+
+def build_line(args, world, ms_max, roof, quant, probe_ms, ceiling, clk, launches, s_launches,
+               s_steps, wall, e2e_max, e2e_steps, h2d, d2h, golden, e2e_hex, probe_hex,
+               replicas_agree, dstat_large, dstat_small, s_ms_max, s_roof, s_quant):
+    ops = step_ops("large")
     value = ops * world / (ms_max * 1e-3) / 1e12
-    h2d = sum(4 * (L["M"] * L["K"] + L["K"] * L["N"]) for L in lin)
-    d2h = sum(4 * L["M"] * L["N"] for L in lin) + 32
-    line = {
+    roof = dict(roof)
+    roof["mma_ceiling_tflops"] = round(ceiling, 1)
+    roof["frac_of_mma_ceiling"] = round(roof["achieved"] / ceiling, 4)
+    roof["mma_ceiling_note"] = ("bsg_mma_ceiling: pair kind::f16 MMAs 256x256x16 issued back to "
+                                "back from shared memory on every resident SM pair, no operand "
+                                "copies or epilogue; median of 5 launches, CUDA events")
+    s_ops = step_ops("small")
+    return {
         "metric": METRIC,
         "value": round(value, 3),
         "unit": "TOPS",
@@ -442,58 +582,51 @@ def run_gpu(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "int8",
         "data": "synthetic",
-        "config": config_dict(world),
-        "roofline": {
-            "bound": "tensor",
-            "kernel": "gemm_tc_kernel (tcgen05 kind::f16, exact int8 contraction + epilogue)",
-            "achieved": round(achieved, 2),
-            "peak": peak,
-            "unit": "TFLOP/s",
-            "frac": round(achieved / peak, 4),
-            "peak_source": f"{peak_kind} bf16 burst (f16 dense rate = bf16 nominal)",
-            "traffic": traffic,
-            "traffic_note": ("DRAM bytes read + written per GEMM launch (mean of the three "
-                             "linears) from the committed ncu summary " + GEMM_PROFILE +
-                             ", taken on this GEMM source; null if the source has changed "
-                             "since"),
-            "algorithmic_bytes": algo_bytes,
-            "per_gemm_ms": {L["name"]: round(g, 4) for L, g in zip(lin, gemm_ms)},
+        "config": config_dict(world, "large"),
+        "roofline": roof,
+        "int8_datasheet": {
+            "tops_per_gpu": round(INT8_DATASHEET_TOPS, 1),
+            "source": INT8_DATASHEET_SOURCE,
+            "frac_step": round(value / world / INT8_DATASHEET_TOPS, 3),
+            "frac_gemm": round(roof["achieved"] / INT8_DATASHEET_TOPS, 3),
+            "note": ("sm_103a has no int8 tensor-core MMA (ptxas rejects tcgen05 kind::i8); the "
+                     "exact contraction runs on the f16 pipe, whose measured rate is the "
+                     "roofline peak; the datasheet INT8 figure is far below it"),
         },
-        "quantize": {
-            "bound": "hbm",
-            "achieved_gbs": round(quant_gbs, 1),
-            "peak_gbs": float(peaks.get("hbm_gbs", 6800.0)),
-            "frac": round(quant_gbs / float(peaks.get("hbm_gbs", 6800.0)), 4),
-            "bytes": "4 B read + 2 B f16 operand write per element of A and B",
-            "per_gemm_ms": {L["name"]: round(q, 4) for L, q in zip(lin, quant_ms)},
-        },
+        "quantize": quant,
         "probe_ms": round(probe_ms, 4),
-        "int8_peak_note": ("sm_103a has no int8 tensor-core MMA (ptxas rejects tcgen05 "
-                           "kind::i8); the exact contraction runs on the f16 pipe, so the "
-                           "roofline peak is the measured 16-bit dense rate"),
         "e2e": {"value": round(ops * world / (e2e_max * 1e-3) / 1e12, 3), "unit": "TOPS",
-                "ms_per_step": round(e2e_max, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
-                "api": "bsgemm_i8_host_batch of the three linears (pinned host A, B in; C out) "
-                       "+ bsg_probe_hash",
-                "one_call_per_linear_ms_per_step": round(e2e_calls_ms, 4),
+                "ms_per_step": round(e2e_max, 4), "steps": e2e_steps,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "bsgemm_i8_host_batch of the step's four GEMMs (pinned host A, B in; "
+                       "C out) + bsg_probe_hash_async with its 32 bytes read back",
                 "probe_hash_matches_golden": (golden == e2e_hex) if golden else None},
         "clocks": clk,
         "gpu_launches": launches,
         "wall_s_timed": round(wall, 4),
         "timing": ("value/ms_per_step: the whole step replayed as one CUDA graph, CUDA events "
                    "around each replay, L2 flushed before each; roofline/quantize/probe: per "
-                   f"launch, each stage captured {R}x back to back in one graph and timed with "
-                   f"events around its replay / {R}, quantize over {R} input copies (reads from "
-                   "HBM), GEMM on the operands its quantize wrote (in L2, as in the step)"),
-        "probe_overlap": bool(args.probe_overlap),
-        "stage_sum_ms": round(statistics.mean(sum(x) for x in stage_ms), 4),
+                   "launch, each stage captured 2x (8x, over 8 input copies, for inputs under "
+                   "256 MiB) back to back in one graph and timed with events around its replay; "
+                   "the GEMM runs on the operands its quantize wrote"),
         "probe_hash": probe_hex,
         "probe_hash_matches_golden": (golden == probe_hex) if golden else None,
         "replicas_agree": replicas_agree,
-        "device_status": dstat,
+        "device_status": dstat_large,
+        "device_status_note": "bit 0 (non-finite input) is not expected; bit 1 is a timeout",
+        "gpt2_linears": {
+            "workload": SMALL_WORKLOAD,
+            "config": config_dict(world, "small"),
+            "value": round(s_ops * world / (s_ms_max * 1e-3) / 1e12, 3),
+            "unit": "TOPS",
+            "steps": s_steps,
+            "ms_per_step": round(s_ms_max, 4),
+            "roofline": s_roof,
+            "quantize": s_quant,
+            "gpu_launches": s_launches,
+            "device_status": dstat_small,
+        },
     }
-    return line
 
 
 # -------------------------------------------------------------- config sweep
@@ -568,13 +701,16 @@ def run_configs(args):
         g_us = timed(lambda: bsg.bsgemm_i8_contract(M, N, K, C, ws, relu=relu, dstatus=dstatus))
         u_us = timed(lambda: bsg.bsgemm_i8(A, B, relu=relu, out=C, dstatus=dstatus, workspace=ws))
         ops = 2 * M * N * K
-        qbytes = 6 * (M * K + K * N)
+        qbytes = quant_algo_bytes(M, N, K)
         return {"config": name, "M": M, "N": N, "K": K, "relu": relu,
                 "unit_us": round(u_us, 2), "unit_tops": round(ops / u_us / 1e6, 1),
                 "gemm_us": round(g_us, 2), "gemm_tflops": round(ops / g_us / 1e6, 1),
                 "gemm_frac_of_measured_bf16": round(ops / g_us / 1e6 / tc_peak, 3),
                 "quantize_us": round(q_us, 2), "quantize_gbs": round(qbytes / q_us / 1e3, 1),
-                "quantize_frac_of_measured_hbm": round(qbytes / q_us / 1e3 / hbm_peak, 3)}
+                "quantize_frac_of_measured_hbm": round(qbytes / q_us / 1e3 / hbm_peak, 3),
+                "quantize_frac_of_nominal_8tbs": round(qbytes / q_us / 1e3 / HBM_NOMINAL_GBS, 3),
+                "quantize_bytes": "4 B read + 1 B code per element + 4 B per scale (the f16 "
+                                  "operand's 2 B per element not counted)"}
 
     lines = []
     lines.append(unit_line("c0 256^3", inputs.normal((256, 256), 1.0, 0).to(dev),
@@ -602,12 +738,11 @@ def run_configs(args):
                   "grouped_tops": round(ops / g_us / 1e6, 1), "separate_us": round(s_us, 1),
                   "separate_tops": round(ops / s_us / 1e6, 1)})
     del X, W, dY, trio
-    for n in (4096, 8192, 16384):
-        lines.append(unit_line(f"c4 {n}^3", inputs.uniform((n, n), -1, 1, 7).to(dev),
-                               inputs.uniform((n, n), -1, 1, 8).to(dev)))
+    for name, *_ in inputs.LARGE_GEMMS:
+        A, B, relu = inputs.large_gemm_inputs(name)
+        lines.append(unit_line("c4 " + name, A.to(dev), B.to(dev), relu))
+        del A, B
         torch.cuda.empty_cache()
-    lines.append(unit_line("c4 ragged", inputs.uniform((4097, 8191), -1, 1, 9).to(dev),
-                           inputs.uniform((8191, 12289), -1, 1, 10).to(dev)))
     lines.append(unit_line("c4 adversarial 4096^3", inputs.adversarial(4096, 4096, 11).to(dev),
                            inputs.adversarial(4096, 4096, 12, along_rows=False).to(dev)))
     torch.cuda.synchronize()
@@ -617,67 +752,92 @@ def run_configs(args):
 
 
 # -------------------------------------------------------------- CPU oracle
+PARTS = ("sq4096", "sq8192", "sq16384", "ragged_adversarial", "probe")
+CLOCK = time.perf_counter   # the oracle sample's clock (tests replace it)
+
+
 def oracle_inputs():
-    """The step's inputs for the oracle, generated once (the same seeded
-    tensors the GPU arm uses)."""
+    """The step's GEMM inputs for the oracle, generated once (the same seeded
+    tensors the GPU arm uses): {name: (A, B, relu)} as numpy arrays."""
     from verifiable_quantize_rows_gb300 import inputs
-    out = []
-    for name, M, N, K, relu, seed in inputs.GPT2_LINEARS:
-        A, B, _ = inputs.gpt2_linear_inputs(name)
-        out.append((A.numpy(), B.numpy(), relu))
+    out = {}
+    for name, *_ in inputs.LARGE_GEMMS:
+        A, B, relu = inputs.large_gemm_inputs(name)
+        out[name] = (A.numpy(), B.numpy(), relu)
     return out
 
 
-PARTS = ("qkv", "fc", "proj", "probe")
+class OracleSample:
+    """Part `part` of the step on the oracle, on a sub-block: the first r
+    rows of A and the first r columns of B (full K: every sampled output
+    cell is computed exactly as in the full GEMM, scales included), or, for
+    the probe, M = r rows (N = K = 1024, hash included)."""
 
+    def __init__(self, orc, data):
+        self.orc = orc
+        self.data = data
+        self.cache = {}
 
-def oracle_part(orc, data, part, rows):
-    """Part `part` of the step on the oracle: a GPT-2 linear on the first
-    `rows` rows of its A (full N, K), or (part 3) the probe with M = `rows`
-    (N = K = 1024, hash included).  Returns (ops, seconds)."""
-    if part < 3:
-        A, B, relu = data[part]
-        a = np.ascontiguousarray(A[:rows])
-        t0 = time.perf_counter()
-        orc.bsgemm_i8(a, B, relu)
-        return 2 * a.shape[0] * B.shape[1] * B.shape[0], time.perf_counter() - t0
-    t0 = time.perf_counter()
-    orc.probe_hash(PROBE_SEED, rows, PROBE[1], PROBE[2])
-    return 2 * rows * PROBE[1] * PROBE[2], time.perf_counter() - t0
+    def prepare(self, part, r):
+        name = PARTS[part]
+        if name == "probe" or (part, r) in self.cache:
+            return
+        A, B, relu = self.data[name]
+        rr, cc = min(r, A.shape[0]), min(r, B.shape[1])
+        self.cache[(part, r)] = (np.ascontiguousarray(A[:rr]), np.ascontiguousarray(B[:, :cc]),
+                                 relu)
 
+    def run(self, part, r):
+        """Returns (ops, seconds) of one oracle call."""
+        if PARTS[part] == "probe":
+            t0 = CLOCK()
+            self.orc.probe_hash(PROBE_SEED, r, PROBE[1], PROBE[2])
+            return 2 * r * PROBE[1] * PROBE[2], CLOCK() - t0
+        self.prepare(part, r)
+        a, b, relu = self.cache[(part, r)]
+        t0 = CLOCK()
+        self.orc.bsgemm_i8(a, b, relu)
+        return 2 * a.shape[0] * b.shape[1] * a.shape[1], CLOCK() - t0
 
-def sample_rows(orc, data, seconds):
-    """Rows per part for about `seconds` of oracle work each, scaled from a
-    256-row calibration run of every part."""
-    rows = []
-    for part in range(len(PARTS)):
-        _, t = oracle_part(orc, data, part, 256)
-        cap = 8192 if part < 3 else PROBE[0]
-        rows.append(max(8, int(min(cap, max(8, 256 * seconds / max(t, 1e-3)))) // 8 * 8))
-    return rows
+    def sizes(self, seconds):
+        """r per part for about `seconds` of oracle work each, scaled from a
+        64-row calibration call (work grows as r^2 for the GEMMs)."""
+        rows = []
+        for part, name in enumerate(PARTS):
+            _, t = self.run(part, 64)
+            if name == "probe":
+                r = int(64 * seconds / max(t, 1e-4))
+                cap = PROBE[0]
+            else:
+                r = int(64 * (seconds / max(t, 1e-4)) ** 0.5)
+                A, B, _ = self.data[name]
+                cap = max(A.shape[0], B.shape[1])
+            rows.append(max(8, min(cap, r)) // 8 * 8)
+        return rows
 
 
 def sample_text(rows):
-    return (f"qkv, fc, proj on their first {rows[0]}, {rows[1]}, {rows[2]} of 8192 rows "
-            f"(full N, K) and the probe at M = {rows[3]} of 1024 (N = K = 1024, hash included)")
+    parts = [f"{n} on a {r}x{r} block of C (first rows of A, first columns of B, full K)"
+             for n, r in zip(PARTS[:-1], rows[:-1])]
+    return "; ".join(parts) + f"; the probe at M = {rows[-1]} of 1024 (N = K = 1024, hash included)"
 
 
-def cpu_baseline(budget_s=12.0):
+def cpu_baseline(budget_s=15.0):
     import oracle
     orc = oracle.load()
-    data = oracle_inputs()
-    rows = sample_rows(orc, data, budget_s / len(PARTS))
-    # repeat the four parts until about budget_s of CPU work (when even the
-    # whole workload takes less)
+    smp = OracleSample(orc, oracle_inputs())
+    rows = smp.sizes(budget_s / len(PARTS))
+    for part in range(len(PARTS)):
+        smp.prepare(part, rows[part])
     total_ops, total_t, reps = 0, 0.0, 0
     while total_t < 0.8 * budget_s or reps == 0:
         for part in range(len(PARTS)):
-            ops, t = oracle_part(orc, data, part, rows[part])
+            ops, t = smp.run(part, rows[part])
             total_ops, total_t = total_ops + ops, total_t + t
         reps += 1
     return {"value": round(total_ops / total_t / 1e12, 6), "unit": "TOPS",
             "cores": orc.num_threads(), "kind": "oracle",
-            "sample": f"{sample_text(rows)}, {reps}x: {total_ops / 1e9:.1f} G ops in "
+            "sample": f"{sample_text(rows)}; {reps}x: {total_ops / 1e9:.1f} G ops in "
                       f"{total_t:.1f} s"}
 
 
@@ -686,22 +846,25 @@ def run_reference(args, rank, world):
         return None
     import oracle
     orc = oracle.load()
-    data = oracle_inputs()
+    smp = OracleSample(orc, oracle_inputs())
     # About two minutes of oracle work for the whole run, whatever K and W
-    # are: step i runs part i mod 4 of the workload (qkv, fc, proj, probe),
-    # each on a row sample sized to the per-step budget.
+    # are: step i runs part i mod 5 of the workload (the four GEMMs, the
+    # probe), each on a sample sized to the per-step budget.
     total_budget = 120.0
     per_step = min(10.0, total_budget / max(1, args.steps + args.warmup))
-    rows = sample_rows(orc, data, per_step)
+    rows = smp.sizes(per_step)
+    for part in range(len(PARTS)):
+        smp.prepare(part, rows[part])
+    n = len(PARTS)
     for i in range(args.warmup):
-        oracle_part(orc, data, i % len(PARTS), rows[i % len(PARTS)])
+        smp.run(i % n, rows[i % n])
     total_ops, total_t = 0, 0.0
     for i in range(args.steps):
-        ops, t = oracle_part(orc, data, i % len(PARTS), rows[i % len(PARTS)])
+        ops, t = smp.run(i % n, rows[i % n])
         total_ops, total_t = total_ops + ops, total_t + t
     value = total_ops / total_t / 1e12
     ms = total_t / max(1, args.steps) * 1e3
-    sample = (f"step i runs part i mod 4 of the step: {sample_text(rows)}; "
+    sample = (f"step i runs part i mod {n} of the step: {sample_text(rows)}; "
               f"{total_ops / 1e9:.2f} G ops in {total_t:.1f} s over {args.steps} steps")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TOPS",
@@ -718,12 +881,10 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--probe-overlap", type=int, default=1,
-                    help="1: the probe runs on a side stream alongside the linears")
     ap.add_argument("--configs", action="store_true",
                     help="time the unit on every workload of the measurement plan instead "
                          "(one JSON line each)")

@@ -203,6 +203,18 @@ bsg_status bsg_selftest_scales(uint32_t first_bits, uint32_t last_bits,
  * pages: it documents this library's schedule. */
 int bsg_gemm_tile_width(int64_t M, int64_t N, int sms);
 
+/* Measurement aid for the roofline: one launch that issues `iters` x 4 pair
+ * MMAs (tcgen05 cta_group::2, kind::f16, 256 x 256 x 16, fp32 accumulators)
+ * back to back on every SM pair that can be resident, from operand tiles
+ * that stay in shared memory -- the contraction's own instruction with no
+ * operand copies and no epilogue.  Its duration (timed by the caller with
+ * events on `stream`) gives the tensor pipe's ceiling for the GEMM at the
+ * clock it runs at.  *flops_host receives the floating-point operations of
+ * the launch (2 * 256 * 256 * 16 per MMA).  1 <= iters <= 2^18.  Asynchronous;
+ * BSG_DSTATUS_TIMEOUT if its bounded final wait expires.  No counterpart in
+ * the pages. */
+bsg_status bsg_mma_ceiling(int iters, int32_t *dstatus, double *flops_host, void *stream);
+
 /* Number of kernels this library has launched in this process (host-side
  * counter; every launch of every entry point counts). */
 uint64_t bsg_launch_count(void);

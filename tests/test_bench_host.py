@@ -35,10 +35,15 @@ def test_code_digest_sees_code_changes():
     assert bench.code_digest([CODE, CODE]) != base
 
 
-def test_profiled_traffic_matches_the_committed_summary():
-    per = bench.profiled_traffic()
-    assert per is not None, "the ncu summary's source digest differs from the GEMM source"
-    assert set(per) == {"qkv", "fc", "proj"}
+@pytest.mark.parametrize("profile,names", [
+    (bench.GEMM_PROFILE, {"sq4096", "sq8192", "sq16384", "ragged_adversarial"}),
+    (bench.SMALL_GEMM_PROFILE, {"qkv", "fc", "proj"})])
+def test_committed_ncu_summaries_parse(profile, names):
+    src, per = bench.parse_profile(profile)
+    if src is None:
+        pytest.skip(f"{profile} not committed")
+    assert len(src) == 16
+    assert set(per) == names
     assert all(isinstance(v, int) and v > 0 for v in per.values())
 
 
@@ -47,77 +52,106 @@ def test_profiled_traffic_is_none_for_another_source(monkeypatch):
     assert bench.profiled_traffic() is None
 
 
-class FakeOracle:
-    """Stands in for the oracle: each call 'takes' time proportional to its
-    rows, and counts the rows it was given."""
-
+class FakeClock:
     def __init__(self):
-        self.rows = []
+        self.t = 0.0
+
+    def __call__(self):
+        return self.t
+
+
+class FakeOracle:
+    """Stands in for the oracle: each call advances a fake clock in
+    proportion to its work and records the block it was given."""
+
+    def __init__(self, clock, per_mac=1e-9):
+        self.clock = clock
+        self.per_mac = per_mac
+        self.calls = []
 
     def num_threads(self):
         return 3
 
     def bsgemm_i8(self, a, b, relu):
-        self.rows.append(("gemm", a.shape[0]))
+        self.calls.append(("gemm", a.shape[0], b.shape[1]))
+        self.clock.t += a.shape[0] * b.shape[1] * a.shape[1] * self.per_mac
         return None, 0
 
     def probe_hash(self, seed, M, N, K):
-        self.rows.append(("probe", M))
+        self.calls.append(("probe", M, N))
+        self.clock.t += M * N * K * self.per_mac
         return b"\0" * 32, 0
 
 
 def small_data():
+    """Stand-ins with the step's shapes along M and N but K = 8."""
     rng = np.random.default_rng(0)
-    return [(rng.standard_normal((8192, 8), dtype=np.float32),
-             rng.standard_normal((8, 4), dtype=np.float32), False) for _ in range(3)]
+    out = {}
+    for name, M, N, K, relu, _ in bench.unit_list("large"):
+        out[name] = (rng.standard_normal((M, 8), dtype=np.float32),
+                     rng.standard_normal((8, N), dtype=np.float32), relu)
+    return out
 
 
-def fake_clock(monkeypatch, per_row):
-    """Each oracle part 'takes' per_row seconds for each row it processes."""
-    orig_part = bench.oracle_part
-
-    def part(orc, data, p, rows):
-        ops, _ = orig_part(orc, data, p, rows)
-        return ops, rows * per_row
-    monkeypatch.setattr(bench, "oracle_part", part)
+def fake(monkeypatch, per_mac=1e-9):
+    clock = FakeClock()
+    monkeypatch.setattr(bench, "CLOCK", clock)
+    return FakeOracle(clock, per_mac)
 
 
-def test_sample_rows_scale_to_the_budget(monkeypatch):
-    fake_clock(monkeypatch, per_row=1e-3)        # 256 rows take 0.256 s
-    orc = FakeOracle()
-    rows = bench.sample_rows(orc, small_data(), seconds=0.5)
-    assert rows[:3] == [496, 496, 496]           # 256 * 0.5 / 0.256, down to a multiple of 8
-    assert rows[3] == 496
-    rows = bench.sample_rows(orc, small_data(), seconds=100.0)
-    assert rows[:3] == [8192] * 3 and rows[3] == 1024   # capped at the full sizes
-    rows = bench.sample_rows(orc, small_data(), seconds=1e-6)
-    assert rows == [8, 8, 8, 8]                  # at least 8 rows
+def test_sample_sizes_scale_to_the_budget(monkeypatch):
+    orc = fake(monkeypatch, per_mac=1e-8)
+    smp = bench.OracleSample(orc, small_data())
+    # a 64 x 64 x 8 block takes 327.68 us: r grows as the square root of the budget
+    rows = smp.sizes(seconds=0.01)
+    assert rows[:4] == [352] * 4             # 64 * sqrt(0.01 / 327.68e-6), multiple of 8
+    rows = smp.sizes(seconds=100.0)
+    assert rows[:4] == [4096, 8192, 16384, 12289 // 8 * 8]   # capped at the larger side
+    assert rows[4] == 1024                   # the probe: at most all 1024 rows
+    rows = smp.sizes(seconds=1e-9)
+    assert rows == [8] * 5                   # at least 8
+
+
+def test_sample_blocks_take_leading_rows_and_columns(monkeypatch):
+    orc = fake(monkeypatch)
+    data = small_data()
+    smp = bench.OracleSample(orc, data)
+    ops, t = smp.run(3, 5000)                # ragged: M = 4097 caps the rows
+    assert orc.calls[-1] == ("gemm", 4097, 5000)
+    assert ops == 2 * 4097 * 5000 * 8 and t > 0
+    a, b, _ = smp.cache[(3, 5000)]
+    assert np.array_equal(a, data["ragged_adversarial"][0][:4097])
+    assert np.array_equal(b, data["ragged_adversarial"][1][:, :5000])
 
 
 def test_reference_arm_is_bounded_and_complete(monkeypatch):
     import oracle
-    fake = FakeOracle()
-    monkeypatch.setattr(oracle, "load", lambda: fake)
+    orc = fake(monkeypatch)
+    monkeypatch.setattr(oracle, "load", lambda: orc)
     monkeypatch.setattr(bench, "oracle_inputs", small_data)
-    fake_clock(monkeypatch, per_row=1e-3)
-    args = type("A", (), {"steps": 1000, "warmup": 5})()
+    args = type("A", (), {"steps": 100, "warmup": 5})()
     line = bench.run_reference(args, 0, 1)
     assert bench.run_reference(args, 1, 2) is None          # only rank 0 runs it
     json.dumps(line)
-    assert line["impl"] == "reference" and line["steps"] == 1000
+    assert line["impl"] == "reference" and line["steps"] == 100
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 3
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["value"] > 0 and line["higher_is_better"] is True
     # the whole run stays near its two-minute budget of (fake) oracle time
-    timed = sum(r for kind, r in fake.rows) * 1e-3
-    assert timed < 200.0
-    # step i ran part i mod 4: the probe every fourth step
-    probe_calls = sum(1 for kind, _ in fake.rows if kind == "probe")
-    assert 250 <= probe_calls <= 260
+    assert orc.clock.t < 200.0
+    # step i ran part i mod 5: the probe every fifth step (+ calibration)
+    probe_calls = sum(1 for c in orc.calls if c[0] == "probe")
+    assert 20 <= probe_calls <= 23
 
 
 def test_config_line_names_the_workload():
     cfg = bench.config_dict(1)
-    assert cfg["workload"].startswith("gpt2_small_linears_M8192")
+    assert cfg["workload"].startswith("large_gemms_4096^3+8192^3+16384^3+ragged")
     names = [g["name"] for g in cfg["gemms"]]
-    assert names == ["qkv", "fc", "proj", "probe"]
+    assert names == ["sq4096", "sq8192", "sq16384", "ragged_adversarial", "probe"]
+    small = bench.config_dict(1, "small")
+    assert [g["name"] for g in small["gemms"]] == ["qkv", "fc", "proj", "probe"]
+
+
+def test_quantize_bytes_count_codes_not_f16_operands():
+    assert bench.quant_algo_bytes(2, 3, 4) == 5 * (8 + 12) + 4 * 5

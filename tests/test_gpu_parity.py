@@ -166,19 +166,14 @@ def test_gpt2_linears_full(orc, name):
     assert_bits_equal(C, Co, name)
 
 
-def test_lm_head_sampled(orc):
+def test_lm_head_full(orc):
     _, M, N, K, relu, seed = inputs.LM_HEAD
     A = inputs.gpt2_activations(M, K, seed, outlier_frac=0.0).numpy()
     B = inputs.gpt2_weights(K, N, seed).numpy()
     C, st = gpu_unit(A, B, relu)
     assert st == 0
-    rows, cols = sample_cells(M, N, 20000, 4)
-    out, S, so = orc.bsgemm_cells(A, B, rows, cols, relu)
-    assert_bits_equal(C[rows, cols], out, "lm_head cells")
-    # whole row and whole column blocks at the tile edges
-    for r in (0, 127, 128, M - 1):
-        o, _, _ = orc.bsgemm_cells(A, B, np.full(N, r), np.arange(N), relu)
-        assert_bits_equal(C[r], o, f"lm_head row {r}")
+    Co, _ = orc.bsgemm_i8(A, B, relu)
+    assert_bits_equal(C, Co, "lm_head")
     assert np.isfinite(C).all()
 
 
@@ -201,29 +196,22 @@ def test_train_trio_full(orc, which):
     assert_bits_equal(C, Co, name)
 
 
-@pytest.mark.parametrize("n", [4096, 8192, 16384])
-def test_squares_sampled(orc, n):
-    seed = dict(inputs.SQUARES)[n]
-    A = inputs.uniform((n, n), -1, 1, seed).numpy()
-    B = inputs.uniform((n, n), -1, 1, seed + 1).numpy()
-    C, st = gpu_unit(A, B)
+@pytest.mark.parametrize("name", [g[0] for g in inputs.LARGE_GEMMS])
+def test_large_gemms_full(orc, name):
+    """The benchmark's GEMMs -- 4096^3, 8192^3, 16384^3 of U(-1, 1) values and
+    the ragged 4097 x 12289 x 8191 with the adversarial mixes -- compared with
+    the oracle over the whole of C, bit for bit."""
+    A, B, relu = inputs.large_gemm_inputs(name)
+    A, B = A.numpy(), B.numpy()
+    C, st = gpu_unit(A, B, relu)
     assert st == 0
-    rows, cols = sample_cells(n, n, 3000, n)
-    out, S, so = orc.bsgemm_cells(A, B, rows, cols)
-    assert_bits_equal(C[rows, cols], out, f"{n}^3 cells")
-
-
-def test_ragged_sampled_and_adversarial(orc):
-    M, N, K, seed = inputs.RAGGED
-    A = inputs.adversarial(M, K, seed).numpy()
-    B = inputs.adversarial(N, K, seed + 1, along_rows=False).numpy()
-    C, st = gpu_unit(A, B)
-    assert st == 0
-    rows, cols = sample_cells(M, N, 3000, 9)
-    out, S, so = orc.bsgemm_cells(A, B, rows, cols)
-    assert_bits_equal(C[rows, cols], out, "ragged cells")
-    o, _, _ = orc.bsgemm_cells(A, B, np.full(N, M - 1), np.arange(N))
-    assert_bits_equal(C[M - 1], o, "ragged last row")
+    Co, _ = orc.bsgemm_i8(A, B, relu)
+    assert_bits_equal(C, Co, name)
+    if name == "ragged_adversarial":
+        # the mix reaches what it is meant to: overflow to +-Inf from the 1e30
+        # vectors, exact zeros from the zero and 1e-30 ones
+        assert np.isposinf(C).any() and np.isneginf(C).any()
+        assert (u32(C) == 0).any()
 
 
 @pytest.mark.parametrize("shape", [(384, 512, 6400), (8192, 768, 3072), (1024, 1024, 1024),

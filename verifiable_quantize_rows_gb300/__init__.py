@@ -101,6 +101,7 @@ def _declare(lib):
         "bsgemm_i8_group": ([ctypes.POINTER(GemmItem), _i32, _vp, _vp], _i32),
         "bsg_wquant_cols": ([_vp, _i64, _i64, _i64, _i32, _i32, _vp, _i64, _vp, _vp, _vp], _i32),
         "bsg_wdequant_cols": ([_vp, _i64, _i64, _i64, _i32, _vp, _vp, _i64, _vp], _i32),
+        "bsg_mma_ceiling": ([_i32, _vp, ctypes.POINTER(ctypes.c_double), _vp], _i32),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -304,6 +305,15 @@ def selftest_scales(first_bits: int = 0, last_bits: int = 0x7F7FFFFF) -> int:
 def gemm_tile_width(M: int, N: int, sms: int) -> int:
     """Output tile width the GEMM kernel picks for an M x N problem."""
     return int(load().bsg_gemm_tile_width(M, N, sms))
+
+
+def mma_ceiling(iters: int, stream=None, dstatus=None) -> float:
+    """Launch the tensor-pipe ceiling kernel (asynchronous); returns the
+    floating-point operations that launch performs."""
+    flops = ctypes.c_double(0.0)
+    _check(load().bsg_mma_ceiling(int(iters), _ptr(dstatus), ctypes.byref(flops),
+                                  _stream_ptr(stream)), "bsg_mma_ceiling")
+    return float(flops.value)
 
 
 def launch_count() -> int:

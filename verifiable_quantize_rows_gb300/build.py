@@ -24,7 +24,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libbsgemm.so")
 
 SOURCES = ["bsgemm_api.cu", "quantize.cu", "gemm_tc.cu", "epilogue.cu", "probe.cu", "noalloc.cu",
-           "audit.cu", "wquant.cu"]
+           "audit.cu", "wquant.cu", "mma_ceiling.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fno-strict-aliasing", "-I", INCLUDE, "-I", CSRC]

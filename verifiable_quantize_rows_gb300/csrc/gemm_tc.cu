@@ -238,13 +238,34 @@ __device__ __forceinline__ void emit_box(const Prob &p, const CUtensorMap *tmap_
         }
         ++nstored;
     } else {
-        const int row = row0 + lane;
-        if (row < p.M) {
-            uint32_t *dst = static_cast<uint32_t *>(p.out) + (int64_t)row * p.ldo;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (col0 + j < p.N) dst[col0 + j] = v[j];
+        // C's rows are not 16-byte aligned (no TMA store): transpose the box
+        // through the first staging box, so that each store instruction
+        // writes 32 consecutive columns of one row (one 128-byte span)
+        // instead of one column of 32 rows.
+        if (nstored > 0) {  // a TMA store of an earlier GEMM of the launch may still read it
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+            nstored = 0;
         }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t off = lane * 128 + ((j ^ (lane & 7)) << 4);
+            *reinterpret_cast<uint4 *>(boxes + off) =
+                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
+        __syncwarp();
+        const int col = col0 + lane;
+        if (col < p.N) {
+            uint32_t *dst = static_cast<uint32_t *>(p.out) + (int64_t)row0 * p.ldo + col;
+            const uint32_t cw = (uint32_t)((lane >> 2) << 4) + (uint32_t)(lane & 3) * 4;
+#pragma unroll 8
+            for (int r = 0; r < 32; ++r) {
+                if (row0 + r >= p.M) break;
+                const uint32_t off = r * 128 + (cw ^ ((uint32_t)(r & 7) << 4));
+                __stcs(dst + (int64_t)r * p.ldo, *reinterpret_cast<const uint32_t *>(boxes + off));
+            }
+        }
+        __syncwarp();  // the box is read before the next piece overwrites it
     }
 }
 

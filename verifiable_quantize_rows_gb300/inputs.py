@@ -30,7 +30,8 @@ import torch
 
 __all__ = ["normal", "uniform", "gpt2_activations", "gpt2_weights", "tiny_shapes",
            "adversarial", "GPT2_LINEARS", "TRAIN_TRIO", "SQUARES", "RAGGED",
-           "LM_HEAD", "PROBE_SHAPE", "ADVERSARIAL_KINDS"]
+           "LM_HEAD", "PROBE_SHAPE", "ADVERSARIAL_KINDS", "LARGE_GEMMS",
+           "large_gemm_inputs", "gpt2_linear_inputs"]
 
 # (name, M, N, K, relu, seed)
 GPT2_LINEARS = [
@@ -180,3 +181,25 @@ def adversarial(rows: int, length: int, seed: int, frac: float = 1.0 / 3.0,
     for t, r in enumerate(picks):
         out[r] = _adversarial_vector(ADVERSARIAL_KINDS[t % len(ADVERSARIAL_KINDS)], length, g)
     return out if along_rows else out.t().contiguous()
+
+
+# The large and adversarial GEMMs, (name, M, N, K, relu, seed): squares of
+# U(-1, 1) values and the ragged shape with the adversarial mixes in A's rows
+# and B's columns.  A takes `seed`, B `seed + 1`.
+LARGE_GEMMS = [
+    ("sq4096", 4096, 4096, 4096, False, SQUARES[0][1]),
+    ("sq8192", 8192, 8192, 8192, False, SQUARES[1][1]),
+    ("sq16384", 16384, 16384, 16384, False, SQUARES[2][1]),
+    ("ragged_adversarial", RAGGED[0], RAGGED[1], RAGGED[2], False, RAGGED[3]),
+]
+
+
+def large_gemm_inputs(name: str):
+    """(A, B, relu) for one of LARGE_GEMMS."""
+    for nm, M, N, K, relu, seed in LARGE_GEMMS:
+        if nm == name:
+            if nm.startswith("sq"):
+                return uniform((M, K), -1, 1, seed), uniform((K, N), -1, 1, seed + 1), relu
+            return (adversarial(M, K, seed), adversarial(N, K, seed + 1, along_rows=False),
+                    relu)
+    raise KeyError(name)
