@@ -184,6 +184,43 @@ bsg_status bsgemm_i8_quantize(const float *A, int64_t lda, int transA, const flo
 bsg_status bsgemm_i8_contract(int64_t M, int64_t N, int64_t K, int relu, float *C, int64_t ldc,
                               void *workspace, size_t ws_bytes, int32_t *dstatus, void *stream);
 
+/* ---- chained units: the output quantized for the next unit ------------------ */
+
+/* The unit, plus C quantized per row as the next unit's A operand: the
+ * W8A8 chain of the presk "Precision" manual's closing list ("quantisation
+ * beyond weights": int8 activations, i32 accumulation, requantisation) and
+ * the B2B chain gate of "Layer 1: exact init gates", where one unit's output
+ * feeds the next.  C = bsgemm_i8(A, B, relu) (M x N f32, packed), and
+ *   Cq (M x N int8, packed), scale (M floats), inv (M floats, may be NULL)
+ * are exactly what bsg_quantize_rows(C) gives.  The GEMM's epilogue gathers
+ * each row's max |C| while C is still in registers (exact: a max of bit
+ * patterns, in any order), so C is quantized in one streaming pass with no
+ * reduction of its own.  A row of C that overflowed to +-Inf sets
+ * BSG_DSTATUS_NONFINITE; that row's codes and scale are then unspecified, as
+ * for any non-finite input of bsg_quantize_rows.  `workspace`:
+ * bsgemm_i8_requant_workspace_size(M, N, K) bytes, 256-byte aligned; the
+ * same second stream as bsgemm_i8 quantizes B. */
+size_t bsgemm_i8_requant_workspace_size(int64_t M, int64_t N, int64_t K);
+bsg_status bsgemm_i8_requant(const float *A, const float *B, int64_t M, int64_t N, int64_t K,
+                             int relu, float *C, int8_t *Cq, float *scale, float *inv,
+                             void *workspace, size_t ws_bytes, int32_t *dstatus, void *stream);
+
+/* Two units in a chain, the second fed by the first:
+ *   C1 = bsgemm_i8(A, B1, relu1)    A: M x K, B1: K x N1, C1: M x N1
+ *   C2 = bsgemm_i8(C1, B2, relu2)   B2: N1 x N2, C2: M x N2
+ * all packed row-major f32 in device memory; both C1 and C2 are written and
+ * each is bit for bit what the two bsgemm_i8 calls give.  C1 is quantized
+ * for the second unit straight from the row maxima its epilogue gathered
+ * (see bsgemm_i8_requant), into the second GEMM's operand, with no separate
+ * absmax pass over C1.  Pages: as bsgemm_i8_requant.  `workspace`:
+ * bsgemm_i8_chain_workspace_size(M, K, N1, N2) bytes, 256-byte aligned.
+ * Every launch goes to `stream` (no second stream). */
+size_t bsgemm_i8_chain_workspace_size(int64_t M, int64_t K, int64_t N1, int64_t N2);
+bsg_status bsgemm_i8_chain(const float *A, const float *B1, const float *B2, int64_t M,
+                           int64_t K, int64_t N1, int64_t N2, int relu1, int relu2, float *C1,
+                           float *C2, void *workspace, size_t ws_bytes, int32_t *dstatus,
+                           void *stream);
+
 /* Self-test of the scale derivation on the current device.  The kernels
  * derive scale and inv with IEEE f32 divides, which equal the f64 definition
  * for every input (the double rounding can never meet an f32 midpoint);

@@ -101,6 +101,12 @@ def _declare(lib):
         "bsgemm_i8_group": ([ctypes.POINTER(GemmItem), _i32, _vp, _vp], _i32),
         "bsg_wquant_cols": ([_vp, _i64, _i64, _i64, _i32, _i32, _vp, _i64, _vp, _vp, _vp], _i32),
         "bsg_wdequant_cols": ([_vp, _i64, _i64, _i64, _i32, _vp, _vp, _i64, _vp], _i32),
+        "bsgemm_i8_requant_workspace_size": ([_i64, _i64, _i64], _sz),
+        "bsgemm_i8_requant": ([_vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _sz,
+                               _vp, _vp], _i32),
+        "bsgemm_i8_chain_workspace_size": ([_i64, _i64, _i64, _i64], _sz),
+        "bsgemm_i8_chain": ([_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _i32, _vp, _vp, _vp,
+                             _sz, _vp, _vp], _i32),
         "bsg_mma_ceiling": ([_i32, _vp, ctypes.POINTER(ctypes.c_double), _vp], _i32),
     }
     for name, (args, res) in sigs.items():
@@ -272,6 +278,50 @@ def bsgemm_i8(A, B, relu: bool = False, out=None, stream=None, dstatus=None, wor
     _check(lib.bsgemm_i8(_ptr(A), _ptr(B), M, N, K, int(bool(relu)), _ptr(C), wp, wn,
                          _ptr(dstatus), _stream_ptr(stream)), "bsgemm_i8")
     return C
+
+
+def bsgemm_i8_requant(A, B, relu: bool = False, stream=None, dstatus=None, workspace=None):
+    """(C, Cq, scale, inv): the unit's C and C quantized per row (int8 codes,
+    row scales and reciprocals) for the next unit."""
+    torch = _torch()
+    _need(A, torch.float32, "A")
+    _need(B, torch.float32, "B")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    lib = load()
+    dev = A.device
+    C = torch.empty((M, N), dtype=torch.float32, device=dev)
+    Cq = torch.empty((M, N), dtype=torch.int8, device=dev)
+    scale = torch.empty(M, dtype=torch.float32, device=dev)
+    inv = torch.empty(M, dtype=torch.float32, device=dev)
+    wp, wn = _ws(workspace, lib.bsgemm_i8_requant_workspace_size(M, N, K))
+    _check(lib.bsgemm_i8_requant(_ptr(A), _ptr(B), M, N, K, int(bool(relu)), _ptr(C), _ptr(Cq),
+                                 _ptr(scale), _ptr(inv), wp, wn, _ptr(dstatus),
+                                 _stream_ptr(stream)), "bsgemm_i8_requant")
+    return C, Cq, scale, inv
+
+
+def bsgemm_i8_chain(A, B1, B2, relu1: bool = False, relu2: bool = False, out1=None, out2=None,
+                    stream=None, dstatus=None, workspace=None):
+    """(C1, C2) with C1 = bsgemm_i8(A, B1), C2 = bsgemm_i8(C1, B2)."""
+    torch = _torch()
+    for t, nm in ((A, "A"), (B1, "B1"), (B2, "B2")):
+        _need(t, torch.float32, nm)
+    M, K = A.shape
+    if B1.shape[0] != K or B2.shape[0] != B1.shape[1]:
+        raise ValueError("inner dimensions differ")
+    N1, N2 = B1.shape[1], B2.shape[1]
+    lib = load()
+    dev = A.device
+    C1 = out1 if out1 is not None else torch.empty((M, N1), dtype=torch.float32, device=dev)
+    C2 = out2 if out2 is not None else torch.empty((M, N2), dtype=torch.float32, device=dev)
+    wp, wn = _ws(workspace, lib.bsgemm_i8_chain_workspace_size(M, K, N1, N2))
+    _check(lib.bsgemm_i8_chain(_ptr(A), _ptr(B1), _ptr(B2), M, K, N1, N2, int(bool(relu1)),
+                               int(bool(relu2)), _ptr(C1), _ptr(C2), wp, wn, _ptr(dstatus),
+                               _stream_ptr(stream)), "bsgemm_i8_chain")
+    return C1, C2
 
 
 def bsgemm_i8_ex(A, B, transA: bool = False, transB: bool = False, relu: bool = False,

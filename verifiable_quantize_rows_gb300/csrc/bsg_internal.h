@@ -58,6 +58,13 @@ cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int
                                  int out_kind, void *Q, int64_t ldq, float *scale, float *inv,
                                  uint32_t *partial, int32_t *dstatus, cudaStream_t st);
 
+// Rows of X quantized with absmax bit patterns given per row (rowmax[r]):
+// scale / inv as in launch_quantize_rows (either may be NULL), codes as int8
+// (Q rows x cols, ldq) or f16 (the GEMM's K-major operand layout).
+cudaError_t launch_requant_rows(const float *X, int64_t rows, int64_t cols, int64_t ldx,
+                                const uint32_t *rowmax, int out_kind, void *Q, int64_t ldq,
+                                float *scale, float *inv, int32_t *dstatus, cudaStream_t st);
+
 // Both operands of the unit in one launch: A (M x K, lda) per row into Aop
 // (M x ldk f16) and sa, B (K x N, ldb) per column into Bop (N x ldk f16,
 // transposed) and sb.  cudaErrorNotSupported (nothing launched) when the
@@ -112,6 +119,10 @@ struct GemmJob {
     int relu;
     void *out;
     int64_t ldo;
+    // f32 mode only, may be NULL: per row of C, the running maximum of |C|
+    // bit patterns (stored columns only), combined by atomicMax; must hold
+    // M uint32 set to zero before the launch.
+    uint32_t *rowmax = nullptr;
 };
 // Up to 3 GEMMs in one launch: their tiles form one list that the launch's
 // CTAs share (one tail instead of three).  Same mode, status word and tile

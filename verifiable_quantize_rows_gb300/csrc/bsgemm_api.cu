@@ -810,3 +810,124 @@ bsg_status bsg_wdequant_cols(const void *Q, int64_t K, int64_t N, int64_t ldq, i
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------ chained units
+// The epilogue of one unit also gathers, per row of C, the maximum of |C|
+// (bit patterns, combined by atomicMax: exact in any order), so that C's
+// per-row quantize for the next unit needs no reduction pass of its own.
+namespace bsg {
+namespace {
+
+// rowmax (uint32 [M]) after the unit workspace of (M, N, K).
+size_t requant_layout(int64_t M, int64_t N, int64_t K, size_t *rowmax_off) {
+    const size_t unit_bytes = unit_layout(M, N, K, 0, 0).total;
+    *rowmax_off = unit_bytes;
+    return unit_bytes + align256((size_t)M * 4);
+}
+
+// Unit (M, N, K) from its quantized workspace into C, with the row maxima of
+// |C| gathered into rowmax (zeroed here first).
+bsg_status contract_with_rowmax(int64_t M, int64_t N, int64_t K, int relu, float *C,
+                                void *ws, uint32_t *rowmax, int32_t *dstatus, cudaStream_t st) {
+    const UnitLayout L = unit_layout(M, N, K, 0, 0);
+    if (cudaMemsetAsync(rowmax, 0, (size_t)M * 4, st) != cudaSuccess) return BSG_ERR_CUDA;
+    GemmJob j;
+    j.Aop = at<__half>(ws, L.aop);
+    j.Bop = at<__half>(ws, L.bop);
+    j.M = M;
+    j.N = N;
+    j.K = K;
+    j.sa = at<float>(ws, L.sa);
+    j.sb = at<float>(ws, L.sb);
+    j.relu = relu;
+    j.out = C;
+    j.ldo = N;
+    j.rowmax = rowmax;
+    return from_cuda(launch_gemm_tc_group(&j, 1, 0, dstatus, at<unsigned int>(ws, L.ticket), st));
+}
+
+}  // namespace
+}  // namespace bsg
+
+extern "C" {
+
+size_t bsgemm_i8_requant_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (!dims_ok(M, N, K)) return 0;
+    size_t off = 0;
+    return requant_layout(M, N, K, &off);
+}
+
+bsg_status bsgemm_i8_requant(const float *A, const float *B, int64_t M, int64_t N, int64_t K,
+                             int relu, float *C, int8_t *Cq, float *scale, float *inv,
+                             void *workspace, size_t ws_bytes, int32_t *dstatus, void *stream) {
+    if (!C || !Cq || !scale) return BSG_ERR_ARG;
+    bsg_status s = check_unit_args(A, K, 0, B, N, 0, M, N, K);
+    if (s != BSG_OK) return s;
+    size_t rm_off = 0;
+    if (!ws_ok(workspace, ws_bytes, requant_layout(M, N, K, &rm_off))) return BSG_ERR_WORKSPACE;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    s = unit_quantize(A, K, 0, B, N, 0, M, N, K, workspace, ws_bytes, dstatus, st);
+    if (s != BSG_OK) return s;
+    uint32_t *rowmax = at<uint32_t>(workspace, rm_off);
+    s = contract_with_rowmax(M, N, K, relu, C, workspace, rowmax, dstatus, st);
+    if (s != BSG_OK) return s;
+    return from_cuda(
+        launch_requant_rows(C, M, N, N, rowmax, kOutInt8, Cq, N, scale, inv, dstatus, st));
+}
+
+// Layer 1 (M, N1, K) in front, layer 2 (M, N2, N1) after it, then the row
+// maxima of C1.
+static size_t chain_layout(int64_t M, int64_t K, int64_t N1, int64_t N2, size_t *ws2_off,
+                           size_t *rowmax_off) {
+    const size_t u1 = align256(unit_layout(M, N1, K, 0, 0).total);
+    *ws2_off = u1;
+    const size_t u2 = align256(unit_layout(M, N2, N1, 0, 0).total);
+    *rowmax_off = u1 + u2;
+    return u1 + u2 + align256((size_t)M * 4);
+}
+
+size_t bsgemm_i8_chain_workspace_size(int64_t M, int64_t K, int64_t N1, int64_t N2) {
+    if (!dims_ok(M, N1, K) || !dims_ok(M, N2, N1)) return 0;
+    size_t a = 0, b = 0;
+    return chain_layout(M, K, N1, N2, &a, &b);
+}
+
+bsg_status bsgemm_i8_chain(const float *A, const float *B1, const float *B2, int64_t M,
+                           int64_t K, int64_t N1, int64_t N2, int relu1, int relu2, float *C1,
+                           float *C2, void *workspace, size_t ws_bytes, int32_t *dstatus,
+                           void *stream) {
+    if (!C1 || !C2 || !B2) return BSG_ERR_ARG;
+    bsg_status s = check_unit_args(A, K, 0, B1, N1, 0, M, N1, K);
+    if (s != BSG_OK) return s;
+    s = check_unit_args(C1, N1, 0, B2, N2, 0, M, N2, N1);
+    if (s != BSG_OK) return s;
+    size_t ws2_off = 0, rm_off = 0;
+    if (!ws_ok(workspace, ws_bytes, chain_layout(M, K, N1, N2, &ws2_off, &rm_off)))
+        return BSG_ERR_WORKSPACE;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void *ws1 = workspace;
+    void *ws2 = static_cast<uint8_t *>(workspace) + ws2_off;
+    uint32_t *rowmax = at<uint32_t>(workspace, rm_off);
+    const UnitLayout L2 = unit_layout(M, N2, N1, 0, 0);
+    // layer 1's operands; layer 2's weights per column
+    s = unit_quantize(A, K, 0, B1, N1, 0, M, N1, K, ws1, ws2_off, dstatus, st);
+    if (s != BSG_OK) return s;
+    if (launch_quantize_cols(B2, N1, N2, N2, kOutHalfKMajor, at<__half>(ws2, L2.bop),
+                             operand_ld(N1), at<float>(ws2, L2.sb), nullptr,
+                             at<uint32_t>(ws2, L2.part_b), dstatus, st) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    // layer 1, gathering C1's row maxima
+    s = contract_with_rowmax(M, N1, K, relu1, C1, ws1, rowmax, dstatus, st);
+    if (s != BSG_OK) return s;
+    // C1 per row, straight into layer 2's f16 operand and row scales; the
+    // tile counter of layer 2 (zeroed by a row quantize launch elsewhere)
+    if (launch_requant_rows(C1, M, N1, N1, rowmax, kOutHalfKMajor, at<__half>(ws2, L2.aop),
+                            operand_ld(N1), at<float>(ws2, L2.sa), nullptr, dstatus,
+                            st) != cudaSuccess ||
+        cudaMemsetAsync(at<unsigned int>(ws2, L2.ticket), 0, 2 * sizeof(unsigned int), st) !=
+            cudaSuccess)
+        return BSG_ERR_CUDA;
+    return unit_contract(M, N2, N1, relu2, C2, N2, ws2, L2.total, dstatus, st);
+}
+
+}  // extern "C"

@@ -124,6 +124,7 @@ struct Prob {
     int64_t ldo;
     int relu;
     int tma_store;  // 1: C's rows are 16-byte aligned; store through its tensor map
+    uint32_t *rowmax;  // NULL, or per row the max of |C| bit patterns (atomicMax)
 };
 
 template <int NP>  // GEMMs the launch was compiled for (1, or kMaxGroup)
@@ -643,6 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // ---- final epilogue of the tile from the sums
             if (!rows_here) continue;
+            uint32_t rmax = 0;  // this thread's row: max |C| bits over its stored columns
 #pragma unroll
             for (int piece = 0; piece < K::kPieces; ++piece) {
                 uint32_t(&v)[32] = *reinterpret_cast<uint32_t(*)[32]>(&acc[piece * 32]);
@@ -653,9 +655,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         epi_piece<true>(v, bl[piece], a, pr.relu);
                     else
                         epi_piece<false>(v, bl[piece], a, pr.relu);
+                    if (pr.rowmax) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < pr.N) rmax = max(rmax, v[j] & 0x7fffffffu);
+                    }
                 }
                 emit_box<K::kBoxes>(pr, &maps.c[pi], boxes, v, row0, col0, lane, nstored);
             }
+            // exact in any order: the max of non-negative bit patterns
+            if (pr.rowmax && row0 + lane < pr.M) atomicMax(pr.rowmax + row0 + lane, rmax);
         }
         if (lane == 0) bulk_wait0();
         __syncwarp();
@@ -868,6 +877,7 @@ cudaError_t launch_group_np(const GemmJob *jobs, int n, int mode, int32_t *dstat
         q.out = j.out;
         q.ldo = j.ldo;
         q.relu = j.relu;
+        q.rowmax = mode == 0 ? j.rowmax : nullptr;
         Ms[i] = j.M;
         Ns[i] = j.N;
         max_m = q.num_m > max_m ? q.num_m : max_m;

@@ -1176,4 +1176,85 @@ cudaError_t launch_i8_cols_to_half(const int8_t *Q, int64_t rows, int64_t cols, 
     return cudaGetLastError();
 }
 
+namespace {
+
+// Rows whose absmax is already known (the per-row maxima of |C| that the
+// GEMM's epilogue gathered): no reduction is left, so each 256-thread block
+// quantizes one 2048-column segment of one row in a single streaming pass,
+// 4 bytes read and 1 (int8) or 2 (f16 operand) written per element, for any
+// row length.  VEC: 16-byte loads of X and 4/8-byte stores of Q.
+constexpr int kRqThreads = 256;
+constexpr int kRqSeg = kRqThreads * 8;  // columns per block
+
+template <int OUT, bool VEC>
+__global__ void __launch_bounds__(kRqThreads)
+    requant_rows_kernel(const float *__restrict__ X, int64_t rows, int64_t cols, int64_t ldx,
+                        const uint32_t *__restrict__ rowmax, void *__restrict__ Q, int64_t ldq,
+                        float *__restrict__ scale, float *__restrict__ inv,
+                        int32_t *__restrict__ dstatus) {
+    const int64_t nseg = (cols + kRqSeg - 1) / kRqSeg;
+    for (int64_t b = blockIdx.x; b < rows * nseg; b += gridDim.x) {
+        const int64_t r = b / nseg;
+        const int64_t seg = b - r * nseg;
+        const uint32_t m = __ldg(rowmax + r);
+        float s, iv;
+        scale_from_max(m, s, iv);
+        if (seg == 0 && threadIdx.x == 0) {
+            if (scale) scale[r] = s;
+            if (inv) inv[r] = iv;
+            if (m >= kNonfiniteBits && dstatus) atomicOr(dstatus, 1);
+        }
+        const float *xr = X + r * ldx;
+        const int64_t qrow = r * ldq;
+        if (VEC) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t c = seg * kRqSeg + 4 * (threadIdx.x + h * kRqThreads);
+                if (c < cols) {  // cols % 4 == 0 here
+                    const float4 x = __ldg(reinterpret_cast<const float4 *>(xr + c));
+                    store4<OUT>(Q, qrow + c, quant(x.x, iv), quant(x.y, iv), quant(x.z, iv),
+                                quant(x.w, iv));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int64_t c = seg * kRqSeg + threadIdx.x + i * kRqThreads;
+                if (c < cols) store1<OUT>(Q, qrow + c, quant(__ldg(xr + c), iv));
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_requant_rows(const float *X, int64_t rows, int64_t cols, int64_t ldx,
+                                const uint32_t *rowmax, int out_kind, void *Q, int64_t ldq,
+                                float *scale, float *inv, int32_t *dstatus, cudaStream_t st) {
+    const size_t qsz = out_kind == kOutInt8 ? 1 : 2;
+    const bool vec = cols % 4 == 0 && ldx % 4 == 0 && ldq % 4 == 0 &&
+                     reinterpret_cast<uintptr_t>(X) % 16 == 0 &&
+                     reinterpret_cast<uintptr_t>(Q) % (4 * qsz) == 0;
+    const int64_t blocks = rows * ((cols + kRqSeg - 1) / kRqSeg);
+    const int grid = (int)(blocks < (int64_t)device_sm_count() * 16 ? blocks
+                                                                     : (int64_t)device_sm_count() * 16);
+    if (out_kind == kOutInt8) {
+        if (vec)
+            requant_rows_kernel<kOutInt8, true><<<grid, kRqThreads, 0, st>>>(
+                X, rows, cols, ldx, rowmax, Q, ldq, scale, inv, dstatus);
+        else
+            requant_rows_kernel<kOutInt8, false><<<grid, kRqThreads, 0, st>>>(
+                X, rows, cols, ldx, rowmax, Q, ldq, scale, inv, dstatus);
+    } else {
+        if (vec)
+            requant_rows_kernel<kOutHalfKMajor, true><<<grid, kRqThreads, 0, st>>>(
+                X, rows, cols, ldx, rowmax, Q, ldq, scale, inv, dstatus);
+        else
+            requant_rows_kernel<kOutHalfKMajor, false><<<grid, kRqThreads, 0, st>>>(
+                X, rows, cols, ldx, rowmax, Q, ldq, scale, inv, dstatus);
+    }
+    count_launches(1);
+    return cudaGetLastError();
+}
+
 }  // namespace bsg
