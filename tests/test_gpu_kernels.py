@@ -99,3 +99,40 @@ def test_long_columns_transposed_a(orc):
     torch.cuda.synchronize()
     Co, _ = orc.bsgemm_i8(np.ascontiguousarray(At.T), B, False)
     assert_bits_equal(host(C), Co, "transA K=6000")
+
+
+COL_SHAPES = [(64, 300, 4097), (130, 129, 5000), (40, 257, 8191), (33, 1000, 9000),
+              (24, 96, 16384), (50, 77, 1000), (3, 5, 7)]
+
+
+@pytest.mark.parametrize("path", ["strip", "twopass", ""])
+@pytest.mark.parametrize("M,N,K", COL_SHAPES, ids=lambda v: str(v))
+def test_every_column_quantize_path_operand(orc, monkeypatch, path, M, N, K):
+    """Each column-quantize path (register strips in clusters, two passes)
+    forced in turn into the GEMM's f16 operand, on columns with the
+    adversarial kinds, short, long, odd and ragged: C bitwise equal to the
+    oracle's.  Strips do not apply beyond 4096 rows; those shapes take two
+    passes whatever is asked."""
+    monkeypatch.setenv("BSG_COLS_PATH", path)
+    A = inputs.normal((M, K), 1.0, M + K).numpy()
+    B = inputs.adversarial(N, K, N + K + 1, along_rows=False).numpy()
+    C = bsg.bsgemm_i8(dev(A), dev(B))
+    torch.cuda.synchronize()
+    Co, _ = orc.bsgemm_i8(A, B, False)
+    assert_bits_equal(host(C), Co, f"{path}/{width} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("path", ["twopass", ""])
+@pytest.mark.parametrize("R,Ncol", [(5000, 129), (4100, 33), (3000, 40), (300, 17), (7, 3)],
+                         ids=lambda v: str(v))
+def test_every_column_quantize_path_int8(orc, monkeypatch, path, R, Ncol):
+    """The int8 column quantize (codes in X's layout, scales and inv) on
+    every path (clusters up to 3072 rows unless two passes are forced),
+    against the oracle, bitwise."""
+    monkeypatch.setenv("BSG_COLS_PATH", path)
+    X = inputs.adversarial(Ncol, R, R + Ncol, along_rows=False).numpy()
+    Q, sc, iv = bsg.quantize_cols(dev(X))
+    Qo, sco, ivo, _ = orc.quantize_cols(X)
+    assert_bits_equal(host(Q), Qo, "Q")
+    assert_bits_equal(host(sc), sco, "scale")
+    assert_bits_equal(host(iv), ivo, "inv")

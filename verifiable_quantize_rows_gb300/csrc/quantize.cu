@@ -20,6 +20,7 @@
 #include <cooperative_groups.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "bsg_internal.h"
@@ -1072,12 +1073,24 @@ cudaError_t launch_quantize_ab(const float *A, int64_t M, int64_t K, int64_t lda
     return e;
 }
 
+// Column quantize path: BSG_COLS_PATH=strip|twopass forces one (strips only
+// where their layout conditions hold; results are the same), for the tests;
+// read on every call.  0 = no preference.
+static int forced_cols_path() {
+    const char *e = getenv("BSG_COLS_PATH");
+    if (!e) return 0;
+    if (!strcmp(e, "strip")) return 1;
+    if (!strcmp(e, "twopass")) return 3;
+    return 0;
+}
+
 cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int64_t ldx,
                                  int out_kind, void *Q, int64_t ldq, float *scale, float *inv,
                                  uint32_t *partial, int32_t *dstatus, cudaStream_t st) {
     int cs = 0, R = 0;
+    const int forced = forced_cols_path();
     // the GEMM's transposed f16 operand, no inv wanted, 16-byte rows: strip CTAs
-    if (out_kind == kOutHalfKMajor && !inv && ldx % 4 == 0 &&
+    if (forced != 3 && out_kind == kOutHalfKMajor && !inv && ldx % 4 == 0 &&
         reinterpret_cast<uintptr_t>(X) % 16 == 0 && ldq % 2 == 0 &&
         reinterpret_cast<uintptr_t>(Q) % 4 == 0 && strip_shape(rows, 16, cs, R)) {
         static bool ready[64] = {false};
@@ -1108,7 +1121,8 @@ cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int
     // up to ~200 KB of shared memory, one per SM.  The GEMM's f16 operand past
     // the strip kernel's rows always takes two passes, the second through the
     // conflict-free transposing tile.
-    if (out_kind != kOutHalfKMajor && rows <= 3072 && cols_cluster_shape(rows, cols, cs, R)) {
+    if (forced != 3 && out_kind != kOutHalfKMajor && rows <= 3072 &&
+        cols_cluster_shape(rows, cols, cs, R)) {
         cudaError_t e = out_kind == kOutInt8
                             ? launch_cols_cluster<kOutInt8>(X, rows, cols, ldx, cs, R, Q, ldq, scale,
                                                             inv, dstatus, st)
