@@ -881,6 +881,61 @@ def run_reference(args, rank, world):
     }
 
 
+# -------------------------------------------------------------- single workloads
+def run_single(args):
+    """`--only small`: the GPT-2 linears step alone; `--unit M,N,K[,relu]`:
+    one bsgemm_i8 of U(-1, 1) inputs, called --steps times after --warmup
+    (CUDA events, L2 flushed before each call).  One JSON line; used to run
+    small cases under a profiler."""
+    import torch
+    import verifiable_quantize_rows_gb300 as bsg
+    from verifiable_quantize_rows_gb300 import build as bsg_build
+    from verifiable_quantize_rows_gb300 import inputs
+    if not os.path.exists(bsg.LIB_PATH):
+        bsg_build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    lib = bsg.load()
+    dstatus = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    if args.only == "small":
+        side = torch.cuda.Stream(device=dev)
+        pws = bsg.Workspace(dev)
+        pws.get(lib.bsg_probe_workspace_size(*PROBE))
+        probe_out = torch.empty(32, dtype=torch.uint8, device=dev)
+        W = Workload("small", dev, lib, side, dstatus, probe_out, pws, with_host=False)
+        step_ms, stage_ms, launches = time_workload(W, args.steps, args.warmup, flush, stream,
+                                                    lambda: None, stage_steps=3)
+        ms = statistics.mean(step_ms)
+        return {"workload": SMALL_WORKLOAD, "ms_per_step": round(ms, 4),
+                "value": round(step_ops("small") / (ms * 1e-3) / 1e12, 3), "unit": "TOPS",
+                "gpu_launches": launches, "device_status": int(dstatus.item())}
+    parts = [int(v) for v in args.unit.split(",")]
+    M, N, K = parts[:3]
+    relu = bool(parts[3]) if len(parts) > 3 else False
+    A = inputs.uniform((M, K), -1, 1, 1).to(dev)
+    B = inputs.uniform((K, N), -1, 1, 2).to(dev)
+    C = torch.empty(M, N, device=dev)
+    ws = bsg.Workspace(dev)
+    ws.get(lib.bsgemm_i8_workspace_size(M, N, K))
+    for _ in range(args.warmup):
+        bsg.bsgemm_i8(A, B, relu=relu, out=C, dstatus=dstatus, workspace=ws)
+    ts = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        bsg.bsgemm_i8(A, B, relu=relu, out=C, dstatus=dstatus, workspace=ws)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = statistics.median(ts)
+    return {"unit": f"{M}x{N}x{K}", "relu": relu, "ms": round(ms, 4),
+            "tops": round(2 * M * N * K / (ms * 1e-3) / 1e12, 2),
+            "device_status": int(dstatus.item())}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -888,6 +943,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["small"], default=None,
+                    help="run the GPT-2 linears step alone (one JSON line)")
+    ap.add_argument("--unit", default=None, metavar="M,N,K[,relu]",
+                    help="time one bsgemm_i8 of this shape instead (one JSON line)")
     ap.add_argument("--configs", action="store_true",
                     help="time the unit on every workload of the measurement plan instead "
                          "(one JSON line each)")
@@ -898,6 +957,10 @@ def main():
     world = env_int("WORLD_SIZE", 1)
     rank = env_int("RANK", 0)
     local_rank = env_int("LOCAL_RANK", 0)
+
+    if args.only or args.unit:
+        print(json.dumps(run_single(args)), flush=True)
+        return
 
     if args.configs:
         for line in run_configs(args):

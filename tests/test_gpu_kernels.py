@@ -136,3 +136,18 @@ def test_every_column_quantize_path_int8(orc, monkeypatch, path, R, Ncol):
     assert_bits_equal(host(Q), Qo, "Q")
     assert_bits_equal(host(sc), sco, "scale")
     assert_bits_equal(host(iv), ivo, "inv")
+
+
+@pytest.mark.parametrize("group", [1, 3, 8, 64])
+def test_tile_raster_does_not_change_results(orc, monkeypatch, group):
+    """The order in which tiles are handed out (BSG_GEMM_GROUP m-units per
+    raster group) changes which CTA computes which tile and when, never a
+    bit of C."""
+    monkeypatch.setenv("BSG_GEMM_GROUP", str(group))
+    M, N, K = 1300, 1100, 2100
+    A = inputs.normal((M, K), 1.0, 31).numpy()
+    B = inputs.normal((K, N), 0.1, 32).numpy()
+    C = bsg.bsgemm_i8(dev(A), dev(B), relu=True)
+    torch.cuda.synchronize()
+    Co, _ = orc.bsgemm_i8(A, B, True)
+    assert_bits_equal(host(C), Co, f"group {group}")
