@@ -730,6 +730,29 @@ def run_configs(args):
                                               workspace=pws))
     lines.append({"config": "c2 probe 1024^3 (fill, unit, hash)", "unit_us": round(p_us, 2),
                   "unit_tops": round(2 * 1024 ** 3 / p_us / 1e6, 1)})
+    # the chained units: the GPT-2 MLP (fc + ReLU, then proj) as one chain
+    # against two units, and one unit + its C's per-row codes against a unit
+    # then a row quantize of C
+    Xm = inputs.gpt2_activations(8192, 768, 2).to(dev)
+    W1 = inputs.gpt2_weights(768, 3072, 2).to(dev)
+    W2 = inputs.gpt2_weights(3072, 768, 3).to(dev)
+    cws, uws1, uws2 = bsg.Workspace(dev), bsg.Workspace(dev), bsg.Workspace(dev)
+    C1 = torch.empty(8192, 3072, device=dev)
+    C2 = torch.empty(8192, 768, device=dev)
+    ch_us = timed(lambda: bsg.bsgemm_i8_chain(Xm, W1, W2, True, False, out1=C1, out2=C2,
+                                              dstatus=dstatus, workspace=cws))
+    two_us = timed(lambda: bsg.bsgemm_i8(bsg.bsgemm_i8(Xm, W1, relu=True, out=C1, dstatus=dstatus,
+                                                       workspace=uws1),
+                                         W2, out=C2, dstatus=dstatus, workspace=uws2))
+    rq_us = timed(lambda: bsg.bsgemm_i8_requant(Xm, W1, relu=True, dstatus=dstatus,
+                                                workspace=cws))
+    uq_us = timed(lambda: bsg.quantize_rows(bsg.bsgemm_i8(Xm, W1, relu=True, out=C1,
+                                                          dstatus=dstatus, workspace=uws1),
+                                            dstatus=dstatus))
+    lines.append({"config": "f1 gpt2 mlp chain 8192x768 -> 3072 (ReLU) -> 768",
+                  "chain_us": round(ch_us, 1), "two_units_us": round(two_us, 1),
+                  "requant_us": round(rq_us, 1), "unit_then_quantize_rows_us": round(uq_us, 1)})
+    del Xm, W1, W2, C1, C2, cws, uws1, uws2
     X, W, dY = (t.to(dev) for t in inputs.train_trio())
     trio = [(X, W, False, False, False), (dY, W, False, True, False), (X, dY, True, False, False)]
     gws = bsg.Workspace(dev)

@@ -214,7 +214,8 @@ bsg_status bsgemm_i8_requant(const float *A, const float *B, int64_t M, int64_t 
  * (see bsgemm_i8_requant), into the second GEMM's operand, with no separate
  * absmax pass over C1.  Pages: as bsgemm_i8_requant.  `workspace`:
  * bsgemm_i8_chain_workspace_size(M, K, N1, N2) bytes, 256-byte aligned.
- * Every launch goes to `stream` (no second stream). */
+ * B2 is quantized on the same second stream as bsgemm_i8 uses, beside the
+ * first unit, and joined back into `stream` before the second GEMM. */
 size_t bsgemm_i8_chain_workspace_size(int64_t M, int64_t K, int64_t N1, int64_t N2);
 bsg_status bsgemm_i8_chain(const float *A, const float *B1, const float *B2, int64_t M,
                            int64_t K, int64_t N1, int64_t N2, int relu1, int relu2, float *C1,

@@ -41,11 +41,12 @@ int device_sm_count();
 // Host-side count of kernel launches made by this library.
 void count_launches(int n);
 
-// zero2 (may be NULL): two words zeroed by the launch (a GEMM tile counter).
+// zero2 (may be NULL): two words zeroed by the launch (a GEMM tile counter);
+// zrows (may be NULL): one word per row zeroed (row maxima a GEMM gathers).
 cudaError_t launch_quantize_rows(const float *X, int64_t rows, int64_t cols, int64_t ldx,
                                  int out_kind, void *Q, int64_t ldq, float *scale, float *inv,
                                  int32_t *dstatus, cudaStream_t st,
-                                 unsigned int *zero2 = nullptr);
+                                 unsigned int *zero2 = nullptr, unsigned int *zrows = nullptr);
 
 // Bytes of the unit workspace for one operand layout (transA / transB as in
 // bsgemm_i8_ex); bsgemm_i8_workspace_size is the largest over the layouts.
@@ -60,10 +61,12 @@ cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int
 
 // Rows of X quantized with absmax bit patterns given per row (rowmax[r]):
 // scale / inv as in launch_quantize_rows (either may be NULL), codes as int8
-// (Q rows x cols, ldq) or f16 (the GEMM's K-major operand layout).
+// (Q rows x cols, ldq) or f16 (the GEMM's K-major operand layout); zero2 as
+// in launch_quantize_rows.  Launched programmatically after the GEMM.
 cudaError_t launch_requant_rows(const float *X, int64_t rows, int64_t cols, int64_t ldx,
                                 const uint32_t *rowmax, int out_kind, void *Q, int64_t ldq,
-                                float *scale, float *inv, int32_t *dstatus, cudaStream_t st);
+                                float *scale, float *inv, int32_t *dstatus, cudaStream_t st,
+                                unsigned int *zero2 = nullptr);
 
 // Both operands of the unit in one launch: A (M x K, lda) per row into Aop
 // (M x ldk f16) and sa, B (K x N, ldb) per column into Bop (N x ldk f16,
@@ -72,7 +75,8 @@ cudaError_t launch_requant_rows(const float *X, int64_t rows, int64_t cols, int6
 cudaError_t launch_quantize_ab(const float *A, int64_t M, int64_t K, int64_t lda,
                                const float *B, int64_t N, int64_t ldb, __half *Aop,
                                __half *Bop, int64_t ldk, float *sa, float *sb,
-                               int32_t *dstatus, unsigned int *zero2, cudaStream_t st);
+                               int32_t *dstatus, unsigned int *zero2, cudaStream_t st,
+                               unsigned int *zrows = nullptr);
 
 // The live audit: `nsamples` seeded cells of C recomputed on the CUDA cores
 // from the f32 inputs; mismatching cells are counted into *mismatches.

@@ -151,7 +151,8 @@ SideStream *side_stream() {
 // side stream at the same time as op(A).
 bsg_status unit_quantize(const float *A, int64_t lda, int transA, const float *B, int64_t ldb,
                          int transB, int64_t M, int64_t N, int64_t K, void *ws, size_t ws_bytes,
-                         int32_t *dstatus, cudaStream_t st, bool overlap = true) {
+                         int32_t *dstatus, cudaStream_t st, bool overlap = true,
+                         unsigned int *zrows = nullptr) {
     bsg_status s = check_unit_args(A, lda, transA, B, ldb, transB, M, N, K);
     if (s != BSG_OK) return s;
     const UnitLayout L = unit_layout(M, N, K, transA, transB);
@@ -171,10 +172,15 @@ bsg_status unit_quantize(const float *A, int64_t lda, int transA, const float *B
     unsigned int *ticket = at<unsigned int>(ws, L.ticket);
     if (transA && cudaMemsetAsync(ticket, 0, 2 * sizeof(unsigned int), st) != cudaSuccess)
         return BSG_ERR_CUDA;
+    // zrows (the chained units' row maxima of C, one word per row of op(A))
+    // is zeroed by op(A)'s row quantize; a column quantize of a stored A^T
+    // cannot, so it is cleared here
+    if (zrows && transA && cudaMemsetAsync(zrows, 0, (size_t)M * 4, st) != cudaSuccess)
+        return BSG_ERR_CUDA;
     // op(A) per row: a row quantize of A, or a column quantize of the stored K x M.
     auto quant_a = [&](cudaStream_t s) {
         return !transA ? launch_quantize_rows(A, M, K, lda, kOutHalfKMajor, aop, ldk, sa, nullptr,
-                                              dstatus, s, ticket)
+                                              dstatus, s, ticket, zrows)
                        : launch_quantize_cols(A, K, M, lda, kOutHalfKMajor, aop, ldk, sa, nullptr,
                                               part_a, dstatus, s);
     };
@@ -188,7 +194,7 @@ bsg_status unit_quantize(const float *A, int64_t lda, int transA, const float *B
     if (!transA && !transB) {
         // the common layout: one launch for both operands
         const cudaError_t ef = launch_quantize_ab(A, M, K, lda, B, N, ldb, aop, bop, ldk, sa, sb,
-                                                  dstatus, ticket, st);
+                                                  dstatus, ticket, st, zrows);
         if (ef == cudaSuccess) return BSG_OK;
         if (ef != cudaErrorNotSupported) return BSG_ERR_CUDA;
     }
@@ -826,11 +832,10 @@ size_t requant_layout(int64_t M, int64_t N, int64_t K, size_t *rowmax_off) {
 }
 
 // Unit (M, N, K) from its quantized workspace into C, with the row maxima of
-// |C| gathered into rowmax (zeroed here first).
+// |C| gathered into rowmax (zeroed by the unit's row quantize).
 bsg_status contract_with_rowmax(int64_t M, int64_t N, int64_t K, int relu, float *C,
                                 void *ws, uint32_t *rowmax, int32_t *dstatus, cudaStream_t st) {
     const UnitLayout L = unit_layout(M, N, K, 0, 0);
-    if (cudaMemsetAsync(rowmax, 0, (size_t)M * 4, st) != cudaSuccess) return BSG_ERR_CUDA;
     GemmJob j;
     j.Aop = at<__half>(ws, L.aop);
     j.Bop = at<__half>(ws, L.bop);
@@ -866,9 +871,9 @@ bsg_status bsgemm_i8_requant(const float *A, const float *B, int64_t M, int64_t 
     size_t rm_off = 0;
     if (!ws_ok(workspace, ws_bytes, requant_layout(M, N, K, &rm_off))) return BSG_ERR_WORKSPACE;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    s = unit_quantize(A, K, 0, B, N, 0, M, N, K, workspace, ws_bytes, dstatus, st);
-    if (s != BSG_OK) return s;
     uint32_t *rowmax = at<uint32_t>(workspace, rm_off);
+    s = unit_quantize(A, K, 0, B, N, 0, M, N, K, workspace, ws_bytes, dstatus, st, true, rowmax);
+    if (s != BSG_OK) return s;
     s = contract_with_rowmax(M, N, K, relu, C, workspace, rowmax, dstatus, st);
     if (s != BSG_OK) return s;
     return from_cuda(
@@ -909,24 +914,34 @@ bsg_status bsgemm_i8_chain(const float *A, const float *B1, const float *B2, int
     void *ws2 = static_cast<uint8_t *>(workspace) + ws2_off;
     uint32_t *rowmax = at<uint32_t>(workspace, rm_off);
     const UnitLayout L2 = unit_layout(M, N2, N1, 0, 0);
-    // layer 1's operands; layer 2's weights per column
-    s = unit_quantize(A, K, 0, B1, N1, 0, M, N1, K, ws1, ws2_off, dstatus, st);
+    // layer 1's operands (A's row quantize also zeroes C1's row maxima)
+    s = unit_quantize(A, K, 0, B1, N1, 0, M, N1, K, ws1, ws2_off, dstatus, st, true, rowmax);
     if (s != BSG_OK) return s;
-    if (launch_quantize_cols(B2, N1, N2, N2, kOutHalfKMajor, at<__half>(ws2, L2.bop),
-                             operand_ld(N1), at<float>(ws2, L2.sb), nullptr,
-                             at<uint32_t>(ws2, L2.part_b), dstatus, st) != cudaSuccess)
+    // layer 2's weights per column, on the library's second stream beside
+    // layer 1 (it depends on nothing of it), joined before layer 2's GEMM
+    std::lock_guard<std::mutex> guard(g_side_lock);
+    SideStream *side = side_stream();
+    cudaStream_t qs = side ? side->st : st;
+    if (side && (cudaEventRecord(side->fork, st) != cudaSuccess ||
+                 cudaStreamWaitEvent(side->st, side->fork, 0) != cudaSuccess))
         return BSG_ERR_CUDA;
+    const cudaError_t eq = launch_quantize_cols(B2, N1, N2, N2, kOutHalfKMajor,
+                                                at<__half>(ws2, L2.bop), operand_ld(N1),
+                                                at<float>(ws2, L2.sb), nullptr,
+                                                at<uint32_t>(ws2, L2.part_b), dstatus, qs);
+    // record the join even after a failed launch, so that no fork is left open
+    if (side && cudaEventRecord(side->join, side->st) != cudaSuccess) return BSG_ERR_CUDA;
+    if (eq != cudaSuccess) return BSG_ERR_CUDA;
     // layer 1, gathering C1's row maxima
     s = contract_with_rowmax(M, N1, K, relu1, C1, ws1, rowmax, dstatus, st);
     if (s != BSG_OK) return s;
-    // C1 per row, straight into layer 2's f16 operand and row scales; the
-    // tile counter of layer 2 (zeroed by a row quantize launch elsewhere)
+    // C1 per row, straight into layer 2's f16 operand and row scales; the same
+    // launch zeroes layer 2's tile counter
     if (launch_requant_rows(C1, M, N1, N1, rowmax, kOutHalfKMajor, at<__half>(ws2, L2.aop),
-                            operand_ld(N1), at<float>(ws2, L2.sa), nullptr, dstatus,
-                            st) != cudaSuccess ||
-        cudaMemsetAsync(at<unsigned int>(ws2, L2.ticket), 0, 2 * sizeof(unsigned int), st) !=
-            cudaSuccess)
+                            operand_ld(N1), at<float>(ws2, L2.sa), nullptr, dstatus, st,
+                            at<unsigned int>(ws2, L2.ticket)) != cudaSuccess)
         return BSG_ERR_CUDA;
+    if (side && cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess) return BSG_ERR_CUDA;
     return unit_contract(M, N2, N1, relu2, C2, N2, ws2, L2.total, dstatus, st);
 }
 

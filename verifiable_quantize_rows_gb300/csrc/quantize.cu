@@ -377,7 +377,8 @@ __device__ __forceinline__ void rows_wide_block(int64_t blk, const float *__rest
                                                 void *__restrict__ Q, int64_t ldq,
                                                 float *__restrict__ scale,
                                                 float *__restrict__ inv,
-                                                int32_t *__restrict__ dstatus) {
+                                                int32_t *__restrict__ dstatus,
+                                                unsigned int *__restrict__ zrows) {
     constexpr int RPB = 8 / WPR;
     __shared__ uint32_t red[8];
     const int warp = threadIdx.x >> 5;
@@ -386,6 +387,9 @@ __device__ __forceinline__ void rows_wide_block(int64_t blk, const float *__rest
     const int wr = warp % WPR;
     const int64_t r = blk * RPB + rloc;
     const bool live = r < rows;
+    // one word per row set to zero (may be NULL): the row maxima a GEMM
+    // epilogue gathers for this matrix's rows
+    if (zrows && live && wr == 0 && lane == 0) zrows[r] = 0u;
     const int64_t c4n = cols / 4;
     const float4 *xr = reinterpret_cast<const float4 *>(X + (live ? r : 0) * ldx);
     float4 v[RV];
@@ -432,14 +436,15 @@ __global__ void __launch_bounds__(256)
     quantize_rows_wide_kernel(const float *__restrict__ X, int64_t rows, int64_t cols,
                               int64_t ldx, void *__restrict__ Q, int64_t ldq,
                               float *__restrict__ scale, float *__restrict__ inv,
-                              int32_t *__restrict__ dstatus, unsigned int *__restrict__ zero2) {
+                              int32_t *__restrict__ dstatus, unsigned int *__restrict__ zero2,
+                              unsigned int *__restrict__ zrows) {
     griddep_wait();  // programmatic launch: the previous kernel is done from here on
     // the next kernel may be placed on SMs as this one drains; it waits for
     // this grid's completion before it touches memory
     griddep_launch_dependents();
     if (zero2 && blockIdx.x == 0 && threadIdx.x == 0) zero2[0] = zero2[1] = 0u;
     rows_wide_block<OUT, WPR, RV>((int64_t)blockIdx.x, X, rows, cols, ldx, Q, ldq, scale, inv,
-                                  dstatus);
+                                  dstatus, zrows);
 }
 
 // Columns, single pass: a cluster of CS CTAs shares a strip of 32 columns;
@@ -664,7 +669,8 @@ __global__ void __launch_bounds__(256)
                        __half *__restrict__ Aop, float *__restrict__ sa,
                        const float *__restrict__ B, int64_t N, int64_t ldb,
                        __half *__restrict__ Bop, float *__restrict__ sb, int64_t ldk, int R,
-                       int strips, int32_t *__restrict__ dstatus, unsigned int *__restrict__ zero2) {
+                       int strips, int32_t *__restrict__ dstatus, unsigned int *__restrict__ zero2,
+                       unsigned int *__restrict__ zrows) {
     griddep_wait();  // programmatic launch: the previous kernel is done from here on
     griddep_launch_dependents();  // see quantize_rows_wide_kernel
     if (zero2 && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
@@ -674,7 +680,7 @@ __global__ void __launch_bounds__(256)
     } else {
         const int64_t blk = (int64_t)(blockIdx.x - strips) * gridDim.y + blockIdx.y;
         rows_wide_block<kOutHalfKMajor, WPR, RV>(blk, A, M, K, lda, Aop, ldk, sa, nullptr,
-                                                 dstatus);
+                                                 dstatus, zrows);
     }
 }
 
@@ -851,7 +857,7 @@ static int grid_for(int64_t work, int per_block) {
 template <int OUT, int WPR, int RV>
 static void launch_rows_wide(const float *X, int64_t rows, int64_t cols, int64_t ldx, void *Q,
                              int64_t ldq, float *scale, float *inv, int32_t *dstatus,
-                             unsigned int *zero2, cudaStream_t st) {
+                             unsigned int *zero2, unsigned int *zrows, cudaStream_t st) {
     constexpr int RPB = 8 / WPR;
     const int64_t blocks = (rows + RPB - 1) / RPB;
     cudaLaunchConfig_t cfg;
@@ -865,7 +871,7 @@ static void launch_rows_wide(const float *X, int64_t rows, int64_t cols, int64_t
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaLaunchKernelEx(&cfg, quantize_rows_wide_kernel<OUT, WPR, RV>, X, rows, cols, ldx, Q, ldq,
-                       scale, inv, dstatus, zero2);
+                       scale, inv, dstatus, zero2, zrows);
 }
 
 // Smallest single-pass layout (warps per row, float4 per lane) that holds a
@@ -880,24 +886,26 @@ static int row_layout(int64_t cols) {
 template <int OUT>
 static bool dispatch_rows_wide(int layout, const float *X, int64_t rows, int64_t cols,
                                int64_t ldx, void *Q, int64_t ldq, float *scale, float *inv,
-                               int32_t *dstatus, unsigned int *zero2, cudaStream_t st) {
+                               int32_t *dstatus, unsigned int *zero2, unsigned int *zrows,
+                               cudaStream_t st) {
     switch (layout) {
-        case 0: launch_rows_wide<OUT, 1, 2>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
-        case 1: launch_rows_wide<OUT, 1, 4>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
-        case 2: launch_rows_wide<OUT, 1, 6>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
-        case 3: launch_rows_wide<OUT, 1, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
-        case 4: launch_rows_wide<OUT, 2, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
-        case 5: launch_rows_wide<OUT, 4, 6>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
-        case 6: launch_rows_wide<OUT, 4, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
-        case 7: launch_rows_wide<OUT, 8, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
-        case 8: launch_rows_wide<OUT, 8, 16>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, st); return true;
+        case 0: launch_rows_wide<OUT, 1, 2>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, zrows, st); return true;
+        case 1: launch_rows_wide<OUT, 1, 4>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, zrows, st); return true;
+        case 2: launch_rows_wide<OUT, 1, 6>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, zrows, st); return true;
+        case 3: launch_rows_wide<OUT, 1, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, zrows, st); return true;
+        case 4: launch_rows_wide<OUT, 2, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, zrows, st); return true;
+        case 5: launch_rows_wide<OUT, 4, 6>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, zrows, st); return true;
+        case 6: launch_rows_wide<OUT, 4, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, zrows, st); return true;
+        case 7: launch_rows_wide<OUT, 8, 8>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, zrows, st); return true;
+        case 8: launch_rows_wide<OUT, 8, 16>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus, zero2, zrows, st); return true;
     }
     return false;
 }
 
 cudaError_t launch_quantize_rows(const float *X, int64_t rows, int64_t cols, int64_t ldx,
                                  int out_kind, void *Q, int64_t ldq, float *scale, float *inv,
-                                 int32_t *dstatus, cudaStream_t st, unsigned int *zero2) {
+                                 int32_t *dstatus, cudaStream_t st, unsigned int *zero2,
+                                 unsigned int *zrows) {
     const size_t qalign = out_kind == kOutInt8 ? 4 : 8;
     const size_t qesz = out_kind == kOutInt8 ? 1 : 2;
     const bool vec = (cols % 4 == 0) && (ldx % 4 == 0) &&
@@ -907,14 +915,16 @@ cudaError_t launch_quantize_rows(const float *X, int64_t rows, int64_t cols, int
     if (layout >= 0) {
         if (out_kind == kOutInt8)
             dispatch_rows_wide<kOutInt8>(layout, X, rows, cols, ldx, Q, ldq, scale, inv, dstatus,
-                                         zero2, st);
+                                         zero2, zrows, st);
         else
             dispatch_rows_wide<kOutHalfKMajor>(layout, X, rows, cols, ldx, Q, ldq, scale, inv, dstatus,
-                                              zero2, st);
+                                              zero2, zrows, st);
         count_launches(1);
         return cudaGetLastError();
     }
     if (zero2 && cudaMemsetAsync(zero2, 0, 2 * sizeof(unsigned int), st) != cudaSuccess)
+        return cudaErrorInvalidValue;
+    if (zrows && cudaMemsetAsync(zrows, 0, (size_t)rows * sizeof(unsigned int), st) != cudaSuccess)
         return cudaErrorInvalidValue;
     const int grid = grid_for(rows, kRowWarps);
     const bool vec2 = (ldx % 4 == 0) && (reinterpret_cast<uintptr_t>(X) % 16 == 0) &&
@@ -1017,7 +1027,7 @@ template <int WPR, int RV>
 static cudaError_t launch_ab(const float *A, int64_t M, int64_t K, int64_t lda, __half *Aop,
                              float *sa, const float *B, int64_t N, int64_t ldb, __half *Bop,
                              float *sb, int64_t ldk, int cs, int R, int32_t *dstatus,
-                             unsigned int *zero2, cudaStream_t st) {
+                             unsigned int *zero2, unsigned int *zrows, cudaStream_t st) {
     constexpr int RPB = 8 / WPR;
     const int64_t strips = (N + kStripCols - 1) / kStripCols;
     const int64_t row_blocks = (M + RPB - 1) / RPB;
@@ -1039,13 +1049,14 @@ static cudaError_t launch_ab(const float *A, int64_t M, int64_t K, int64_t lda, 
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, quantize_ab_kernel<WPR, RV>, A, M, K, lda, Aop, sa, B, N, ldb,
-                              Bop, sb, ldk, R, (int)strips, dstatus, zero2);
+                              Bop, sb, ldk, R, (int)strips, dstatus, zero2, zrows);
 }
 
 cudaError_t launch_quantize_ab(const float *A, int64_t M, int64_t K, int64_t lda,
                                const float *B, int64_t N, int64_t ldb, __half *Aop,
                                __half *Bop, int64_t ldk, float *sa, float *sb,
-                               int32_t *dstatus, unsigned int *zero2, cudaStream_t st) {
+                               int32_t *dstatus, unsigned int *zero2, cudaStream_t st,
+                               unsigned int *zrows) {
     const bool vecA = (K % 4 == 0) && (lda % 4 == 0) &&
                       (reinterpret_cast<uintptr_t>(A) % 16 == 0) && ((ldk * 2) % 8 == 0) &&
                       (reinterpret_cast<uintptr_t>(Aop) % 8 == 0);
@@ -1060,13 +1071,13 @@ cudaError_t launch_quantize_ab(const float *A, int64_t M, int64_t K, int64_t lda
     if (layout < 0 || !vecB || !strip_shape(K, 8, cs, R)) return cudaErrorNotSupported;
     cudaError_t e = cudaErrorNotSupported;
     switch (layout) {
-        case 0: e = launch_ab<1, 2>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, st); break;
-        case 1: e = launch_ab<1, 4>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, st); break;
-        case 2: e = launch_ab<1, 6>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, st); break;
-        case 3: e = launch_ab<1, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, st); break;
-        case 4: e = launch_ab<2, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, st); break;
-        case 5: e = launch_ab<4, 6>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, st); break;
-        case 6: e = launch_ab<4, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, st); break;
+        case 0: e = launch_ab<1, 2>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, zrows, st); break;
+        case 1: e = launch_ab<1, 4>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, zrows, st); break;
+        case 2: e = launch_ab<1, 6>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, zrows, st); break;
+        case 3: e = launch_ab<1, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, zrows, st); break;
+        case 4: e = launch_ab<2, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, zrows, st); break;
+        case 5: e = launch_ab<4, 6>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, zrows, st); break;
+        case 6: e = launch_ab<4, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, zrows, st); break;
         default: return cudaErrorNotSupported;  // rows longer than 4096: not fused
     }
     count_launches(1);
@@ -1194,18 +1205,23 @@ namespace {
 
 // Rows whose absmax is already known (the per-row maxima of |C| that the
 // GEMM's epilogue gathered): no reduction is left, so each 256-thread block
-// quantizes one 2048-column segment of one row in a single streaming pass,
+// quantizes one 4096-column segment of one row in a single streaming pass,
 // 4 bytes read and 1 (int8) or 2 (f16 operand) written per element, for any
-// row length.  VEC: 16-byte loads of X and 4/8-byte stores of Q.
+// row length.  VEC: 16-byte loads of X (all four issued before any store)
+// and 4/8-byte stores of Q.
 constexpr int kRqThreads = 256;
-constexpr int kRqSeg = kRqThreads * 8;  // columns per block
+constexpr int kRqVec = 4;                         // float4 per thread
+constexpr int kRqSeg = kRqThreads * 4 * kRqVec;   // columns per block
 
 template <int OUT, bool VEC>
 __global__ void __launch_bounds__(kRqThreads)
     requant_rows_kernel(const float *__restrict__ X, int64_t rows, int64_t cols, int64_t ldx,
                         const uint32_t *__restrict__ rowmax, void *__restrict__ Q, int64_t ldq,
                         float *__restrict__ scale, float *__restrict__ inv,
-                        int32_t *__restrict__ dstatus) {
+                        int32_t *__restrict__ dstatus, unsigned int *__restrict__ zero2) {
+    griddep_wait();  // programmatic launch: the GEMM that gathered rowmax is done
+    griddep_launch_dependents();
+    if (zero2 && blockIdx.x == 0 && threadIdx.x == 0) zero2[0] = zero2[1] = 0u;
     const int64_t nseg = (cols + kRqSeg - 1) / kRqSeg;
     for (int64_t b = blockIdx.x; b < rows * nseg; b += gridDim.x) {
         const int64_t r = b / nseg;
@@ -1221,18 +1237,23 @@ __global__ void __launch_bounds__(kRqThreads)
         const float *xr = X + r * ldx;
         const int64_t qrow = r * ldq;
         if (VEC) {
+            float4 x[kRqVec];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < kRqVec; ++h) {
                 const int64_t c = seg * kRqSeg + 4 * (threadIdx.x + h * kRqThreads);
-                if (c < cols) {  // cols % 4 == 0 here
-                    const float4 x = __ldg(reinterpret_cast<const float4 *>(xr + c));
-                    store4<OUT>(Q, qrow + c, quant(x.x, iv), quant(x.y, iv), quant(x.z, iv),
-                                quant(x.w, iv));
-                }
+                if (c < cols)  // cols % 4 == 0 here
+                    x[h] = __ldcs(reinterpret_cast<const float4 *>(xr + c));
+            }
+#pragma unroll
+            for (int h = 0; h < kRqVec; ++h) {
+                const int64_t c = seg * kRqSeg + 4 * (threadIdx.x + h * kRqThreads);
+                if (c < cols)
+                    store4<OUT>(Q, qrow + c, quant(x[h].x, iv), quant(x[h].y, iv),
+                                quant(x[h].z, iv), quant(x[h].w, iv));
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 4 * kRqVec; ++i) {
                 const int64_t c = seg * kRqSeg + threadIdx.x + i * kRqThreads;
                 if (c < cols) store1<OUT>(Q, qrow + c, quant(__ldg(xr + c), iv));
             }
@@ -1244,31 +1265,37 @@ __global__ void __launch_bounds__(kRqThreads)
 
 cudaError_t launch_requant_rows(const float *X, int64_t rows, int64_t cols, int64_t ldx,
                                 const uint32_t *rowmax, int out_kind, void *Q, int64_t ldq,
-                                float *scale, float *inv, int32_t *dstatus, cudaStream_t st) {
+                                float *scale, float *inv, int32_t *dstatus, cudaStream_t st,
+                                unsigned int *zero2) {
     const size_t qsz = out_kind == kOutInt8 ? 1 : 2;
     const bool vec = cols % 4 == 0 && ldx % 4 == 0 && ldq % 4 == 0 &&
                      reinterpret_cast<uintptr_t>(X) % 16 == 0 &&
                      reinterpret_cast<uintptr_t>(Q) % (4 * qsz) == 0;
     const int64_t blocks = rows * ((cols + kRqSeg - 1) / kRqSeg);
-    const int grid = (int)(blocks < (int64_t)device_sm_count() * 16 ? blocks
-                                                                     : (int64_t)device_sm_count() * 16);
-    if (out_kind == kOutInt8) {
-        if (vec)
-            requant_rows_kernel<kOutInt8, true><<<grid, kRqThreads, 0, st>>>(
-                X, rows, cols, ldx, rowmax, Q, ldq, scale, inv, dstatus);
-        else
-            requant_rows_kernel<kOutInt8, false><<<grid, kRqThreads, 0, st>>>(
-                X, rows, cols, ldx, rowmax, Q, ldq, scale, inv, dstatus);
-    } else {
-        if (vec)
-            requant_rows_kernel<kOutHalfKMajor, true><<<grid, kRqThreads, 0, st>>>(
-                X, rows, cols, ldx, rowmax, Q, ldq, scale, inv, dstatus);
-        else
-            requant_rows_kernel<kOutHalfKMajor, false><<<grid, kRqThreads, 0, st>>>(
-                X, rows, cols, ldx, rowmax, Q, ldq, scale, inv, dstatus);
-    }
+    const int64_t cap = (int64_t)device_sm_count() * 16;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)(blocks < cap ? blocks : cap), 1, 1);
+    cfg.blockDim = dim3(kRqThreads, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (out_kind == kOutInt8)
+        e = vec ? cudaLaunchKernelEx(&cfg, requant_rows_kernel<kOutInt8, true>, X, rows, cols, ldx,
+                                     rowmax, Q, ldq, scale, inv, dstatus, zero2)
+                : cudaLaunchKernelEx(&cfg, requant_rows_kernel<kOutInt8, false>, X, rows, cols, ldx,
+                                     rowmax, Q, ldq, scale, inv, dstatus, zero2);
+    else
+        e = vec ? cudaLaunchKernelEx(&cfg, requant_rows_kernel<kOutHalfKMajor, true>, X, rows, cols,
+                                     ldx, rowmax, Q, ldq, scale, inv, dstatus, zero2)
+                : cudaLaunchKernelEx(&cfg, requant_rows_kernel<kOutHalfKMajor, false>, X, rows, cols,
+                                     ldx, rowmax, Q, ldq, scale, inv, dstatus, zero2);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace bsg
