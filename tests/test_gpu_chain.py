@@ -68,7 +68,7 @@ def test_requant_overflowed_rows_set_nonfinite(orc):
     assert st & 1
 
 
-@pytest.mark.parametrize("case", ["gpt2_mlp", "ragged", "wide"])
+@pytest.mark.parametrize("case", ["gpt2_mlp", "ragged", "wide", "deep"])
 def test_chain_matches_two_units(orc, case):
     if case == "gpt2_mlp":
         # the GPT-2-small MLP at M = 8192: fc (768 -> 3072, ReLU) then proj
@@ -81,6 +81,12 @@ def test_chain_matches_two_units(orc, case):
         B1 = inputs.normal((130, 517), 0.1, 6)
         B2 = inputs.normal((517, 75), 0.1, 7)
         relu1, relu2 = False, True
+    elif case == "deep":
+        # K > 2048: the first unit quantizes B1 on the second stream too
+        A = inputs.normal((130, 3000), 1.0, 11)
+        B1 = inputs.normal((3000, 700), 0.05, 12)
+        B2 = inputs.normal((700, 64), 0.05, 13)
+        relu1, relu2 = True, True
     else:
         A = inputs.normal((256, 512), 1.0, 8)
         B1 = inputs.normal((512, 5000), 0.05, 9)

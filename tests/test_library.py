@@ -20,7 +20,8 @@ def test_header_declares_the_boundary():
     for required in ("bsg_quantize_rows", "bsg_quantize_cols", "bsg_gemm_s32", "bsg_epilogue",
                      "bsgemm_i8", "bsgemm_i8_ex", "bsgemm_i8_host", "bsgemm_i8_host_batch", "bsg_hash_f32",
                      "bsg_probe_hash", "bsg_probe_hash_async", "bsg_status_str", "bsg_audit",
-                     "bsg_selftest"):
+                     "bsg_selftest", "bsgemm_i8_requant", "bsgemm_i8_chain", "bsgemm_i8_noalloc",
+                     "bsg_mma_ceiling"):
         assert required in names
 
 
@@ -101,6 +102,26 @@ def test_argument_errors_without_gpu(lib):
     hitems[1].A_host = 256
     hitems[1].ws_bytes = 64
     assert lib.bsgemm_i8_host_batch(hitems, 2, None, None) == 3
+    # chained units: null outputs, bad sizes, a too-small workspace
+    assert lib.bsgemm_i8_requant(dummy, dummy, 4, 4, 4, 0, None, dummy, dummy, None, dummy,
+                                 1 << 20, None, None) == 1
+    assert lib.bsgemm_i8_requant(dummy, dummy, 4, 4, 4, 0, dummy, dummy, None, None, dummy,
+                                 1 << 20, None, None) == 1
+    assert lib.bsgemm_i8_requant(dummy, dummy, 4, 4, 4, 0, dummy, dummy, dummy, None, dummy,
+                                 16, None, None) == 3
+    assert lib.bsgemm_i8_chain(dummy, dummy, None, 4, 4, 4, 4, 0, 0, dummy, dummy, dummy,
+                               1 << 20, None, None) == 1
+    assert lib.bsgemm_i8_chain(dummy, dummy, dummy, 4, 4, 0, 4, 0, 0, dummy, dummy, dummy,
+                               1 << 20, None, None) == 1
+    assert lib.bsgemm_i8_chain(dummy, dummy, dummy, 4, 4, 4, 4, 0, 0, dummy, dummy, dummy,
+                               16, None, None) == 3
+    need = lib.bsgemm_i8_chain_workspace_size(8192, 768, 3072, 768)
+    assert need > lib.bsgemm_i8_requant_workspace_size(8192, 3072, 768)
+    assert lib.bsgemm_i8_requant_workspace_size(8192, 3072, 768) > 8192 * 4
+    assert lib.bsgemm_i8_chain_workspace_size(0, 4, 4, 4) == 0
+    # the tensor-pipe ceiling: iterations out of range
+    assert lib.bsg_mma_ceiling(0, None, None, None) == 1
+    assert lib.bsg_mma_ceiling((1 << 18) + 1, None, None, None) == 1
     # self-test: missing or small workspace
     assert lib.bsg_selftest(None, 0, None, None) == 3
     assert lib.bsg_selftest(dummy, 16, None, None) == 3
