@@ -929,10 +929,15 @@ def run_single(args):
         probe_out = torch.empty(32, dtype=torch.uint8, device=dev)
         W = Workload("small", dev, lib, side, dstatus, probe_out, pws, with_host=False)
         step_ms, stage_ms, launches = time_workload(W, args.steps, args.warmup, flush, stream,
-                                                    lambda: None, stage_steps=3)
+                                                    lambda: None, stage_steps=20)
         ms = statistics.mean(step_ms)
+        peaks, peak_kind = load_peaks()
+        roof, quant, _ = summarize(W, step_ms, stage_ms, peaks, peak_kind, ms, 1,
+                                   SMALL_GEMM_PROFILE)
         return {"workload": SMALL_WORKLOAD, "ms_per_step": round(ms, 4),
                 "value": round(step_ops("small") / (ms * 1e-3) / 1e12, 3), "unit": "TOPS",
+                "gemm_frac": roof["frac"], "gemm_ms": roof["per_gemm_ms"],
+                "quantize_ms": quant["per_gemm_ms"],
                 "gpu_launches": launches, "device_status": int(dstatus.item())}
     parts = [int(v) for v in args.unit.split(",")]
     M, N, K = parts[:3]

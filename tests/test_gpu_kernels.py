@@ -119,7 +119,7 @@ def test_every_column_quantize_path_operand(orc, monkeypatch, path, M, N, K):
     C = bsg.bsgemm_i8(dev(A), dev(B))
     torch.cuda.synchronize()
     Co, _ = orc.bsgemm_i8(A, B, False)
-    assert_bits_equal(host(C), Co, f"{path}/{width} {M}x{N}x{K}")
+    assert_bits_equal(host(C), Co, f"{path} {M}x{N}x{K}")
 
 
 @pytest.mark.parametrize("path", ["twopass", ""])
