@@ -873,8 +873,12 @@ cudaError_t launch_group_np(const GemmJob *jobs, int n, int mode, int32_t *dstat
         if (!make_tmap_2d(&maps.a[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, j.Aop, (uint64_t)j.K,
                           (uint64_t)j.M, (uint64_t)operand_ld(j.K), kBK, kBM))
             return cudaErrorInvalidValue;
-        const bool aligned =
-            ((j.ldo * 4) % 16 == 0) && (reinterpret_cast<uintptr_t>(j.out) % 16 == 0);
+        // TMA stores need 16-byte aligned rows, and a row length that is a
+        // whole number of 16-byte chunks: at the right edge the store writes
+        // whole chunks, so with N % 4 != 0 it would write up to 3 elements
+        // past column N - 1 into the caller's row padding (ldc > N)
+        const bool aligned = ((j.ldo * 4) % 16 == 0) && ((j.N * 4) % 16 == 0) &&
+                             (reinterpret_cast<uintptr_t>(j.out) % 16 == 0);
         Prob &q = p.prob[i];
         q.tma_store = aligned && make_tmap_2d(&maps.c[i],
                                               mode == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
