@@ -180,3 +180,73 @@ def test_weight_storage_writes_only_its_codes(orc, bits):
     assert (Qh[:K, width:] == -86).all() and (Qh[K:] == -86).all()
     assert_bits_equal(host(sc)[:N], sco, "scales")
     assert (host(sc)[N:].view(np.uint32) == CANARY_F32).all()
+
+
+@pytest.mark.parametrize("M,N,K,extra", [(257, 1025, 1100, 3), (130, 96, 2100, 4)],
+                         ids=lambda v: str(v))
+def test_int32_accumulators_write_only_their_s(orc, M, N, K, extra):
+    """bsg_gemm_s32 (the contraction with int32 S stored) into a padded S."""
+    rng = np.random.default_rng(M + N + K)
+    Aq = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    Bq = rng.integers(-127, 128, (K, N)).astype(np.int8)
+    Ad, Bd = torch.from_numpy(Aq).cuda(), torch.from_numpy(Bq).cuda()
+    lds = N + extra
+    S = torch.full(((M + 2) * lds,), CANARY_F32, dtype=torch.int32, device="cuda")
+    nws = lib().bsg_gemm_s32_workspace_size(M, N, K)
+    ws, off = workspace(nws)
+    assert lib().bsg_gemm_s32(ptr(Ad), K, ptr(Bd), N, M, N, K, ptr(S), lds, ptr(ws, off), nws,
+                              None, stream()) == 0
+    torch.cuda.synchronize()
+    Sh = host(S).reshape(M + 2, lds)
+    So, _ = orc.gemm_s32(Aq, Bq)
+    assert_bits_equal(np.ascontiguousarray(Sh[:M, :N]), So, "S")
+    assert (Sh[:M, N:] == CANARY_F32).all() and (Sh[M:] == CANARY_F32).all()
+    assert tail_intact(ws, off, nws)
+
+
+def test_grouped_launch_writes_only_its_cs(orc):
+    """Three units in one launch, each C padded differently."""
+    shapes = [(300, 150, 200, 1), (257, 1025, 1100, 3), (129, 96, 700, 4)]
+    items = (bsg.GemmItem * 3)()
+    keep, want = [], []
+    for i, (M, N, K, extra) in enumerate(shapes):
+        A = inputs.normal((M, K), 1.0, 40 + i).numpy()
+        B = inputs.normal((K, N), 0.1, 50 + i).numpy()
+        Ad, Bd = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+        ldc = N + extra
+        C = canary_f32((M + 2) * ldc)
+        nws = lib().bsgemm_i8_workspace_size(M, N, K)
+        ws, off = workspace(nws)
+        items[i] = bsg.GemmItem(Ad.data_ptr(), K, 0, Bd.data_ptr(), N, 0, M, N, K, i % 2,
+                                C.data_ptr(), ldc, ws.data_ptr() + off, nws)
+        keep.append((Ad, Bd, C, ws, off, nws, M, N, ldc))
+        want.append(orc.bsgemm_i8(A, B, bool(i % 2))[0])
+    assert lib().bsgemm_i8_group(items, 3, None, stream()) == 0
+    torch.cuda.synchronize()
+    for (Ad, Bd, C, ws, off, nws, M, N, ldc), Co in zip(keep, want):
+        Ch = host(C).reshape(M + 2, ldc)
+        assert_bits_equal(np.ascontiguousarray(Ch[:M, :N]), Co, f"group C {M}x{N}")
+        assert (Ch[:M, N:].view(np.uint32) == CANARY_F32).all()
+        assert (Ch[M:].view(np.uint32) == CANARY_F32).all()
+        assert tail_intact(ws, off, nws)
+
+
+def test_host_entry_point_writes_only_its_c(orc):
+    """bsgemm_i8_host: C on the host followed by canaries, and the device
+    workspace's tail."""
+    M, N, K = 700, 333, 900
+    A = inputs.normal((M, K), 1.0, 61)
+    B = inputs.normal((K, N), 0.1, 62)
+    Ah, Bh = A.pin_memory(), B.pin_memory()
+    C = torch.full((M * N + 64,), CANARY_F32, dtype=torch.int32).view(torch.float32).pin_memory()
+    nws = lib().bsgemm_i8_host_workspace_size(M, N, K)
+    ws, off = workspace(nws)
+    st = ctypes.c_int32(-1)
+    assert lib().bsgemm_i8_host(ptr(Ah), ptr(Bh), M, N, K, 0, ptr(C), ptr(ws, off), nws,
+                                ctypes.byref(st), stream()) == 0
+    assert st.value == 0
+    Co, _ = orc.bsgemm_i8(A.numpy(), B.numpy(), False)
+    Cn = C.numpy()
+    assert_bits_equal(Cn[:M * N].reshape(M, N), Co, "host C")
+    assert (Cn[M * N:].view(np.uint32) == CANARY_F32).all()
+    assert tail_intact(ws, off, nws)
