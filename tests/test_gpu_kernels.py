@@ -138,12 +138,13 @@ def test_every_column_quantize_path_int8(orc, monkeypatch, path, R, Ncol):
     assert_bits_equal(host(iv), ivo, "inv")
 
 
-@pytest.mark.parametrize("group", [1, 3, 8, 64])
-def test_tile_raster_does_not_change_results(orc, monkeypatch, group):
+@pytest.mark.parametrize("group,snake", [(1, "1"), (3, "1"), (8, "1"), (8, "0"), (64, "1")])
+def test_tile_raster_does_not_change_results(orc, monkeypatch, group, snake):
     """The order in which tiles are handed out (BSG_GEMM_GROUP m-units per
-    raster group) changes which CTA computes which tile and when, never a
-    bit of C."""
+    raster group, serpentine or not) changes which CTA computes which tile
+    and when, never a bit of C."""
     monkeypatch.setenv("BSG_GEMM_GROUP", str(group))
+    monkeypatch.setenv("BSG_GEMM_SNAKE", snake)
     M, N, K = 1300, 1100, 2100
     A = inputs.normal((M, K), 1.0, 31).numpy()
     B = inputs.normal((K, N), 0.1, 32).numpy()

@@ -108,6 +108,7 @@ int gemm_tile_width(int64_t M, int64_t N, int sms);
 int gemm_group_tile_width(const int64_t *M, const int64_t *N, int n, int sms);
 bool gemm_pairs_enabled();
 int gemm_group_m();
+int gemm_snake();
 // The tensor-core GEMM.  Aop: M x ldk f16, Bop: N x ldk f16 (both K-major,
 // ldk = operand_ld(K)).  mode 0: C = epi(S, sa, sb) (+ReLU) as float;
 // mode 1: S stored as int32.  sa / sb must hold round_up(M, kBM) /

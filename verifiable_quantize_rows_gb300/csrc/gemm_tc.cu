@@ -139,6 +139,7 @@ struct Params {
     int num_units;  // tiles of the launch, all GEMMs
     int mode;       // 0: f32 epilogue, 1: int32 accumulators
     int group_m;    // tile raster: m-units per group
+    int snake;      // 1: odd raster groups take their n-tiles in reverse
     int32_t *dstatus;
     // ticket[0]: tiles claimed beyond the first wave; ticket[1]: CTAs (pairs)
     // done claiming.  Zero at launch; the last CTA to finish claiming sets
@@ -171,6 +172,9 @@ __device__ __forceinline__ int tile_coords(const Params<NP> &p, int u, int &mu, 
     const int r = u - g * per_group;
     mu = first_m + r % gm;
     nb = r / gm;
+    // serpentine: odd groups walk the n-tiles backwards, so that a group's
+    // first waves use the B columns the previous group's last waves left in L2
+    if (p.snake && (g & 1)) nb = q.num_n - 1 - nb;
     return pi;
 }
 
@@ -810,6 +814,13 @@ int gemm_group_m() {
     return (v >= 1 && v <= 64) ? v : kGroupM;
 }
 
+// Serpentine raster (default on); BSG_GEMM_SNAKE=0 turns it off (same
+// results, another order of the tiles).
+int gemm_snake() {
+    const char *e = getenv("BSG_GEMM_SNAKE");
+    return (e && e[0] == '0' && e[1] == 0) ? 0 : 1;
+}
+
 // BSG_GEMM_BN=64|128|192|256 forces the tile width (same results); anything
 // else, or nothing, leaves the choice to gemm_tile_width.
 static int forced_tile_width() {
@@ -864,6 +875,7 @@ cudaError_t launch_group_np(const GemmJob *jobs, int n, int mode, int32_t *dstat
     p.nprob = n;
     p.mode = mode;
     p.group_m = gemm_group_m();
+    p.snake = gemm_snake();
     p.dstatus = dstatus;
     p.ticket = ticket;
     int64_t Ms[kMaxGroup], Ns[kMaxGroup];
