@@ -214,6 +214,20 @@ def test_large_gemms_full(orc, name):
         assert (u32(C) == 0).any()
 
 
+@pytest.mark.parametrize("name", ["sq4096", "sq8192", "ragged_adversarial"])
+def test_large_int32_accumulators_full(orc, name):
+    """The contraction alone at the benchmark's sizes: the oracle's int8
+    codes of A and B through bsg_gemm_s32 (the same tensor-core kernel,
+    int32 S stored instead of the epilogue), compared with the oracle's
+    exact S over the whole matrix."""
+    A, B, _ = inputs.large_gemm_inputs(name)
+    Aq, _, _, _ = orc.quantize_rows(A.numpy())
+    Bq, _, _, _ = orc.quantize_cols(B.numpy())
+    S = host(bsg.gemm_s32(dev(Aq), dev(Bq)))
+    So, _ = orc.gemm_s32(Aq, Bq)
+    assert_bits_equal(S, So, name + " S")
+
+
 @pytest.mark.parametrize("shape", [(384, 512, 6400), (8192, 768, 3072), (1024, 1024, 1024),
                                    (1280, 2560, 1100), (640, 300, 4097), (150 * 128, 256, 768)],
                          ids=lambda s: "x".join(map(str, s)))
