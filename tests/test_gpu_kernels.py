@@ -152,3 +152,24 @@ def test_tile_raster_does_not_change_results(orc, monkeypatch, group, snake):
     torch.cuda.synchronize()
     Co, _ = orc.bsgemm_i8(A, B, True)
     assert_bits_equal(host(C), Co, f"group {group}")
+
+
+@pytest.mark.parametrize("peel", ["1", "0"])
+@pytest.mark.parametrize("rows,cols", [(33, 65), (300, 1001), (17, 8191), (5, 20001), (64, 70)],
+                         ids=lambda v: str(v))
+def test_unaligned_rows_both_paths(orc, monkeypatch, peel, rows, cols):
+    """Rows that are not 16-byte aligned (ldx % 4 != 0): the kernel that peels
+    each row to its 16-byte boundary and the scalar one, forced in turn, for
+    the int8 API and inside the unit (the f16 operand), against the oracle."""
+    monkeypatch.setenv("BSG_ROWS_PEEL", peel)
+    X = inputs.adversarial(rows, cols, rows * 7 + cols).numpy()
+    Q, sc, iv = bsg.quantize_rows(dev(X))
+    Qo, sco, ivo, _ = orc.quantize_rows(X)
+    assert_bits_equal(host(Q), Qo, "Q")
+    assert_bits_equal(host(sc), sco, "scale")
+    assert_bits_equal(host(iv), ivo, "inv")
+    B = inputs.normal((cols, 40), 0.1, cols).numpy()
+    C = bsg.bsgemm_i8(dev(X), dev(B))
+    torch.cuda.synchronize()
+    Co, _ = orc.bsgemm_i8(X, B, False)
+    assert_bits_equal(host(C), Co, "C")

@@ -198,6 +198,72 @@ __global__ void __launch_bounds__(kRowWarps * 32)
     }
 }
 
+// Rows that are not 16-byte aligned (ldx % 4 != 0, e.g. K = 8191): one warp
+// per row.  The maximum: the few elements before the row's first 16-byte
+// boundary and after its last read one by one, the body with 128-bit loads,
+// eight in flight per lane.  The codes: the row read again (mostly from
+// L1/L2) with lanes on consecutive elements, so that every store instruction
+// writes one contiguous span (the codes are as unaligned as the row).
+template <int OUT>
+__global__ void __launch_bounds__(kRowWarps * 32)
+    quantize_rows_peel_kernel(const float *__restrict__ X, int64_t rows, int64_t cols,
+                              int64_t ldx, void *__restrict__ Q, int64_t ldq,
+                              float *__restrict__ scale, float *__restrict__ inv,
+                              int32_t *__restrict__ dstatus) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp_global = (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+    const int64_t warp_stride = (int64_t)gridDim.x * kRowWarps;
+    for (int64_t r = warp_global; r < rows; r += warp_stride) {
+        const float *xr = X + r * ldx;
+        // elements before the first 16-byte boundary (X is 4-byte aligned)
+        int64_t h = (int64_t)((16u - (uint32_t)(reinterpret_cast<uintptr_t>(xr) & 15u)) & 15u) / 4;
+        if (h > cols) h = cols;
+        const int64_t nb4 = (cols - h) / 4;  // float4 of the body
+        const int64_t t0 = h + 4 * nb4;      // first element of the tail
+        const float4 *body = reinterpret_cast<const float4 *>(xr + h);
+        uint32_t m = 0, m1 = 0;
+        if (lane < h) m = absbits(__ldg(xr + lane));
+        if (t0 + lane < cols) m = max(m, absbits(__ldg(xr + t0 + lane)));
+        int64_t c4 = lane;
+        for (; c4 + 224 < nb4; c4 += 256) {
+            float4 a[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) a[u] = __ldg(body + c4 + 32 * u);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                m = max(m, max(absbits(a[u].x), absbits(a[u].y)));
+                m1 = max(m1, max(absbits(a[u].z), absbits(a[u].w)));
+            }
+        }
+        for (; c4 < nb4; c4 += 32) {
+            const float4 a = __ldg(body + c4);
+            m = max(m, max(absbits(a.x), absbits(a.y)));
+            m1 = max(m1, max(absbits(a.z), absbits(a.w)));
+        }
+        m = __reduce_max_sync(0xffffffffu, max(m, m1));
+        float sc = 0.f, iv = 0.f;
+        if (lane == 0) {
+            scale_from_max(m, sc, iv);
+            scale[r] = sc;
+            if (inv) inv[r] = iv;
+            if (m >= kNonfiniteBits && dstatus) atomicOr(dstatus, 1);
+        }
+        iv = __shfl_sync(0xffffffffu, iv, 0);
+        // the codes: the row again (mostly from L1/L2), lanes on consecutive
+        // elements so that each store covers one contiguous span
+        const int64_t qrow = r * ldq;
+        int64_t c = lane;
+        for (; c + 224 < cols; c += 256) {
+            float a[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) a[u] = __ldcs(xr + c + 32 * u);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) store1<OUT>(Q, qrow + c + 32 * u, quant(a[u], iv));
+        }
+        for (; c < cols; c += 32) store1<OUT>(Q, qrow + c, quant(__ldcs(xr + c), iv));
+    }
+}
+
 // Column quantize, pass 1: partial |x| maxima of 128-column groups over
 // slices of rows.  Block = 32 column lanes (VW columns each) x 8 row lanes;
 // each thread keeps 4 row loads in flight.
@@ -929,9 +995,16 @@ cudaError_t launch_quantize_rows(const float *X, int64_t rows, int64_t cols, int
     const int grid = grid_for(rows, kRowWarps);
     const bool vec2 = (ldx % 4 == 0) && (reinterpret_cast<uintptr_t>(X) % 16 == 0) &&
                       ((ldq * qesz) % qalign == 0) && (reinterpret_cast<uintptr_t>(Q) % qalign == 0);
+    // rows long enough to gain from 128-bit loads take the peeling kernel
+    // when they are not 16-byte aligned (BSG_ROWS_PEEL=0 keeps the scalar one)
+    const char *pe = getenv("BSG_ROWS_PEEL");
+    const bool peel = !vec2 && cols >= 64 && !(pe && pe[0] == '0');
     if (out_kind == kOutInt8) {
         if (vec2)
             quantize_rows_kernel<kOutInt8, true><<<grid, kRowWarps * 32, 0, st>>>(
+                X, rows, cols, ldx, Q, ldq, scale, inv, dstatus);
+        else if (peel)
+            quantize_rows_peel_kernel<kOutInt8><<<grid, kRowWarps * 32, 0, st>>>(
                 X, rows, cols, ldx, Q, ldq, scale, inv, dstatus);
         else
             quantize_rows_kernel<kOutInt8, false><<<grid, kRowWarps * 32, 0, st>>>(
@@ -939,6 +1012,9 @@ cudaError_t launch_quantize_rows(const float *X, int64_t rows, int64_t cols, int
     } else {
         if (vec2)
             quantize_rows_kernel<kOutHalfKMajor, true><<<grid, kRowWarps * 32, 0, st>>>(
+                X, rows, cols, ldx, Q, ldq, scale, inv, dstatus);
+        else if (peel)
+            quantize_rows_peel_kernel<kOutHalfKMajor><<<grid, kRowWarps * 32, 0, st>>>(
                 X, rows, cols, ldx, Q, ldq, scale, inv, dstatus);
         else
             quantize_rows_kernel<kOutHalfKMajor, false><<<grid, kRowWarps * 32, 0, st>>>(
