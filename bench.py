@@ -504,7 +504,7 @@ def run_gpu(args, rank, world, local_rank):
         side.synchronize()
         return bytes(e2e_hash_host.tolist())
 
-    e2e_steps = max(3, min(args.steps, 10))
+    e2e_steps = max(3, min(args.steps, 20))
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
@@ -517,12 +517,17 @@ def run_gpu(args, rank, world, local_rank):
         e2e_hex = e2e_step().hex()         # synchronizes: C and the hash are on the host
         e2e_times.append(time.perf_counter() - t)
     barrier()
-    e2e_ms = statistics.mean(e2e_times) * 1e3
+    # the median: a host-side stall (seen: 51 and 157 ms steps among 18 ms
+    # ones) would otherwise decide the figure; the mean and every step are
+    # reported beside it
+    e2e_ms = statistics.median(e2e_times) * 1e3
+    e2e_mean_ms = statistics.mean(e2e_times) * 1e3
     e2e_all_ms = [round(t * 1e3, 3) for t in e2e_times]
     h2d = sum(4 * (u["M"] * u["K"] + u["K"] * u["N"]) for u in W.units)
     d2h = sum(4 * u["M"] * u["N"] for u in W.units) + 32
     peaks, peak_kind = load_peaks()
-    ms_max, e2e_max = max_over_ranks([ms_per_step, e2e_ms], device=dev)
+    ms_max, e2e_max, e2e_mean_max = max_over_ranks([ms_per_step, e2e_ms, e2e_mean_ms],
+                                                   device=dev)
     roof, quant, probe_ms = summarize(W, step_ms, stage_ms, peaks, peak_kind, ms_max, world,
                                       GEMM_PROFILE)
     dstat_large = int(dstatus.item())
@@ -554,16 +559,18 @@ def run_gpu(args, rank, world, local_rank):
     if rank != 0:
         return None
     return build_line(args, world, ms_max, roof, quant, probe_ms, ceiling, clk, launches,
-                      s_launches, s_steps, wall, e2e_max, e2e_all_ms, h2d, d2h, golden, e2e_hex,
+                      s_launches, s_steps, wall, (e2e_max, e2e_mean_max), e2e_all_ms, h2d, d2h,
+                      golden, e2e_hex,
                       probe_hex, replicas_agree, dstat_large, dstat_small, s_ms_max, s_roof,
                       s_quant)
 
 
 def build_line(args, world, ms_max, roof, quant, probe_ms, ceiling, clk, launches, s_launches,
-               s_steps, wall, e2e_max, e2e_all_ms, h2d, d2h, golden, e2e_hex, probe_hex,
+               s_steps, wall, e2e_ms2, e2e_all_ms, h2d, d2h, golden, e2e_hex, probe_hex,
                replicas_agree, dstat_large, dstat_small, s_ms_max, s_roof, s_quant):
     ops = step_ops("large")
     value = ops * world / (ms_max * 1e-3) / 1e12
+    e2e_max, e2e_mean_max = e2e_ms2
     roof = dict(roof)
     roof["mma_ceiling_tflops"] = round(ceiling, 1)
     roof["frac_of_mma_ceiling"] = round(roof["achieved"] / ceiling, 4)
@@ -598,8 +605,10 @@ def build_line(args, world, ms_max, roof, quant, probe_ms, ceiling, clk, launche
         "quantize": quant,
         "probe_ms": round(probe_ms, 4),
         "e2e": {"value": round(ops * world / (e2e_max * 1e-3) / 1e12, 3), "unit": "TOPS",
-                "ms_per_step": round(e2e_max, 4), "steps": len(e2e_all_ms),
-                "step_ms": e2e_all_ms,
+                "ms_per_step": round(e2e_max, 4), "statistic": "median over the steps",
+                "mean_ms_per_step": round(e2e_mean_max, 4),
+                "value_from_mean": round(ops * world / (e2e_mean_max * 1e-3) / 1e12, 3),
+                "steps": len(e2e_all_ms), "step_ms": e2e_all_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": "bsgemm_i8_host_batch of the step's four GEMMs (pinned host A, B in; "
                        "C out) + bsg_probe_hash_async with its 32 bytes read back",
