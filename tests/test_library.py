@@ -52,6 +52,10 @@ def test_argument_errors_without_gpu(lib):
     # null pointers, bad sizes, K over the limit, too-small workspace
     assert lib.bsgemm_i8(None, dummy, 4, 4, 4, 0, dummy, dummy, 1 << 20, None, None) == 1
     assert lib.bsgemm_i8(dummy, dummy, 0, 4, 4, 0, dummy, dummy, 1 << 20, None, None) == 1
+    # C beyond 2^40 elements (each side under 2^31): rejected, not overflowed
+    assert lib.bsgemm_i8(dummy, dummy, 1 << 30, 1 << 11, 4, 0, dummy, dummy, 1 << 20, None,
+                         None) == 1
+    assert lib.bsgemm_i8_workspace_size(1 << 30, (1 << 10) + 1, 4) == 0
     assert lib.bsgemm_i8(dummy, dummy, 4, 4, bsg.MAX_K + 1, 0, dummy, dummy, 1 << 30, None,
                          None) == 2
     assert lib.bsgemm_i8(dummy, dummy, 4, 4, 4, 0, dummy, dummy, 16, None, None) == 3

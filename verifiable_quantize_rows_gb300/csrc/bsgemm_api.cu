@@ -90,8 +90,12 @@ bool ws_ok(const void *ws, size_t have, size_t need) {
     return ws != nullptr && (reinterpret_cast<uintptr_t>(ws) % 256) == 0 && have >= need;
 }
 
+// Sizes the kernels index: M, N below 2^31, and C at most 2^40 elements (4 TiB
+// of f32, beyond any GPU's memory), which keeps every tile count and element
+// offset inside the kernels' integer types.
 bool dims_ok(int64_t M, int64_t N, int64_t K) {
-    return M >= 1 && N >= 1 && K >= 1 && M <= INT32_MAX && N <= INT32_MAX;
+    return M >= 1 && N >= 1 && K >= 1 && M <= INT32_MAX && N <= INT32_MAX &&
+           M <= (int64_t(1) << 40) / N;
 }
 
 template <typename T>
