@@ -520,12 +520,16 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     e2e_times, e2e_hex = [], ""
+    import gc
+    gc.collect()
+    gc.disable()    # no collector pause inside a timed host step
     for _ in range(e2e_steps):
         flush.zero_()
         torch.cuda.synchronize()
         t = time.perf_counter()
         e2e_hex = e2e_step().hex()         # synchronizes: C and the hash are on the host
         e2e_times.append(time.perf_counter() - t)
+    gc.enable()
     barrier()
     # the median: a host-side stall (seen: 51 and 157 ms steps among 18 ms
     # ones) would otherwise decide the figure; the mean and every step are
