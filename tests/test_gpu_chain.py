@@ -103,3 +103,43 @@ def test_chain_matches_two_units(orc, case):
     # and the same as two separate units on the GPU
     C2s = bsg.bsgemm_i8(bsg.bsgemm_i8(dev(A), dev(B1), relu=relu1), dev(B2), relu=relu2)
     assert_bits_equal(host(C2), host(C2s), case + " C2 vs two units")
+
+
+def _tie_inputs(M=64, N=96, seed=3):
+    """A = 127 I (row scales 1) and B with a row of 127 (column scales 1) and
+    rows of odd values +-1 holding one +-2: the first unit's C is exactly
+    127 B, so each C row below the first has max 254 (scale 2, inv 1/2) and
+    its odd entries quantize from x * inv = +-63.5, exact ties."""
+    rng = np.random.default_rng(seed)
+    A = (127.0 * np.eye(M)).astype(np.float32)
+    B = rng.choice([-1.0, 1.0], size=(M, N)).astype(np.float32)
+    B[0, :] = 127.0
+    for i in range(1, M):
+        B[i, rng.integers(0, N)] = 2.0 * rng.choice([-1.0, 1.0])
+    return A, B
+
+
+def test_chain_gate_hunts_quantize_ties(orc):
+    """The chain gate of "Layer 1: exact init gates": inputs on which the
+    spec's floor(x*inv + 0.5) and round-half-to-even disagree in the second
+    unit's quantize, so that agreeing with the oracle is not vacuous."""
+    A, B = _tie_inputs()
+    C, Cq, sc, _, st = requant(A, B, False)
+    assert st == 0
+    Co, _ = orc.bsgemm_i8(A, B, False)
+    assert_bits_equal(C, (127.0 * B).astype(np.float32), "C = 127 B exactly")
+    Qo, sco, _, _ = orc.quantize_rows(Co)
+    assert_bits_equal(Cq, Qo, "codes follow the spec")
+    assert (sc[1:] == 2.0).all()
+    # the round-half-to-even reading differs on every -63.5
+    rne = np.rint(C[1:] * 0.5).astype(np.int8)
+    disagree = (rne != Qo[1:]).sum()
+    assert disagree > 0 and (Cq[1:][C[1:] == -127.0] == -63).all()
+    # the chained second unit inherits the tie rule: C2 = 2 * (q(C1) . B2)
+    B2 = np.zeros((B.shape[1], 8), np.float32)
+    B2[np.arange(8), np.arange(8)] = 127.0
+    Cd1, Cd2 = bsg.bsgemm_i8_chain(dev(A), dev(B), dev(B2))
+    torch.cuda.synchronize()
+    C2o, _ = orc.bsgemm_i8(Co, B2, False)
+    assert_bits_equal(host(Cd2), C2o, "chain C2")
+    assert (host(Cd2)[1:] != (2.0 * 127.0 * rne[:, :8]).astype(np.float32)).any()
