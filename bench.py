@@ -893,6 +893,11 @@ def cpu_baseline(budget_s=15.0):
 def run_reference(args, rank, world):
     if rank != 0:
         return None
+    if world > 1:
+        # torchrun sets OMP_NUM_THREADS=1 for every rank; rank 0 runs the
+        # oracle alone, on the host's cores as at N = 1 (read when the
+        # oracle's OpenMP runtime loads, below)
+        os.environ["OMP_NUM_THREADS"] = str(len(os.sched_getaffinity(0)))
     import oracle
     orc = oracle.load()
     smp = OracleSample(orc, oracle_inputs())
