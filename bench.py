@@ -1036,7 +1036,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     line = run_gpu(args, rank, world, local_rank)
     if line is not None:
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and world == 1:   # the CPU baseline is an N = 1 figure
             line["cpu_baseline"] = cpu_baseline()
         print(json.dumps(line), flush=True)
     if world > 1:
