@@ -776,6 +776,41 @@ def run_configs(args):
                   "chain_us": round(ch_us, 1), "two_units_us": round(two_us, 1),
                   "requant_us": round(rq_us, 1), "unit_then_quantize_rows_us": round(uq_us, 1)})
     del Xm, W1, W2, C1, C2, cws, uws1, uws2
+    # the live audit (f2): 4096 seeded cells of a finished qkv unit, and the
+    # init gate (probe + known answer + audit of 4096 cells), per call
+    A, B, _ = inputs.gpt2_linear_inputs("qkv")
+    A, B = A.to(dev), B.to(dev)
+    Cq = bsg.bsgemm_i8(A, B)
+    mism = torch.zeros(1, dtype=torch.int32, device=dev)
+    a_us = timed(lambda: bsg.audit(A, B, Cq, nsamples=4096, mismatches=mism))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(5):
+        bsg.selftest()
+    st_ms = (time.perf_counter() - t0) / 5 * 1e3
+    lines.append({"config": "f2 live audit, 4096 cells of qkv 8192x2304x768",
+                  "audit_us": round(a_us, 1), "mismatches": int(mism.item()),
+                  "selftest_ms_host": round(st_ms, 2)})
+    del A, B, Cq
+    # the weight storage (f4): codes and stored weights of a GPT-2 fc weight
+    # and of an 8192 x 8192 one.  Bytes: the weight read twice (maximum, then
+    # codes) + codes written; codes read + f32 written.
+    for K, N in ((768, 3072), (8192, 8192)):
+        Wt = inputs.gpt2_weights(K, N, 5).to(dev)
+        for bits in (8, 4):
+            cb = 1.0 if bits == 8 else 0.5
+            q_us = timed(lambda: bsg.wquant_cols(Wt, bits=bits))
+            Q, sc = bsg.wquant_cols(Wt, bits=bits)
+            d_us = timed(lambda: bsg.wdequant_cols(Q, sc, N, bits=bits))
+            qb = K * N * (8 + cb)
+            db = K * N * (cb + 4)
+            lines.append({"config": f"f4 weight storage int{bits} {K}x{N}",
+                          "wquant_us": round(q_us, 2), "wquant_gbs": round(qb / q_us / 1e3, 1),
+                          "wquant_frac_of_measured_hbm": round(qb / q_us / 1e3 / hbm_peak, 3),
+                          "wdequant_us": round(d_us, 2), "wdequant_gbs": round(db / d_us / 1e3, 1),
+                          "wdequant_frac_of_measured_hbm": round(db / d_us / 1e3 / hbm_peak, 3),
+                          "bytes": "wquant: 8 B read (twice) + code bytes; wdequant: code bytes + 4 B"})
+        del Wt
     X, W, dY = (t.to(dev) for t in inputs.train_trio())
     trio = [(X, W, False, False, False), (dY, W, False, True, False), (X, dY, True, False, False)]
     gws = bsg.Workspace(dev)

@@ -33,7 +33,8 @@ def weights(K, N, seed, std=1.0):
     return W
 
 
-@pytest.mark.parametrize("shape", [(37, 23), (5, 1), (300, 7), (1000, 66), (64, 1)],
+@pytest.mark.parametrize("shape", [(37, 23), (5, 1), (300, 7), (1000, 66), (64, 1), (5000, 77),
+                                   (8192, 40), (257, 130)],
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("bits_", [8, 4])
 @pytest.mark.parametrize("pow2", [False, True], ids=["absmax", "pow2"])
@@ -76,3 +77,25 @@ def test_nonfinite_sets_status():
     bsg.wquant_cols(dev(W), 8, False, dstatus=st)
     torch.cuda.synchronize()
     assert int(st.item()) & 1
+
+
+@pytest.mark.parametrize("bits_", [8, 4])
+def test_unaligned_weight_rows(orc, bits_):
+    """A weight whose rows are not 16-byte aligned (a column slice of a wider
+    matrix, ldw = 69): the element-by-element load path, against the oracle."""
+    K, N, ldw = 600, 66, 69
+    Wfull = weights(K, ldw, 11 + bits_)
+    Wd = dev(Wfull)
+    width = N if bits_ == 8 else (N + 1) // 2
+    Q = torch.zeros((K, width), dtype=torch.int8 if bits_ == 8 else torch.uint8, device="cuda")
+    sc = torch.zeros(N, dtype=torch.float32, device="cuda")
+    import ctypes
+    rc = bsg.load().bsg_wquant_cols(ctypes.c_void_p(Wd.data_ptr()), K, N, ldw, bits_, 0,
+                                    ctypes.c_void_p(Q.data_ptr()), width,
+                                    ctypes.c_void_p(sc.data_ptr()), None, None)
+    assert rc == 0
+    torch.cuda.synchronize()
+    Qo, so, _ = orc.wquant_cols(np.ascontiguousarray(Wfull[:, :N]), bits_, False)
+    assert_bits_equal(host(sc), so, "scales")
+    want = Qo if bits_ == 8 else orc.pack_int4(Qo)
+    assert (host(Q) == want).all()

@@ -15,16 +15,23 @@
 // to a byte along each row (column 2i in bits 0-3 of byte i, 2i+1 in bits
 // 4-7, the high nibble of a last odd column zero).
 //
-// One CTA per strip of 32 columns reads the strip twice: once for the column
-// maxima, once (from L2) to quantize.  The quotient is taken in f64 and
-// rounded to an integer with ties to even: its f64 rounding error (2^-53
-// relative) is far below the distance (~2^-25 relative) at which an f32
-// quotient that is not exactly k + 1/2 can lie from k + 1/2, so the integer
-// is the one nearest the exact quotient.
+// A strip of 32 columns is quantized by a cluster of CTAs, each owning a slice
+// of its rows: each reads its slice for the column maxima, the cluster
+// combines them through distributed shared memory, and each reads its slice
+// again (from L2) to quantize it.  The code is the integer nearest the exact
+// quotient w / s, ties to even, found with integer arithmetic on the two
+// floats' significands (no divide is rounded before the comparison): 2|w|/s
+// = mw * 2^sh / ms exactly, its integer part and remainder decide the
+// rounding.  The f64 divide the first version used per element ran on
+// GB300's FP64 pipe and made the kernel compute-bound.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "bsg_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace bsg {
 namespace {
@@ -46,28 +53,99 @@ __device__ __forceinline__ float wq_pow2_up(float s) {
     return __uint_as_float(p);
 }
 
-template <int BITS, bool POW2>
+// The integer nearest w / s, ties to even, clamped to [-qmax, qmax]; w and s
+// finite, s > 0.  With w = mw 2^(ew-150) and s = ms 2^(es-150) (significands
+// with the implicit bit; subnormals take exponent field 1 and no implicit
+// bit), 2|w|/s = mw 2^sh / ms with sh = ew - es + 1, a ratio of integers.
+__device__ __forceinline__ int wq_round_quotient_exact(float w, float s, int qmax) {
+    const uint32_t wb = __float_as_uint(w);
+    const uint32_t aw = wb & 0x7fffffffu;
+    const int neg = (int)(wb >> 31);
+    if (aw == 0) return 0;
+    const uint32_t sb = __float_as_uint(s);
+    const int ew = (int)(aw >> 23), es = (int)(sb >> 23);
+    const uint64_t mw = (aw & 0x7fffffu) | (ew ? 0x800000u : 0u);
+    const uint64_t ms = (sb & 0x7fffffu) | (es ? 0x800000u : 0u);
+    const int sh = (ew ? ew : 1) - (es ? es : 1) + 1;
+    // sh <= -25: 2|w|/s < 2^24 2^-25 = 1/2, so |w|/s < 1/4 and the code is 0;
+    // sh >= 33: 2|w|/s > 2^33 / 2^24 = 512, beyond any qmax
+    if (sh <= -25) return 0;
+    if (sh >= 33) return neg ? -qmax : qmax;
+    const uint64_t num = sh >= 0 ? mw << sh : mw;          // < 2^56
+    const uint64_t den = sh >= 0 ? ms : ms << (-sh);        // < 2^48
+    if (num >= (uint64_t)(2 * qmax + 2) * den) return neg ? -qmax : qmax;  // |w|/s >= qmax + 1
+    // q2 = floor(2|w|/s) <= 2 qmax + 1: a float estimate, corrected exactly
+    uint32_t q2 = (uint32_t)__fdividef((float)num, (float)den);
+    if ((uint64_t)q2 * den > num) --q2;
+    if ((uint64_t)(q2 + 1) * den <= num) ++q2;
+    const uint64_t rem = num - (uint64_t)q2 * den;
+    uint32_t q = q2 >> 1;                                   // |w|/s = q + (q2 odd) / 2 + rem / (2 den)
+    if (q2 & 1) q += (rem != 0 || (q & 1)) ? 1u : 0u;       // above a half: up; on it: to even
+    if ((int)q > qmax) q = (uint32_t)qmax;
+    return neg ? -(int)q : (int)q;
+}
+
+// The same integer, first from the correctly rounded f32 quotient x: its
+// error is at most half an ulp (2^-18 below 128), so when x lies more than
+// 2^-16 from the nearest half-integer h, the exact quotient lies on the same
+// side of h and rounds to rint(x).  (x - h is exact there: for |x| >= 1, x and
+// h are within a factor of two; below, h = +-1/2 and |x - h| >= 1/4 unless
+// |x| >= 1/4.)  Only quotients near a half-integer take the exact path.
+__device__ __forceinline__ int wq_round_quotient(float w, float s, int qmax) {
+    const float x = __fdiv_rn(w, s);
+    const float ax = fabsf(x);
+    if (ax < 128.0f) {
+        const float h = __fadd_rn(floorf(x), 0.5f);
+        if (fabsf(__fsub_rn(x, h)) > 0x1p-16f) {
+            const int q = (int)rintf(x);
+            return q < -qmax ? -qmax : (q > qmax ? qmax : q);
+        }
+    }
+    return wq_round_quotient_exact(w, s, qmax);
+}
+
+// grid (strips, CS), cluster (1, CS, 1): CTA `rank` owns rows [rank R, rank R + R).
+// VEC: W 16-byte aligned with ldw % 4 == 0 (float4 loads of each 4-column group).
+template <int BITS, bool POW2, bool VEC>
 __global__ void __launch_bounds__(256)
-    wquant_cols_kernel(const float *__restrict__ W, int64_t K, int64_t N, int64_t ldw,
-                       uint8_t *__restrict__ Q, int64_t ldq, float *__restrict__ scale,
-                       int32_t *__restrict__ dstatus) {
-    constexpr float kQmax = BITS == 8 ? 127.0f : 7.0f;
+    wquant_cols_kernel(const float *__restrict__ W, int64_t K, int64_t N, int64_t ldw, int R,
+                       uint8_t *__restrict__ Q, int64_t ldq, int qvec,
+                       float *__restrict__ scale, int32_t *__restrict__ dstatus) {
+    constexpr int kQmax = BITS == 8 ? 127 : 7;
     __shared__ uint32_t red[32][33];
+    __shared__ uint32_t part[kWStrip];
     __shared__ float s_col[kWStrip];
     __shared__ int s_bad;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int cs = (int)cluster.num_blocks();
     const int t = threadIdx.x;
     const int c4 = t & 7, rs = t >> 3;
     const int64_t col = (int64_t)blockIdx.x * kWStrip + 4 * c4;
-    auto load = [&](int64_t r, int u) -> float {
-        return col + u < N ? __ldg(W + r * ldw + col + u) : 0.0f;
+    const int64_t r0 = (int64_t)rank * R;
+    const int64_t left = K - r0;
+    const int nr = left <= 0 ? 0 : (left < R ? (int)left : R);
+    const bool full4 = col + 3 < N;
+    auto load4 = [&](int r) {
+        const float *p = W + (r0 + r) * ldw + col;
+        if (VEC && full4) return __ldg(reinterpret_cast<const float4 *>(p));
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (col < N) v.x = __ldg(p);
+        if (col + 1 < N) v.y = __ldg(p + 1);
+        if (col + 2 < N) v.z = __ldg(p + 2);
+        if (col + 3 < N) v.w = __ldg(p + 3);
+        return v;
     };
     if (t == 0) s_bad = 0;
     uint32_t m[4] = {0u, 0u, 0u, 0u};  // |x| bit patterns: NaN left out, Inf kept
     bool bad = false;
-    for (int64_t r = rs; r < K; r += 32) {
+#pragma unroll 4
+    for (int r = rs; r < nr; r += 32) {
+        const float4 v = load4(r);
+        const float x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const uint32_t a = wq_absbits(load(r, u));
+            const uint32_t a = wq_absbits(x[u]);
             if (a <= 0x7f800000u) m[u] = max(m[u], a);
             bad = bad || a >= 0x7f800000u;
         }
@@ -78,61 +156,157 @@ __global__ void __launch_bounds__(256)
     if (bad) s_bad = 1;
     if (t < kWStrip) {
         uint32_t mm = 0;
+#pragma unroll 8
         for (int i = 0; i < 32; ++i) mm = max(mm, red[i][t]);
-        const int64_t j = (int64_t)blockIdx.x * kWStrip + t;
-        float s = __fdiv_rn(__uint_as_float(mm), kQmax);
-        if (POW2 && isfinite(s)) s = wq_pow2_up(s);
-        s_col[t] = s;
-        if (j < N) scale[j] = s;
+        part[t] = mm;
     }
-    __syncthreads();
-    if (t == 0 && s_bad && dstatus) atomicOr(dstatus, 1);  // Inf or NaN in this strip
+    cluster.sync();  // every CTA's partial maxima are visible cluster-wide
+    if (t < kWStrip) {
+        uint32_t mm = 0;
+        for (int k = 0; k < cs; ++k) mm = max(mm, *cluster.map_shared_rank(&part[t], k));
+        const int64_t j = (int64_t)blockIdx.x * kWStrip + t;
+        float sc = __fdiv_rn(__uint_as_float(mm), (float)kQmax);
+        if (POW2 && isfinite(sc)) sc = wq_pow2_up(sc);
+        s_col[t] = sc;
+        if (rank == 0 && j < N) scale[j] = sc;
+    }
+    if (t == 0 && s_bad && dstatus) atomicOr(dstatus, 1);  // Inf or NaN in this slice
+    cluster.sync();  // s_col is complete; no CTA leaves while another reads its maxima
     float sv[4];
+    bool use[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) sv[u] = s_col[4 * c4 + u];
-    for (int64_t r = rs; r < K; r += 32) {
+    for (int u = 0; u < 4; ++u) {
+        sv[u] = s_col[4 * c4 + u];
+        use[u] = sv[u] != 0.0f && isfinite(sv[u]);
+    }
+#pragma unroll 4
+    for (int r = rs; r < nr; r += 32) {
+        const float4 v = load4(r);
+        const float x[4] = {v.x, v.y, v.z, v.w};
         int q[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float w = load(r, u);
-            int v = 0;
-            if (sv[u] != 0.0f && isfinite(sv[u]) && isfinite(w))
-                v = __double2int_rn(__ddiv_rn((double)w, (double)sv[u]));
-            q[u] = v < -(int)kQmax ? -(int)kQmax : (v > (int)kQmax ? (int)kQmax : v);
-        }
-        uint8_t *row = Q + r * ldq;
+        for (int u = 0; u < 4; ++u)
+            q[u] = (use[u] && isfinite(x[u])) ? wq_round_quotient(x[u], sv[u], kQmax) : 0;
+        uint8_t *row = Q + (r0 + r) * ldq;
         if (BITS == 8) {
+            if (qvec && full4) {
+                *reinterpret_cast<char4 *>(row + col) =
+                    make_char4((signed char)q[0], (signed char)q[1], (signed char)q[2],
+                               (signed char)q[3]);
+            } else {
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (col + u < N) row[col + u] = (uint8_t)(int8_t)q[u];
+                for (int u = 0; u < 4; ++u)
+                    if (col + u < N) row[col + u] = (uint8_t)(int8_t)q[u];
+            }
         } else {
-            // columns col..col+3 (col even) -> bytes col/2 and col/2 + 1
-            if (col < N)
-                row[col / 2] = (uint8_t)((q[0] & 0xf) | ((col + 1 < N ? q[1] & 0xf : 0) << 4));
-            if (col + 2 < N)
-                row[col / 2 + 1] = (uint8_t)((q[2] & 0xf) | ((col + 3 < N ? q[3] & 0xf : 0) << 4));
+            // columns col..col+3 (col % 4 == 0) -> bytes col/2 and col/2 + 1
+            const uint8_t b0 = (uint8_t)((q[0] & 0xf) | ((col + 1 < N ? q[1] & 0xf : 0) << 4));
+            const uint8_t b1 = (uint8_t)((q[2] & 0xf) | ((col + 3 < N ? q[3] & 0xf : 0) << 4));
+            if (qvec && col + 2 < N) {
+                *reinterpret_cast<uint16_t *>(row + col / 2) = (uint16_t)(b0 | (b1 << 8));
+            } else {
+                if (col < N) row[col / 2] = b0;
+                if (col + 2 < N) row[col / 2 + 1] = b1;
+            }
         }
     }
 }
 
-template <int BITS>
-__global__ void wdequant_cols_kernel(const uint8_t *__restrict__ Q, int64_t K, int64_t N,
-                                     int64_t ldq, const float *__restrict__ scale,
-                                     float *__restrict__ out, int64_t ldo) {
-    const int64_t total = K * N;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t k = e / N, j = e - k * N;
-        int q;
+// out[k][j] = f32(q * s_j).  grid (column blocks of 1024, row groups); each
+// thread takes 4 consecutive columns of one row at a time.  VEC: 4-byte (int8)
+// or 2-byte (int4) code loads and 16-byte stores.
+template <int BITS, bool VEC>
+__global__ void __launch_bounds__(256)
+    wdequant_cols_kernel(const uint8_t *__restrict__ Q, int64_t K, int64_t N, int64_t ldq,
+                         const float *__restrict__ scale, float *__restrict__ out,
+                         int64_t ldo) {
+    const int64_t c = ((int64_t)blockIdx.x * 256 + threadIdx.x) * 4;
+    if (c >= N) return;
+    const bool full4 = c + 3 < N;
+    float sv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) sv[u] = c + u < N ? __ldg(scale + c + u) : 0.0f;
+    for (int64_t r = blockIdx.y; r < K; r += gridDim.y) {
+        const uint8_t *qr = Q + r * ldq;
+        int q[4] = {0, 0, 0, 0};
         if (BITS == 8) {
-            q = (int8_t)Q[k * ldq + j];
+            if (VEC && full4) {
+                const char4 v = *reinterpret_cast<const char4 *>(qr + c);
+                q[0] = v.x; q[1] = v.y; q[2] = v.z; q[3] = v.w;
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (c + u < N) q[u] = (int8_t)qr[c + u];
+            }
         } else {
-            const uint8_t byte = Q[k * ldq + j / 2];
-            const int nib = (j & 1) ? (byte >> 4) : (byte & 0xf);
-            q = nib >= 8 ? nib - 16 : nib;
+            uint32_t bytes;
+            if (VEC && c + 2 < N)
+                bytes = *reinterpret_cast<const uint16_t *>(qr + c / 2);
+            else
+                bytes = qr[c / 2] | (c + 2 < N ? (uint32_t)qr[c / 2 + 1] << 8 : 0u);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int nib = (int)((bytes >> (4 * u)) & 0xfu);
+                q[u] = nib >= 8 ? nib - 16 : nib;
+            }
         }
-        out[k * ldo + j] = __fmul_rn((float)q, scale[j]);
+        float o[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) o[u] = __fmul_rn((float)q[u], sv[u]);
+        float *orow = out + r * ldo;
+        if (VEC && full4) {
+            *reinterpret_cast<float4 *>(orow + c) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (c + u < N) orow[c + u] = o[u];
+        }
     }
+}
+
+
+template <int BITS, bool POW2, bool VEC>
+static cudaError_t launch_wq(const float *W, int64_t K, int64_t N, int64_t ldw, uint8_t *Q,
+                            int64_t ldq, int qvec, float *scale, int32_t *dstatus,
+                            cudaStream_t st) {
+    static bool ready[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!ready[dev]) {  // clusters of up to 16 CTAs
+        const cudaError_t e = cudaFuncSetAttribute(wquant_cols_kernel<BITS, POW2, VEC>,
+                                                   cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        ready[dev] = true;
+    }
+    // a CTA per 256 rows of the strip, at most 16 (longer slices beyond 4096 rows)
+    int cs = (int)((K + 255) / 256);
+    cs = cs < 1 ? 1 : (cs > 16 ? 16 : cs);
+    const int R = (int)((K + cs - 1) / cs);
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)((N + kWStrip - 1) / kWStrip), (unsigned)cs, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)cs;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, wquant_cols_kernel<BITS, POW2, VEC>, W, K, N,
+                                             ldw, R, Q, ldq, qvec, scale, dstatus);
+    count_launches(1);
+    return e;
+}
+
+template <int BITS, bool POW2>
+static cudaError_t launch_wq_vec(const float *W, int64_t K, int64_t N, int64_t ldw, uint8_t *Q,
+                                int64_t ldq, int qvec, float *scale, int32_t *dstatus,
+                                cudaStream_t st) {
+    const bool vec = ldw % 4 == 0 && reinterpret_cast<uintptr_t>(W) % 16 == 0;
+    return vec ? launch_wq<BITS, POW2, true>(W, K, N, ldw, Q, ldq, qvec, scale, dstatus, st)
+               : launch_wq<BITS, POW2, false>(W, K, N, ldw, Q, ldq, qvec, scale, dstatus, st);
 }
 
 }  // namespace
@@ -140,30 +314,39 @@ __global__ void wdequant_cols_kernel(const uint8_t *__restrict__ Q, int64_t K, i
 cudaError_t launch_wquant_cols(const float *W, int64_t K, int64_t N, int64_t ldw, int bits,
                                int pow2, void *Q, int64_t ldq, float *scale, int32_t *dstatus,
                                cudaStream_t st) {
-    const unsigned grid = (unsigned)((N + kWStrip - 1) / kWStrip);
     uint8_t *q = static_cast<uint8_t *>(Q);
-    if (bits == 8 && !pow2)
-        wquant_cols_kernel<8, false><<<grid, 256, 0, st>>>(W, K, N, ldw, q, ldq, scale, dstatus);
-    else if (bits == 8)
-        wquant_cols_kernel<8, true><<<grid, 256, 0, st>>>(W, K, N, ldw, q, ldq, scale, dstatus);
-    else if (!pow2)
-        wquant_cols_kernel<4, false><<<grid, 256, 0, st>>>(W, K, N, ldw, q, ldq, scale, dstatus);
-    else
-        wquant_cols_kernel<4, true><<<grid, 256, 0, st>>>(W, K, N, ldw, q, ldq, scale, dstatus);
-    count_launches(1);
-    return cudaGetLastError();
+    const uintptr_t qa = reinterpret_cast<uintptr_t>(Q);
+    const int qvec = bits == 8 ? (ldq % 4 == 0 && qa % 4 == 0) : (ldq % 2 == 0 && qa % 2 == 0);
+    if (bits == 8)
+        return pow2 ? launch_wq_vec<8, true>(W, K, N, ldw, q, ldq, qvec, scale, dstatus, st)
+                    : launch_wq_vec<8, false>(W, K, N, ldw, q, ldq, qvec, scale, dstatus, st);
+    return pow2 ? launch_wq_vec<4, true>(W, K, N, ldw, q, ldq, qvec, scale, dstatus, st)
+                : launch_wq_vec<4, false>(W, K, N, ldw, q, ldq, qvec, scale, dstatus, st);
 }
 
 cudaError_t launch_wdequant_cols(const void *Q, int64_t K, int64_t N, int64_t ldq, int bits,
                                  const float *scale, float *out, int64_t ldo, cudaStream_t st) {
-    const int64_t blocks = (K * N + 255) / 256;
-    const int64_t cap = (int64_t)device_sm_count() * 8;
-    const unsigned grid = (unsigned)(blocks < cap ? (blocks < 1 ? 1 : blocks) : cap);
     const uint8_t *q = static_cast<const uint8_t *>(Q);
-    if (bits == 8)
-        wdequant_cols_kernel<8><<<grid, 256, 0, st>>>(q, K, N, ldq, scale, out, ldo);
-    else
-        wdequant_cols_kernel<4><<<grid, 256, 0, st>>>(q, K, N, ldq, scale, out, ldo);
+    const uintptr_t qa = reinterpret_cast<uintptr_t>(Q);
+    const bool vec = ldo % 4 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0 &&
+                     (bits == 8 ? (ldq % 4 == 0 && qa % 4 == 0) : (ldq % 2 == 0 && qa % 2 == 0));
+    const int64_t xblocks = (N + 1023) / 1024;
+    int64_t yblocks = ((int64_t)device_sm_count() * 16 + xblocks - 1) / xblocks;
+    if (yblocks > K) yblocks = K;
+    if (yblocks > 65535) yblocks = 65535;
+    if (yblocks < 1) yblocks = 1;
+    const dim3 grid((unsigned)xblocks, (unsigned)yblocks, 1);
+    if (bits == 8) {
+        if (vec)
+            wdequant_cols_kernel<8, true><<<grid, 256, 0, st>>>(q, K, N, ldq, scale, out, ldo);
+        else
+            wdequant_cols_kernel<8, false><<<grid, 256, 0, st>>>(q, K, N, ldq, scale, out, ldo);
+    } else {
+        if (vec)
+            wdequant_cols_kernel<4, true><<<grid, 256, 0, st>>>(q, K, N, ldq, scale, out, ldo);
+        else
+            wdequant_cols_kernel<4, false><<<grid, 256, 0, st>>>(q, K, N, ldq, scale, out, ldo);
+    }
     count_launches(1);
     return cudaGetLastError();
 }
