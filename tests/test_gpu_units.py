@@ -135,3 +135,30 @@ def test_scale_derivation_selftest_exhaustive():
     """The device's f32 scale derivation equals its own f64 definition for
     every finite non-negative absmax bit pattern."""
     assert bsg.selftest_scales(0, 0x7F7FFFFF) == 0
+
+
+@pytest.mark.parametrize("rows,cols,ldx", [(3, 20001, 20004), (40, 50304, 50304), (1, 16385, 16388)],
+                         ids=lambda v: str(v))
+def test_quantize_wide_rows_strided(orc, rows, cols, ldx):
+    """Rows longer than 16384 columns (maxima by segments, then one streaming
+    pass), with a row stride past the row and a tail that is not a whole
+    float4: codes, scales and inv against the oracle, and the padding of X
+    never read into the result."""
+    import ctypes
+    Xfull = inputs.adversarial(rows, ldx, rows + cols).numpy()
+    Xfull[:, cols:] = np.float32(1e30)          # padding that must not count
+    X = np.ascontiguousarray(Xfull[:, :cols])
+    Xd = dev(Xfull)
+    Q = torch.zeros(rows, cols, dtype=torch.int8, device="cuda")
+    sc = torch.zeros(rows, dtype=torch.float32, device="cuda")
+    iv = torch.zeros(rows, dtype=torch.float32, device="cuda")
+    rc = bsg.load().bsg_quantize_rows(ctypes.c_void_p(Xd.data_ptr()), rows, cols, ldx,
+                                      ctypes.c_void_p(Q.data_ptr()), cols,
+                                      ctypes.c_void_p(sc.data_ptr()), ctypes.c_void_p(iv.data_ptr()),
+                                      None, None)
+    assert rc == 0
+    torch.cuda.synchronize()
+    Qo, sco, ivo, _ = orc.quantize_rows(X)
+    assert_bits_equal(host(Q), Qo, "Q")
+    assert_bits_equal(host(sc), sco, "scale")
+    assert_bits_equal(host(iv), ivo, "inv")

@@ -914,6 +914,66 @@ size_t colmax_partial_bytes(int64_t rows, int64_t cols) {
     return (size_t)colmax_nsplit(rows, cols) * (size_t)cols * sizeof(uint32_t);
 }
 
+namespace {
+
+// Rows longer than the register-resident kernel takes (> 16384 columns):
+// each 256-thread block reduces one 8192-column segment of a row to its max
+// |x| bit pattern and folds it into rowmax[r] (zeroed before) by atomicMax;
+// the requantize kernel then quantizes the rows in one streaming pass.  VEC:
+// X 16-byte aligned with ldx % 4 == 0 (then cols % 4 may be anything: the
+// tail is read element by element).
+constexpr int kRmSeg = 256 * 4 * 8;  // columns per block
+
+__global__ void __launch_bounds__(256)
+    rowmax_seg_kernel(const float *__restrict__ X, int64_t rows, int64_t cols, int64_t ldx,
+                      uint32_t *__restrict__ rowmax) {
+    __shared__ uint32_t wmax[8];
+    const int64_t c0 = (int64_t)blockIdx.x * kRmSeg;
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+        const float *xr = X + r * ldx;
+        uint32_t m = 0;
+        const int64_t c4n = cols / 4;
+        float4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int64_t c4 = c0 / 4 + threadIdx.x + 256 * i;
+            v[i] = c4 < c4n ? __ldcs(reinterpret_cast<const float4 *>(xr) + c4)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            m = max(m, max(max(absbits(v[i].x), absbits(v[i].y)),
+                           max(absbits(v[i].z), absbits(v[i].w))));
+        // the tail past the last whole float4, in the last segment
+        for (int64_t c = 4 * c4n + threadIdx.x; c < cols && c >= c0 && c < c0 + kRmSeg; c += 256)
+            m = max(m, absbits(__ldg(xr + c)));
+        m = __reduce_max_sync(0xffffffffu, m);
+        if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            uint32_t mm = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) mm = max(mm, wmax[w]);
+            atomicMax(rowmax + r, mm);
+        }
+        __syncthreads();
+    }
+}
+
+// scale[r] and inv[r] from the max bit pattern left in scale[r] (in place).
+__global__ void scales_from_bits_kernel(int64_t rows, float *__restrict__ scale,
+                                        float *__restrict__ inv) {
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows;
+         r += (int64_t)gridDim.x * blockDim.x) {
+        float sc, iv;
+        scale_from_max(__float_as_uint(scale[r]), sc, iv);
+        scale[r] = sc;
+        if (inv) inv[r] = iv;
+    }
+}
+
+}  // namespace
+
 static int grid_for(int64_t work, int per_block) {
     const int64_t b = (work + per_block - 1) / per_block;
     const int64_t cap = (int64_t)device_sm_count() * 32;
@@ -992,6 +1052,23 @@ cudaError_t launch_quantize_rows(const float *X, int64_t rows, int64_t cols, int
         return cudaErrorInvalidValue;
     if (zrows && cudaMemsetAsync(zrows, 0, (size_t)rows * sizeof(unsigned int), st) != cudaSuccess)
         return cudaErrorInvalidValue;
+    // rows beyond the register-resident kernel: row maxima by segments (kept
+    // in scale[] as bit patterns), the streaming requantize, then the scales
+    if (cols > 16384 && ldx % 4 == 0 && reinterpret_cast<uintptr_t>(X) % 16 == 0) {
+        uint32_t *mx = reinterpret_cast<uint32_t *>(scale);
+        if (cudaMemsetAsync(mx, 0, (size_t)rows * sizeof(uint32_t), st) != cudaSuccess)
+            return cudaErrorInvalidValue;
+        const int64_t nseg = (cols + kRmSeg - 1) / kRmSeg;
+        const dim3 g1((unsigned)nseg, (unsigned)(rows < 65535 ? rows : 65535), 1);
+        rowmax_seg_kernel<<<g1, 256, 0, st>>>(X, rows, cols, ldx, mx);
+        count_launches(1);
+        cudaError_t e = launch_requant_rows(X, rows, cols, ldx, mx, out_kind, Q, ldq, nullptr,
+                                            nullptr, dstatus, st, nullptr);
+        if (e != cudaSuccess) return e;
+        scales_from_bits_kernel<<<grid_for(rows, 256), 256, 0, st>>>(rows, scale, inv);
+        count_launches(1);
+        return cudaGetLastError();
+    }
     const int grid = grid_for(rows, kRowWarps);
     const bool vec2 = (ldx % 4 == 0) && (reinterpret_cast<uintptr_t>(X) % 16 == 0) &&
                       ((ldq * qesz) % qalign == 0) && (reinterpret_cast<uintptr_t>(Q) % qalign == 0);
