@@ -408,11 +408,10 @@ def summarize(W, step_ms, stage_ms, peaks, peak_kind, ms_max, world, profile):
     f16_extra = [2 * (u["M"] * u["K"] + u["K"] * u["N"]) for u in units]
     hbm = float(peaks.get("hbm_gbs", 6800.0))
     q_gbs = sum(qbytes) / (sum(quant_ms) * 1e-3) / 1e9
-    # bytes the kernels actually move: A read once and its f16 operand written
-    # (6 B per element); B the same when its columns fit the single-pass strip
-    # kernel (K <= 4096, rows 16-byte aligned), else read twice (10 B)
-    moved = [6 * u["M"] * u["K"] + (6 if (u["K"] <= 4096 and u["N"] % 4 == 0) else 10)
-             * u["K"] * u["N"] for u in units]
+    # bytes the kernels move to and from HBM: each operand read once and its
+    # f16 operand written, 6 B per element (columns longer than the strip
+    # kernel holds are read a second time, from L2)
+    moved = [6 * (u["M"] * u["K"] + u["K"] * u["N"]) for u in units]
     roof = {
         "bound": "tensor",
         "kernel": "gemm_tc_kernel (tcgen05 kind::f16, exact int8 contraction + epilogue)",
@@ -444,8 +443,9 @@ def summarize(W, step_ms, stage_ms, peaks, peak_kind, ms_max, world, profile):
         "moved_bytes": sum(moved),
         "moved_gbs": round(sum(moved) / (sum(quant_ms) * 1e-3) / 1e9, 1),
         "moved_frac": round(sum(moved) / (sum(quant_ms) * 1e-3) / 1e9 / hbm, 4),
-        "moved_note": ("bytes the kernels move: A read once + f16 operand written (6 B per "
-                       "element); B likewise when K <= 4096, else read twice (10 B)"),
+        "moved_note": ("HBM bytes the kernels move: A and B read once + their f16 operands "
+                       "written (6 B per element); B's columns longer than 4096 rows are read "
+                       "again from L2"),
         "per_gemm_ms": {u["name"]: round(q, 4) for u, q in zip(units, quant_ms)},
         "per_gemm_frac": {u["name"]: round(b / (q * 1e-3) / 1e9 / hbm, 4)
                           for u, b, q in zip(units, qbytes, quant_ms)},

@@ -105,14 +105,15 @@ COL_SHAPES = [(64, 300, 4097), (130, 129, 5000), (40, 257, 8191), (33, 1000, 900
               (24, 96, 16384), (50, 77, 1000), (3, 5, 7)]
 
 
-@pytest.mark.parametrize("path", ["strip", "twopass", ""])
+@pytest.mark.parametrize("path", ["strip", "lag", "twopass", ""])
 @pytest.mark.parametrize("M,N,K", COL_SHAPES, ids=lambda v: str(v))
 def test_every_column_quantize_path_operand(orc, monkeypatch, path, M, N, K):
-    """Each column-quantize path (register strips in clusters, two passes)
-    forced in turn into the GEMM's f16 operand, on columns with the
-    adversarial kinds, short, long, odd and ragged: C bitwise equal to the
-    oracle's.  Strips do not apply beyond 4096 rows; those shapes take two
-    passes whatever is asked."""
+    """Each column-quantize path (register strips in clusters, the one-read
+    list of max and quantize items, two passes) forced in turn into the
+    GEMM's f16 operand, on columns with the adversarial kinds, short, long,
+    odd and ragged: C bitwise equal to the oracle's.  Strips do not apply
+    beyond 4096 rows; those shapes take the one-read path unless two passes
+    are forced."""
     monkeypatch.setenv("BSG_COLS_PATH", path)
     A = inputs.normal((M, K), 1.0, M + K).numpy()
     B = inputs.adversarial(N, K, N + K + 1, along_rows=False).numpy()
@@ -120,6 +121,27 @@ def test_every_column_quantize_path_operand(orc, monkeypatch, path, M, N, K):
     torch.cuda.synchronize()
     Co, _ = orc.bsgemm_i8(A, B, False)
     assert_bits_equal(host(C), Co, f"{path} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("lag", ["1", "2", "7", "4096"])
+@pytest.mark.parametrize("M,N,K", [(64, 999, 5000), (40, 129, 16384), (8, 3001, 600)],
+                         ids=lambda v: str(v))
+def test_one_read_column_quantize_any_lag(orc, monkeypatch, lag, M, N, K):
+    """The one-read column quantize with its lag forced from one panel (each
+    panel's quantize items right after the next panel's max items) to more
+    panels than there are (all max items first): the same bits every time,
+    the oracle's.  N is odd, so B's rows are not 16-byte aligned, which the
+    path's scalar loads take as they are."""
+    monkeypatch.setenv("BSG_COLS_PATH", "lag")
+    monkeypatch.setenv("BSG_COLQ_LAG", lag)
+    A = inputs.normal((M, K), 1.0, 3 * M + K).numpy()
+    B = inputs.adversarial(N, K, N + K + 5, along_rows=False).numpy()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    C = bsg.bsgemm_i8(dev(A), dev(B), dstatus=st)
+    torch.cuda.synchronize()
+    Co, _ = orc.bsgemm_i8(A, B, False)
+    assert_bits_equal(host(C), Co, f"lag {lag} {M}x{N}x{K}")
+    assert not int(st.item()) & 2, "a bounded wait expired"
 
 
 @pytest.mark.parametrize("path", ["twopass", ""])

@@ -52,9 +52,11 @@ cudaError_t launch_quantize_rows(const float *X, int64_t rows, int64_t cols, int
 // bsgemm_i8_ex); bsgemm_i8_workspace_size is the largest over the layouts.
 size_t unit_workspace_bytes(int64_t M, int64_t N, int64_t K, int transA, int transB);
 
-// Columns: a partial-max pass over row slices, then a quantize pass.
-// kOutInt8 keeps X's layout (Q is rows x cols); kOutHalfKMajor writes the
-// transpose (Q is cols x ldq, each row a column of X).
+// Columns.  kOutInt8 keeps X's layout (Q is rows x cols): clusters, or a
+// partial-max pass over row slices then a quantize pass.  kOutHalfKMajor
+// writes the transpose (Q is cols x ldq, each row a column of X): register
+// strips in clusters, or one HBM read through a list of max and quantize
+// items.  `partial` is colmax_partial_bytes(rows, cols) of scratch.
 cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int64_t ldx,
                                  int out_kind, void *Q, int64_t ldq, float *scale, float *inv,
                                  uint32_t *partial, int32_t *dstatus, cudaStream_t st);

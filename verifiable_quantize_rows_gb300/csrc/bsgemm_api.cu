@@ -57,9 +57,10 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 //   sb   f32 [round_up(N, 256) + 256] (a tile of any width may read its
 //        whole last tile of scales; entries past N are never used)
 //   the GEMM's tile counter (one uint32 in 256 bytes)
-//   partial column maxima (uint32) of op(A), then of op(B), for the
-//   column quantizes that need two passes (separate, since the two
-//   operands may be quantized at the same time)
+//   column-quantize scratch (uint32: partial or whole column maxima and
+//   the one-read path's counters) of op(A), then of op(B), for columns
+//   longer than the strip kernel holds (separate, since the two operands
+//   may be quantized at the same time)
 struct UnitLayout {
     size_t aop, bop, sa, sb, ticket, part, part_b, total;
 };

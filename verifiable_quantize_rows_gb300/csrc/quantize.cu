@@ -14,9 +14,11 @@
 // >= 0x7f800000).  Columns of up to 4096 rows are read once too: a strip of
 // 32 columns sits in the registers of a cluster of CTAs, which exchange
 // their partial maxima through distributed shared memory (fused with the
-// row quantize of A in one launch when K <= 2048).  Longer columns take a
-// partial-max pass over row slices, then a quantize pass whose tiles also
-// transpose B into the GEMM's K-major operand.
+// row quantize of A in one launch when K <= 2048).  Longer columns are read
+// once from HBM into the GEMM's K-major operand by a list of max and
+// quantize items whose second read of each tile comes from L2; the int8
+// codes in X's layout take a partial-max pass over row slices, then a
+// quantize pass.
 #include <cooperative_groups.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -841,6 +843,209 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Column quantize into the GEMM's K-major f16 operand with one read of X
+// from HBM, for columns too long for the strip kernel.  The work is a list
+// of items, each a run of rows of one 128-column panel.  For each panel the
+// list holds first its max items (the tile's |x| maxima, atomicMax into the
+// panel's column maxima, then one count on the panel's counter) and, `lag`
+// panels further on, its quantize items, which read the same tiles again --
+// from L2, where the max items left them -- wait until the panel's count is
+// complete, and write the transposed codes.  CTAs claim items in list order
+// from a counter and work through the items they hold in the order they
+// claimed them.  A max item never waits, and all of a panel's max items
+// come before its quantize items in the list, so the lowest unfinished item
+// is always being worked on and never waits on anything unfinished: every
+// wait ends.  The wait is bounded all the same.
+//
+// Each thread reads one column of 32 rows straight into registers (the
+// lanes of a warp take consecutive columns, so each load instruction reads
+// one 128-byte line); a slice is 32 RQ rows (RQ warps per 32-column group)
+// and an item covers kLagChunk consecutive slices of its panel, so the
+// atomics, the fence and the wait are paid once per item.  Measured on a
+// GB300 (16384 x 16384 B): RQ = 2 with 2 slices per item 344 us, RQ = 4 or
+// one slice per item 380-410 us, 4 or 8 slices 400-570 us; the two-pass
+// kernels 442 us.  A version that staged the tiles in a 3-stage
+// shared-memory ring by cp.async, one CTA per SM, ran at half this speed:
+// the chain of barriers, atomics and waits of each item then stalls the SM.
+constexpr int kLagCols = 128;
+constexpr int kLagRq = 2;
+constexpr int kLagChunk = 2;
+
+// Item `it` of the list for P panels of S slices and a lag of L panels.
+__device__ __forceinline__ void lag_item(int64_t it, int64_t P, int64_t S, int64_t L,
+                                         bool &quantize, int64_t &panel, int64_t &slice) {
+    const int64_t lead = P < L ? P : L;      // panels whose max items come alone
+    const int64_t both = P > L ? P - L : 0;  // steps with max and quantize items
+    if (it < lead * S) {
+        quantize = false;
+        panel = it / S;
+        slice = it % S;
+        return;
+    }
+    it -= lead * S;
+    if (it < both * 2 * S) {
+        const int64_t step = L + it / (2 * S), r = it % (2 * S);
+        quantize = r >= S;
+        panel = quantize ? step - L : step;
+        slice = quantize ? r - S : r;
+        return;
+    }
+    it -= both * 2 * S;
+    quantize = true;
+    panel = both + it / S;
+    slice = it % S;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Load one thread's 32 rows of its column (zero past X's edge).  LAST: the
+// last read of these lines (evict first).
+template <bool LAST>
+__device__ __forceinline__ void lag_load(const float *X, int64_t rows, int64_t cols, int64_t ldx,
+                                         int64_t col, int64_t r0, float (&x)[32]) {
+    const float *xp = X + r0 * ldx + col;
+    if (col < cols && r0 + 32 <= rows) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = LAST ? __ldcs(xp + i * ldx) : __ldg(xp + i * ldx);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            x[i] = (col < cols && r0 + i < rows) ? __ldg(xp + i * ldx) : 0.0f;
+    }
+}
+
+// ws: [0] the item counter, [1, 1 + P) the panels' counts, then the column
+// maxima (bit patterns); all zero at launch.  An item covers C consecutive
+// slices (32 RQ rows each) of its panel; S is the number of items per panel.
+template <int RQ>
+__global__ void __launch_bounds__(128 * RQ, 8 / RQ)
+    quantize_cols_lag_kernel(const float *__restrict__ X, int64_t rows, int64_t cols,
+                             int64_t ldx, int64_t P, int64_t S, int64_t L, int C,
+                             uint32_t *__restrict__ ws, __half *__restrict__ Q, int64_t ldq,
+                             float *__restrict__ scale, float *__restrict__ inv,
+                             int32_t *__restrict__ dstatus) {
+    constexpr int kThreads = 128 * RQ, kRows = 32 * RQ;
+    __shared__ __align__(16) __half tile[kLagCols][kRows + 2];  // [column][row]
+    __shared__ uint32_t red[RQ][kLagCols];
+    __shared__ float s_inv[kLagCols];
+    __shared__ unsigned int s_item[2];
+    unsigned int *claim = ws;
+    uint32_t *count = ws + 1;
+    uint32_t *colmax = ws + 1 + P;
+    griddep_wait();  // programmatic launch: the previous kernel is done from here on
+    griddep_launch_dependents();
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int cj = 32 * (w & 3) + lane;  // this thread's column of the tile
+    const int rq = w >> 2;               // and its 32 rows of each slice: 32 rq .. 32 rq + 31
+    const int64_t total = 2 * P * S;
+    const int64_t nslices = (rows + kRows - 1) / kRows;
+    if (t == 0) s_item[0] = atomicAdd(claim, 1u);
+    __syncthreads();
+    for (int k = 0;; k ^= 1) {
+        const int64_t it = s_item[k];
+        if (it >= total) break;
+        if (t == 0) s_item[k ^ 1] = atomicAdd(claim, 1u);  // the next item, claimed early
+        bool quantize;
+        int64_t panel, chunk;
+        lag_item(it, P, S, L, quantize, panel, chunk);
+        const int64_t col = panel * kLagCols + cj;
+        const int64_t sl0 = chunk * C;
+        const int64_t sl1 = sl0 + C < nslices ? sl0 + C : nslices;
+        float x[32];
+        if (!quantize) {
+            uint32_t m = 0;
+            for (int64_t sl = sl0; sl < sl1; ++sl) {
+                lag_load<false>(X, rows, cols, ldx, col, sl * kRows + 32 * rq, x);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) m = max(m, absbits(x[i]));
+            }
+            red[rq][cj] = m;
+            __syncthreads();
+            if (t < kLagCols) {
+                const int64_t c = panel * kLagCols + t;
+                uint32_t mm = red[0][t];
+#pragma unroll
+                for (int q = 1; q < RQ; ++q) mm = max(mm, red[q][t]);
+                if (c < cols && mm != 0) atomicMax(colmax + c, mm);
+            }
+            __syncthreads();
+            if (t == 0) {
+                // the barrier orders the CTA's maxima before this release
+                __threadfence();
+                atomicAdd(count + panel, 1u);
+            }
+        } else {
+            lag_load<true>(X, rows, cols, ldx, col, sl0 * kRows + 32 * rq, x);
+            if (t == 0) {
+                // every max item of the panel has counted (bounded wait)
+                bool ok = ld_acquire_gpu(count + panel) >= (uint32_t)S;
+                const long long t0 = clock64();
+                while (!ok) {
+                    __nanosleep(64);
+                    ok = ld_acquire_gpu(count + panel) >= (uint32_t)S;
+                    if (!ok && clock64() - t0 > kWaitLimitCycles) break;
+                }
+                if (!ok && dstatus) atomicOr(dstatus, BSG_DSTATUS_TIMEOUT);
+            }
+            __syncthreads();
+            if (t < kLagCols) {
+                const int64_t c = panel * kLagCols + t;
+                float iv = 0.0f;
+                if (c < cols) {
+                    const uint32_t m = ld_relaxed_gpu(colmax + c);
+                    float sc;
+                    scale_from_max(m, sc, iv);
+                    if (chunk == 0) {
+                        scale[c] = sc;
+                        if (inv) inv[c] = iv;
+                        if (m >= kNonfiniteBits && dstatus) atomicOr(dstatus, BSG_DSTATUS_NONFINITE);
+                    }
+                }
+                s_inv[t] = iv;
+            }
+            __syncthreads();
+            const float iv = s_inv[cj];
+            const int64_t cc = cols - panel * kLagCols;
+            const int jmax = cc < kLagCols ? (int)cc : kLagCols;
+            for (int64_t sl = sl0; sl < sl1; ++sl) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    *reinterpret_cast<__half2 *>(&tile[cj][32 * rq + 2 * i]) =
+                        __floats2half2_rn(quant(x[2 * i], iv), quant(x[2 * i + 1], iv));
+                __syncthreads();
+                // the next slice's loads are in flight while the tile is copied out
+                if (sl + 1 < sl1) lag_load<true>(X, rows, cols, ldx, col, (sl + 1) * kRows + 32 * rq, x);
+                // each warp copies whole output rows (columns of X) to Q
+                const int64_t rr = rows - sl * kRows;
+                const int nr = rr < kRows ? (int)rr : kRows;  // valid halves per row
+                for (int j = w; j < jmax; j += kThreads / 32) {
+                    __half *dst = Q + (panel * kLagCols + j) * ldq + sl * kRows;
+#pragma unroll
+                    for (int e = 2 * lane; e < kRows; e += 64) {
+                        if (e + 1 < nr)
+                            *reinterpret_cast<__half2 *>(dst + e) =
+                                *reinterpret_cast<const __half2 *>(&tile[j][e]);
+                        else if (e < nr)
+                            dst[e] = tile[j][e];
+                    }
+                }
+                __syncthreads();  // the tile is free again
+            }
+        }
+        __syncthreads();  // s_item[k ^ 1] is visible; red and s_inv are free again
+    }
+}
+
 __global__ void i8_rows_to_half_kernel(const int8_t *__restrict__ Q, int64_t rows, int64_t cols,
                                        int64_t ldq, __half *__restrict__ out, int64_t ldo) {
     const int64_t total = rows * cols;
@@ -911,7 +1116,11 @@ int colmax_nsplit(int64_t rows, int64_t cols) {
 }
 
 size_t colmax_partial_bytes(int64_t rows, int64_t cols) {
-    return (size_t)colmax_nsplit(rows, cols) * (size_t)cols * sizeof(uint32_t);
+    // the two-pass kernels' partial maxima, or the one-read kernel's item
+    // counter, panel counts and column maxima, whichever is larger
+    const size_t split = (size_t)colmax_nsplit(rows, cols) * (size_t)cols;
+    const size_t lag = 1 + (size_t)((cols + kLagCols - 1) / kLagCols) + (size_t)cols;
+    return (split > lag ? split : lag) * sizeof(uint32_t);
 }
 
 namespace {
@@ -1237,15 +1446,62 @@ cudaError_t launch_quantize_ab(const float *A, int64_t M, int64_t K, int64_t lda
     return e;
 }
 
-// Column quantize path: BSG_COLS_PATH=strip|twopass forces one (strips only
-// where their layout conditions hold; results are the same), for the tests;
-// read on every call.  0 = no preference.
+// Column quantize path: BSG_COLS_PATH=strip|lag|twopass forces one (strips
+// only where their layout conditions hold; results are the same), for the
+// tests; read on every call.  0 = no preference.
 static int forced_cols_path() {
     const char *e = getenv("BSG_COLS_PATH");
     if (!e) return 0;
     if (!strcmp(e, "strip")) return 1;
+    if (!strcmp(e, "lag")) return 2;
     if (!strcmp(e, "twopass")) return 3;
     return 0;
+}
+
+// The one-read column quantize's lag, in panels: about 32 MiB of X read
+// between a panel's max items and its quantize items.  Measured on a GB300,
+// the best lag held 24-32 MiB at every column length (16384 rows: 4 panels,
+// 344 us, 2 panels 443 us, 16 panels 418 us; 8192 rows: 8 panels; 4097
+// rows: 12-16): shorter lags wait for the max items, longer ones lose the
+// tiles from L2 before they are read again.  BSG_COLQ_LAG=1..4096
+// overrides it (same results).
+static int64_t colq_lag(int64_t rows) {
+    const char *e = getenv("BSG_COLQ_LAG");
+    const int v = e ? atoi(e) : 0;
+    if (v >= 1 && v <= 4096) return v;
+    const int64_t panel_bytes = rows * kLagCols * (int64_t)sizeof(float);
+    const int64_t L = (((int64_t)32 << 20) + panel_bytes / 2) / panel_bytes;
+    return L < 2 ? 2 : L;
+}
+
+static cudaError_t launch_cols_lag(const float *X, int64_t rows, int64_t cols, int64_t ldx,
+                                   __half *Q, int64_t ldq, float *scale, float *inv,
+                                   uint32_t *ws, int32_t *dstatus, cudaStream_t st) {
+    constexpr int kThreads = 128 * kLagRq, kRows = 32 * kLagRq;
+    static int per_sm[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (per_sm[dev] == 0) {
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_cols_lag_kernel<kLagRq>,
+                                                          kThreads, 0);
+        if (e != cudaSuccess) return e;
+        per_sm[dev] = n > 0 ? n : 1;
+    }
+    const int64_t P = (cols + kLagCols - 1) / kLagCols;
+    const int64_t S = ((rows + kRows - 1) / kRows + kLagChunk - 1) / kLagChunk;  // items per panel
+    if (2 * P * S >= 0xffff0000LL) return cudaErrorInvalidValue;  // the 32-bit item counter
+    int64_t grid = (int64_t)per_sm[dev] * device_sm_count();
+    if (grid > 2 * P * S) grid = 2 * P * S;
+    const int64_t L = colq_lag(rows);
+    e = cudaMemsetAsync(ws, 0, (size_t)(1 + P + cols) * sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
+    quantize_cols_lag_kernel<kLagRq><<<(unsigned)grid, kThreads, 0, st>>>(
+        X, rows, cols, ldx, P, S, L, kLagChunk, ws, Q, ldq, scale, inv, dstatus);
+    count_launches(1);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int64_t ldx,
@@ -1254,7 +1510,7 @@ cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int
     int cs = 0, R = 0;
     const int forced = forced_cols_path();
     // the GEMM's transposed f16 operand, no inv wanted, 16-byte rows: strip CTAs
-    if (forced != 3 && out_kind == kOutHalfKMajor && !inv && ldx % 4 == 0 &&
+    if (forced != 3 && forced != 2 && out_kind == kOutHalfKMajor && !inv && ldx % 4 == 0 &&
         reinterpret_cast<uintptr_t>(X) % 16 == 0 && ldq % 2 == 0 &&
         reinterpret_cast<uintptr_t>(Q) % 4 == 0 && strip_shape(rows, 16, cs, R)) {
         static bool ready[64] = {false};
@@ -1283,8 +1539,8 @@ cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int
     // X's layout): beyond, two passes measured faster (8192 rows 108 against
     // 191 us, 4096 rows 30 against 35 us), the cluster kernel's CTAs holding
     // up to ~200 KB of shared memory, one per SM.  The GEMM's f16 operand past
-    // the strip kernel's rows always takes two passes, the second through the
-    // conflict-free transposing tile.
+    // the strip kernel's rows takes the one-read list of items (two passes
+    // only when BSG_COLS_PATH=twopass asks for them).
     if (forced != 3 && out_kind != kOutHalfKMajor && rows <= 3072 &&
         cols_cluster_shape(rows, cols, cs, R)) {
         cudaError_t e = out_kind == kOutInt8
@@ -1305,6 +1561,9 @@ cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int
     dim3 g1(gx, (unsigned)nsplit), g2(gx, (unsigned)((rows + 63) / 64));
     if (out_kind == kOutHalfKMajor) {
         if (reinterpret_cast<uintptr_t>(Q) % 4 != 0 || ldq % 2 != 0) return cudaErrorInvalidValue;
+        if (forced != 3)
+            return launch_cols_lag(X, rows, cols, ldx, static_cast<__half *>(Q), ldq, scale, inv,
+                                   partial, dstatus, st);
         if (vec)
             colmax_partial_kernel<4><<<g1, 256, 0, st>>>(X, rows, cols, ldx, rps, partial);
         else
