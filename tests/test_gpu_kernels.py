@@ -176,14 +176,22 @@ def test_tile_raster_does_not_change_results(orc, monkeypatch, group, snake):
     assert_bits_equal(host(C), Co, f"group {group}")
 
 
-@pytest.mark.parametrize("peel", ["1", "0"])
-@pytest.mark.parametrize("rows,cols", [(33, 65), (300, 1001), (17, 8191), (5, 20001), (64, 70)],
+UNALIGNED_PATHS = {"shift": {}, "peel": {"BSG_ROWS_SHIFT": "0"},
+                   "scalar": {"BSG_ROWS_SHIFT": "0", "BSG_ROWS_PEEL": "0"}}
+
+
+@pytest.mark.parametrize("path", list(UNALIGNED_PATHS))
+@pytest.mark.parametrize("rows,cols", [(33, 65), (300, 1001), (17, 8191), (5, 20001), (64, 70),
+                                       (40, 2049), (9, 12287), (6, 16383), (3, 8193)],
                          ids=lambda v: str(v))
-def test_unaligned_rows_both_paths(orc, monkeypatch, peel, rows, cols):
-    """Rows that are not 16-byte aligned (ldx % 4 != 0): the kernel that peels
-    each row to its 16-byte boundary and the scalar one, forced in turn, for
-    the int8 API and inside the unit (the f16 operand), against the oracle."""
-    monkeypatch.setenv("BSG_ROWS_PEEL", peel)
+def test_unaligned_rows_every_path(orc, monkeypatch, path, rows, cols):
+    """Rows that are not 16-byte aligned (ldx % 4 != 0): the register-resident
+    kernel that loads each row from its first 16-byte boundary (long rows),
+    the kernel that peels each row to that boundary and the scalar one,
+    forced in turn, for the int8 API and inside the unit (the f16 operand),
+    against the oracle."""
+    for k, v in UNALIGNED_PATHS[path].items():
+        monkeypatch.setenv(k, v)
     X = inputs.adversarial(rows, cols, rows * 7 + cols).numpy()
     Q, sc, iv = bsg.quantize_rows(dev(X))
     Qo, sco, ivo, _ = orc.quantize_rows(X)
@@ -195,3 +203,34 @@ def test_unaligned_rows_both_paths(orc, monkeypatch, peel, rows, cols):
     torch.cuda.synchronize()
     Co, _ = orc.bsgemm_i8(X, B, False)
     assert_bits_equal(host(C), Co, "C")
+
+
+@pytest.mark.parametrize("pad", [1, 2, 3])
+@pytest.mark.parametrize("cols", [2049, 6000, 8192, 12001, 16384])
+def test_unaligned_rows_int8_aligned_output(orc, pad, cols):
+    """The int8 API with X's rows not 16-byte aligned (ldx = cols + pad) and
+    Q's rows 16-byte aligned (ldq a multiple of 16), the layout the
+    register-resident kernel takes for the int8 codes: codes, scales and inv
+    bitwise the oracle's, and Q's padding columns untouched."""
+    import ctypes
+    rows = 21
+    ldx, ldq = cols + pad, (cols + 15) // 16 * 16 + 16
+    Xw = inputs.adversarial(rows, ldx, cols + pad).numpy()
+    X = np.ascontiguousarray(Xw[:, :cols])
+    dX = dev(Xw)
+    Q = torch.full((rows, ldq), 0x5A, dtype=torch.int8, device="cuda")
+    sc = torch.empty(rows, dtype=torch.float32, device="cuda")
+    iv = torch.empty(rows, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib = bsg.load()
+    rc = lib.bsg_quantize_rows(ctypes.c_void_p(dX.data_ptr()), rows, cols, ldx,
+                               ctypes.c_void_p(Q.data_ptr()), ldq, ctypes.c_void_p(sc.data_ptr()),
+                               ctypes.c_void_p(iv.data_ptr()), ctypes.c_void_p(st.data_ptr()), None)
+    assert rc == 0
+    torch.cuda.synchronize()
+    Qo, sco, ivo, _ = orc.quantize_rows(X)
+    Qh = host(Q)
+    assert_bits_equal(Qh[:, :cols], Qo, "Q")
+    assert (Qh[:, cols:] == 0x5A).all(), "Q's padding was written"
+    assert_bits_equal(host(sc), sco, "scale")
+    assert_bits_equal(host(iv), ivo, "inv")

@@ -497,6 +497,107 @@ __device__ __forceinline__ void rows_wide_block(int64_t blk, const float *__rest
     }
 }
 
+// Rows whose start is not 16-byte aligned (a row pitch that is not a
+// multiple of 4 floats), of up to 4096 RV + 3 columns, one row per block:
+// the row is held in registers as 128-bit loads from its first 16-byte
+// boundary (consecutive threads on consecutive chunks), the 0-3 elements
+// before that boundary and the 0-3 after the last whole chunk are loaded one
+// by one; the codes are then staged in shared memory at their column
+// positions and copied out in 16-byte pieces (the output rows are 16-byte
+// aligned).  One read of X from HBM, like the aligned rows.  Measured on a
+// GB300 (rows alone, L2 flushed): 4097 x 8191 79.5 -> 49.1 us against the
+// peeling kernel, 1024 x 16383 57.2 -> 34.8 us; at 2049 columns it was
+// slower (8192 rows 39.0 -> 42.9 us), so it takes rows above 4096 columns.
+template <int OUT, int RV>
+__global__ void __launch_bounds__(256, RV == 8 ? 4 : 2)
+    quantize_rows_shift_kernel(const float *__restrict__ X, int64_t rows, int64_t cols,
+                               int64_t ldx, void *__restrict__ Q, int64_t ldq,
+                               float *__restrict__ scale, float *__restrict__ inv,
+                               int32_t *__restrict__ dstatus) {
+    constexpr int kQ = OUT == kOutInt8 ? 1 : 2;  // bytes per code
+    __shared__ __align__(16) uint8_t stage[(1024 * RV + 16) * kQ];
+    __shared__ uint32_t red[8];
+    griddep_wait();  // programmatic launch: the previous kernel is done from here on
+    griddep_launch_dependents();
+    const int64_t r = blockIdx.x;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const float *xr = X + r * ldx;
+    int hd = (int)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(xr) & 15u)) & 15u) >> 2);
+    if (hd > cols) hd = (int)cols;
+    const int64_t nb = (cols - hd) / 4;             // whole 16-byte chunks
+    const int tl = (int)(cols - hd - 4 * nb);       // elements after them (0-3)
+    const float4 *xb = reinterpret_cast<const float4 *>(xr + hd);
+    float4 v[RV];
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < RV; ++i) {
+        const int64_t c4 = t + 256 * i;
+        if (c4 < nb) {
+            v[i] = __ldcs(xb + c4);
+            m = max(m, max(max(absbits(v[i].x), absbits(v[i].y)), max(absbits(v[i].z), absbits(v[i].w))));
+        } else {
+            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    float ends[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // thread 0: the head, then the tail
+    if (t == 0) {
+        for (int j = 0; j < hd; ++j) ends[j] = xr[j];
+        for (int j = 0; j < tl; ++j) ends[3 + j] = xr[hd + 4 * nb + j];
+#pragma unroll
+        for (int j = 0; j < 6; ++j) m = max(m, absbits(ends[j]));
+    }
+    m = __reduce_max_sync(0xffffffffu, m);
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) m = max(m, red[w]);
+    float sc, iv;
+    scale_from_max(m, sc, iv);
+    if (t == 0) {
+        scale[r] = sc;
+        if (inv) inv[r] = iv;
+        if (m >= kNonfiniteBits && dstatus) atomicOr(dstatus, 1);
+    }
+    // the codes at their column positions
+#pragma unroll
+    for (int i = 0; i < RV; ++i) {
+        const int64_t c4 = t + 256 * i;
+        if (c4 < nb) {
+            const int c = hd + 4 * (int)c4;
+            const float q[4] = {quant(v[i].x, iv), quant(v[i].y, iv), quant(v[i].z, iv),
+                                quant(v[i].w, iv)};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (OUT == kOutInt8)
+                    stage[c + j] = (uint8_t)(int8_t)(int)q[j];
+                else
+                    reinterpret_cast<__half *>(stage)[c + j] = __float2half_rn(q[j]);
+            }
+        }
+    }
+    if (t == 0) {
+        for (int j = 0; j < hd + tl; ++j) {
+            const int c = j < hd ? j : hd + 4 * (int)nb + (j - hd);
+            const float q = quant(ends[j < hd ? j : 3 + (j - hd)], iv);
+            if (OUT == kOutInt8)
+                stage[c] = (uint8_t)(int8_t)(int)q;
+            else
+                reinterpret_cast<__half *>(stage)[c] = __float2half_rn(q);
+        }
+    }
+    __syncthreads();
+    const int64_t nbytes = cols * kQ;
+    uint8_t *qr = static_cast<uint8_t *>(Q) + r * ldq * kQ;
+    for (int64_t b = 16 * (int64_t)t; b < nbytes; b += 16 * 256) {
+        if (b + 16 <= nbytes) {
+            *reinterpret_cast<uint4 *>(qr + b) = *reinterpret_cast<const uint4 *>(stage + b);
+        } else {
+            for (int64_t j = b; j < nbytes; ++j) qr[j] = stage[j];
+        }
+    }
+}
+
 // zero2 (may be NULL): two words set to zero by one thread -- the tile
 // counter of the GEMM that reads this launch's output.  The explicit minimum
 // of one block per SM changes how ptxas schedules the loads: measured on a
@@ -1285,6 +1386,27 @@ cudaError_t launch_quantize_rows(const float *X, int64_t rows, int64_t cols, int
     const int grid = grid_for(rows, kRowWarps);
     const bool vec2 = (ldx % 4 == 0) && (reinterpret_cast<uintptr_t>(X) % 16 == 0) &&
                       ((ldq * qesz) % qalign == 0) && (reinterpret_cast<uintptr_t>(Q) % qalign == 0);
+    // long rows that are not 16-byte aligned, into 16-byte aligned output
+    // rows: held in registers from their first 16-byte boundary
+    const char *se = getenv("BSG_ROWS_SHIFT");
+    if (!vec2 && cols > 4096 && cols <= 16384 && rows <= 0x7fffffff &&
+        reinterpret_cast<uintptr_t>(X) % 4 == 0 && (ldq * qesz) % 16 == 0 &&
+        reinterpret_cast<uintptr_t>(Q) % 16 == 0 && !(se && se[0] == '0')) {
+        const bool r8 = cols <= 8192;
+        if (out_kind == kOutInt8) {
+            if (r8)
+                quantize_rows_shift_kernel<kOutInt8, 8><<<(unsigned)rows, 256, 0, st>>>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus);
+            else
+                quantize_rows_shift_kernel<kOutInt8, 16><<<(unsigned)rows, 256, 0, st>>>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus);
+        } else {
+            if (r8)
+                quantize_rows_shift_kernel<kOutHalfKMajor, 8><<<(unsigned)rows, 256, 0, st>>>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus);
+            else
+                quantize_rows_shift_kernel<kOutHalfKMajor, 16><<<(unsigned)rows, 256, 0, st>>>(X, rows, cols, ldx, Q, ldq, scale, inv, dstatus);
+        }
+        count_launches(1);
+        return cudaGetLastError();
+    }
     // rows long enough to gain from 128-bit loads take the peeling kernel
     // when they are not 16-byte aligned (BSG_ROWS_PEEL=0 keeps the scalar one)
     const char *pe = getenv("BSG_ROWS_PEEL");
