@@ -298,13 +298,18 @@ bsg_status bsgemm_i8_noalloc(const float *A, const float *B, int64_t M, int64_t 
  * bits = 8: Q is K x N int8 (ldq >= N).  bits = 4: Q is K rows of ceil(N/2)
  * bytes (ldq >= ceil(N/2)), 4-bit two's complement codes, column 2i in bits
  * 0-3 of byte i and column 2i+1 in bits 4-7 (zero past the last column).
- * scale: DEVICE f32[N].  Inf or NaN in W sets BSG_DSTATUS_NONFINITE in
- * *dstatus (may be NULL); the codes and scales of such columns are then
- * unspecified.  Asynchronous.  These are the pages' stored-weight semantics
- * for a presk realization, a different scheme from the block-scaled unit's
- * floor(x * inv + 0.5) codes. */
+ * scale: DEVICE f32[N].  `workspace`: bsg_wquant_cols_workspace_size(K, N)
+ * bytes of DEVICE memory (256-byte aligned; counters and column maxima of
+ * the one-read path that columns of more than 4096 rows take), owned by the
+ * caller and not used after the call's work completes on `stream`.  Inf or
+ * NaN in W sets BSG_DSTATUS_NONFINITE in *dstatus (may be NULL); the codes
+ * and scales of such columns are then unspecified.  Asynchronous.  These are
+ * the pages' stored-weight semantics for a presk realization, a different
+ * scheme from the block-scaled unit's floor(x * inv + 0.5) codes. */
+size_t bsg_wquant_cols_workspace_size(int64_t K, int64_t N);
 bsg_status bsg_wquant_cols(const float *W, int64_t K, int64_t N, int64_t ldw, int bits, int pow2,
-                           void *Q, int64_t ldq, float *scale, int32_t *dstatus, void *stream);
+                           void *Q, int64_t ldq, float *scale, void *workspace, size_t ws_bytes,
+                           int32_t *dstatus, void *stream);
 
 /* The stored weights: W_hat[k][j] = f32(q[k][j] * s_j), one rounding (exact
  * with pow2 scales).  Q and bits as written by bsg_wquant_cols; W_hat: DEVICE

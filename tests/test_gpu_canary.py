@@ -158,17 +158,20 @@ def test_chained_units_write_only_their_outputs(orc):
     assert tail_intact(ws, off, nws)
 
 
+@pytest.mark.parametrize("K", [77, 5000])
 @pytest.mark.parametrize("bits", [8, 4])
-def test_weight_storage_writes_only_its_codes(orc, bits):
-    K, N = 77, 41
+def test_weight_storage_writes_only_its_codes(orc, bits, K):
+    N = 41
     W = inputs.normal((K, N), 0.02, 9).numpy()
     Wd = torch.from_numpy(W).cuda()
     width = N if bits == 8 else (N + 1) // 2
     ldq = width + 3
     Q = torch.full(((K + 1) * ldq,), -86, dtype=torch.int8, device="cuda")
     sc = canary_f32(N + 8)
-    assert lib().bsg_wquant_cols(ptr(Wd), K, N, N, bits, 0, ptr(Q), ldq, ptr(sc), None,
-                                 stream()) == 0
+    nws = lib().bsg_wquant_cols_workspace_size(K, N)
+    ws, off = workspace(nws)
+    assert lib().bsg_wquant_cols(ptr(Wd), K, N, N, bits, 0, ptr(Q), ldq, ptr(sc), ptr(ws, off),
+                                 nws, None, stream()) == 0
     torch.cuda.synchronize()
     Qh = host(Q).reshape(K + 1, ldq)
     Qo, sco, _ = orc.wquant_cols(W, bits=bits)
@@ -180,6 +183,7 @@ def test_weight_storage_writes_only_its_codes(orc, bits):
     assert (Qh[:K, width:] == -86).all() and (Qh[K:] == -86).all()
     assert_bits_equal(host(sc)[:N], sco, "scales")
     assert (host(sc)[N:].view(np.uint32) == CANARY_F32).all()
+    assert tail_intact(ws, off, nws)
 
 
 @pytest.mark.parametrize("M,N,K,extra", [(257, 1025, 1100, 3), (130, 96, 2100, 4)],

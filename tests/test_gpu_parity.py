@@ -113,6 +113,32 @@ def test_exactness_saturated_and_cancelling(orc, K):
     assert int(So[0, 0]) == 127 * 127 * K
 
 
+@pytest.mark.parametrize("M", [5, 129])
+def test_unit_at_max_k(orc, M):
+    """The whole f32 unit at K = BSG_MAX_K: A's rows beyond 16384 columns
+    (segmented maxima, then the streaming pass), B's 133144-row columns (the
+    one-read column quantize), and saturated rows whose integer sums reach
+    127^2 K, just inside int32; C bitwise the oracle's."""
+    K, N = bsg.MAX_K, 9
+    rng = np.random.default_rng(K + M)
+    A = rng.uniform(-1, 1, (M, K)).astype(np.float32)
+    B = rng.uniform(-1, 1, (K, N)).astype(np.float32)
+    A[0] = 1.0                                  # codes 127 everywhere
+    A[1] = np.where(np.arange(K) % 2 == 0, 1.0, -1.0)
+    B[:, 0] = 1.0
+    B[:, 1] = np.where(np.arange(K) % 2 == 0, 1.0, -1.0)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    C = bsg.bsgemm_i8(dev(A), dev(B), dstatus=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    Co, rc = orc.bsgemm_i8(A, B, False)
+    assert rc == 0
+    assert_bits_equal(host(C), Co, f"M={M} K={K}")
+    # S[0][0] = 127^2 K exactly; C = S * (1/127) * (1/127) in f32 steps
+    assert Co[0, 0] == np.float32(np.float32(np.float32(127 * 127 * K) * np.float32(1 / 127))
+                                  * np.float32(1 / 127))
+
+
 def test_max_k_limit_and_status():
     A = torch.ones(2, 8, device="cuda")
     B = torch.ones(8, 2, device="cuda")

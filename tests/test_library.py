@@ -78,8 +78,16 @@ def test_argument_errors_without_gpu(lib):
     assert lib.bsg_audit(dummy, bsg.MAX_K + 1, dummy, 4, dummy, 4, 4, 4, bsg.MAX_K + 1, 0, 0, 8,
                          dummy, None, None) == 2
     # weight storage: bits other than 8/4, ldq too small for the packed int4 rows
-    assert lib.bsg_wquant_cols(dummy, 4, 4, 4, 6, 0, dummy, 4, dummy, None, None) == 1
-    assert lib.bsg_wquant_cols(dummy, 4, 5, 5, 4, 0, dummy, 2, dummy, None, None) == 1
+    assert lib.bsg_wquant_cols(dummy, 4, 4, 4, 6, 0, dummy, 4, dummy, dummy, 1 << 20, None,
+                               None) == 1
+    assert lib.bsg_wquant_cols(dummy, 4, 5, 5, 4, 0, dummy, 2, dummy, dummy, 1 << 20, None,
+                               None) == 1
+    # weight storage without its workspace, or with too little of it
+    assert lib.bsg_wquant_cols(dummy, 4, 5, 5, 8, 0, dummy, 5, dummy, None, 0, None, None) == 3
+    assert lib.bsg_wquant_cols(dummy, 5000, 300, 300, 8, 0, dummy, 300, dummy, dummy, 256, None,
+                               None) == 3
+    assert lib.bsg_wquant_cols_workspace_size(5000, 300) >= (1 + 3 + 300) * 4
+    assert lib.bsg_wquant_cols_workspace_size(0, 300) == 0
     assert lib.bsg_wdequant_cols(dummy, 4, 4, 4, 8, dummy, dummy, 3, None) == 1
     # grouped call: no items, too many items
     assert lib.bsgemm_i8_group(None, 1, None, None) == 1

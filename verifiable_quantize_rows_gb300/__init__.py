@@ -99,7 +99,9 @@ def _declare(lib):
         "bsg_selftest_workspace_size": ([], _sz),
         "bsg_selftest": ([_vp, _sz, _vp, _vp], _i32),
         "bsgemm_i8_group": ([ctypes.POINTER(GemmItem), _i32, _vp, _vp], _i32),
-        "bsg_wquant_cols": ([_vp, _i64, _i64, _i64, _i32, _i32, _vp, _i64, _vp, _vp, _vp], _i32),
+        "bsg_wquant_cols_workspace_size": ([_i64, _i64], _sz),
+        "bsg_wquant_cols": ([_vp, _i64, _i64, _i64, _i32, _i32, _vp, _i64, _vp, _vp, _sz, _vp,
+                             _vp], _i32),
         "bsg_wdequant_cols": ([_vp, _i64, _i64, _i64, _i32, _vp, _vp, _i64, _vp], _i32),
         "bsgemm_i8_requant_workspace_size": ([_i64, _i64, _i64], _sz),
         "bsgemm_i8_requant": ([_vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _sz,
@@ -528,7 +530,8 @@ def bsgemm_i8_group(items, dstatus=None, stream=None, workspace=None):
     return outs
 
 
-def wquant_cols(W, bits: int = 8, pow2: bool = False, dstatus=None, stream=None):
+def wquant_cols(W, bits: int = 8, pow2: bool = False, dstatus=None, stream=None,
+                workspace=None):
     """Weight storage codes of a K x N f32 weight (per-column scales):
     (Q, scale).  bits 8: Q int8 K x N; bits 4: Q uint8 K x ceil(N/2), two
     4-bit codes per byte."""
@@ -540,8 +543,10 @@ def wquant_cols(W, bits: int = 8, pow2: bool = False, dstatus=None, stream=None)
     else:
         Q = torch.empty((K, (N + 1) // 2), dtype=torch.uint8, device=W.device)
     sc = torch.empty(N, dtype=torch.float32, device=W.device)
-    _check(load().bsg_wquant_cols(_ptr(W), K, N, N, int(bits), int(bool(pow2)), _ptr(Q),
-                                  Q.shape[1], _ptr(sc), _ptr(dstatus), _stream_ptr(stream)),
+    lib = load()
+    wp, wn = _ws(workspace, lib.bsg_wquant_cols_workspace_size(K, N))
+    _check(lib.bsg_wquant_cols(_ptr(W), K, N, N, int(bits), int(bool(pow2)), _ptr(Q),
+                               Q.shape[1], _ptr(sc), wp, wn, _ptr(dstatus), _stream_ptr(stream)),
            "bsg_wquant_cols")
     return Q, sc
 

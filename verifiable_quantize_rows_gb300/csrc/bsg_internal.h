@@ -87,9 +87,12 @@ cudaError_t launch_audit(const float *A, int64_t lda, const float *B, int64_t ld
                          int nsamples, uint32_t *mismatches, int64_t *cells, cudaStream_t st);
 
 // Weight storage as int8 / int4 codes with per-column scales, and back.
+// ws: wquant_workspace_bytes(K, N) of scratch (the one-read path's
+// counters and column maxima; columns of up to 4096 rows use none of it).
+size_t wquant_workspace_bytes(int64_t K, int64_t N);
 cudaError_t launch_wquant_cols(const float *W, int64_t K, int64_t N, int64_t ldw, int bits,
-                               int pow2, void *Q, int64_t ldq, float *scale, int32_t *dstatus,
-                               cudaStream_t st);
+                               int pow2, void *Q, int64_t ldq, float *scale, void *ws,
+                               int32_t *dstatus, cudaStream_t st);
 cudaError_t launch_wdequant_cols(const void *Q, int64_t K, int64_t N, int64_t ldq, int bits,
                                  const float *scale, float *out, int64_t ldo, cudaStream_t st);
 

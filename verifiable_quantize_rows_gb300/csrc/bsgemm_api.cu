@@ -797,16 +797,23 @@ bsg_status bsg_selftest(void *workspace, size_t ws_bytes, uint32_t *audit_mismat
     return (hash_ok && mis == 0) ? BSG_OK : BSG_ERR_SELFTEST;
 }
 
+size_t bsg_wquant_cols_workspace_size(int64_t K, int64_t N) {
+    if (K < 1 || N < 1) return 0;
+    return wquant_workspace_bytes(K, N);
+}
+
 bsg_status bsg_wquant_cols(const float *W, int64_t K, int64_t N, int64_t ldw, int bits, int pow2,
-                           void *Q, int64_t ldq, float *scale, int32_t *dstatus, void *stream) {
+                           void *Q, int64_t ldq, float *scale, void *workspace, size_t ws_bytes,
+                           int32_t *dstatus, void *stream) {
     if (!W || !Q || !scale || K < 1 || N < 1 || ldw < N || (bits != 8 && bits != 4) ||
         (pow2 != 0 && pow2 != 1))
         return BSG_ERR_ARG;
     if (ldq < (bits == 8 ? N : (N + 1) / 2)) return BSG_ERR_ARG;
+    if (!ws_ok(workspace, ws_bytes, wquant_workspace_bytes(K, N))) return BSG_ERR_WORKSPACE;
     bsg_status s = check_device();
     if (s != BSG_OK) return s;
-    return from_cuda(launch_wquant_cols(W, K, N, ldw, bits, pow2, Q, ldq, scale, dstatus,
-                                        static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_wquant_cols(W, K, N, ldw, bits, pow2, Q, ldq, scale, workspace,
+                                        dstatus, static_cast<cudaStream_t>(stream)));
 }
 
 bsg_status bsg_wdequant_cols(const void *Q, int64_t K, int64_t N, int64_t ldq, int bits,

@@ -27,6 +27,7 @@
 
 #include "bsg_internal.h"
 #include "bsg_ptx.cuh"
+#include "lag_list.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -949,18 +950,11 @@ __global__ void __launch_bounds__(256)
 }
 
 // Column quantize into the GEMM's K-major f16 operand with one read of X
-// from HBM, for columns too long for the strip kernel.  The work is a list
-// of items, each a run of rows of one 128-column panel.  For each panel the
-// list holds first its max items (the tile's |x| maxima, atomicMax into the
-// panel's column maxima, then one count on the panel's counter) and, `lag`
-// panels further on, its quantize items, which read the same tiles again --
-// from L2, where the max items left them -- wait until the panel's count is
-// complete, and write the transposed codes.  CTAs claim items in list order
-// from a counter and work through the items they hold in the order they
-// claimed them.  A max item never waits, and all of a panel's max items
-// come before its quantize items in the list, so the lowest unfinished item
-// is always being worked on and never waits on anything unfinished: every
-// wait ends.  The wait is bounded all the same.
+// from HBM, for columns too long for the strip kernel, through the item list
+// of lag_list.cuh: a max item takes its rows' |x| maxima (atomicMax into the
+// panel's column maxima, then one count on the panel's counter); a quantize
+// item waits (bounded) until its panel's count is complete and writes the
+// transposed codes.
 //
 // Each thread reads one column of 32 rows straight into registers (the
 // lanes of a warp take consecutive columns, so each load instruction reads
@@ -972,46 +966,7 @@ __global__ void __launch_bounds__(256)
 // kernels 442 us.  A version that staged the tiles in a 3-stage
 // shared-memory ring by cp.async, one CTA per SM, ran at half this speed:
 // the chain of barriers, atomics and waits of each item then stalls the SM.
-constexpr int kLagCols = 128;
 constexpr int kLagRq = 2;
-constexpr int kLagChunk = 2;
-
-// Item `it` of the list for P panels of S slices and a lag of L panels.
-__device__ __forceinline__ void lag_item(int64_t it, int64_t P, int64_t S, int64_t L,
-                                         bool &quantize, int64_t &panel, int64_t &slice) {
-    const int64_t lead = P < L ? P : L;      // panels whose max items come alone
-    const int64_t both = P > L ? P - L : 0;  // steps with max and quantize items
-    if (it < lead * S) {
-        quantize = false;
-        panel = it / S;
-        slice = it % S;
-        return;
-    }
-    it -= lead * S;
-    if (it < both * 2 * S) {
-        const int64_t step = L + it / (2 * S), r = it % (2 * S);
-        quantize = r >= S;
-        panel = quantize ? step - L : step;
-        slice = quantize ? r - S : r;
-        return;
-    }
-    it -= both * 2 * S;
-    quantize = true;
-    panel = both + it / S;
-    slice = it % S;
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p) {
-    uint32_t v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
 
 // Load one thread's 32 rows of its column (zero past X's edge).  LAST: the
 // last read of these lines (evict first).
@@ -1582,22 +1537,6 @@ static int forced_cols_path() {
     if (!strcmp(e, "lag")) return 2;
     if (!strcmp(e, "twopass")) return 3;
     return 0;
-}
-
-// The one-read column quantize's lag, in panels: about 32 MiB of X read
-// between a panel's max items and its quantize items.  Measured on a GB300,
-// the best lag held 24-32 MiB at every column length (16384 rows: 4 panels,
-// 344 us, 2 panels 443 us, 16 panels 418 us; 8192 rows: 8 panels; 4097
-// rows: 12-16): shorter lags wait for the max items, longer ones lose the
-// tiles from L2 before they are read again.  BSG_COLQ_LAG=1..4096
-// overrides it (same results).
-static int64_t colq_lag(int64_t rows) {
-    const char *e = getenv("BSG_COLQ_LAG");
-    const int v = e ? atoi(e) : 0;
-    if (v >= 1 && v <= 4096) return v;
-    const int64_t panel_bytes = rows * kLagCols * (int64_t)sizeof(float);
-    const int64_t L = (((int64_t)32 << 20) + panel_bytes / 2) / panel_bytes;
-    return L < 2 ? 2 : L;
 }
 
 static cudaError_t launch_cols_lag(const float *X, int64_t rows, int64_t cols, int64_t ldx,

@@ -18,18 +18,23 @@
 // A strip of 32 columns is quantized by a cluster of CTAs, each owning a slice
 // of its rows: each reads its slice for the column maxima, the cluster
 // combines them through distributed shared memory, and each reads its slice
-// again (from L2) to quantize it.  The code is the integer nearest the exact
-// quotient w / s, ties to even, found with integer arithmetic on the two
-// floats' significands (no divide is rounded before the comparison): 2|w|/s
-// = mw * 2^sh / ms exactly, its integer part and remainder decide the
-// rounding.  The f64 divide the first version used per element ran on
-// GB300's FP64 pipe and made the kernel compute-bound.
+// again (from L2) to quantize it; columns of more than 4096 rows take the
+// one-read item list of lag_list.cuh instead.  The code is the integer
+// nearest the exact quotient w / s, ties to even: almost always rint of
+// RN(w * RN(1/s)), which lies within 2^-16 of the exact quotient, when that
+// product is more than 2^-14 from a half-integer; otherwise found with
+// integer arithmetic on the two floats' significands (2|w|/s = mw * 2^sh /
+// ms exactly; its integer part and remainder decide the rounding).  The f64
+// divide the first version used per element ran on GB300's FP64 pipe, and
+// an f32 divide per element still made the kernel compute-bound.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
 
 #include "bsg_internal.h"
+#include "bsg_ptx.cuh"
+#include "lag_list.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -85,23 +90,29 @@ __device__ __forceinline__ int wq_round_quotient_exact(float w, float s, int qma
     return neg ? -(int)q : (int)q;
 }
 
-// The same integer, first from the correctly rounded f32 quotient x: its
-// error is at most half an ulp (2^-18 below 128), so when x lies more than
-// 2^-16 from the nearest half-integer h, the exact quotient lies on the same
-// side of h and rounds to rint(x).  (x - h is exact there: for |x| >= 1, x and
-// h are within a factor of two; below, h = +-1/2 and |x - h| >= 1/4 unless
-// |x| >= 1/4.)  Only quotients near a half-integer take the exact path.
-__device__ __forceinline__ int wq_round_quotient(float w, float s, int qmax) {
-    const float x = __fdiv_rn(w, s);
-    const float ax = fabsf(x);
-    if (ax < 128.0f) {
-        const float h = __fadd_rn(floorf(x), 0.5f);
-        if (fabsf(__fsub_rn(x, h)) > 0x1p-16f) {
-            const int q = (int)rintf(x);
-            return q < -qmax ? -qmax : (q > qmax ? qmax : q);
-        }
-    }
-    return wq_round_quotient_exact(w, s, qmax);
+// The same integer, first from x = RN(w * r) with r = RN(1 / s) (one
+// reciprocal per column instead of a divide per element): x is within
+// |w/s| 2^-23 of the exact quotient (two roundings of 2^-24; r is a normal
+// float, since s <= FLT_MAX / 7 < 2^126), below 2^-16 while |x| < 128, so
+// when x lies more than 2^-14 from the nearest half-integer h, the exact
+// quotient lies on the same side of h and rounds to rint(x).  (x - h is
+// exact there: for |x| >= 1, x and h are within a factor of two; below,
+// h = +-1/2 and |x - h| >= 1/4 unless |x| >= 1/4.)  Quotients near a
+// half-integer, and any x that is not finite (r overflowing for a tiny s),
+// take the exact path.
+__device__ __forceinline__ bool wq_fast_code(float w, float r, int qmax, int &q) {
+    const float x = __fmul_rn(w, r);
+    if (!(fabsf(x) < 128.0f)) return false;
+    const float h = __fadd_rn(floorf(x), 0.5f);
+    if (!(fabsf(__fsub_rn(x, h)) > 0x1p-14f)) return false;
+    q = (int)rintf(x);
+    q = q < -qmax ? -qmax : (q > qmax ? qmax : q);
+    return true;
+}
+
+__device__ __forceinline__ int wq_round_quotient(float w, float s, float r, int qmax) {
+    int q;
+    return wq_fast_code(w, r, qmax, q) ? q : wq_round_quotient_exact(w, s, qmax);
 }
 
 // grid (strips, CS), cluster (1, CS, 1): CTA `rank` owns rows [rank R, rank R + R).
@@ -172,12 +183,13 @@ __global__ void __launch_bounds__(256)
     }
     if (t == 0 && s_bad && dstatus) atomicOr(dstatus, 1);  // Inf or NaN in this slice
     cluster.sync();  // s_col is complete; no CTA leaves while another reads its maxima
-    float sv[4];
+    float sv[4], rv[4];
     bool use[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         sv[u] = s_col[4 * c4 + u];
         use[u] = sv[u] != 0.0f && isfinite(sv[u]);
+        rv[u] = use[u] ? __frcp_rn(sv[u]) : 0.0f;
     }
 #pragma unroll 4
     for (int r = rs; r < nr; r += 32) {
@@ -186,7 +198,7 @@ __global__ void __launch_bounds__(256)
         int q[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-            q[u] = (use[u] && isfinite(x[u])) ? wq_round_quotient(x[u], sv[u], kQmax) : 0;
+            q[u] = (use[u] && isfinite(x[u])) ? wq_round_quotient(x[u], sv[u], rv[u], kQmax) : 0;
         uint8_t *row = Q + (r0 + r) * ldq;
         if (BITS == 8) {
             if (qvec && full4) {
@@ -210,6 +222,210 @@ __global__ void __launch_bounds__(256)
             }
         }
     }
+}
+
+// Long weight columns: the one-read item list of lag_list.cuh, with this
+// scheme's maxima (NaN left out, Inf kept and reported), scales and codes;
+// the codes go to Q in W's layout.  Each thread takes one column of 32 rows
+// of each 64-row slice (lanes on consecutive columns, so each load reads one
+// 128-byte line and each int8 store writes 32 consecutive bytes).
+constexpr int kWqRows = 64;  // rows per slice
+
+template <bool LAST>
+__device__ __forceinline__ void wq_load32(const float *W, int64_t K, int64_t N, int64_t ldw,
+                                          int64_t col, int64_t r0, float (&x)[32]) {
+    const float *p = W + r0 * ldw + col;
+    if (col < N && r0 + 32 <= K) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = LAST ? __ldcs(p + i * ldw) : __ldg(p + i * ldw);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = (col < N && r0 + i < K) ? __ldg(p + i * ldw) : 0.0f;
+    }
+}
+
+// ws: [0] the item counter, [1, 1 + P) the panels' counts, then the column
+// maxima (bit patterns); all zero at launch.
+template <int BITS, bool POW2>
+__global__ void __launch_bounds__(256, 4)
+    wquant_cols_lag_kernel(const float *__restrict__ W, int64_t K, int64_t N, int64_t ldw,
+                           int64_t P, int64_t S, int64_t L, uint32_t *__restrict__ ws,
+                           uint8_t *__restrict__ Q, int64_t ldq, int qvec,
+                           float *__restrict__ scale, int32_t *__restrict__ dstatus) {
+    constexpr int kQmax = BITS == 8 ? 127 : 7;
+    __shared__ uint32_t red[2][kLagCols];
+    __shared__ float s_sc[kLagCols];
+    __shared__ unsigned int s_item[2];
+    __shared__ int s_bad;
+    __shared__ __align__(16) int8_t qt[kWqRows][kLagCols];  // a slice's codes, then copied out
+    unsigned int *claim = ws;
+    uint32_t *count = ws + 1;
+    uint32_t *colmax = ws + 1 + P;
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int cj = 32 * (w & 3) + lane;  // this thread's column of the panel
+    const int rq = w >> 2;               // and its 32 rows of each slice
+    const int64_t total = 2 * P * S;
+    const int64_t nslices = (K + kWqRows - 1) / kWqRows;
+    if (t == 0) {
+        s_item[0] = atomicAdd(claim, 1u);
+        s_bad = 0;
+    }
+    __syncthreads();
+    for (int k = 0;; k ^= 1) {
+        const int64_t it = s_item[k];
+        if (it >= total) break;
+        if (t == 0) s_item[k ^ 1] = atomicAdd(claim, 1u);  // the next item, claimed early
+        bool quantize;
+        int64_t panel, chunk;
+        lag_item(it, P, S, L, quantize, panel, chunk);
+        const int64_t col = panel * kLagCols + cj;
+        const int64_t sl0 = chunk * kLagChunk;
+        const int64_t sl1 = sl0 + kLagChunk < nslices ? sl0 + kLagChunk : nslices;
+        float x[32];
+        if (!quantize) {
+            uint32_t m = 0;
+            bool bad = false;
+            for (int64_t sl = sl0; sl < sl1; ++sl) {
+                wq_load32<false>(W, K, N, ldw, col, sl * kWqRows + 32 * rq, x);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const uint32_t a = wq_absbits(x[i]);
+                    if (a <= 0x7f800000u) m = max(m, a);
+                    bad = bad || a >= 0x7f800000u;
+                }
+            }
+            if (bad) s_bad = 1;
+            red[rq][cj] = m;
+            __syncthreads();
+            if (t < kLagCols) {
+                const int64_t c = panel * kLagCols + t;
+                const uint32_t mm = max(red[0][t], red[1][t]);
+                if (c < N && mm != 0) atomicMax(colmax + c, mm);
+            }
+            __syncthreads();
+            if (t == 0) {
+                // the barrier orders the CTA's maxima before this release
+                __threadfence();
+                atomicAdd(count + panel, 1u);
+            }
+        } else {
+            wq_load32<true>(W, K, N, ldw, col, sl0 * kWqRows + 32 * rq, x);
+            if (t == 0) {
+                // every max item of the panel has counted (bounded wait)
+                bool ok = ld_acquire_gpu(count + panel) >= (uint32_t)S;
+                const long long t0 = clock64();
+                while (!ok) {
+                    __nanosleep(64);
+                    ok = ld_acquire_gpu(count + panel) >= (uint32_t)S;
+                    if (!ok && clock64() - t0 > kWaitLimitCycles) break;
+                }
+                if (!ok && dstatus) atomicOr(dstatus, BSG_DSTATUS_TIMEOUT);
+            }
+            __syncthreads();
+            if (t < kLagCols) {
+                const int64_t c = panel * kLagCols + t;
+                float sc = 0.0f;
+                if (c < N) {
+                    sc = __fdiv_rn(__uint_as_float(ld_relaxed_gpu(colmax + c)), (float)kQmax);
+                    if (POW2 && isfinite(sc)) sc = wq_pow2_up(sc);
+                    if (chunk == 0) scale[c] = sc;
+                }
+                s_sc[t] = sc;
+            }
+            __syncthreads();
+            const float sv = s_sc[cj];
+            const bool use = sv != 0.0f && isfinite(sv);
+            const float rv = use ? __frcp_rn(sv) : 0.0f;
+            for (int64_t sl = sl0; sl < sl1; ++sl) {
+                if (sl > sl0) wq_load32<true>(W, K, N, ldw, col, sl * kWqRows + 32 * rq, x);
+                const int64_t r0 = sl * kWqRows + 32 * rq;
+                // the 32 codes as bytes: the fast test of wq_fast_code decides
+                // almost every one; the few it leaves are redone exactly, from
+                // W read again
+                uint32_t pk[8];
+                uint32_t slow = 0;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    int q = 0;
+                    if (use && isfinite(x[i]) && !wq_fast_code(x[i], rv, kQmax, q)) {
+                        q = 0;
+                        slow |= 1u << i;
+                    }
+                    if ((i & 3) == 0) pk[i >> 2] = 0u;
+                    pk[i >> 2] |= (uint32_t)(q & 0xff) << (8 * (i & 3));
+                }
+                while (slow) {
+                    const int i = __ffs(slow) - 1;
+                    slow &= slow - 1;
+                    const int q = wq_round_quotient_exact(__ldg(W + (r0 + i) * ldw + col), sv, kQmax);
+                    const uint32_t sh = 8u * (uint32_t)(i & 3);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (j == (i >> 2)) pk[j] = (pk[j] & ~(0xffu << sh)) | ((uint32_t)(q & 0xff) << sh);
+                }
+                if (qvec) {
+                    // through the tile: each row of codes leaves in 16-byte
+                    // (int8) or 4-byte (int4, two codes a byte) pieces
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        qt[32 * rq + i][cj] = (int8_t)(uint8_t)(pk[i >> 2] >> (8 * (i & 3)));
+                    __syncthreads();
+                    const int64_t cc = N - panel * kLagCols;
+                    const int ncol = cc < kLagCols ? (int)cc : kLagCols;  // valid columns
+                    const int64_t rbase = sl * kWqRows;
+                    if (BITS == 8) {
+                        for (int e = t; e < kWqRows * (kLagCols / 16); e += 256) {
+                            const int r = e >> 3, c16 = (e & 7) * 16;
+                            if (rbase + r >= K || c16 >= ncol) continue;
+                            uint8_t *dst = Q + (rbase + r) * ldq + panel * kLagCols + c16;
+                            if (c16 + 16 <= ncol)
+                                *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(&qt[r][c16]);
+                            else
+                                for (int j = 0; j < ncol - c16; ++j) dst[j] = (uint8_t)qt[r][c16 + j];
+                        }
+                    } else {
+                        const int nbyte = (ncol + 1) / 2;  // a last odd column's high nibble is 0
+                        for (int e = t; e < kWqRows * (kLagCols / 8); e += 256) {
+                            const int r = e >> 4, c8 = (e & 15) * 8;
+                            if (rbase + r >= K || c8 >= ncol) continue;
+                            const uint2 v = *reinterpret_cast<const uint2 *>(&qt[r][c8]);
+                            uint32_t packed = 0;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const uint32_t word = j < 2 ? v.x : v.y;
+                                const uint32_t lo = (word >> (16 * (j & 1))) & 0xfu;
+                                const uint32_t hi = (word >> (16 * (j & 1) + 8)) & 0xfu;
+                                packed |= (lo | (hi << 4)) << (8 * j);
+                            }
+                            uint8_t *dst = Q + (rbase + r) * ldq + panel * (kLagCols / 2) + c8 / 2;
+                            if (c8 / 2 + 4 <= nbyte)
+                                *reinterpret_cast<uint32_t *>(dst) = packed;
+                            else
+                                for (int j = 0; j < nbyte - c8 / 2; ++j) dst[j] = (uint8_t)(packed >> (8 * j));
+                        }
+                    }
+                    __syncthreads();  // the tile is free for the next slice
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int q = (int)(int8_t)(uint8_t)(pk[i >> 2] >> (8 * (i & 3)));
+                        const int64_t row = r0 + i;
+                        if (BITS == 8) {
+                            if (row < K && col < N) Q[row * ldq + col] = (uint8_t)(int8_t)q;
+                        } else {
+                            // lanes 2i and 2i + 1 hold columns 2c and 2c + 1: one byte
+                            const int qn = __shfl_down_sync(0xffffffffu, q, 1);
+                            if (!(lane & 1) && row < K && col < N)
+                                Q[row * ldq + col / 2] =
+                                    (uint8_t)((q & 0xf) | ((col + 1 < N ? qn & 0xf : 0) << 4));
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();  // s_item[k ^ 1] is visible; red and s_sc are free again
+    }
+    if (t == 0 && s_bad && dstatus) atomicOr(dstatus, BSG_DSTATUS_NONFINITE);
 }
 
 // out[k][j] = f32(q * s_j).  grid (column blocks of 1024, row groups); each
@@ -309,11 +525,68 @@ static cudaError_t launch_wq_vec(const float *W, int64_t K, int64_t N, int64_t l
                : launch_wq<BITS, POW2, false>(W, K, N, ldw, Q, ldq, qvec, scale, dstatus, st);
 }
 
+template <int BITS, bool POW2>
+static cudaError_t launch_wq_lag(const float *W, int64_t K, int64_t N, int64_t ldw, uint8_t *Q,
+                                 int64_t ldq, float *scale, uint32_t *ws, int32_t *dstatus,
+                                 cudaStream_t st) {
+    static int per_sm[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (per_sm[dev] == 0) {
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, wquant_cols_lag_kernel<BITS, POW2>,
+                                                          256, 0);
+        if (e != cudaSuccess) return e;
+        per_sm[dev] = n > 0 ? n : 1;
+    }
+    const int64_t P = (N + kLagCols - 1) / kLagCols;
+    const int64_t S = ((K + kWqRows - 1) / kWqRows + kLagChunk - 1) / kLagChunk;
+    if (2 * P * S >= 0xffff0000LL) return cudaErrorInvalidValue;  // the 32-bit item counter
+    int64_t grid = (int64_t)per_sm[dev] * device_sm_count();
+    if (grid > 2 * P * S) grid = 2 * P * S;
+    e = cudaMemsetAsync(ws, 0, (size_t)(1 + P + N) * sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
+    // whole-piece stores of the code rows: 16 bytes (int8) or 4 (int4)
+    const uintptr_t qa = reinterpret_cast<uintptr_t>(Q);
+    const int qvec = BITS == 8 ? (ldq % 16 == 0 && qa % 16 == 0) : (ldq % 4 == 0 && qa % 4 == 0);
+    wquant_cols_lag_kernel<BITS, POW2><<<(unsigned)grid, 256, 0, st>>>(
+        W, K, N, ldw, P, S, colq_lag(K), ws, Q, ldq, qvec, scale, dstatus);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// Long columns take the one-read item list (the cluster kernel reads its
+// rows twice and waits on two cluster barriers per strip); BSG_WQ_PATH=
+// cluster|lag forces one (same results), for the tests.
+static bool wq_use_lag(int64_t K) {
+    const char *e = getenv("BSG_WQ_PATH");
+    if (e && !strcmp(e, "cluster")) return false;
+    if (e && !strcmp(e, "lag")) return true;
+    return K > 4096;
+}
+
 }  // namespace
 
+size_t wquant_workspace_bytes(int64_t K, int64_t N) {
+    (void)K;
+    const size_t words = 1 + (size_t)((N + kLagCols - 1) / kLagCols) + (size_t)N;
+    return (words * sizeof(uint32_t) + 255) / 256 * 256;
+}
+
 cudaError_t launch_wquant_cols(const float *W, int64_t K, int64_t N, int64_t ldw, int bits,
-                               int pow2, void *Q, int64_t ldq, float *scale, int32_t *dstatus,
-                               cudaStream_t st) {
+                               int pow2, void *Q, int64_t ldq, float *scale, void *ws,
+                               int32_t *dstatus, cudaStream_t st) {
+    if (wq_use_lag(K)) {
+        uint8_t *q8 = static_cast<uint8_t *>(Q);
+        uint32_t *w32 = static_cast<uint32_t *>(ws);
+        if (bits == 8)
+            return pow2 ? launch_wq_lag<8, true>(W, K, N, ldw, q8, ldq, scale, w32, dstatus, st)
+                        : launch_wq_lag<8, false>(W, K, N, ldw, q8, ldq, scale, w32, dstatus, st);
+        return pow2 ? launch_wq_lag<4, true>(W, K, N, ldw, q8, ldq, scale, w32, dstatus, st)
+                    : launch_wq_lag<4, false>(W, K, N, ldw, q8, ldq, scale, w32, dstatus, st);
+    }
     uint8_t *q = static_cast<uint8_t *>(Q);
     const uintptr_t qa = reinterpret_cast<uintptr_t>(Q);
     const int qvec = bits == 8 ? (ldq % 4 == 0 && qa % 4 == 0) : (ldq % 2 == 0 && qa % 2 == 0);
