@@ -793,8 +793,8 @@ def run_configs(args):
                   "selftest_ms_host": round(st_ms, 2)})
     del A, B, Cq
     # the weight storage (f4): codes and stored weights of a GPT-2 fc weight
-    # and of an 8192 x 8192 one.  Bytes: the weight read twice (maximum, then
-    # codes) + codes written; codes read + f32 written.
+    # and of an 8192 x 8192 one.  Bytes: the weight read once + codes written;
+    # codes read + f32 written.
     for K, N in ((768, 3072), (8192, 8192)):
         Wt = inputs.gpt2_weights(K, N, 5).to(dev)
         for bits in (8, 4):
@@ -802,14 +802,14 @@ def run_configs(args):
             q_us = timed(lambda: bsg.wquant_cols(Wt, bits=bits))
             Q, sc = bsg.wquant_cols(Wt, bits=bits)
             d_us = timed(lambda: bsg.wdequant_cols(Q, sc, N, bits=bits))
-            qb = K * N * (8 + cb)
+            qb = K * N * (4 + cb)
             db = K * N * (cb + 4)
             lines.append({"config": f"f4 weight storage int{bits} {K}x{N}",
                           "wquant_us": round(q_us, 2), "wquant_gbs": round(qb / q_us / 1e3, 1),
                           "wquant_frac_of_measured_hbm": round(qb / q_us / 1e3 / hbm_peak, 3),
                           "wdequant_us": round(d_us, 2), "wdequant_gbs": round(db / d_us / 1e3, 1),
                           "wdequant_frac_of_measured_hbm": round(db / d_us / 1e3 / hbm_peak, 3),
-                          "bytes": "wquant: 8 B read (twice) + code bytes; wdequant: code bytes + 4 B"})
+                          "bytes": "wquant: 4 B read + code bytes; wdequant: code bytes + 4 B"})
         del Wt
     X, W, dY = (t.to(dev) for t in inputs.train_trio())
     trio = [(X, W, False, False, False), (dY, W, False, True, False), (X, dY, True, False, False)]
