@@ -18,8 +18,8 @@
 // A strip of 32 columns is quantized by a cluster of CTAs, each owning a slice
 // of its rows: each reads its slice for the column maxima, the cluster
 // combines them through distributed shared memory, and each reads its slice
-// again (from L2) to quantize it; columns of more than 4096 rows take the
-// one-read item list of lag_list.cuh instead.  The code is the integer
+// again (from L2) to quantize it; long columns take the one-read item list
+// of lag_list.cuh instead.  The code is the integer
 // nearest the exact quotient w / s, ties to even: almost always rint of
 // RN(w * RN(1/s)), which lies within 2^-16 of the exact quotient, when that
 // product is more than 2^-14 from a half-integer; otherwise found with
@@ -558,13 +558,17 @@ static cudaError_t launch_wq_lag(const float *W, int64_t K, int64_t N, int64_t l
 }
 
 // Long columns take the one-read item list (the cluster kernel reads its
-// rows twice and waits on two cluster barriers per strip); BSG_WQ_PATH=
-// cluster|lag forces one (same results), for the tests.
-static bool wq_use_lag(int64_t K) {
+// rows twice and waits on two cluster barriers per strip), and so do
+// columns of 2048 rows or more in weights of 2^23 elements or more.
+// Measured (int8 / int4): 4096 x 4096 61 / 72 us in clusters against
+// 52 / 53 us on the list, 2048 x 8192 51 / 59 against 52 / 52-56 us, but
+// 3072 x 768 18 / 19 against 21 / 22 us.  BSG_WQ_PATH=cluster|lag forces
+// one (same results), for the tests.
+static bool wq_use_lag(int64_t K, int64_t N) {
     const char *e = getenv("BSG_WQ_PATH");
     if (e && !strcmp(e, "cluster")) return false;
     if (e && !strcmp(e, "lag")) return true;
-    return K > 4096;
+    return K > 4096 || (K >= 2048 && K * N >= ((int64_t)1 << 23));
 }
 
 }  // namespace
@@ -578,7 +582,7 @@ size_t wquant_workspace_bytes(int64_t K, int64_t N) {
 cudaError_t launch_wquant_cols(const float *W, int64_t K, int64_t N, int64_t ldw, int bits,
                                int pow2, void *Q, int64_t ldq, float *scale, void *ws,
                                int32_t *dstatus, cudaStream_t st) {
-    if (wq_use_lag(K)) {
+    if (wq_use_lag(K, N)) {
         uint8_t *q8 = static_cast<uint8_t *>(Q);
         uint32_t *w32 = static_cast<uint32_t *>(ws);
         if (bits == 8)
