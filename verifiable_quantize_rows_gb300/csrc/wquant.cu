@@ -228,7 +228,9 @@ __global__ void __launch_bounds__(256)
 // scheme's maxima (NaN left out, Inf kept and reported), scales and codes;
 // the codes go to Q in W's layout.  Each thread takes one column of 32 rows
 // of each 64-row slice (lanes on consecutive columns, so each load reads one
-// 128-byte line and each int8 store writes 32 consecutive bytes).
+// 128-byte line); a slice's codes are staged in shared memory and leave in
+// 16-byte (int8) or 4-byte (packed int4) pieces where Q's rows allow, else
+// one code (or code pair) at a time.
 constexpr int kWqRows = 64;  // rows per slice
 
 template <bool LAST>
