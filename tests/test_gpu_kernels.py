@@ -234,3 +234,33 @@ def test_unaligned_rows_int8_aligned_output(orc, pad, cols):
     assert (Qh[:, cols:] == 0x5A).all(), "Q's padding was written"
     assert_bits_equal(host(sc), sco, "scale")
     assert_bits_equal(host(iv), ivo, "inv")
+
+
+@pytest.mark.parametrize("case", ["B long columns", "B long columns, two passes",
+                                  "A unaligned long rows", "A wide rows", "A rows beyond 16384"])
+def test_nonfinite_on_every_long_path_sets_status(monkeypatch, case):
+    """An Inf or NaN on each long-vector quantize path (the one-read column
+    list, the two passes, the register-resident unaligned rows, the wide
+    rows, the segmented rows beyond 16384 columns) sets the non-finite bit,
+    and no bounded wait expires."""
+    M, N, K = 6, 300, 5000
+    if case == "A unaligned long rows":
+        K = 8191
+    elif case == "A wide rows":
+        K = 16384
+    elif case == "A rows beyond 16384":
+        K = 20000
+    if case.endswith("two passes"):
+        monkeypatch.setenv("BSG_COLS_PATH", "twopass")
+    A = inputs.normal((M, K), 1.0, K).numpy()
+    B = inputs.normal((K, N), 0.1, K + 1).numpy()
+    if case.startswith("B"):
+        B[4000, 17] = np.inf
+    else:
+        A[3, K - 9] = np.nan
+        A[1, 9] = -np.inf
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bsg.bsgemm_i8(dev(A), dev(B), dstatus=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & bsg.DSTATUS_NONFINITE
+    assert not int(st.item()) & 2
