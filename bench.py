@@ -971,8 +971,9 @@ def run_reference(args, rank, world):
 def run_single(args):
     """`--only small`: the GPT-2 linears step alone; `--unit M,N,K[,relu]`:
     one bsgemm_i8 of U(-1, 1) inputs, called --steps times after --warmup
-    (CUDA events, L2 flushed before each call).  One JSON line; used to run
-    small cases under a profiler."""
+    (CUDA events, L2 flushed before each call); `--wquant K,N[,bits]`: the
+    weight-storage quantize of a seeded N(0, 0.02) weight, the same way.  One
+    JSON line; used to run small cases under a profiler."""
     import torch
     import verifiable_quantize_rows_gb300 as bsg
     from verifiable_quantize_rows_gb300 import build as bsg_build
@@ -1002,6 +1003,27 @@ def run_single(args):
                 "gemm_frac": roof["frac"], "gemm_ms": roof["per_gemm_ms"],
                 "quantize_ms": quant["per_gemm_ms"],
                 "gpu_launches": launches, "device_status": int(dstatus.item())}
+    if args.wquant:
+        parts = [int(v) for v in args.wquant.split(",")]
+        K, N = parts[:2]
+        bits = parts[2] if len(parts) > 2 else 8
+        Wt = inputs.gpt2_weights(K, N, 5).to(dev)
+        wws = bsg.Workspace(dev)
+        for _ in range(args.warmup):
+            bsg.wquant_cols(Wt, bits=bits, dstatus=dstatus, workspace=wws)
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            bsg.wquant_cols(Wt, bits=bits, dstatus=dstatus, workspace=wws)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        return {"wquant": f"{K}x{N} int{bits}", "ms": round(ms, 4),
+                "gbs": round(K * N * (4 + bits / 8) / (ms * 1e-3) / 1e9, 1),
+                "device_status": int(dstatus.item())}
     parts = [int(v) for v in args.unit.split(",")]
     M, N, K = parts[:3]
     relu = bool(parts[3]) if len(parts) > 3 else False
@@ -1038,6 +1060,8 @@ def main():
                     help="run the GPT-2 linears step alone (one JSON line)")
     ap.add_argument("--unit", default=None, metavar="M,N,K[,relu]",
                     help="time one bsgemm_i8 of this shape instead (one JSON line)")
+    ap.add_argument("--wquant", default=None, metavar="K,N[,bits]",
+                    help="time one weight-storage quantize of this shape instead (one JSON line)")
     ap.add_argument("--configs", action="store_true",
                     help="time the unit on every workload of the measurement plan instead "
                          "(one JSON line each)")
@@ -1049,7 +1073,7 @@ def main():
     rank = env_int("RANK", 0)
     local_rank = env_int("LOCAL_RANK", 0)
 
-    if args.only or args.unit:
+    if args.only or args.unit or args.wquant:
         print(json.dumps(run_single(args)), flush=True)
         return
 
