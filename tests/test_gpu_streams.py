@@ -1,7 +1,9 @@
 """Streams, graphs and host threads.
 
-- Capture into a CUDA graph: bsgemm_i8 on the fused quantize path (K <= 2048)
-  and on the path that quantizes B on the library's second stream (K > 2048),
+- Capture into a CUDA graph: bsgemm_i8 on the fused quantize path (K <= 2048),
+  on the path that quantizes B on the library's second stream (K > 2048), and
+  with B's columns on the one-read item list (K > 4096, its scratch cleared by
+  a captured memset),
   and bsgemm_i8_chain (its second weight matrix on that stream too), each
   captured after a first eager call on the device, then replayed with new
   inputs copied into the captured buffers: every replay is bitwise the
@@ -25,7 +27,8 @@ import verifiable_quantize_rows_gb300 as bsg
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("M,N,K", [(640, 520, 700), (300, 260, 3000)], ids=lambda v: str(v))
+@pytest.mark.parametrize("M,N,K", [(640, 520, 700), (300, 260, 3000), (256, 300, 5000)],
+                         ids=lambda v: str(v))
 def test_unit_replays_from_a_cuda_graph(orc, M, N, K):
     A = torch.empty(M, K, device="cuda")
     B = torch.empty(K, N, device="cuda")
