@@ -7,8 +7,8 @@ Rule: "Precision" manual (docs.presk-lang.org/presk_manual/precision), section
 - stored weights f32(q*s).
 
 Parity covers the codes (int4 packed, byte for byte), the scales and the
-dequantized weights on ragged shapes with all-zero, underflowing and tie
-columns, plus the GPT-2 fc weight at full size, and the non-finite status bit.
+dequantized weights on ragged shapes with all-zero, underflowing, subnormal
+and tie columns, plus the GPT-2 fc weight at full size, and the non-finite status bit.
 """
 import numpy as np
 import pytest
@@ -30,6 +30,10 @@ def weights(K, N, seed, std=1.0):
         # a tie column: pow2 scale 1/2 at 4 bits, entries odd quarters (w/s = k + 1/2)
         col = np.float32([3.0, 1.25, 0.75, -1.25, -0.75, 0.25, -0.25, 1.75])
         W[:, 2] = np.resize(col, K)
+    if N > 4:
+        # subnormal entries: a scale near 2^-137, whose f32 reciprocal
+        # overflows to +Inf, so every code takes the kernels' exact path
+        W[:, 3] = (rng.standard_normal(K) * 2.0 ** -130).astype(np.float32)
     return W
 
 

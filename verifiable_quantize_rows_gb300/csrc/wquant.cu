@@ -343,13 +343,17 @@ __global__ void __launch_bounds__(256, 4)
                 const int64_t r0 = sl * kWqRows + 32 * rq;
                 // the 32 codes as bytes: the fast test of wq_fast_code decides
                 // almost every one; the few it leaves are redone exactly, from
-                // W read again
+                // W read again.  Rows past K (zero padding, never stored) keep
+                // code 0 and are never read again: with rv = +Inf (a column of
+                // subnormal maxima) 0 * rv is NaN, which the fast test rejects.
+                const int64_t left = col < N ? K - r0 : 0;
+                const int nvalid = left <= 0 ? 0 : (left < 32 ? (int)left : 32);
                 uint32_t pk[8];
                 uint32_t slow = 0;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     int q = 0;
-                    if (use && isfinite(x[i]) && !wq_fast_code(x[i], rv, kQmax, q)) {
+                    if (use && i < nvalid && isfinite(x[i]) && !wq_fast_code(x[i], rv, kQmax, q)) {
                         q = 0;
                         slow |= 1u << i;
                     }
