@@ -336,20 +336,19 @@ __global__ void __launch_bounds__(256)
 }
 
 // Column quantize, pass 2: a 64-row x (32 * VW)-column tile with per-column
-// scales from the partial maxima (at most kMaxSplit of them).  kOutInt8
-// writes Q in X's layout; kOutHalfKMajor writes the transposed tile,
-// Q[col][row], as f16 rows of 64 halves.
+// scales from the partial maxima (at most kMaxSplit of them), int8 codes in
+// X's layout.  (The GEMM's transposed f16 operand takes quantize_cols_t16_kernel
+// as its second pass.)
 constexpr int kMaxSplit = 32;
 
-template <int OUT, int VW>
+template <int VW>
 __global__ void __launch_bounds__(256)
     quantize_cols_kernel(const float *__restrict__ X, int64_t rows, int64_t cols, int64_t ldx,
-                         const uint32_t *__restrict__ partial, int nsplit, void *__restrict__ Q,
+                         const uint32_t *__restrict__ partial, int nsplit, int8_t *__restrict__ Q,
                          int64_t ldq, float *__restrict__ scale, float *__restrict__ inv,
                          int32_t *__restrict__ dstatus) {
     constexpr int TC = kColLanes * VW;  // tile columns
     __shared__ float s_inv[TC];
-    __shared__ __align__(16) __half tile[OUT == kOutHalfKMajor ? TC : 1][64 + 8];
     const int t = threadIdx.x;
     const int64_t c0 = (int64_t)blockIdx.x * TC;
     const int64_t r0 = (int64_t)blockIdx.y * 64;
@@ -402,35 +401,16 @@ __global__ void __launch_bounds__(256)
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int rr = rg + kColRows * i;
-        const int64_t row = r0 + rr;
-        if (OUT == kOutInt8) {
-            if (row < rows && col < cols) {
-                if (VW == 4) {
-                    const char4 q = make_char4((signed char)(int)quant(x[i][0], ivv[0]),
-                                               (signed char)(int)quant(x[i][VW > 1 ? 1 : 0], ivv[VW > 1 ? 1 : 0]),
-                                               (signed char)(int)quant(x[i][VW > 2 ? 2 : 0], ivv[VW > 2 ? 2 : 0]),
-                                               (signed char)(int)quant(x[i][VW > 3 ? 3 : 0], ivv[VW > 3 ? 3 : 0]));
-                    *reinterpret_cast<char4 *>(static_cast<int8_t *>(Q) + row * ldq + col) = q;
-                } else {
-                    static_cast<int8_t *>(Q)[row * ldq + col] = (int8_t)(int)quant(x[i][0], ivv[0]);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int v = 0; v < VW; ++v) tile[cl * VW + v][rr] = __float2half_rn(quant(x[i][v], ivv[v]));
-        }
-    }
-    if (OUT == kOutHalfKMajor) {
-        __syncthreads();
-        // TC output rows (columns of X) of 64 halves (128 bytes): 8 threads per row.
-        for (int idx = t; idx < TC * 8; idx += blockDim.x) {
-            const int j = idx >> 3;
-            const int part = idx & 7;
-            const int64_t orow = c0 + j;
-            if (orow < cols) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(&tile[j][part * 8]);
-                *reinterpret_cast<uint4 *>(static_cast<__half *>(Q) + orow * ldq + r0 + part * 8) = v;
+        const int64_t row = r0 + rg + kColRows * i;
+        if (row < rows && col < cols) {
+            if (VW == 4) {
+                const char4 q = make_char4((signed char)(int)quant(x[i][0], ivv[0]),
+                                           (signed char)(int)quant(x[i][VW > 1 ? 1 : 0], ivv[VW > 1 ? 1 : 0]),
+                                           (signed char)(int)quant(x[i][VW > 2 ? 2 : 0], ivv[VW > 2 ? 2 : 0]),
+                                           (signed char)(int)quant(x[i][VW > 3 ? 3 : 0], ivv[VW > 3 ? 3 : 0]));
+                *reinterpret_cast<char4 *>(Q + row * ldq + col) = q;
+            } else {
+                Q[row * ldq + col] = (int8_t)(int)quant(x[i][0], ivv[0]);
             }
         }
     }
@@ -624,21 +604,18 @@ __global__ void __launch_bounds__(256, 1)
 // Columns, single pass: a cluster of CS CTAs shares a strip of 32 columns;
 // CTA `rank` stages rows [rank * R, rank * R + R) of the strip in shared
 // memory (one HBM read), the CTAs exchange their partial |x| maxima through
-// distributed shared memory, and each quantizes its rows from shared memory.
-// kOutHalfKMajor writes the transposed strip (Q[col][row], f16) through a
-// shared-memory transpose; kOutInt8 writes Q in X's layout.
+// distributed shared memory, and each quantizes its rows from shared memory
+// into int8 codes in X's layout.  (The GEMM's transposed f16 operand takes
+// the strip, one-read or two-pass kernels below.)
 constexpr int kStripCols = 32;
 
-template <int OUT>
 __global__ void __launch_bounds__(256)
     quantize_cols_cluster_kernel(const float *__restrict__ X, int64_t rows, int64_t cols,
-                                 int64_t ldx, int R, int vec, void *__restrict__ Q, int64_t ldq,
+                                 int64_t ldx, int R, int vec, int8_t *__restrict__ Q, int64_t ldq,
                                  float *__restrict__ scale, float *__restrict__ inv,
                                  int32_t *__restrict__ dstatus) {
     extern __shared__ __align__(16) uint8_t dsm[];
-    float *xs = reinterpret_cast<float *>(dsm);                           // [R][32]
-    __half *ts = reinterpret_cast<__half *>(dsm + (size_t)R * kStripCols * 4);  // [32][R + 2]
-    const int tstride = R + 2;
+    float *xs = reinterpret_cast<float *>(dsm);  // [R][32]
     __shared__ uint32_t red[8][kStripCols];
     __shared__ uint32_t part[kStripCols];
     __shared__ float s_inv[kStripCols];
@@ -697,28 +674,9 @@ __global__ void __launch_bounds__(256)
     }
     __syncthreads();
     const float iv = s_inv[c];
-    if (OUT == kOutInt8) {
-        if (c0 + c < cols)
-            for (int row = g; row < nr; row += 8)
-                static_cast<int8_t *>(Q)[(r0 + row) * ldq + c0 + c] =
-                    (int8_t)(int)quant(xs[row * kStripCols + c], iv);
-    } else {
+    if (c0 + c < cols)
         for (int row = g; row < nr; row += 8)
-            ts[c * tstride + row] = __float2half_rn(quant(xs[row * kStripCols + c], iv));
-        __syncthreads();
-        // 32 output rows (columns of X), nr halves each, from row r0: one
-        // warp per output row at a time, 4-byte pairs, coalesced.
-        const int w = t >> 5, lane = t & 31;
-        const int pairs = nr >> 1;
-        for (int n = w; n < kStripCols; n += 8) {
-            if (c0 + n >= cols) continue;
-            __half *dst = static_cast<__half *>(Q) + (c0 + n) * ldq + r0;
-            const __half *src = ts + n * tstride;
-            for (int k2 = lane; k2 < pairs; k2 += 32)
-                reinterpret_cast<uint32_t *>(dst)[k2] = reinterpret_cast<const uint32_t *>(src)[k2];
-            if ((nr & 1) && lane == 0) dst[nr - 1] = src[nr - 1];
-        }
-    }
+            Q[(r0 + row) * ldq + c0 + c] = (int8_t)(int)quant(xs[row * kStripCols + c], iv);
     cluster.sync();  // no CTA leaves while another may still read its maxima
 }
 
@@ -1409,19 +1367,16 @@ static bool cols_cluster_shape(int64_t rows, int64_t cols, int &cs, int &R) {
     return true;
 }
 
-static size_t cols_cluster_smem(int R) {
-    return (size_t)R * kStripCols * 4 + (size_t)kStripCols * (R + 2) * 2 + 16;
-}
+static size_t cols_cluster_smem(int R) { return (size_t)R * kStripCols * 4 + 16; }
 
-template <int OUT>
 static cudaError_t launch_cols_cluster(const float *X, int64_t rows, int64_t cols, int64_t ldx,
-                                       int cs, int R, void *Q, int64_t ldq, float *scale,
+                                       int cs, int R, int8_t *Q, int64_t ldq, float *scale,
                                        float *inv, int32_t *dstatus, cudaStream_t st) {
     static bool attr_set[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(quantize_cols_cluster_kernel<OUT>,
+        cudaError_t e = cudaFuncSetAttribute(quantize_cols_cluster_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)cols_cluster_smem(1024));
         if (e != cudaSuccess) return e;
@@ -1441,7 +1396,7 @@ static cudaError_t launch_cols_cluster(const float *X, int64_t rows, int64_t col
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, quantize_cols_cluster_kernel<OUT>, X, rows, cols, ldx, R, vec,
+    return cudaLaunchKernelEx(&cfg, quantize_cols_cluster_kernel, X, rows, cols, ldx, R, vec,
                               Q, ldq, scale, inv, dstatus);
 }
 
@@ -1606,13 +1561,11 @@ cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int
     // up to ~200 KB of shared memory, one per SM.  The GEMM's f16 operand past
     // the strip kernel's rows takes the one-read list of items (two passes
     // only when BSG_COLS_PATH=twopass asks for them).
-    if (forced != 3 && out_kind != kOutHalfKMajor && rows <= 3072 &&
+    if (forced != 3 && out_kind == kOutInt8 && rows <= 3072 &&
         cols_cluster_shape(rows, cols, cs, R)) {
-        cudaError_t e = out_kind == kOutInt8
-                            ? launch_cols_cluster<kOutInt8>(X, rows, cols, ldx, cs, R, Q, ldq, scale,
-                                                            inv, dstatus, st)
-                            : launch_cols_cluster<kOutHalfKMajor>(X, rows, cols, ldx, cs, R, Q, ldq,
-                                                                  scale, inv, dstatus, st);
+        const cudaError_t e = launch_cols_cluster(X, rows, cols, ldx, cs, R,
+                                                  static_cast<int8_t *>(Q), ldq, scale, inv,
+                                                  dstatus, st);
         count_launches(1);
         return e;
     }
@@ -1641,22 +1594,16 @@ cudaError_t launch_quantize_cols(const float *X, int64_t rows, int64_t cols, int
         count_launches(2);
         return cudaGetLastError();
     }
+    // int8 codes in X's layout
+    int8_t *q8 = static_cast<int8_t *>(Q);
     if (vec) {
         colmax_partial_kernel<4><<<g1, 256, 0, st>>>(X, rows, cols, ldx, rps, partial);
-        if (out_kind == kOutInt8)
-            quantize_cols_kernel<kOutInt8, 4><<<g2, 256, 0, st>>>(X, rows, cols, ldx, partial, nsplit,
-                                                                 Q, ldq, scale, inv, dstatus);
-        else
-            quantize_cols_kernel<kOutHalfKMajor, 4><<<g2, 256, 0, st>>>(
-                X, rows, cols, ldx, partial, nsplit, Q, ldq, scale, inv, dstatus);
+        quantize_cols_kernel<4><<<g2, 256, 0, st>>>(X, rows, cols, ldx, partial, nsplit, q8, ldq,
+                                                    scale, inv, dstatus);
     } else {
         colmax_partial_kernel<1><<<g1, 256, 0, st>>>(X, rows, cols, ldx, rps, partial);
-        if (out_kind == kOutInt8)
-            quantize_cols_kernel<kOutInt8, 1><<<g2, 256, 0, st>>>(X, rows, cols, ldx, partial, nsplit,
-                                                                 Q, ldq, scale, inv, dstatus);
-        else
-            quantize_cols_kernel<kOutHalfKMajor, 1><<<g2, 256, 0, st>>>(
-                X, rows, cols, ldx, partial, nsplit, Q, ldq, scale, inv, dstatus);
+        quantize_cols_kernel<1><<<g2, 256, 0, st>>>(X, rows, cols, ldx, partial, nsplit, q8, ldq,
+                                                    scale, inv, dstatus);
     }
     count_launches(2);
     return cudaGetLastError();
