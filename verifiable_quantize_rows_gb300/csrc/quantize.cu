@@ -1146,9 +1146,9 @@ namespace {
 // Rows longer than the register-resident kernel takes (> 16384 columns):
 // each 256-thread block reduces one 8192-column segment of a row to its max
 // |x| bit pattern and folds it into rowmax[r] (zeroed before) by atomicMax;
-// the requantize kernel then quantizes the rows in one streaming pass.  VEC:
-// X 16-byte aligned with ldx % 4 == 0 (then cols % 4 may be anything: the
-// tail is read element by element).
+// the requantize kernel then quantizes the rows in one streaming pass.  X
+// must be 16-byte aligned with ldx % 4 == 0 (the launcher's condition);
+// cols % 4 may be anything: the tail is read element by element.
 constexpr int kRmSeg = 256 * 4 * 8;  // columns per block
 
 __global__ void __launch_bounds__(256)
