@@ -15,7 +15,7 @@ independent of it:
 - constructed ties;
 - the page's error rule;
 - pow2 exactness;
-- the zero and underflow channels;
+- the zero and underflow channels, and a channel of subnormal entries;
 - the int4 nibble layout.
 """
 from fractions import Fraction
@@ -53,6 +53,10 @@ def columns(K, N, seed, scale=1.0):
     W[:, 0] = 0.0                                   # all-zero channel
     if N > 2:
         W[:, 1] = np.float32(2.0 ** -149)           # absmax/7 and /127 round to 0 (reading P2)
+    if N > 3:
+        # subnormal entries: a subnormal, non-zero scale (its reciprocal is
+        # beyond binary32's range, so no product with it can give the codes)
+        W[:, 2] = (rng.standard_normal(K) * 2.0 ** -130).astype(np.float32)
     return W
 
 
