@@ -343,27 +343,28 @@ __global__ void __launch_bounds__(256, 4)
                 const int64_t r0 = sl * kWqRows + 32 * rq;
                 // the 32 codes as bytes: the fast test of wq_fast_code decides
                 // almost every one; the few it leaves are redone exactly, from
-                // W read again.  Rows past K (zero padding, never stored) keep
-                // code 0 and are never read again: with rv = +Inf (a column of
-                // subnormal maxima) 0 * rv is NaN, which the fast test rejects.
-                const int64_t left = col < N ? K - r0 : 0;
-                const int nvalid = left <= 0 ? 0 : (left < 32 ? (int)left : 32);
+                // W read again
                 uint32_t pk[8];
                 uint32_t slow = 0;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     int q = 0;
-                    if (use && i < nvalid && isfinite(x[i]) && !wq_fast_code(x[i], rv, kQmax, q)) {
+                    if (use && isfinite(x[i]) && !wq_fast_code(x[i], rv, kQmax, q)) {
                         q = 0;
                         slow |= 1u << i;
                     }
                     if ((i & 3) == 0) pk[i >> 2] = 0u;
                     pk[i >> 2] |= (uint32_t)(q & 0xff) << (8 * (i & 3));
                 }
+                // Zero padding past K or N (never stored) reaches this loop when
+                // rv = +Inf (a column of subnormal maxima: 0 * rv is NaN); it
+                // is not read again, and its exact code is 0.
+                const bool in_cols = col < N;
                 while (slow) {
                     const int i = __ffs(slow) - 1;
                     slow &= slow - 1;
-                    const int q = wq_round_quotient_exact(__ldg(W + (r0 + i) * ldw + col), sv, kQmax);
+                    const float wv = (in_cols && r0 + i < K) ? __ldg(W + (r0 + i) * ldw + col) : 0.0f;
+                    const int q = wq_round_quotient_exact(wv, sv, kQmax);
                     const uint32_t sh = 8u * (uint32_t)(i & 3);
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
