@@ -609,6 +609,23 @@ __global__ void __launch_bounds__(256, 1)
 // the strip, one-read or two-pass kernels below.)
 constexpr int kStripCols = 32;
 
+// The second cluster barrier of the strip kernels, split in two: a CTA
+// arrives as soon as it has read its peers' partial maxima -- before any
+// global store, so the release has nothing of its own to wait for -- and
+// waits only before it exits, so that no CTA leaves while a peer may still
+// read its shared memory.  (A full barrier after the stores made each CTA's
+// release wait for them.)  Measured on a GB300: the standalone strip kernel
+// dropped from 54 to 48 registers and 4096^3's quantize went 50.5 -> 48.2 us;
+// the fused launch at 768 rows did not change.  Every thread of every CTA
+// executes both, once (the forms without .aligned: a warp need not be
+// converged there).
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(256)
     quantize_cols_cluster_kernel(const float *__restrict__ X, int64_t rows, int64_t cols,
                                  int64_t ldx, int R, int vec, int8_t *__restrict__ Q, int64_t ldq,
@@ -660,24 +677,25 @@ __global__ void __launch_bounds__(256)
         part[t] = mm;
     }
     cluster.sync();  // every CTA's partial maxima are visible cluster-wide
+    uint32_t mm = 0;
+    float sc = 0.f, iv0 = 0.f;
     if (t < kStripCols) {
-        uint32_t mm = 0;
         for (int rk = 0; rk < cs; ++rk) mm = max(mm, *cluster.map_shared_rank(&part[t], rk));
-        float sc, iv;
-        scale_from_max(mm, sc, iv);
-        s_inv[t] = iv;
-        if (rank == 0 && c0 + t < cols) {
-            scale[c0 + t] = sc;
-            if (inv) inv[c0 + t] = iv;
-            if (mm >= kNonfiniteBits && dstatus) atomicOr(dstatus, 1);
-        }
+        scale_from_max(mm, sc, iv0);
+        s_inv[t] = iv0;
+    }
+    cluster_arrive_release();  // done with the peers' maxima
+    if (t < kStripCols && rank == 0 && c0 + t < cols) {
+        scale[c0 + t] = sc;
+        if (inv) inv[c0 + t] = iv0;
+        if (mm >= kNonfiniteBits && dstatus) atomicOr(dstatus, 1);
     }
     __syncthreads();
     const float iv = s_inv[c];
     if (c0 + c < cols)
         for (int row = g; row < nr; row += 8)
             Q[(r0 + row) * ldq + c0 + c] = (int8_t)(int)quant(xs[row * kStripCols + c], iv);
-    cluster.sync();  // no CTA leaves while another may still read its maxima
+    cluster_wait_acquire();  // no CTA leaves while another may still read its maxima
 }
 
 // Both operands of the unit in one launch, for the common layout (A stored
@@ -755,16 +773,18 @@ __device__ __forceinline__ void cols_strip_block(const float *__restrict__ X, in
         part[t] = mm;
     }
     cluster.sync();  // every CTA's partial maxima are visible cluster-wide
+    uint32_t mm = 0;
+    float sc = 0.f;
     if (t < kStripCols) {
-        uint32_t mm = 0;
         for (int k = 0; k < cs; ++k) mm = max(mm, *cluster.map_shared_rank(&part[t], k));
-        float sc, iv;
+        float iv;
         scale_from_max(mm, sc, iv);
         s_inv[t] = iv;
-        if (rank == 0 && c0 + t < cols) {
-            scale[c0 + t] = sc;
-            if (mm >= kNonfiniteBits && dstatus) atomicOr(dstatus, 1);
-        }
+    }
+    cluster_arrive_release();  // done with the peers' maxima
+    if (t < kStripCols && rank == 0 && c0 + t < cols) {
+        scale[c0 + t] = sc;
+        if (mm >= kNonfiniteBits && dstatus) atomicOr(dstatus, 1);
     }
     __syncthreads();
     const float i0 = s_inv[4 * c4], i1 = s_inv[4 * c4 + 1], i2 = s_inv[4 * c4 + 2],
@@ -792,7 +812,7 @@ __device__ __forceinline__ void cols_strip_block(const float *__restrict__ X, in
                 dst[k2] = ts[n][k2];
         }
     }
-    cluster.sync();  // no CTA leaves while another may still read its maxima
+    cluster_wait_acquire();  // no CTA leaves while another may still read its maxima
 }
 
 template <int WPR, int RV>
