@@ -28,6 +28,10 @@ CASES = [
 def main():
     orc = oracle.load()
     lines = ["# probe hash written by tests/golden/make_golden.py from the CPU oracle",
+             "# the kernel probe of \"Verification -- why you can trust the numbers\",",
+             "# section \"Layer 3: the kernel probe\"; the page fixes neither the inputs",
+             "# nor the hash, so these follow the oracle's readings: SplitMix64 inputs",
+             "# in [-1, 1), a BLAKE2s-256 tree over C's little-endian f32 bytes",
              "# format: <seed> <M> <N> <K> <hash hex>"]
     for seed, M, N, K in CASES:
         h, st = orc.probe_hash(seed, M, N, K)
