@@ -22,6 +22,10 @@ than itself) live in ``tests/``.  Parity status per function:
 * SplitMix64 probe inputs: pinned by the generator's published outputs.
 * probe hash as a whole: "parity unpinned" against the pages' system (the
   pages give neither the probe's inputs nor its hash function).
+* presk weight storage (scales, int8 / int4 codes, stored weights): pinned by
+  exact rationals (the scale's f32 rounding, the nearest integer with ties to
+  even, subnormal channels included), constructed ties, the page's error
+  rule, pow2 exactness and the nibble layout.
 """
 from __future__ import annotations
 

@@ -37,6 +37,8 @@
  *   R7  the probe hash is a BLAKE2s-256 (RFC 7693) tree in the BLAKE2 tree
  *       mode -- fanout 4, leaves of 256 bytes of C's little-endian bytes,
  *       row-major, rows packed.
+ * Because of R6 and R7 the probe hash as a whole is "parity unpinned"
+ * against the pages' own system; its parts are pinned to their standards.
  */
 #include <math.h>
 #include <stddef.h>
