@@ -22,8 +22,10 @@ constexpr int kLagCols = 128;  // columns per panel
 constexpr int kLagChunk = 2;   // slices per item
 
 // Item `it` of the list for P panels of S slices and a lag of L panels.
-__device__ __forceinline__ void lag_item(int64_t it, int64_t P, int64_t S, int64_t L,
-                                         bool &quantize, int64_t &panel, int64_t &slice) {
+// (Host-callable too, so that a host test can walk the whole list.)
+__host__ __device__ __forceinline__ void lag_item(int64_t it, int64_t P, int64_t S, int64_t L,
+                                                  bool &quantize, int64_t &panel,
+                                                  int64_t &slice) {
     const int64_t lead = P < L ? P : L;      // panels whose max items come alone
     const int64_t both = P > L ? P - L : 0;  // steps with max and quantize items
     if (it < lead * S) {
