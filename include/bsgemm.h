@@ -300,7 +300,8 @@ bsg_status bsgemm_i8_noalloc(const float *A, const float *B, int64_t M, int64_t 
  * 0-3 of byte i and column 2i+1 in bits 4-7 (zero past the last column).
  * scale: DEVICE f32[N].  `workspace`: bsg_wquant_cols_workspace_size(K, N)
  * bytes of DEVICE memory (256-byte aligned; counters and column maxima of
- * the one-read path that columns of more than 4096 rows take), owned by the
+ * the one-read path that long columns take: more than 4096 rows, or 2048 or
+ * more in a weight of 2^23 elements or more), owned by the
  * caller and not used after the call's work completes on `stream`.  Inf or
  * NaN in W sets BSG_DSTATUS_NONFINITE in *dstatus (may be NULL); the codes
  * and scales of such columns are then unspecified.  Asynchronous.  These are
