@@ -815,8 +815,13 @@ __device__ __forceinline__ void cols_strip_block(const float *__restrict__ X, in
     cluster_wait_acquire();  // no CTA leaves while another may still read its maxima
 }
 
+// One-warp rows of at most 768 columns (the GPT-2 linears, the LM head) are
+// held to 48 registers, five CTAs per SM instead of four, without spills.
+// Measured on a GB300: fc's quantize 10.5 -> 10.1 us, the LM head unit 520.9
+// -> 516.7 us, qkv's quantize 9.6 -> 10.0 us (the GPT-2 step 164.5 -> 163.9
+// us).  Wider rows keep the unbounded register count (they spill at 48).
 template <int WPR, int RV>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, WPR == 1 && RV <= 6 ? 5 : 0)
     quantize_ab_kernel(const float *__restrict__ A, int64_t M, int64_t K, int64_t lda,
                        __half *__restrict__ Aop, float *__restrict__ sa,
                        const float *__restrict__ B, int64_t N, int64_t ldb,
