@@ -75,6 +75,8 @@ MUTANTS = {
     "wquant_pow2_rounds_down": [("return ldexpf(1.0f, e);        /* 2^e",
                                  "return ldexpf(1.0f, e - 1);    /* 2^e")],
     "wquant_zero_channel_floored": [("float s = m / qmax;", "float s = fmaxf(m / qmax, 1e-8f);")],
+    "wquant_subnormal_scale_flushed": [("float s = m / qmax;",
+                                        "float s = m / qmax;\n        if (s < 1.17549435e-38f) s = 0.0f;")],
     "int4_nibbles_swapped": [("P[k * ldp + i] = (uint8_t)(lo | (hi << 4));",
                               "P[k * ldp + i] = (uint8_t)(hi | (lo << 4));")],
     "wdequant_next_channel_scale": [("What[k * ldo + j] = (float)Q[k * ldq + j] * scale[j];",
