@@ -43,6 +43,7 @@ MUTANTS = {
     "no_scale_floor": [("if (s < 1e-8) s = 1e-8;", "")],
     "divide_by_128": [("(double)m / 127.0", "(double)m / 128.0")],
     "signed_max_not_absmax": [("float a = fabsf(v); /* |-0| = +0 */", "float a = v;")],
+    "nan_not_flagged": [("if (!isfinite(v)) finite = 0;", "if (isinf(v)) finite = 0;")],
     "absmax_skips_last": [("for (int64_t k = 0; k < n; ++k) {\n        float v = x[k * stride];",
                            "for (int64_t k = 0; k < n - 1; ++k) {\n        float v = x[k * stride];")],
     "dropped_k_tail": [("for (int64_t k = 0; k < K; ++k) {\n                int64_t a = Aq[i * K + k];",
@@ -166,6 +167,19 @@ def pin_int32_range(o):
     assert st != 0
 
 
+def pin_nonfinite(o):
+    # a NaN alone, and an Inf alone, flag the row, the column and the weight
+    # channel that hold them (the boundary's rule: inputs must be finite, and
+    # a non-finite one is reported in the status)
+    for bad in (np.nan, np.inf):
+        A = np.ones((2, 8), np.float32)
+        A[1, 5] = bad
+        assert o.quantize_rows(A)[3] == 5
+        assert o.quantize_cols(np.ascontiguousarray(A.T))[3] == 5
+        assert o.wquant_cols(np.ascontiguousarray(A.T), 8, False)[2] == 5
+    assert o.quantize_rows(np.ones((2, 8), np.float32))[3] == 0
+
+
 def pin_zero_row(o):
     A = inputs.normal((5, 30), 1.0, 1).numpy()
     A[2] = -0.0
@@ -228,7 +242,7 @@ def pin_wquant(o):
 F32 = R.BINARY32
 
 BATTERY = [pin_quantize_referee, pin_epilogue_referee, pin_bruteforce, pin_unit_scales,
-           pin_int32_range, pin_zero_row, pin_hash, pin_probe, pin_wquant]
+           pin_int32_range, pin_nonfinite, pin_zero_row, pin_hash, pin_probe, pin_wquant]
 
 
 def run_battery(o):
