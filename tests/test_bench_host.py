@@ -1,7 +1,8 @@
 """Host logic of bench.py, without a GPU: the GEMM source digest that guards
-the committed ncu counters, the parsing of those counters, and the reference
+the committed ncu counters, the parsing of those counters, the reference
 arm's bounded sampling (with a stand-in for the oracle, so that it runs in
-milliseconds)."""
+milliseconds), and the JSON line's contract built from synthetic stage
+times."""
 import json
 import os
 import sys
@@ -155,3 +156,56 @@ def test_config_line_names_the_workload():
 
 def test_quantize_bytes_count_codes_not_f16_operands():
     assert bench.quant_algo_bytes(2, 3, 4) == 5 * (8 + 12) + 4 * 5
+
+
+def _fake_workload(kind):
+    from types import SimpleNamespace
+    units = [dict(name=n, M=M, N=N, K=K) for n, M, N, K, _, _ in bench.unit_list(kind)]
+    return SimpleNamespace(units=units)
+
+
+def test_bench_line_keeps_the_contract():
+    """The JSON line built from synthetic stage times: every key of the
+    contract, the throughput arithmetic, and one line of JSON."""
+    W = _fake_workload("large")
+    ms = {"sq4096": 0.1, "sq8192": 0.6, "sq16384": 4.4, "ragged_adversarial": 0.5}
+    qms = {"sq4096": 0.05, "sq8192": 0.17, "sq16384": 0.68, "ragged_adversarial": 0.19}
+    stage_ms = {}
+    for u in W.units:
+        stage_ms["gemm_" + u["name"]] = [ms[u["name"]]] * 3
+        stage_ms["quantize_" + u["name"]] = [qms[u["name"]]] * 3
+    stage_ms["probe"] = [0.08]
+    peaks = {"bf16_tflops": 1908.6, "bf16_tflops_sustained": 1695.1, "hbm_gbs": 6789.3}
+    roof, quant, probe_ms = bench.summarize(W, [6.7], stage_ms, peaks, "measured", 6.7, 1,
+                                            bench.GEMM_PROFILE)
+    ops = sum(2 * u["M"] * u["N"] * u["K"] for u in W.units)
+    assert roof["achieved"] == pytest.approx(ops / (sum(ms.values()) * 1e-3) / 1e12, rel=1e-6)
+    assert roof["frac"] == pytest.approx(roof["achieved"] / 1908.6, abs=1e-4)
+    assert roof["bound"] == "tensor" and roof["unit"] == "TFLOP/s" and roof["peak"] == 1908.6
+    assert roof["traffic"] is None or isinstance(roof["traffic"], int)
+    qbytes = sum(bench.quant_algo_bytes(u["M"], u["N"], u["K"]) for u in W.units)
+    assert quant["achieved_gbs"] == pytest.approx(qbytes / (sum(qms.values()) * 1e-3) / 1e9,
+                                                  abs=0.1)
+    args = type("A", (), {"steps": 100, "warmup": 5})()
+    clk = {"sm_mhz": 1790.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    line = bench.build_line(args, 1, 6.7, roof, quant, probe_ms, 2100.0, clk, 2010, 6000, 400,
+                            0.9, (18.3, 27.4), [18.3] * 20, 3355443192, 1610678308, None, "ab",
+                            "ab", True, 0, 0, 0.165, roof, quant)
+    text = json.dumps(line)
+    assert "\n" not in text
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "e2e", "clocks", "gpu_launches"):
+        assert key in line, key
+    assert line["value"] == pytest.approx(bench.step_ops("large") / (6.7e-3) / 1e12, rel=1e-6)
+    assert line["unit"] == "TOPS" and line["higher_is_better"] is True
+    assert line["scaling"] == "weak" and line["vs_baseline"] is None
+    assert line["n_gpus"] == 1 and line["steps"] == 100 and line["warmup"] == 5
+    assert line["config"]["workload"] == bench.WORKLOAD
+    for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert key in line["roofline"], key
+    e2e = line["e2e"]
+    assert e2e["unit"] == "TOPS" and e2e["h2d_bytes_per_step"] == 3355443192
+    assert e2e["d2h_bytes_per_step"] == 1610678308
+    assert e2e["value"] == pytest.approx(bench.step_ops("large") / 18.3e-3 / 1e12, rel=1e-3)
+    assert line["gpu_launches"] == 2010 and line["clocks"]["sm_mhz"] == 1790.0
