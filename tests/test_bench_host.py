@@ -209,3 +209,35 @@ def test_bench_line_keeps_the_contract():
     assert e2e["d2h_bytes_per_step"] == 1610678308
     assert e2e["value"] == pytest.approx(bench.step_ops("large") / 18.3e-3 / 1e12, rel=1e-3)
     assert line["gpu_launches"] == 2010 and line["clocks"]["sm_mhz"] == 1790.0
+
+
+def test_clock_log_summary(tmp_path, monkeypatch):
+    """The clocks key from an nvidia-smi log in the sampler's format: the
+    median SM clock, the maximum, and every throttle reason seen active
+    (malformed lines skipped)."""
+    monkeypatch.setenv("BSG_CLOCKS_DIR", str(tmp_path))
+    s = bench.ClockSampler(0)
+    rows = ["0, 2070, 2070, 176.67, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "0, 1785, 2070, 1390.2, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 1770, 2070, 1401.0, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, [N/A], 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "garbage",
+            "0, 1650, 2070, 1399.9, 0x8, Active, Not Active, Not Active, Active"]
+
+    class Proc:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    s.f = open(s.path, "w")
+    s.f.write("\n".join(rows) + "\n")
+    s.proc = Proc()
+    clk = s.stop()
+    assert clk["samples"] == 4
+    assert clk["sm_mhz"] == pytest.approx((1770 + 1785) / 2)
+    assert clk["sm_max_mhz"] == 2070.0
+    assert clk["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    empty = bench.ClockSampler(1)
+    assert empty.stop()["reasons"] == ["nvidia-smi unavailable"]
