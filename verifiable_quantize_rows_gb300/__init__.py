@@ -8,6 +8,13 @@ library is missing or the device is not sm_103, calls raise.
 
 Functions take contiguous row-major CUDA tensors and run on the current
 PyTorch stream (or the ``stream`` given).
+
+Workspaces: a call given no ``workspace`` uses one buffer per device shared
+by every such call.  Calls that may run at the same time (on different
+streams, or from different host threads) must each pass their own
+``Workspace``, and so should calls on a stream other than PyTorch's current
+one: when the shared buffer grows, the old one goes back to PyTorch's
+allocator, which tracks only the stream it was allocated on.
 """
 from __future__ import annotations
 
@@ -173,7 +180,8 @@ def _need(t, dtype, name):
 
 
 class Workspace:
-    """A growable device byte buffer (256-byte aligned, from PyTorch)."""
+    """A growable device byte buffer (256-byte aligned, from PyTorch).  One
+    per stream of concurrent calls; see the module notes on workspaces."""
 
     def __init__(self, device=None):
         self.device = device
