@@ -819,7 +819,8 @@ __device__ __forceinline__ void cols_strip_block(const float *__restrict__ X, in
 // held to 48 registers, five CTAs per SM instead of four, without spills.
 // Measured on a GB300: fc's quantize 10.5 -> 10.1 us, the LM head unit 520.9
 // -> 516.7 us, qkv's quantize 9.6 -> 10.0 us (the GPT-2 step 164.5 -> 163.9
-// us).  Wider rows keep the unbounded register count (they spill at 48).
+// us).  Wider rows (up to K = 2048, the fused launch's limit) keep the
+// unbounded register count (they spill at 48).
 template <int WPR, int RV>
 __global__ void __launch_bounds__(256, WPR == 1 && RV <= 6 ? 5 : 0)
     quantize_ab_kernel(const float *__restrict__ A, int64_t M, int64_t K, int64_t lda,
@@ -1499,9 +1500,7 @@ cudaError_t launch_quantize_ab(const float *A, int64_t M, int64_t K, int64_t lda
         case 2: e = launch_ab<1, 6>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, zrows, st); break;
         case 3: e = launch_ab<1, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, zrows, st); break;
         case 4: e = launch_ab<2, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, zrows, st); break;
-        case 5: e = launch_ab<4, 6>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, zrows, st); break;
-        case 6: e = launch_ab<4, 8>(A, M, K, lda, Aop, sa, B, N, ldb, Bop, sb, ldk, cs, R, dstatus, zero2, zrows, st); break;
-        default: return cudaErrorNotSupported;  // rows longer than 4096: not fused
+        default: return cudaErrorNotSupported;  // not reached: strip_shape caps K at 2048
     }
     count_launches(1);
     return e;
