@@ -159,3 +159,21 @@ def test_selftest_known_answer_is_the_oracle_golden():
         if len(p) == 5 and p[:4] == ["0", "1024", "1024", "1024"]:
             golden = p[4]
     assert golden is not None and compiled == golden
+
+
+def test_binding_refuses_host_tensors():
+    """No CPU fallback: host tensors, wrong dtypes and non-contiguous views
+    are refused before anything runs."""
+    import torch
+    A = torch.ones(4, 8)
+    B = torch.ones(8, 3)
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        bsg.bsgemm_i8(A, B)
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        bsg.quantize_rows(A)
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        bsg.quantize_cols(A)
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        bsg.wquant_cols(A)
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        bsg.bsgemm_i8(A.double(), B.double())
