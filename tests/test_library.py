@@ -177,3 +177,44 @@ def test_binding_refuses_host_tensors():
         bsg.wquant_cols(A)
     with pytest.raises(TypeError, match="CUDA tensor"):
         bsg.bsgemm_i8(A.double(), B.double())
+
+
+def test_product_path_never_touches_the_oracle():
+    """Static check: the package, its CUDA sources and the header never
+    import, load or link the oracle's module or library; bench.py imports it
+    only inside its two CPU legs (cpu_baseline and the reference arm); the
+    oracle never imports the package."""
+    import ast
+    import re
+    ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    pkg = os.path.join(ROOT, "verifiable_quantize_rows_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath or "__pycache__" in dirpath:
+            continue
+        for f in files:
+            if not f.endswith((".py", ".cu", ".cuh", ".h", ".c")):
+                continue
+            text = open(os.path.join(dirpath, f)).read()
+            if f.endswith(".py"):
+                tree = ast.parse(text)
+                for node in ast.walk(tree):
+                    if isinstance(node, ast.Import):
+                        assert all(not a.name.startswith("oracle") for a in node.names), f
+                    if isinstance(node, ast.ImportFrom):
+                        assert not (node.module or "").startswith("oracle"), f
+            assert "bsg_oracle" not in text, f
+            assert not re.search(r"dlopen|CDLL\([^)]*oracle", text), f
+    header = open(os.path.join(ROOT, "include", "bsgemm.h")).read()
+    assert "bsg_oracle" not in header and "orc_" not in header
+    tree = ast.parse(open(os.path.join(ROOT, "bench.py")).read())
+    users = set()
+    for fn in ast.walk(tree):
+        if isinstance(fn, ast.FunctionDef):
+            for node in ast.walk(fn):
+                if isinstance(node, ast.Import) and any(a.name == "oracle" for a in node.names):
+                    users.add(fn.name)
+    top = [n for n in tree.body if isinstance(n, (ast.Import, ast.ImportFrom))]
+    assert all("oracle" not in ast.dump(n) for n in top)
+    assert users <= {"cpu_baseline", "run_reference", "oracle_inputs"}, users
+    orc_src = open(os.path.join(ROOT, "oracle", "__init__.py")).read()
+    assert "verifiable_quantize_rows_gb300" not in orc_src
