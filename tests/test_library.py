@@ -218,3 +218,7 @@ def test_product_path_never_touches_the_oracle():
     assert users <= {"cpu_baseline", "run_reference", "oracle_inputs"}, users
     orc_src = open(os.path.join(ROOT, "oracle", "__init__.py")).read()
     assert "verifiable_quantize_rows_gb300" not in orc_src
+    # the oracle's C source includes system headers only: no shared header
+    c_src = open(os.path.join(ROOT, "oracle", "bsg_oracle.c")).read()
+    includes = re.findall(r"#\s*include\s*(\S+)", c_src)
+    assert includes and all(i.startswith("<") for i in includes), includes
